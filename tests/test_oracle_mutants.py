@@ -1,0 +1,150 @@
+"""Plant plausible mistakes in the oracle (on the CPU) and check that the pins catch them.
+
+Each mutant replaces one oracle function with a subtly wrong version; the pin tests of
+test_oracle_pins.py are then run against the mutated module and at least one must fail.
+"""
+import math
+
+import numpy as np
+import pytest
+
+from oracle import kvsel_oracle as O
+import tests.test_oracle_pins as P
+
+ORIG = {name: getattr(O, name) for name in dir(O) if callable(getattr(O, name))}
+
+
+def _logits_no_scale(q, k, scale=None, causal=True):
+    return ORIG["window_logits"](q, k, 1.0, causal)
+
+
+def _logits_causal_off_by_one(q, k, scale=None, causal=True):
+    G, W, d = q.shape
+    n = k.shape[0]
+    if scale is None or scale == 0.0:
+        scale = 1.0 / math.sqrt(d)
+    l = np.matmul(q.reshape(G * W, d), k.T).reshape(G, W, n) * scale
+    if causal:
+        pos = n - W + np.arange(W)
+        mask = np.arange(n)[None, :] >= pos[:, None]
+        l = np.where(mask[None], -np.inf, l)
+    return l
+
+
+def _reduce_mean_over_group_only(p, op):
+    if op == "mean":
+        return p.sum(axis=1).mean(axis=0) if p.ndim == 3 else p.mean(axis=0)
+    return ORIG["reduce_rows"](p, op)
+
+
+def _avgpool_divides_by_count(s, kind, kernel):
+    if kind != "avg" or kernel <= 1:
+        return ORIG["pool1d"](s, kind, kernel)
+    n = s.shape[0]
+    h = kernel // 2
+    out = np.empty(n)
+    for i in range(n):
+        a, b = max(0, i - h), min(n, i + h + 1)
+        out[i] = s[a:b].mean()
+    return out
+
+
+def _value_norm_l2(v, w_o, h, group, mode="group_sum", row_block=4096):
+    sl = O.wo_slices(w_o, h, group, v.shape[1])
+    wbar = sum(sl)
+    return np.sqrt(((v @ wbar.T) ** 2).sum(1))
+
+
+def _value_norm_first_slice_only(v, w_o, h, group, mode="group_sum", row_block=4096):
+    sl = O.wo_slices(w_o, h, group, v.shape[1])
+    return np.abs(v @ (group * sl[0]).T).sum(1)
+
+
+def _combine_no_eps(s_pool, nu, eps=1e-4):
+    return s_pool * nu
+
+
+def _top_b_ties_descending(scores, budget, forced):
+    n = scores.shape[0]
+    key = np.where(forced, np.inf, scores)
+    order = np.lexsort((-np.arange(n), -key))
+    return np.sort(order[:budget])
+
+
+def _two_stage_ceil(s_pool, s_val, budget, forced, alpha=0.5):
+    b1 = int(math.ceil(alpha * budget))
+    s1 = ORIG["top_b"](s_pool, max(b1, int(forced.sum())), forced)
+    keep = np.zeros_like(forced)
+    keep[s1] = True
+    return ORIG["top_b"](s_val, budget, keep)
+
+
+def _two_stage_without_stage1(s_pool, s_val, budget, forced, alpha=0.5):
+    return ORIG["top_b"](s_val, budget, forced)
+
+
+def _forced_recent_off_by_one(n, n_sink, n_recent):
+    f = np.zeros(n, dtype=bool)
+    f[:n_sink] = True
+    if n_recent > 0:
+        f[max(n - n_recent - 1, 0):] = True
+    return f
+
+
+def _query_agnostic_mean(q, k, scale=None, q_chunk=0):
+    G, m, d = q.shape
+    p = O.softmax_rows((q.reshape(-1, d) @ k.T) / math.sqrt(d))
+    return p.mean(axis=0)
+
+
+def _per_layer_ignores_floor(scores, budget, forced, floor_per_head):
+    return ORIG["select_per_layer"](scores, budget, forced, 0)
+
+
+MUTANTS = {
+    "no_scale": ("window_logits", _logits_no_scale),
+    "causal_off_by_one": ("window_logits", _logits_causal_off_by_one),
+    "mean_over_group_only": ("reduce_rows", _reduce_mean_over_group_only),
+    "avgpool_divides_by_count": ("pool1d", _avgpool_divides_by_count),
+    "value_norm_l2": ("value_norm", _value_norm_l2),
+    "value_norm_first_slice": ("value_norm", _value_norm_first_slice_only),
+    "combine_no_eps": ("combine", _combine_no_eps),
+    "ties_descending": ("top_b", _top_b_ties_descending),
+    "two_stage_ceil": ("select_two_stage", _two_stage_ceil),
+    "two_stage_skips_stage1": ("select_two_stage", _two_stage_without_stage1),
+    "forced_recent_off_by_one": ("forced_mask", _forced_recent_off_by_one),
+    "query_agnostic_mean": ("query_agnostic_scores", _query_agnostic_mean),
+    "per_layer_ignores_floor": ("select_per_layer", _per_layer_ignores_floor),
+}
+
+
+def _pin_calls():
+    calls = []
+    for name in dir(P):
+        if not name.startswith("test_"):
+            continue
+        fn = getattr(P, name)
+        marks = getattr(fn, "pytestmark", [])
+        params = [m for m in marks if m.name == "parametrize"]
+        if not params:
+            calls.append((name, fn, {}))
+            continue
+        argnames, values = params[0].args[0], params[0].args[1]
+        names = [a.strip() for a in argnames.split(",")]
+        for val in values:
+            vals = val if isinstance(val, tuple) else (val,)
+            calls.append((f"{name}{vals}", fn, dict(zip(names, vals))))
+    return calls
+
+
+@pytest.mark.parametrize("mutant", sorted(MUTANTS))
+def test_pins_catch_mutant(mutant, monkeypatch):
+    attr, fake = MUTANTS[mutant]
+    monkeypatch.setattr(O, attr, fake)
+    failed = []
+    for name, fn, kw in _pin_calls():
+        try:
+            fn(**kw)
+        except (Exception, pytest.fail.Exception):
+            failed.append(name)
+    assert failed, f"no pin caught mutant {mutant}"

@@ -1,0 +1,435 @@
+"""Pins of the fp64 oracle against facts fixed outside the oracle itself.
+
+Each test ties one oracle function to a hand-computed fixture (tests/golden), a closed
+form, a library routine for a special case, brute force on tiny inputs, or an invariant
+stated by the pages.  Together they are chosen so that a plausible slip (missing scale,
+off-by-one causal mask, wrong reduction axis, transposed W_O, wrong pooling padding,
+tie order) breaks at least one of them; test_oracle_mutants.py plants such slips.
+"""
+import itertools
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import scipy.ndimage
+import scipy.special
+
+from oracle import kvsel_oracle as O
+from kv_cache_eviction_window_gb300 import datagen
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def load_golden(name):
+    vals = {}
+    for line in open(os.path.join(GOLDEN, name)):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        key, rest = line.split(":", 1)
+        vals[key.strip()] = [Fraction(t) for t in rest.split()]
+    return vals
+
+
+def f64(x):
+    return np.array([float(v) for v in x])
+
+
+# --------------------------------------------------------------------- decoding
+def test_bf16_decode_closed_form():
+    bits = np.array([0x3F80, 0xC000, 0x3F81, 0x0001, 0x7F7F, 0x8000], np.uint16)
+    want = [1.0, -2.0, 1.0 + 2.0 ** -7, 2.0 ** -133, (2 - 2.0 ** -7) * 2.0 ** 127, -0.0]
+    got = O.bf16_to_f64(bits)
+    assert list(got) == want
+
+
+# --------------------------------------------------------------------- hand example
+def hand_inputs():
+    q = np.array([[[1.0, 0.0], [1.0, 0.0]]])            # [G=1][W=2][d=2]
+    k = np.array([[i, 0.0] for i in range(4)])           # [n=4][d=2]
+    return q, k, math.log(2.0)
+
+
+def test_hand_softmax_rows():
+    g = load_golden("hand_example.txt")
+    q, k, sc = hand_inputs()
+    p = O.softmax_rows(O.window_logits(q, k, sc, causal=True))
+    np.testing.assert_allclose(p[0, 0], f64(g["p_row0"]), rtol=1e-14, atol=0)
+    np.testing.assert_allclose(p[0, 1], f64(g["p_row1"]), rtol=1e-14, atol=0)
+    assert p[0, 0, 3] == 0.0
+
+
+@pytest.mark.parametrize("op,key", [("sum", "s_sum"), ("mean", "s_mean"), ("max", "s_max")])
+def test_hand_reductions(op, key):
+    g = load_golden("hand_example.txt")
+    q, k, sc = hand_inputs()
+    s = O.window_scores(q, k, op, sc, causal=True)
+    np.testing.assert_allclose(s, f64(g[key]), rtol=1e-14)
+
+
+def test_hand_pooling_and_selection():
+    g = load_golden("hand_example.txt")
+    s = f64(g["s_sum"])
+    np.testing.assert_allclose(O.pool1d(s, "max", 3), f64(g["maxpool3_sum"]), rtol=1e-14)
+    np.testing.assert_allclose(O.pool1d(s, "avg", 3), f64(g["avgpool3_sum"]), rtol=1e-14)
+    none = np.zeros(4, bool)
+    assert list(O.top_b(s, 2, none)) == [int(v) for v in g["top2_sum"]]
+    assert list(O.top_b(O.pool1d(s, "max", 3), 2, none)) == [int(v) for v in g["top2_maxpool3"]]
+
+
+def test_hand_value_norm_and_two_stage():
+    g = load_golden("hand_example.txt")
+    w_o = np.array([[1.0, 2.0], [3.0, -4.0]])
+    v = np.array([[1.0, 1.0], [2.0, -1.0], [0.0, 0.0], [-1.0, 0.0]])
+    nu = O.value_norm(v, w_o, h=0, group=1)
+    np.testing.assert_array_equal(nu, f64(g["nu"]))
+    s = f64(g["s_sum"])
+    sv = O.combine(s, nu, 1e-4)
+    np.testing.assert_allclose(sv, f64(g["s_val_sum"]), rtol=1e-14)
+    none = np.zeros(4, bool)
+    assert list(O.top_b(sv, 2, none)) == [int(x) for x in g["top2_val"]]
+    assert list(O.select_two_stage(s, sv, 2, none, 0.5)) == [int(x) for x in g["two_stage_b2"]]
+
+
+# --------------------------------------------------------------------- scoring
+def test_textbook_softmax_special_case():
+    """G = W = 1, no mask, no pooling: the score is the plain softmax of q K^T / sqrt(d)."""
+    rng = np.random.default_rng(0)
+    d, n = 16, 37
+    q = rng.standard_normal((1, 1, d))
+    k = rng.standard_normal((n, d))
+    s = O.window_scores(q, k, "sum", None, causal=False)
+    ref = scipy.special.softmax(k @ q[0, 0] / math.sqrt(d))
+    np.testing.assert_allclose(s, ref, rtol=1e-13)
+    s_mean = O.window_scores(q, k, "mean", None, causal=False)
+    np.testing.assert_allclose(s_mean, ref, rtol=1e-13)
+
+
+def test_causal_mask_positions_and_row_sums():
+    rng = np.random.default_rng(1)
+    G, W, d, n = 3, 5, 8, 11
+    q = rng.standard_normal((G, W, d))
+    k = rng.standard_normal((n, d))
+    p = O.softmax_rows(O.window_logits(q, k, None, causal=True))
+    for w in range(W):
+        pos = n - W + w
+        assert np.all(p[:, w, pos + 1:] == 0.0)
+        assert np.all(p[:, w, :pos + 1] > 0.0)
+    np.testing.assert_allclose(p.sum(-1), 1.0, rtol=1e-14)
+
+
+def test_reductions_relate():
+    rng = np.random.default_rng(2)
+    G, W, d, n = 4, 6, 8, 20
+    q = rng.standard_normal((G, W, d))
+    k = rng.standard_normal((n, d))
+    s_sum = O.window_scores(q, k, "sum")
+    s_mean = O.window_scores(q, k, "mean")
+    s_max = O.window_scores(q, k, "max")
+    np.testing.assert_allclose(s_mean * G * W, s_sum, rtol=1e-13)
+    # brute force over rows
+    p = O.softmax_rows(O.window_logits(q, k, None, True))
+    for i in range(n):
+        assert s_max[i] == max(p[g, w, i] for g in range(G) for w in range(W))
+    # the window rows are probability distributions: scores sum to the row count
+    assert abs(s_sum.sum() - G * W) < 1e-12
+
+
+def test_scale_enters_logits():
+    rng = np.random.default_rng(3)
+    q = rng.standard_normal((1, 2, 4))
+    k = rng.standard_normal((6, 4))
+    l1 = O.window_logits(q, k, None, causal=False)
+    l2 = O.window_logits(q, k, 1.0, causal=False)
+    np.testing.assert_allclose(l1 * 2.0, l2, rtol=1e-14)  # 1/sqrt(4) = 1/2
+
+
+# --------------------------------------------------------------------- pooling
+def test_pool_identity_and_global_max():
+    rng = np.random.default_rng(4)
+    s = rng.random(13)
+    np.testing.assert_array_equal(O.pool1d(s, "max", 1), s)
+    np.testing.assert_array_equal(O.pool1d(s, "avg", 1), s)
+    np.testing.assert_array_equal(O.pool1d(s, "none", 7), s)
+    np.testing.assert_array_equal(O.pool1d(s, "max", 2 * 13 - 1), np.full(13, s.max()))
+
+
+@pytest.mark.parametrize("k", [3, 5, 7])
+def test_pool_matches_library(k):
+    rng = np.random.default_rng(5 + k)
+    s = rng.random(50)
+    ref_max = scipy.ndimage.maximum_filter1d(s, size=k, mode="nearest")
+    np.testing.assert_array_equal(O.pool1d(s, "max", k), ref_max)
+    ref_avg = np.convolve(s, np.ones(k), mode="same") / k
+    np.testing.assert_allclose(O.pool1d(s, "avg", k), ref_avg, rtol=1e-14)
+
+
+# --------------------------------------------------------------------- value norm
+def test_value_norm_identity_slices_closed_form():
+    """W_O^(h,g) = [I_d; 0] for every g: group sum gives G*||v||_1, per head the same."""
+    rng = np.random.default_rng(6)
+    H, G, d, D, n = 2, 3, 4, 6, 9
+    w_o = np.zeros((D, H * G * d))
+    for q in range(H * G):
+        w_o[:d, q * d:(q + 1) * d] = np.eye(d)
+    v = rng.standard_normal((n, d))
+    for h in range(H):
+        np.testing.assert_allclose(O.value_norm(v, w_o, h, G), G * np.abs(v).sum(1), rtol=1e-14)
+        np.testing.assert_allclose(O.value_norm(v, w_o, h, G, "per_head"),
+                                   G * np.abs(v).sum(1), rtol=1e-14)
+
+
+def test_value_norm_readings_differ_on_opposite_slices():
+    d, D, G = 3, 3, 2
+    w_o = np.concatenate([np.eye(d), -np.eye(d)], axis=1)   # head 0: +I, head 1: -I
+    v = np.array([[1.0, -2.0, 3.0]])
+    assert O.value_norm(v, w_o, 0, G)[0] == 0.0
+    assert O.value_norm(v, w_o, 0, G, "per_head")[0] == 12.0
+
+
+def test_value_norm_brute_force():
+    """Explicit loops over outputs j, columns c and group heads g on tiny random data."""
+    rng = np.random.default_rng(7)
+    H, G, d, D, n = 2, 2, 3, 5, 4
+    w_o = rng.standard_normal((D, H * G * d))
+    v = rng.standard_normal((n, d))
+    for h in range(H):
+        got = O.value_norm(v, w_o, h, G)
+        got_i = O.value_norm(v, w_o, h, G, "per_head")
+        for i in range(n):
+            tot = 0.0
+            tot_i = 0.0
+            for j in range(D):
+                acc = 0.0
+                for g in range(G):
+                    acc_g = 0.0
+                    for c in range(d):
+                        acc_g += w_o[j, (h * G + g) * d + c] * v[i, c]
+                    acc += acc_g
+                    tot_i += abs(acc_g)
+                tot += abs(acc)
+            assert abs(got[i] - tot) < 1e-12
+            assert abs(got_i[i] - tot_i) < 1e-12
+
+
+def test_value_norm_row_blocks_do_not_matter():
+    rng = np.random.default_rng(8)
+    w_o = rng.standard_normal((7, 2 * 2 * 4))
+    v = rng.standard_normal((23, 4))
+    a = O.value_norm(v, w_o, 1, 2, row_block=5)
+    b = O.value_norm(v, w_o, 1, 2, row_block=4096)
+    np.testing.assert_array_equal(a, b)
+
+
+# --------------------------------------------------------------------- selection
+def brute_top(scores, budget, forced):
+    """Best subset by enumeration: contains every forced entry; compare subsets by their
+    scores sorted descending, then by their indices sorted ascending."""
+    n = len(scores)
+    best = None
+    for sub in itertools.combinations(range(n), budget):
+        if not all(i in sub for i in np.flatnonzero(forced)):
+            continue
+        free = [i for i in sub if not forced[i]]
+        key = (sorted((-scores[i] for i in free)), sorted(free))
+        if best is None or key < best[0]:
+            best = (key, sub)
+    return list(best[1])
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_top_b_brute_force(seed):
+    rng = np.random.default_rng(100 + seed)
+    n = int(rng.integers(6, 12))
+    s = rng.integers(0, 5, size=n).astype(float)   # many exact ties
+    forced = np.zeros(n, bool)
+    forced[rng.choice(n, size=int(rng.integers(0, 3)), replace=False)] = True
+    for budget in range(int(forced.sum()), n + 1):
+        assert list(O.top_b(s, budget, forced)) == brute_top(s, budget, forced)
+
+
+def test_two_stage_degenerates_to_attention_only():
+    """CriticalKV App. C.4 (Theorem C.1): with stage 2 scored like stage 1 the algorithm is
+    the attention-only selection; alpha = 1 leaves no stage-2 budget."""
+    rng = np.random.default_rng(9)
+    n = 200
+    s = rng.random(n)
+    sv = rng.random(n)
+    f = O.forced_mask(n, 4, 8)
+    for b in (12, 50, 199):
+        ref = O.top_b(s, b, f)
+        np.testing.assert_array_equal(O.select_two_stage(s, s, b, f, 0.5), ref)
+        np.testing.assert_array_equal(O.select_two_stage(s, sv, b, f, 1.0), ref)
+
+
+def test_large_eps_ranks_by_value_norm():
+    rng = np.random.default_rng(10)
+    n = 64
+    s = rng.random(n) * 1e-3
+    nu = rng.random(n) + 0.5
+    f = np.zeros(n, bool)
+    sv = O.combine(s, nu, eps=1e6)
+    np.testing.assert_array_equal(O.select_two_stage(s, sv, 20, f, 0.0), O.top_b(nu, 20, f))
+
+
+def test_two_stage_brute_force():
+    rng = np.random.default_rng(11)
+    n = 10
+    for _ in range(20):
+        s = rng.integers(0, 4, n).astype(float)
+        sv = rng.integers(0, 4, n).astype(float)
+        f = np.zeros(n, bool)
+        f[0] = True
+        for b in range(1, n + 1):
+            b1 = max(int(math.floor(0.5 * b)), 1)
+            s1 = brute_top(s, b1, f)
+            keep = np.zeros(n, bool)
+            keep[s1] = True
+            want = brute_top(sv, b, keep)
+            assert list(O.select_two_stage(s, sv, b, f, 0.5)) == want
+
+
+def test_selection_invariants_and_identity():
+    rng = np.random.default_rng(12)
+    n = 500
+    s = rng.random(n)
+    f = O.forced_mask(n, 4, 32)
+    for b in (36, 100, 499, 500):
+        idx = O.top_b(s, b, f)
+        assert len(idx) == b
+        assert np.all(np.diff(idx) > 0) and idx[0] >= 0 and idx[-1] < n
+        assert set(np.flatnonzero(f)) <= set(idx.tolist())
+    np.testing.assert_array_equal(O.top_b(s, n, f), np.arange(n))
+    with pytest.raises(ValueError):
+        O.top_b(s, 35, f)
+
+
+def test_forced_mask():
+    f = O.forced_mask(10, 4, 3)
+    assert f.tolist() == [True] * 4 + [False] * 3 + [True] * 3
+    assert O.forced_mask(5, 4, 0).tolist() == [True] * 4 + [False]
+
+
+def test_per_layer_special_cases():
+    rng = np.random.default_rng(13)
+    H, n = 3, 40
+    s = rng.random((H, n))
+    none = np.zeros((H, n), bool)
+    # no floor, no forced: plain flattened top-B
+    got = O.select_per_layer(s, 30, none, 0)
+    flat = np.sort(np.argsort(-s.reshape(-1), kind="stable")[:30])
+    want = [flat[(flat >= h * n) & (flat < (h + 1) * n)] - h * n for h in range(H)]
+    for a, b in zip(got, want):
+        np.testing.assert_array_equal(a, b)
+    # one head: same as the per-head selection
+    f = O.forced_mask(n, 4, 5)[None]
+    np.testing.assert_array_equal(O.select_per_layer(s[:1], 17, f, 10)[0], O.top_b(s[0], 17, f[0]))
+
+
+def test_per_layer_floors_invariants():
+    rng = np.random.default_rng(14)
+    H, n = 4, 300
+    s = rng.random((H, n)) ** 4
+    s[0] *= 10.0  # head 0 dominates the flattened order
+    f = np.stack([O.forced_mask(n, 4, 16)] * H)
+    budget, fl = 240, 30
+    idx = O.select_per_layer(s, budget, f, fl)
+    assert sum(len(i) for i in idx) == budget
+    for h in range(H):
+        assert len(idx[h]) >= fl
+        assert set(np.flatnonzero(f[h])) <= set(idx[h].tolist())
+        assert np.all(np.diff(idx[h]) > 0)
+        # each head's floor picks are its own top entries
+        assert set(O.top_b(s[h], fl, f[h]).tolist()) <= set(idx[h].tolist())
+    # everything kept beyond the floors outranks everything dropped
+    kept = np.zeros((H, n), bool)
+    for h in range(H):
+        kept[h, idx[h]] = True
+    floor_keep = np.zeros((H, n), bool)
+    for h in range(H):
+        floor_keep[h, O.top_b(s[h], fl, f[h])] = True
+    extra = kept & ~floor_keep
+    dropped = ~kept
+    assert s[extra].min() >= s[dropped].max()
+
+
+# --------------------------------------------------------------------- permutation
+def test_permutation_consistency():
+    """Permuting prefix keys that every window row sees permutes the scores (no pooling)."""
+    rng = np.random.default_rng(15)
+    G, W, d, n = 2, 4, 8, 40
+    q = rng.standard_normal((G, W, d))
+    k = rng.standard_normal((n, d))
+    lo, hi = 4, n - W
+    perm = np.arange(n)
+    perm[lo:hi] = lo + rng.permutation(hi - lo)
+    s = O.window_scores(q, k, "mean")
+    sp = O.window_scores(q, k[perm], "mean")
+    np.testing.assert_allclose(sp, s[perm], rtol=1e-12)
+    f = O.forced_mask(n, 4, W)
+    a = O.top_b(s, 15, f)
+    b = O.top_b(sp, 15, f)
+    np.testing.assert_array_equal(np.sort(perm[b]), a)
+
+
+# --------------------------------------------------------------------- query-agnostic
+def test_query_agnostic_brute_force_and_chunks():
+    rng = np.random.default_rng(16)
+    G, m, d, n = 2, 7, 4, 9
+    q = rng.standard_normal((G, m, d))
+    k = rng.standard_normal((n, d))
+    S = O.query_agnostic_scores(q, k)
+    for i in range(n):
+        best = 0.0
+        for g in range(G):
+            for j in range(m):
+                logits = [float(q[g, j] @ k[t]) / math.sqrt(d) for t in range(n)]
+                mx = max(logits)
+                z = sum(math.exp(x - mx) for x in logits)
+                best = max(best, math.exp(logits[i] - mx) / z)
+        assert abs(S[i] - best) < 1e-14
+    np.testing.assert_array_equal(O.query_agnostic_scores(q, k, q_chunk=3), S)
+
+
+def test_max_trick_identity():
+    """max_r softmax_r[i] == exp(max_r (l_ri - logsumexp_r)) on small inputs."""
+    rng = np.random.default_rng(17)
+    q = rng.standard_normal((1, 64, 8))
+    k = rng.standard_normal((64, 8))
+    l = (q[0] @ k.T) / math.sqrt(8)
+    c = scipy.special.logsumexp(l, axis=1)
+    np.testing.assert_allclose(np.exp((l - c[:, None]).max(axis=0)),
+                               O.query_agnostic_scores(q, k), rtol=1e-13)
+
+
+# --------------------------------------------------------------------- compaction
+def test_compact_and_paging():
+    wl = datagen.WORKLOADS[4].replace(batch=3, n_min=40, n_ctx=90)
+    inp = datagen.make_layer(wl, 0)
+    pg = inp["paged"]
+    for b, n in enumerate(inp["n_ctx"]):
+        kb = O.unpage(pg["k_pool"], pg["block_table"][b], n)
+        vb = O.unpage(pg["v_pool"], pg["block_table"][b], n)
+        np.testing.assert_array_equal(kb, inp["k"][b])
+        np.testing.assert_array_equal(vb, inp["v"][b])
+    k = inp["k"][0][0]
+    idx = np.array([0, 3, 17, 39])
+    np.testing.assert_array_equal(O.compact(k, idx), np.stack([k[i] for i in idx]))
+    np.testing.assert_array_equal(O.compact(k, np.arange(k.shape[0])), k)
+
+
+# --------------------------------------------------------------------- end to end
+def test_run_layer_small_invariants():
+    wl = datagen.WORKLOADS[2].replace(layers=1, n_ctx=700, d_model=256)
+    inp = datagen.make_layer(wl, 0, n_ctx=700)
+    r = O.run_workload_layer(wl, inp)[0]
+    B = O.head_budget(700, wl.budget_ratio)
+    f = O.forced_mask(700, 4, 32)
+    for h in range(wl.h_kv):
+        assert len(r["idx"][h]) == B
+        assert set(np.flatnonzero(f)) <= set(r["idx"][h].tolist())
+        np.testing.assert_array_equal(r["k_out"][h], inp["k"][0][h][r["idx"][h]])
+    assert np.all(r["nu"] > 0)
+    np.testing.assert_allclose(r["s_raw"].sum(1), 1.0 * 1, rtol=1e-9)  # mean of prob rows
