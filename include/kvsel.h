@@ -1,0 +1,193 @@
+/*
+ * kvsel.h — end-of-prefill KV-cache importance scoring, top-B selection and compaction
+ * on one NVIDIA GB300 (sm_103a).
+ *
+ * The operations follow the pages this library restates:
+ *   - Observation-window scoring: the last W prompt queries of each GQA group attend to
+ *     all n cached keys; the fp32 softmax weights are reduced over window rows and the
+ *     G query heads of the group, then 1-D pooled along the sequence
+ *     ("CriticalKV: 출력 섭동 관점에서 KV 캐시 축출을 최적화하기", §3.4 Algorithm 2;
+ *     SnapKV kernel 7 / window 32 per its §4.1).
+ *   - Value-aware criterion (A + eps) * ||W_O v||_1 and two-stage selection with
+ *     alpha = 0.5 (same page, §3.3 Theorem 3.3, §3.4 Algorithm 1, §3.5, footnote 3).
+ *   - Query-agnostic maximum cross-attention score and a budget shared by the heads of a
+ *     layer ("KVzip: Query-Agnostic KV Cache Compression with Context Reconstruction",
+ *     §3.2, §3.4, §4.2).
+ *   - Attention sinks and the recent window are always kept ("VestigeKV: The NoPE-MLA KV
+ *     Cache Carries Its Own Eviction Signal in a Vestigial Branch", §4.1; "AnchorKV:
+ *     Anchor-Residual KV Cache Compression", §3.2).
+ *   - Eviction acts on the un-replicated KV heads; the result is a per-head
+ *     variable-length cache (KVzip §4.2, §7.1).
+ *
+ * Conventions (all entry points):
+ *   - Every pointer named device is a CUDA device pointer, 16-byte aligned; bf16 data is
+ *     IEEE bfloat16.  Host pointers are marked host.
+ *   - The caller owns every buffer.  The library never allocates device or host memory;
+ *     scratch space is the caller's workspace (kvsel_workspace_size).
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls are asynchronous
+ *     on that stream; argument errors are returned before anything is launched.
+ *   - Return value: KVSEL_OK or a negative KVSEL_E* code (kvsel_strerror).  Errors found
+ *     on the device (a bounded wait that ran out) are recorded in the workspace's status
+ *     word and read with kvsel_get_device_status after the stream work.
+ *   - head_dim must be 128.
+ *
+ * Data layouts (row-major, innermost last):
+ *   q (window scoring)         [batch][h_kv][group][window][head_dim] bf16
+ *   q (query-agnostic, window=0) [h_kv][group][n_ctx][head_dim]      bf16, batch 1
+ *   k, v (contiguous)          element (b, h, i, c) at b*stride_req + h*stride_head
+ *                              + i*stride_tok + c (elements; stride_tok >= head_dim)
+ *   k, v (paged)               pool [num_blocks][block_size][h_kv][head_dim]; token i of
+ *                              request b is slot i % block_size of block
+ *                              block_table[b*max_blocks + i / block_size]
+ *   w_o                        [d_model][h_kv*group*head_dim] bf16 (nn.Linear weight);
+ *                              query head h*group+g owns columns [(h*group+g)*d, +d)
+ *   scores (s_attn, s_val)     fp32, packed by request: request b starts at
+ *                              h_kv * (n_0 + ... + n_{b-1}); head h of it at + h*n_b
+ *   idx                        int32 token positions, ascending within each (b, h)
+ *                              segment; segment (b, h) starts at offsets[b*h_kv + h]
+ *   counts / offsets           [batch*h_kv] int32 / int64 (exclusive prefix sum of counts)
+ *   k_out, v_out               [total kept][head_dim] bf16, same packing as idx
+ */
+#ifndef KVSEL_H
+#define KVSEL_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ------------------------------------------------------------------ */
+#define KVSEL_OK 0
+#define KVSEL_EINVAL (-1)        /* NULL / misaligned pointer, bad size or enum value    */
+#define KVSEL_EBUDGET (-2)       /* forced entries exceed the budget, or budget > n*H    */
+#define KVSEL_EUNSUPPORTED (-3)  /* valid request outside what the kernels implement    */
+#define KVSEL_EWORKSPACE (-4)    /* workspace NULL or smaller than kvsel_workspace_size  */
+#define KVSEL_ECUDA (-5)         /* a CUDA runtime/driver call or launch failed          */
+#define KVSEL_ETIMEOUT (-6)      /* a bounded device-side wait ran out (status word)     */
+#define KVSEL_EDEVICE (-7)       /* other device-side error recorded in the status word  */
+
+/* ---- enumerations ------------------------------------------------------------------- */
+enum { KVSEL_REDUCE_SUM = 0, KVSEL_REDUCE_MEAN = 1, KVSEL_REDUCE_MAX = 2 };
+enum { KVSEL_POOL_NONE = 0, KVSEL_POOL_MAX = 1, KVSEL_POOL_AVG = 2 };
+enum { KVSEL_BUDGET_PER_HEAD = 0, KVSEL_BUDGET_PER_LAYER = 1 };
+enum { KVSEL_WO_GROUP_SUM = 0, KVSEL_WO_PER_HEAD = 1 };
+enum { KVSEL_LAYOUT_CONTIGUOUS = 0, KVSEL_LAYOUT_PAGED = 1 };
+
+#define KVSEL_MAX_BATCH 128
+
+/* ---- parameters --------------------------------------------------------------------- */
+typedef struct kvsel_params {
+  int32_t h_kv;         /* KV heads H                                                    */
+  int32_t group;        /* query heads per KV head G (GQA, KVzip §2.2)                   */
+  int32_t head_dim;     /* d; must be 128                                                */
+  int32_t d_model;      /* D, rows of W_O (value-aware only); multiple of 128            */
+  int32_t n_ctx;        /* context length n (all requests when n_ctx_per_req is NULL)    */
+  int32_t window;       /* W observation-window queries per group head (Algorithm 2's
+                           n'); 0 = query-agnostic scoring over all n positions (KVzip)  */
+  int32_t q_chunk;      /* query-agnostic: query positions per chunk (KVzip §3.4); 0=all */
+  int32_t causal;       /* 1: window row w (position n-W+w) sees keys <= n-W+w           */
+  float scale;          /* logit scale; 0 = 1/sqrt(head_dim)                             */
+  int32_t reduce;       /* KVSEL_REDUCE_*: over window rows and group heads              */
+  int32_t pool;         /* KVSEL_POOL_*: 1-D pooling along n, stride 1, centred window   */
+  int32_t pool_kernel;  /* odd pooling width k (max ignores out-of-range positions, avg
+                           pads with zeros and divides by k)                             */
+  int32_t value_aware;  /* 1: s_val = (s_attn + eps) * ||W_O v||_1 and two-stage select */
+  int32_t wo_mode;      /* KVSEL_WO_*: GQA reading of W_O^h (group sum, default)         */
+  float eps;            /* 1e-4 (CriticalKV footnote 3)                                  */
+  float alpha;          /* first-stage share of the budget (0.5, CriticalKV §3.5)        */
+  int32_t n_sink;       /* first n_sink positions always kept (4)                        */
+  int32_t n_recent;     /* last n_recent positions always kept (W)                       */
+  int32_t budget_mode;  /* KVSEL_BUDGET_*                                                */
+  double budget_ratio;  /* per head: B = floor(ratio*n); per layer: floor(ratio*n*H)     */
+  double floor_ratio;   /* per layer: each head keeps at least floor(floor_ratio*n)      */
+  int32_t batch;        /* requests in the call (<= KVSEL_MAX_BATCH)                      */
+  const int32_t* n_ctx_per_req; /* host [batch] context lengths, or NULL                  */
+} kvsel_params;
+
+/* K/V cache view, contiguous or paged (block_size tokens per block). */
+typedef struct kvsel_kv {
+  const void* k;                /* device bf16                                          */
+  const void* v;                /* device bf16                                          */
+  int32_t layout;               /* KVSEL_LAYOUT_*                                       */
+  int64_t stride_req;           /* contiguous: elements between requests                */
+  int64_t stride_head;          /* contiguous: elements between heads                   */
+  int64_t stride_tok;           /* contiguous: elements between tokens                  */
+  const int32_t* block_table;   /* paged: device [batch][max_blocks]                    */
+  int32_t block_size;           /* paged: tokens per block: 8, 16, 32 or 64             */
+  int32_t max_blocks;           /* paged: row length of block_table                     */
+  int32_t num_blocks;           /* paged: blocks in the pool                            */
+} kvsel_kv;
+
+/* ---- sizes --------------------------------------------------------------------------- */
+
+/* Bytes of device workspace that kvsel_score / kvsel_select / kvsel_run_layer need for
+ * these parameters on the current device.  Host-only; no CUDA work. */
+int kvsel_workspace_size(const kvsel_params* p, size_t* bytes);
+
+/* Output sizes: *n_scores = elements of s_attn / s_val (H * sum of n_b), *n_kept = total
+ * kept entries (length of idx and rows of k_out / v_out), *n_segments = batch * h_kv
+ * (length of counts / offsets).  Any output pointer may be NULL. */
+int kvsel_output_size(const kvsel_params* p, int64_t* n_scores, int64_t* n_kept, int64_t* n_segments);
+
+/* Zero the workspace's device status word (do once after allocating a workspace). */
+int kvsel_workspace_init(void* ws, size_t ws_bytes, void* stream);
+
+/* ---- the path ------------------------------------------------------------------------ */
+
+/* Score every cached key (CriticalKV Algorithm 2; KVzip §3.2 when window == 0).
+ *   q       device bf16, layout above
+ *   kv      K/V view (V is read only when value_aware)
+ *   w_o     device bf16 [d_model][h_kv*group*head_dim], or NULL unless value_aware
+ *   s_attn  device fp32 [n_scores]: pooled attention score
+ *   s_val   device fp32 [n_scores]: (s_attn + eps) * nu, or NULL unless value_aware
+ *   ws      device workspace of ws_bytes >= kvsel_workspace_size
+ * Query-agnostic scoring (window == 0) supports batch 1, non-causal, reduce MAX. */
+int kvsel_score(const kvsel_params* p, const void* q, const kvsel_kv* kv, const void* w_o, float* s_attn,
+                float* s_val, void* ws, size_t ws_bytes, void* stream);
+
+/* Select the kept entries from the scores (CriticalKV Algorithm 1 when value_aware;
+ * per-layer budget with per-head floors, KVzip §4.2, when budget_mode is PER_LAYER).
+ * Forced entries (sinks, recent window) are always kept and count inside the budget.
+ *   s_attn  device fp32 [n_scores]; s_val device fp32 [n_scores] or NULL
+ *   idx     device int32 [n_kept]; counts device int32 [batch*h_kv];
+ *   offsets device int64 [batch*h_kv]
+ * Order: score descending, ties by index ascending (flat index h*n+i per layer). */
+int kvsel_select(const kvsel_params* p, const float* s_attn, const float* s_val, int32_t* idx, int32_t* counts,
+                 int64_t* offsets, void* ws, size_t ws_bytes, void* stream);
+
+/* Gather the kept K/V rows into dense per-segment buffers (bit-exact copies).
+ *   idx/counts/offsets as produced by kvsel_select (device)
+ *   k_out, v_out  device bf16 [n_kept][head_dim]
+ * Indices outside [0, n_b) are skipped and flagged in the status word when ws != NULL. */
+int kvsel_compact(const kvsel_params* p, const kvsel_kv* kv, const int32_t* idx, const int32_t* counts,
+                  const int64_t* offsets, void* k_out, void* v_out, void* ws, size_t ws_bytes, void* stream);
+
+/* score -> select -> compact for one layer, enqueued back to back on `stream`.
+ * s_attn / s_val are written as in kvsel_score (s_val may be NULL when !value_aware). */
+int kvsel_run_layer(const kvsel_params* p, const void* q, const kvsel_kv* kv, const void* w_o, float* s_attn,
+                    float* s_val, int32_t* idx, int32_t* counts, int64_t* offsets, void* k_out, void* v_out,
+                    void* ws, size_t ws_bytes, void* stream);
+
+/* ---- diagnostics --------------------------------------------------------------------- */
+
+/* Synchronise `stream`, read and clear the workspace's device status word.  *status is
+ * KVSEL_OK, KVSEL_ETIMEOUT (a bounded device wait ran out) or KVSEL_EDEVICE. */
+int kvsel_get_device_status(void* ws, void* stream, int* status);
+
+/* Cycle budget of one device-side wait (default ~1 s at the boost clock).  Lowering it to
+ * 0 makes every wait that is not already satisfied give up at once; the tests use this
+ * to exercise the timeout path.  Host-side setting for subsequent launches. */
+void kvsel_set_wait_limit(uint64_t cycles);
+
+/* Static description of an error code. */
+const char* kvsel_strerror(int code);
+
+/* Library version string. */
+const char* kvsel_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* KVSEL_H */

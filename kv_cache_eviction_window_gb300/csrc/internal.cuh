@@ -1,0 +1,116 @@
+// Internal declarations shared by the C-ABI host layer and the kernel translation units.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "ptx.cuh"
+
+namespace kvsel {
+
+constexpr int kMaxBatch = 128;
+constexpr int kHeadDim = 128;
+
+// Per-request table passed by value to kernels.
+struct ReqTable {
+  int B;                          // requests
+  int H;                          // KV heads
+  int n[kMaxBatch];               // context length of request b
+  long long soff[kMaxBatch];      // offset of request b in the packed score arrays
+};
+
+// Where K/V tiles come from: a 4-D tensor map over the contiguous cache
+// (d, token, head, request) or over the block pool (d, head, slot, block).
+struct KvSource {
+  int paged;
+  int block_size;
+  int max_blocks;
+  int num_blocks;
+  const int* block_table;   // device [B][max_blocks]
+};
+
+// Key-range decomposition shared by the two window-scoring passes: every (b, h) is cut
+// into chunks of `chunk_len` keys; chunk ids run request-major, then head, then chunk.
+struct ChunkTable {
+  int chunk_len;                  // multiple of 256
+  int total;                      // chunks over all requests and heads
+  int base[kMaxBatch + 1];        // first chunk id of request b
+  int per_head[kMaxBatch];        // chunks per head of request b
+};
+
+struct WinScoreArgs {
+  ReqTable rq;
+  ChunkTable ck;
+  KvSource src;
+  int G, W, R, R_pad;             // R = G*W window rows per KV head, R_pad = roundup(R, 32)
+  int causal;
+  int reduce;                     // KVSEL_REDUCE_*
+  float s2;                       // logit scale * log2(e)
+  float* part;                    // [ck.total][2][R_pad]: row max (log2 units) and sum
+  float* s_raw;                   // packed [sum_b H*n_b] reduced scores
+  WaitCtl wc;
+};
+
+struct VnormArgs {
+  ReqTable rq;
+  KvSource src;
+  int D;                          // rows of W_O (output features)
+  int Dw;                         // rows of the combined weight per head (D or G*D)
+  int units_total;                // (b, h, token block) work units
+  int unit_base[kMaxBatch + 1];   // first unit of request b
+  int blocks_per_head[kMaxBatch]; // token blocks per head of request b
+  float* nu;                      // packed [sum_b H*n_b]
+  WaitCtl wc;
+};
+
+// Host-side launchers (return cudaError_t of the launch).
+cudaError_t launch_win_rowstats(const WinScoreArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, int mt,
+                                cudaStream_t st);
+cudaError_t launch_win_keysum(const WinScoreArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, cudaStream_t st);
+
+cudaError_t launch_wbar(const uint16_t* w_o, uint16_t* wbar, int H, int G, int D, int wo_mode, cudaStream_t st);
+cudaError_t launch_vnorm(const VnormArgs& a, const CUtensorMap& tv, const CUtensorMap& tw, cudaStream_t st);
+int vnorm_token_block();
+
+cudaError_t launch_finalize(const ReqTable& rq, const float* s_raw, const float* nu, float* s_attn, float* s_val,
+                            int pool, int pool_kernel, float eps, cudaStream_t st);
+
+// Selection.  One cluster of CTAs per segment (b, h) in per-head mode, per request in
+// per-layer mode.
+struct SelectArgs {
+  ReqTable rq;
+  int mode;                       // KVSEL_BUDGET_*
+  int two_stage;
+  float alpha;
+  int n_sink, n_recent;
+  int budget[kMaxBatch];          // per head (per-head mode) or per layer (per-layer mode)
+  int budget1[kMaxBatch];         // two-stage: stage-1 budget max(floor(alpha*B), |F|)
+  int floor_h[kMaxBatch];         // per-layer mode: per-head floor
+  const float* s1;                // stage-1 scores (s_attn)
+  const float* s2;                // stage-2 scores (s_val) or null
+  int32_t* idx;
+  int32_t* counts;
+  int64_t* offsets;               // written for every segment
+  long long seg_out[kMaxBatch];   // output offset of request b's first segment
+};
+cudaError_t launch_select(const SelectArgs& a, int cluster, int chunk_cap, cudaStream_t st);
+int select_cluster_size(int max_len, int* chunk_cap);
+
+struct CompactArgs {
+  ReqTable rq;
+  KvSource src;
+  const uint16_t* k;
+  const uint16_t* v;
+  long long stride_req, stride_head, stride_tok;
+  const int32_t* idx;
+  const int32_t* counts;
+  const int64_t* offsets;
+  uint16_t* k_out;
+  uint16_t* v_out;
+  int* status;                    // may be null
+};
+cudaError_t launch_compact(const CompactArgs& a, int max_count, int num_sms, cudaStream_t st);
+
+}  // namespace kvsel

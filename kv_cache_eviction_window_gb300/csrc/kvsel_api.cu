@@ -1,0 +1,496 @@
+// C-ABI host layer of libkvsel: argument validation, the per-call plan (budgets, key
+// chunking, workspace layout), TMA tensor maps, and the launches of the scoring,
+// selection and compaction kernels on the caller's stream.  Nothing here allocates
+// device or host memory.
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/kvsel.h"
+#include "internal.cuh"
+
+using namespace kvsel;
+
+namespace {
+
+std::atomic<unsigned long long> g_wait_limit{2000000000ull};   // ~1 s at the boost clock
+
+constexpr size_t kStatusBytes = 256;
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+struct Plan {
+  int B = 0, H = 0, G = 0, D = 0, W = 0, R = 0, R_pad = 0, n_max = 0, mt = 1, Dw = 0;
+  bool qa = false;     // query-agnostic scoring (window == 0)
+  ReqTable rq{};
+  long long n_scores = 0;
+  long long n_kept = 0;
+  int budget[kMaxBatch]{}, budget1[kMaxBatch]{}, floor_h[kMaxBatch]{}, nforced[kMaxBatch]{};
+  long long seg_out[kMaxBatch + 1]{};
+  int max_count = 0;
+  ChunkTable ck{};
+  int units_total = 0, unit_base[kMaxBatch + 1]{}, blocks_per_head[kMaxBatch]{};
+  int num_sms = 0;
+  size_t ws_part = 0, ws_sraw = 0, ws_nu = 0, ws_wbar = 0, ws_total = 0;
+};
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int device_sms(int* sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return KVSEL_ECUDA;
+  if (cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return KVSEL_ECUDA;
+  return KVSEL_OK;
+}
+
+// Everything derived from the parameters alone (no pointers).  `need_device` asks for
+// the SM count, which sets the key chunking and therefore the workspace size.
+int make_plan(const kvsel_params* p, Plan& pl, bool need_device) {
+  if (!p) return KVSEL_EINVAL;
+  if (p->head_dim != kHeadDim) return KVSEL_EUNSUPPORTED;
+  if (p->h_kv < 1 || p->h_kv > 64 || p->group < 1 || p->batch < 1 || p->batch > kMaxBatch) return KVSEL_EINVAL;
+  if (p->reduce < 0 || p->reduce > 2 || p->pool < 0 || p->pool > 2) return KVSEL_EINVAL;
+  if (p->pool != KVSEL_POOL_NONE && (p->pool_kernel < 1 || (p->pool_kernel & 1) == 0)) return KVSEL_EINVAL;
+  if (p->budget_mode != KVSEL_BUDGET_PER_HEAD && p->budget_mode != KVSEL_BUDGET_PER_LAYER) return KVSEL_EINVAL;
+  if (!(p->budget_ratio >= 0.0 && p->budget_ratio <= 1.0) || !(p->floor_ratio >= 0.0 && p->floor_ratio <= 1.0))
+    return KVSEL_EINVAL;
+  if (p->n_sink < 0 || p->n_recent < 0 || p->window < 0 || !(p->scale >= 0.f) || std::isinf(p->scale))
+    return KVSEL_EINVAL;
+  if (p->value_aware) {
+    if (p->wo_mode != KVSEL_WO_GROUP_SUM && p->wo_mode != KVSEL_WO_PER_HEAD) return KVSEL_EINVAL;
+    if (p->d_model < 128 || p->d_model % 128 != 0) return KVSEL_EUNSUPPORTED;
+    if (!(p->alpha >= 0.f && p->alpha <= 1.f) || !(p->eps >= 0.f)) return KVSEL_EINVAL;
+    if (p->budget_mode != KVSEL_BUDGET_PER_HEAD) return KVSEL_EUNSUPPORTED;
+  }
+  pl.B = p->batch;
+  pl.H = p->h_kv;
+  pl.G = p->group;
+  pl.D = p->d_model;
+  pl.W = p->window;
+  pl.qa = (p->window == 0);
+  pl.rq.B = pl.B;
+  pl.rq.H = pl.H;
+  long long so = 0;
+  for (int b = 0; b < pl.B; ++b) {
+    const int n = p->n_ctx_per_req ? p->n_ctx_per_req[b] : p->n_ctx;
+    if (n < 0) return KVSEL_EINVAL;
+    pl.rq.n[b] = n;
+    pl.rq.soff[b] = so;
+    so += static_cast<long long>(pl.H) * n;
+    pl.n_max = n > pl.n_max ? n : pl.n_max;
+  }
+  pl.n_scores = so;
+  if (so > (1ll << 31) - 1) return KVSEL_EUNSUPPORTED;
+  if (pl.qa) {
+    return KVSEL_EUNSUPPORTED;   // query-agnostic scoring is served by its own entry (not in this build)
+  }
+  for (int b = 0; b < pl.B; ++b)
+    if (pl.rq.n[b] > 0 && pl.W > pl.rq.n[b]) return KVSEL_EINVAL;
+  pl.R = pl.G * pl.W;
+  if (pl.R > 512 || pl.R % 32 != 0) return KVSEL_EUNSUPPORTED;
+  pl.R_pad = (pl.R + 63) / 64 * 64;
+  pl.mt = pl.R <= 128 ? 1 : (pl.R <= 256 ? 2 : 4);
+  pl.Dw = p->value_aware ? (p->wo_mode == KVSEL_WO_PER_HEAD ? pl.G * pl.D : pl.D) : 0;
+
+  // budgets and output layout
+  long long out = 0;
+  for (int b = 0; b < pl.B; ++b) {
+    const int n = pl.rq.n[b];
+    const int nf = static_cast<int>(std::min<long long>(n, static_cast<long long>(p->n_sink) + p->n_recent));
+    pl.nforced[b] = nf;
+    pl.seg_out[b] = out;
+    if (p->budget_mode == KVSEL_BUDGET_PER_HEAD) {
+      const long long B = static_cast<long long>(std::floor(p->budget_ratio * static_cast<double>(n)));
+      if (B < nf || B > n) return KVSEL_EBUDGET;
+      pl.budget[b] = static_cast<int>(B);
+      long long b1 = static_cast<long long>(std::floor(static_cast<double>(p->alpha) * static_cast<double>(B)));
+      if (b1 < nf) b1 = nf;
+      pl.budget1[b] = static_cast<int>(b1);
+      out += static_cast<long long>(pl.H) * B;
+      pl.max_count = std::max(pl.max_count, static_cast<int>(B));
+    } else {
+      const long long BL =
+          static_cast<long long>(std::floor(p->budget_ratio * static_cast<double>(n) * static_cast<double>(pl.H)));
+      const long long fl = static_cast<long long>(std::floor(p->floor_ratio * static_cast<double>(n)));
+      const long long fh = std::min<long long>(n, std::max<long long>(fl, nf));
+      if (BL < fh * pl.H || BL > static_cast<long long>(n) * pl.H) return KVSEL_EBUDGET;
+      pl.budget[b] = static_cast<int>(BL);
+      pl.floor_h[b] = static_cast<int>(fl);
+      out += BL;
+      pl.max_count = std::max(pl.max_count, static_cast<int>(std::min<long long>(BL, n)));
+    }
+  }
+  pl.seg_out[pl.B] = out;
+  pl.n_kept = out;
+
+  if (!need_device) return KVSEL_OK;
+  int rc = device_sms(&pl.num_sms);
+  if (rc) return rc;
+
+  // key chunks: about one chunk per SM over all (request, head) pairs
+  long long t256 = 0;
+  for (int b = 0; b < pl.B; ++b) t256 += static_cast<long long>(pl.H) * ((pl.rq.n[b] + 255) / 256);
+  long long tpc = (t256 + pl.num_sms - 1) / std::max(pl.num_sms, 1);
+  if (tpc < 1) tpc = 1;
+  pl.ck.chunk_len = static_cast<int>(256 * tpc);
+  int cb = 0;
+  for (int b = 0; b < pl.B; ++b) {
+    pl.ck.base[b] = cb;
+    pl.ck.per_head[b] = (pl.rq.n[b] + pl.ck.chunk_len - 1) / pl.ck.chunk_len;
+    cb += pl.H * pl.ck.per_head[b];
+  }
+  pl.ck.base[pl.B] = cb;
+  pl.ck.total = cb;
+
+  const int tb = vnorm_token_block();
+  int ub = 0;
+  for (int b = 0; b < pl.B; ++b) {
+    pl.unit_base[b] = ub;
+    pl.blocks_per_head[b] = (pl.rq.n[b] + tb - 1) / tb;
+    ub += pl.H * pl.blocks_per_head[b];
+  }
+  pl.unit_base[pl.B] = ub;
+  pl.units_total = p->value_aware ? ub : 0;
+
+  size_t off = kStatusBytes;
+  pl.ws_part = off;
+  off = align256(off + static_cast<size_t>(pl.ck.total) * 2 * pl.R_pad * sizeof(float));
+  pl.ws_sraw = off;
+  off = align256(off + static_cast<size_t>(pl.n_scores) * sizeof(float));
+  if (p->value_aware) {
+    pl.ws_nu = off;
+    off = align256(off + static_cast<size_t>(pl.n_scores) * sizeof(float));
+    pl.ws_wbar = off;
+    off = align256(off + static_cast<size_t>(pl.H) * pl.Dw * kHeadDim * 2);
+  }
+  pl.ws_total = off;
+  return KVSEL_OK;
+}
+
+int check_kv(const kvsel_kv* kv, const Plan& pl, bool need_v) {
+  if (!kv || !kv->k || (need_v && !kv->v)) return KVSEL_EINVAL;
+  if (!aligned16(kv->k) || (kv->v && !aligned16(kv->v))) return KVSEL_EINVAL;
+  if (kv->layout == KVSEL_LAYOUT_CONTIGUOUS) {
+    if (kv->stride_tok < kHeadDim || kv->stride_head < 0 || kv->stride_req < 0) return KVSEL_EINVAL;
+    if ((kv->stride_tok * 2) % 16 || (kv->stride_head * 2) % 16 || (kv->stride_req * 2) % 16) return KVSEL_EINVAL;
+    if (pl.H > 1 && kv->stride_head == 0) return KVSEL_EINVAL;
+    if (pl.B > 1 && kv->stride_req == 0) return KVSEL_EINVAL;
+  } else if (kv->layout == KVSEL_LAYOUT_PAGED) {
+    const int bs = kv->block_size;
+    if (!kv->block_table || !(bs == 8 || bs == 16 || bs == 32 || bs == 64)) return KVSEL_EINVAL;
+    if (kv->num_blocks < 1 || kv->max_blocks < (pl.n_max + bs - 1) / bs) return KVSEL_EINVAL;
+  } else {
+    return KVSEL_EINVAL;
+  }
+  return KVSEL_OK;
+}
+
+// The driver's tensor-map encoder, looked up through the runtime so that the library
+// loads on machines without a driver (symbol checks) and links no libcuda.
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+bool encode(CUtensorMap* m, const void* ptr, int rank, const cuuint64_t* dims, const cuuint64_t* strides_bytes,
+            const cuuint32_t* box) {
+  cuuint32_t es[5] = {1, 1, 1, 1, 1};
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encoder();
+  if (!enc) return false;
+  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(ptr), dims,
+                                            strides_bytes, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// K or V tiles of `rows` tokens.
+bool kv_map(CUtensorMap* m, const void* base, const kvsel_kv* kv, const Plan& pl, int rows) {
+  if (kv->layout == KVSEL_LAYOUT_CONTIGUOUS) {
+    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(std::max(pl.n_max, 1)),
+                                static_cast<cuuint64_t>(pl.H), static_cast<cuuint64_t>(pl.B)};
+    const long long sh = pl.H > 1 ? kv->stride_head : static_cast<long long>(std::max(pl.n_max, 1)) * kv->stride_tok;
+    const long long sr = pl.B > 1 ? kv->stride_req : sh * pl.H;
+    const cuuint64_t strides[3] = {static_cast<cuuint64_t>(kv->stride_tok * 2), static_cast<cuuint64_t>(sh * 2),
+                                   static_cast<cuuint64_t>(sr * 2)};
+    const cuuint32_t box[4] = {64, static_cast<cuuint32_t>(rows), 1, 1};
+    return encode(m, base, 4, dims, strides, box);
+  }
+  const int bs = kv->block_size;
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(pl.H),
+                              static_cast<cuuint64_t>(bs), static_cast<cuuint64_t>(kv->num_blocks)};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(kHeadDim * 2), static_cast<cuuint64_t>(pl.H) * kHeadDim * 2,
+                                 static_cast<cuuint64_t>(bs) * pl.H * kHeadDim * 2};
+  const cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(bs), 1};
+  return encode(m, base, 4, dims, strides, box);
+}
+
+KvSource kv_source(const kvsel_kv* kv) {
+  KvSource s{};
+  s.paged = kv->layout == KVSEL_LAYOUT_PAGED;
+  s.block_size = kv->block_size;
+  s.max_blocks = kv->max_blocks;
+  s.num_blocks = kv->num_blocks;
+  s.block_table = kv->block_table;
+  return s;
+}
+
+int launch_rc(cudaError_t e) { return e == cudaSuccess ? KVSEL_OK : KVSEL_ECUDA; }
+
+int check_ws(const Plan& pl, void* ws, size_t ws_bytes) {
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u)) return KVSEL_EWORKSPACE;
+  if (ws_bytes < pl.ws_total) return KVSEL_EWORKSPACE;
+  return KVSEL_OK;
+}
+
+WaitCtl wait_ctl(void* ws) { return WaitCtl{g_wait_limit.load(), static_cast<int*>(ws)}; }
+
+int do_score(const kvsel_params* p, const Plan& pl, const void* q, const kvsel_kv* kv, const void* w_o, float* s_attn,
+             float* s_val, void* ws, cudaStream_t st) {
+  uint8_t* wsb = static_cast<uint8_t*>(ws);
+  float* part = reinterpret_cast<float*>(wsb + pl.ws_part);
+  float* s_raw = reinterpret_cast<float*>(wsb + pl.ws_sraw);
+  if (pl.n_scores == 0) return KVSEL_OK;
+
+  CUtensorMap tq, tk1, tk2;
+  {
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(pl.B) * pl.H * pl.R};
+    const cuuint64_t strides[1] = {kHeadDim * 2};
+    const cuuint32_t box[2] = {64, 32};
+    if (!encode(&tq, q, 2, dims, strides, box)) return KVSEL_EINVAL;
+  }
+  const int nt1 = pl.mt == 4 ? 64 : 128;
+  if (!kv_map(&tk1, kv->k, kv, pl, kv->layout == KVSEL_LAYOUT_PAGED ? 0 : nt1)) return KVSEL_EINVAL;
+  if (!kv_map(&tk2, kv->k, kv, pl, kv->layout == KVSEL_LAYOUT_PAGED ? 0 : 128)) return KVSEL_EINVAL;
+
+  WinScoreArgs a{};
+  a.rq = pl.rq;
+  a.ck = pl.ck;
+  a.src = kv_source(kv);
+  a.G = pl.G;
+  a.W = pl.W;
+  a.R = pl.R;
+  a.R_pad = pl.R_pad;
+  a.causal = p->causal ? 1 : 0;
+  a.reduce = p->reduce;
+  const float scale = p->scale > 0.f ? p->scale : 1.f / std::sqrt(static_cast<float>(kHeadDim));
+  a.s2 = scale * 1.4426950408889634f;
+  a.part = part;
+  a.s_raw = s_raw;
+  a.wc = wait_ctl(ws);
+  int rc = launch_rc(launch_win_rowstats(a, tq, tk1, pl.mt, st));
+  if (rc) return rc;
+  rc = launch_rc(launch_win_keysum(a, tq, tk2, st));
+  if (rc) return rc;
+
+  float* nu = nullptr;
+  if (p->value_aware) {
+    nu = reinterpret_cast<float*>(wsb + pl.ws_nu);
+    uint16_t* wbar = reinterpret_cast<uint16_t*>(wsb + pl.ws_wbar);
+    rc = launch_rc(launch_wbar(static_cast<const uint16_t*>(w_o), wbar, pl.H, pl.G, pl.D, p->wo_mode, st));
+    if (rc) return rc;
+    CUtensorMap tv, tw;
+    if (!kv_map(&tv, kv->v, kv, pl, kv->layout == KVSEL_LAYOUT_PAGED ? 0 : 128)) return KVSEL_EINVAL;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(pl.Dw),
+                                static_cast<cuuint64_t>(pl.H)};
+    const cuuint64_t strides[2] = {kHeadDim * 2, static_cast<cuuint64_t>(pl.Dw) * kHeadDim * 2};
+    const cuuint32_t box[3] = {64, 128, 1};
+    if (!encode(&tw, wbar, 3, dims, strides, box)) return KVSEL_EINVAL;
+    VnormArgs v{};
+    v.rq = pl.rq;
+    v.src = kv_source(kv);
+    v.D = pl.D;
+    v.Dw = pl.Dw;
+    v.units_total = pl.units_total;
+    for (int b = 0; b <= pl.B; ++b) v.unit_base[b] = pl.unit_base[b];
+    for (int b = 0; b < pl.B; ++b) v.blocks_per_head[b] = pl.blocks_per_head[b];
+    v.nu = nu;
+    v.wc = wait_ctl(ws);
+    rc = launch_rc(launch_vnorm(v, tv, tw, st));
+    if (rc) return rc;
+  }
+  return launch_rc(launch_finalize(pl.rq, s_raw, nu, s_attn, p->value_aware ? s_val : nullptr, p->pool,
+                                   p->pool_kernel, p->eps, st));
+}
+
+int do_select(const kvsel_params* p, const Plan& pl, const float* s_attn, const float* s_val, int32_t* idx,
+              int32_t* counts, int64_t* offsets, cudaStream_t st) {
+  SelectArgs a{};
+  a.rq = pl.rq;
+  a.mode = p->budget_mode;
+  a.two_stage = p->value_aware ? 1 : 0;
+  a.alpha = p->alpha;
+  a.n_sink = p->n_sink;
+  a.n_recent = p->n_recent;
+  for (int b = 0; b < pl.B; ++b) {
+    a.budget[b] = pl.budget[b];
+    a.budget1[b] = pl.budget1[b];
+    a.floor_h[b] = pl.floor_h[b];
+    a.seg_out[b] = pl.seg_out[b];
+  }
+  a.s1 = s_attn;
+  a.s2 = s_val;
+  a.idx = idx;
+  a.counts = counts;
+  a.offsets = offsets;
+  const int max_len = p->budget_mode == KVSEL_BUDGET_PER_LAYER ? pl.H * pl.n_max : pl.n_max;
+  int cap = 0;
+  const int cs = select_cluster_size(std::max(max_len, 1), &cap);
+  if (cs < 0) return KVSEL_EUNSUPPORTED;
+  return launch_rc(launch_select(a, cs, cap, st));
+}
+
+int do_compact(const Plan& pl, const kvsel_kv* kv, const int32_t* idx, const int32_t* counts, const int64_t* offsets,
+               void* k_out, void* v_out, void* ws, cudaStream_t st) {
+  CompactArgs c{};
+  c.rq = pl.rq;
+  c.src = kv_source(kv);
+  c.k = static_cast<const uint16_t*>(kv->k);
+  c.v = static_cast<const uint16_t*>(kv->v);
+  c.stride_req = kv->stride_req;
+  c.stride_head = kv->stride_head;
+  c.stride_tok = kv->stride_tok;
+  c.idx = idx;
+  c.counts = counts;
+  c.offsets = offsets;
+  c.k_out = static_cast<uint16_t*>(k_out);
+  c.v_out = static_cast<uint16_t*>(v_out);
+  c.status = static_cast<int*>(ws);
+  int sms = pl.num_sms;
+  if (!sms && device_sms(&sms)) return KVSEL_ECUDA;
+  return launch_rc(launch_compact(c, pl.max_count, sms, st));
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* kvsel_version(void) { return "kvsel 0.1 (sm_103a)"; }
+
+const char* kvsel_strerror(int code) {
+  switch (code) {
+    case KVSEL_OK: return "ok";
+    case KVSEL_EINVAL: return "invalid argument (pointer, alignment, size or enum)";
+    case KVSEL_EBUDGET: return "budget below the forced entries or above the number of entries";
+    case KVSEL_EUNSUPPORTED: return "unsupported configuration";
+    case KVSEL_EWORKSPACE: return "workspace missing, misaligned or too small";
+    case KVSEL_ECUDA: return "CUDA call or kernel launch failed";
+    case KVSEL_ETIMEOUT: return "a bounded device-side wait ran out";
+    case KVSEL_EDEVICE: return "device-side error (out-of-range index skipped)";
+    default: return "unknown error";
+  }
+}
+
+void kvsel_set_wait_limit(uint64_t cycles) { g_wait_limit.store(cycles); }
+
+int kvsel_workspace_size(const kvsel_params* p, size_t* bytes) {
+  if (!bytes) return KVSEL_EINVAL;
+  Plan pl;
+  const int rc = make_plan(p, pl, true);
+  if (rc) return rc;
+  *bytes = pl.ws_total;
+  return KVSEL_OK;
+}
+
+int kvsel_output_size(const kvsel_params* p, int64_t* n_scores, int64_t* n_kept, int64_t* n_segments) {
+  Plan pl;
+  const int rc = make_plan(p, pl, false);
+  if (rc) return rc;
+  if (n_scores) *n_scores = pl.n_scores;
+  if (n_kept) *n_kept = pl.n_kept;
+  if (n_segments) *n_segments = static_cast<int64_t>(pl.B) * pl.H;
+  return KVSEL_OK;
+}
+
+int kvsel_workspace_init(void* ws, size_t ws_bytes, void* stream) {
+  if (!ws || ws_bytes < kStatusBytes) return KVSEL_EWORKSPACE;
+  return launch_rc(cudaMemsetAsync(ws, 0, kStatusBytes, static_cast<cudaStream_t>(stream)));
+}
+
+int kvsel_score(const kvsel_params* p, const void* q, const kvsel_kv* kv, const void* w_o, float* s_attn,
+                float* s_val, void* ws, size_t ws_bytes, void* stream) {
+  Plan pl;
+  int rc = make_plan(p, pl, true);
+  if (rc) return rc;
+  if (!q || !aligned16(q) || !s_attn) return KVSEL_EINVAL;
+  if (p->value_aware && (!w_o || !aligned16(w_o) || !s_val)) return KVSEL_EINVAL;
+  if ((rc = check_kv(kv, pl, p->value_aware != 0))) return rc;
+  if ((rc = check_ws(pl, ws, ws_bytes))) return rc;
+  return do_score(p, pl, q, kv, w_o, s_attn, s_val, ws, static_cast<cudaStream_t>(stream));
+}
+
+int kvsel_select(const kvsel_params* p, const float* s_attn, const float* s_val, int32_t* idx, int32_t* counts,
+                 int64_t* offsets, void* ws, size_t ws_bytes, void* stream) {
+  (void)ws;
+  (void)ws_bytes;
+  Plan pl;
+  const int rc = make_plan(p, pl, false);
+  if (rc) return rc;
+  if (!s_attn || !idx || !counts || !offsets || (p->value_aware && !s_val)) return KVSEL_EINVAL;
+  if (pl.n_scores == 0) return KVSEL_OK;
+  return do_select(p, pl, s_attn, s_val, idx, counts, offsets, static_cast<cudaStream_t>(stream));
+}
+
+int kvsel_compact(const kvsel_params* p, const kvsel_kv* kv, const int32_t* idx, const int32_t* counts,
+                  const int64_t* offsets, void* k_out, void* v_out, void* ws, size_t ws_bytes, void* stream) {
+  Plan pl;
+  int rc = make_plan(p, pl, false);
+  if (rc) return rc;
+  if (!idx || !counts || !offsets || !k_out || !v_out || !aligned16(k_out) || !aligned16(v_out)) return KVSEL_EINVAL;
+  if ((rc = check_kv(kv, pl, true))) return rc;
+  if (ws && ws_bytes < kStatusBytes) return KVSEL_EWORKSPACE;
+  if (pl.n_kept == 0) return KVSEL_OK;
+  return do_compact(pl, kv, idx, counts, offsets, k_out, v_out, ws, static_cast<cudaStream_t>(stream));
+}
+
+int kvsel_run_layer(const kvsel_params* p, const void* q, const kvsel_kv* kv, const void* w_o, float* s_attn,
+                    float* s_val, int32_t* idx, int32_t* counts, int64_t* offsets, void* k_out, void* v_out, void* ws,
+                    size_t ws_bytes, void* stream) {
+  Plan pl;
+  int rc = make_plan(p, pl, true);
+  if (rc) return rc;
+  if (!q || !aligned16(q) || !s_attn || !idx || !counts || !offsets || !k_out || !v_out) return KVSEL_EINVAL;
+  if (!aligned16(k_out) || !aligned16(v_out)) return KVSEL_EINVAL;
+  if (p->value_aware && (!w_o || !aligned16(w_o) || !s_val)) return KVSEL_EINVAL;
+  if ((rc = check_kv(kv, pl, true))) return rc;
+  if ((rc = check_ws(pl, ws, ws_bytes))) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (pl.n_scores == 0) return KVSEL_OK;
+  if ((rc = do_score(p, pl, q, kv, w_o, s_attn, s_val, ws, st))) return rc;
+  if ((rc = do_select(p, pl, s_attn, s_val, idx, counts, offsets, st))) return rc;
+  if (pl.n_kept == 0) return KVSEL_OK;
+  return do_compact(pl, kv, idx, counts, offsets, k_out, v_out, ws, st);
+}
+
+int kvsel_get_device_status(void* ws, void* stream, int* status) {
+  if (!ws || !status) return KVSEL_EINVAL;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int word = 0;
+  if (cudaMemcpyAsync(&word, ws, sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess) return KVSEL_ECUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return KVSEL_ECUDA;
+  if (word) {
+    if (cudaMemsetAsync(ws, 0, sizeof(int), st) != cudaSuccess) return KVSEL_ECUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return KVSEL_ECUDA;
+  }
+  if (word & (DEV_TIMEOUT_PIPE | DEV_TIMEOUT_DRAIN))
+    *status = KVSEL_ETIMEOUT;
+  else if (word)
+    *status = KVSEL_EDEVICE;
+  else
+    *status = KVSEL_OK;
+  return KVSEL_OK;
+}
+
+}  // extern "C"

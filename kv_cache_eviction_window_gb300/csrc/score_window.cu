@@ -1,0 +1,534 @@
+// Observation-window scoring on tcgen05 tensor cores
+// ("CriticalKV: 출력 섭동 관점에서 KV 캐시 축출을 최적화하기", §3.4 Algorithm 2:
+//  A = softmax(Q_hat K^T) over the last W queries, reduced over window rows; GQA: the
+//  G query heads of a group share one KV head, "KVzip ...", §2.2).
+//
+// Exact softmax needs each row's max and normaliser over all n keys before any key's
+// probability is final, so scoring runs in two passes over the key range:
+//
+//   pass 1 (win_rowstats_kernel): UMMA with A = window queries (M = 128 rows per tile),
+//     B = a K tile (N keys), logits in TMEM; every epilogue thread owns one query row and
+//     keeps an online (max, sum of exp) over its key chunk.  Partials per key chunk go
+//     to the workspace.
+//   pass 2 (win_keysum_kernel): UMMA with A = a K tile (M = 128 keys), B = all R window
+//     rows; every epilogue thread owns one key and sums exp2(l*s2 - c_r) over the rows,
+//     c_r = m_r + log2 Z_r merged from the pass-1 partials (or takes the max).
+//
+// Both passes stream K through a TMA ring (128-byte swizzled K-major tiles); K of a
+// layer is re-read by pass 2 mostly from L2.  Warp roles: warps 0-7 epilogue (two
+// warps per TMEM lane quadrant, splitting the columns), warp 8 TMA producer, warp 9
+// UMMA issuer.  Every wait is bounded (ptx.cuh).
+#include "internal.cuh"
+
+namespace kvsel {
+namespace {
+
+constexpr int kEpiWarps = 8;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kThreads = 320;
+constexpr float kNegBig = -1.0e30f;   // finite "minus infinity" for running maxima
+constexpr float kLog2e = 1.4426950408889634f;
+
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+
+// Barrier over the 8 epilogue warps that also ORs a predicate across them, so that an
+// abort seen by one warp ends the loop of all of them at the same iteration.
+__device__ __forceinline__ bool epi_any(bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, 1, 256, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(pred))
+      : "memory");
+  return r != 0;
+}
+
+__host__ __device__ constexpr uint32_t pow2_cols(uint32_t c) {
+  return c <= 32 ? 32 : c <= 64 ? 64 : c <= 128 ? 128 : c <= 256 ? 256 : 512;
+}
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~static_cast<uintptr_t>(1023));
+}
+
+__device__ __forceinline__ void chunk_coords(const ChunkTable& ck, int B, int id, int& b, int& h, int& c) {
+  b = 0;
+  while (b + 1 < B && ck.base[b + 1] <= id) ++b;
+  const int rem = id - ck.base[b];
+  h = rem / ck.per_head[b];
+  c = rem - h * ck.per_head[b];
+}
+
+// TMA loads of `rows` tokens [tok0, tok0 + rows) of KV head h of request b into a
+// K-major 128B-swizzled tile [2 column halves][rows][128 B].
+__device__ __forceinline__ void load_kv_tile(const CUtensorMap* map, const KvSource& src, int b, int h, int n,
+                                             int tok0, int rows, uint8_t* dst, uint64_t* bar, int* status) {
+  const int half = rows * 128;
+  if (!src.paged) {
+    tma_load_4d(dst, map, bar, 0, tok0, h, b);
+    tma_load_4d(dst + half, map, bar, 64, tok0, h, b);
+  } else {
+    const int bs = src.block_size;
+    const int nblk_req = (n + bs - 1) / bs;
+    for (int j = 0; j < rows / bs; ++j) {
+      const int lb = tok0 / bs + j;
+      int pb = -1;
+      if (lb < nblk_req && lb < src.max_blocks) pb = __ldg(src.block_table + (size_t)b * src.max_blocks + lb);
+      if (pb < 0 || pb >= src.num_blocks) {
+        if (lb < nblk_req) atomicOr(status, DEV_BAD_INDEX);
+        pb = 0;  // tokens past the request (masked by the epilogue) or a bad entry
+      }
+      tma_load_4d(dst + j * bs * 128, map, bar, 0, h, 0, pb);
+      tma_load_4d(dst + half + j * bs * 128, map, bar, 64, h, 0, pb);
+    }
+  }
+}
+
+// Window rows [0, R) of (b, h) from the 2-D query map (d, B*H*R rows), 32-row boxes,
+// into [2 halves][R_pad rows][128 B].
+__device__ __forceinline__ void load_q_rows(const CUtensorMap* map, int row0, int R, int half_bytes, uint8_t* dst,
+                                            uint64_t* bar) {
+  for (int rb = 0; rb < R; rb += 32) {
+    tma_load_2d(dst + rb * 128, map, bar, 0, row0 + rb);
+    tma_load_2d(dst + half_bytes + rb * 128, map, bar, 64, row0 + rb);
+  }
+}
+
+// ------------------------------------------------------------------------------------
+// pass 1: per-row max / sum of exp over one key chunk
+// ------------------------------------------------------------------------------------
+template <int MT, int NT, int STAGES>
+__global__ void __launch_bounds__(kThreads, 1)
+    win_rowstats_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                        const WinScoreArgs a) {
+  constexpr int kAcc = 2;
+  constexpr uint32_t kAccCols = MT * NT;
+  constexpr uint32_t kTmemCols = pow2_cols(kAcc * kAccCols);
+  constexpr int kQHalf = MT * 128 * 128;
+  constexpr int kKStage = NT * 256;
+  constexpr int kCh = NT / 2;          // columns per epilogue thread per M tile
+  static_assert(kCh % 32 == 0 && kCh <= 64, "column split");
+  static_assert(kAcc * kAccCols <= 512, "TMEM");
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  uint8_t* sQ = smem;
+  uint8_t* sK = smem + 2 * kQHalf;
+
+  __shared__ __align__(8) uint64_t full_bar[STAGES], empty_bar[STAGES], accf_bar[kAcc], acce_bar[kAcc];
+  __shared__ __align__(8) uint64_t q_bar, done_bar;
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_abort;
+  __shared__ float s_xm[MT][4][32], s_xz[MT][4][32];
+
+  const int warp = warp_id(), lane = lane_id();
+  int b, h, c;
+  chunk_coords(a.ck, a.rq.B, blockIdx.x, b, h, c);
+  const int n = a.rq.n[b];
+  const int key_begin = c * a.ck.chunk_len;
+  const int key_end = min(n, key_begin + a.ck.chunk_len);
+  const int ntiles = key_end > key_begin ? (key_end - key_begin + NT - 1) / NT : 0;
+  int* status = a.wc.status;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    for (int s = 0; s < kAcc; ++s) {
+      mbar_init(&accf_bar[s], 1);
+      mbar_init(&acce_bar[s], kEpiWarps);
+    }
+    mbar_init(&q_bar, 1);
+    mbar_init(&done_bar, 1);
+    s_abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(&s_tmem, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = s_tmem;
+
+  if (warp == kProducerWarp) {
+    if (lane == 0 && ntiles > 0) {
+      tma_prefetch_desc(&tq);
+      tma_prefetch_desc(&tk);
+      mbar_arrive_expect_tx(&q_bar, a.R * 256);
+      load_q_rows(&tq, (b * a.rq.H + h) * a.R, a.R, kQHalf, sQ, &q_bar);
+      int t = 0;
+      for (; t < ntiles; ++t) {
+        const int s = t % STAGES, u = t / STAGES;
+        if (!mbar_wait(&empty_bar[s], (u & 1) ^ 1, &s_abort, a.wc)) break;
+        mbar_arrive_expect_tx(&full_bar[s], kKStage);
+        load_kv_tile(&tk, a.src, b, h, n, key_begin + t * NT, NT, sK + s * kKStage, &full_bar[s], status);
+      }
+      // every issued copy lands before the CTA can exit
+      for (int tt = max(0, t - STAGES); tt < t; ++tt) mbar_drain(&full_bar[tt % STAGES], (tt / STAGES) & 1, status);
+      mbar_drain(&q_bar, 0, status);
+    }
+  } else if (warp == kMmaWarp) {
+    if (lane == 0 && ntiles > 0) {
+      bool ok = mbar_wait(&q_bar, 0, &s_abort, a.wc);
+      constexpr uint32_t idesc = idesc_bf16_f32(128, NT);
+      for (int t = 0; ok && t < ntiles; ++t) {
+        const int s = t % STAGES, u = t / STAGES;
+        const int acc = t % kAcc, ua = t / kAcc;
+        if (!mbar_wait(&full_bar[s], u & 1, &s_abort, a.wc)) break;
+        if (!mbar_wait(&acce_bar[acc], (ua & 1) ^ 1, &s_abort, a.wc)) break;
+        tc_fence_after();
+        const uint32_t kbase = smem_u32(sK + s * kKStage);
+        const uint32_t qbase = smem_u32(sQ);
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const uint32_t koff = (k & 3) * 32;
+            const uint64_t da = sdesc_kmajor_sw128(qbase + (k >> 2) * kQHalf + mt * 16384 + koff);
+            const uint64_t db = sdesc_kmajor_sw128(kbase + (k >> 2) * (NT * 128) + koff);
+            umma_bf16(tbase + acc * kAccCols + mt * NT, da, db, idesc, k > 0 ? 1u : 0u);
+          }
+        }
+        umma_commit(&empty_bar[s]);
+        umma_commit(&accf_bar[acc]);
+      }
+      umma_commit(&done_bar);
+      mbar_drain(&done_bar, 0, status);
+    }
+  } else {
+    // ---------------- epilogue: warps 0-7 ----------------
+    const int q4 = warp & 3, cg = warp >> 2;
+    const float s2 = a.s2;
+    const int W = a.W, R = a.R;
+    // keys below lim_all are visible to every row (causal bound of row w=0, and n)
+    const int lim_all = a.causal ? (n - W + 1) : n;
+    float m[MT], z[MT];
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+      m[mt] = kNegBig;
+      z[mt] = 0.f;
+    }
+    for (int t = 0; t < ntiles; ++t) {
+      const int acc = t % kAcc, ua = t / kAcc;
+      bool ok = mbar_wait(&accf_bar[acc], ua & 1, &s_abort, a.wc);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      const int kcol0 = key_begin + t * NT + cg * kCh;
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+        float v[kCh];
+        const uint32_t taddr = tbase + (static_cast<uint32_t>(q4 * 32) << 16) + acc * kAccCols + mt * NT + cg * kCh;
+#pragma unroll
+        for (int j = 0; j < kCh / 32; ++j) tmem_ld32(taddr + j * 32, v + j * 32);
+        tmem_ld_wait();
+        const int r = mt * 128 + q4 * 32 + lane;
+        if (!(kcol0 + kCh <= lim_all) || r >= R) {
+          const int lim_r = (r >= R) ? -1 : (a.causal ? min(n - 1, n - W + (r % W)) : n - 1);
+#pragma unroll
+          for (int j = 0; j < kCh; ++j)
+            if (kcol0 + j > lim_r) v[j] = -INFINITY;
+        }
+        float cmax = v[0];
+#pragma unroll
+        for (int j = 1; j < kCh; ++j) cmax = fmaxf(cmax, v[j]);
+        const float mn = fmaxf(m[mt], cmax * s2);
+        float p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
+#pragma unroll
+        for (int j = 0; j < kCh; j += 4) {
+          p0 += ex2_approx(fmaf(v[j + 0], s2, -mn));
+          p1 += ex2_approx(fmaf(v[j + 1], s2, -mn));
+          p2 += ex2_approx(fmaf(v[j + 2], s2, -mn));
+          p3 += ex2_approx(fmaf(v[j + 3], s2, -mn));
+        }
+        z[mt] = z[mt] * ex2_approx(m[mt] - mn) + ((p0 + p1) + (p2 + p3));
+        m[mt] = mn;
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acce_bar[acc]);
+    }
+    // merge the two column groups of each row and write the chunk partials
+    if (cg == 1) {
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+        s_xm[mt][q4][lane] = m[mt];
+        s_xz[mt][q4][lane] = z[mt];
+      }
+    }
+    epi_bar();
+    if (cg == 0) {
+      float* part = a.part + static_cast<size_t>(blockIdx.x) * 2 * a.R_pad;
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+        const int r = mt * 128 + q4 * 32 + lane;
+        if (r < R) {
+          const float m1 = s_xm[mt][q4][lane], z1 = s_xz[mt][q4][lane];
+          const float mm = fmaxf(m[mt], m1);
+          part[r] = mm;
+          part[a.R_pad + r] = z[mt] * ex2_approx(m[mt] - mm) + z1 * ex2_approx(m1 - mm);
+        }
+      }
+    }
+  }
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tbase, kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------------------------------
+// pass 2: per-key sum (or max) of normalised window probabilities
+// ------------------------------------------------------------------------------------
+constexpr int kTileKeys = 128;
+constexpr int kKTileBytes = kTileKeys * 256;
+
+__global__ void __launch_bounds__(kThreads, 1)
+    win_keysum_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                      const WinScoreArgs a, int stages, int nacc, uint32_t tmem_cols) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  const int RP = a.R_pad;             // multiple of 64
+  const int qhalf = RP * 128;
+  uint8_t* sQ = smem;
+  uint8_t* sK = smem + 2 * qhalf;
+  float* s_c2 = reinterpret_cast<float*>(sK + stages * kKTileBytes);
+
+  __shared__ __align__(8) uint64_t full_bar[4], empty_bar[4], accf_bar[2], acce_bar[2];
+  __shared__ __align__(8) uint64_t q_bar, done_bar;
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_abort;
+  __shared__ float s_x[4][32];
+
+  const int warp = warp_id(), lane = lane_id();
+  int b, h, c;
+  chunk_coords(a.ck, a.rq.B, blockIdx.x, b, h, c);
+  const int n = a.rq.n[b];
+  const int key_begin = c * a.ck.chunk_len;
+  const int key_end = min(n, key_begin + a.ck.chunk_len);
+  const int ntiles = key_end > key_begin ? (key_end - key_begin + kTileKeys - 1) / kTileKeys : 0;
+  int* status = a.wc.status;
+  const int R = a.R;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < stages; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    for (int s = 0; s < nacc; ++s) {
+      mbar_init(&accf_bar[s], 1);
+      mbar_init(&acce_bar[s], kEpiWarps);
+    }
+    mbar_init(&q_bar, 1);
+    mbar_init(&done_bar, 1);
+    s_abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(&s_tmem, tmem_cols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = s_tmem;
+
+  if (warp == kProducerWarp) {
+    if (lane == 0 && ntiles > 0) {
+      tma_prefetch_desc(&tq);
+      tma_prefetch_desc(&tk);
+      mbar_arrive_expect_tx(&q_bar, R * 256);
+      load_q_rows(&tq, (b * a.rq.H + h) * R, R, qhalf, sQ, &q_bar);
+      int t = 0;
+      for (; t < ntiles; ++t) {
+        const int s = t % stages, u = t / stages;
+        if (!mbar_wait(&empty_bar[s], (u & 1) ^ 1, &s_abort, a.wc)) break;
+        mbar_arrive_expect_tx(&full_bar[s], kKTileBytes);
+        load_kv_tile(&tk, a.src, b, h, n, key_begin + t * kTileKeys, kTileKeys, sK + s * kKTileBytes, &full_bar[s],
+                     status);
+      }
+      for (int tt = max(0, t - stages); tt < t; ++tt) mbar_drain(&full_bar[tt % stages], (tt / stages) & 1, status);
+      mbar_drain(&q_bar, 0, status);
+    }
+  } else if (warp == kMmaWarp) {
+    if (lane == 0 && ntiles > 0) {
+      bool ok = mbar_wait(&q_bar, 0, &s_abort, a.wc);
+      for (int t = 0; ok && t < ntiles; ++t) {
+        const int s = t % stages, u = t / stages;
+        const int acc = t % nacc, ua = t / nacc;
+        if (!mbar_wait(&full_bar[s], u & 1, &s_abort, a.wc)) break;
+        if (!mbar_wait(&acce_bar[acc], (ua & 1) ^ 1, &s_abort, a.wc)) break;
+        tc_fence_after();
+        const uint32_t kbase = smem_u32(sK + s * kKTileBytes);
+        const uint32_t qbase = smem_u32(sQ);
+        for (int n0 = 0; n0 < R; n0 += 256) {
+          const int nc = min(256, R - n0);
+          const uint32_t idesc = idesc_bf16_f32(128, nc);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const uint32_t koff = (k & 3) * 32;
+            const uint64_t da = sdesc_kmajor_sw128(kbase + (k >> 2) * (kTileKeys * 128) + koff);
+            const uint64_t db = sdesc_kmajor_sw128(qbase + (k >> 2) * qhalf + n0 * 128 + koff);
+            umma_bf16(tbase + acc * RP + n0, da, db, idesc, k > 0 ? 1u : 0u);
+          }
+        }
+        umma_commit(&empty_bar[s]);
+        umma_commit(&accf_bar[acc]);
+      }
+      umma_commit(&done_bar);
+      mbar_drain(&done_bar, 0, status);
+    }
+  } else {
+    // ---------------- epilogue: warps 0-7 ----------------
+    // merged row statistics c2[r] = m_r + log2 Z_r  (log2 units)
+    {
+      const int nch = a.ck.per_head[b];
+      const float* part = a.part + static_cast<size_t>(a.ck.base[b] + h * nch) * 2 * RP;
+      for (int r = threadIdx.x; r < RP; r += kEpiWarps * 32) {
+        float c2 = 0.f;
+        if (r < R) {
+          float mm = kNegBig;
+          for (int j = 0; j < nch; ++j) mm = fmaxf(mm, part[static_cast<size_t>(j) * 2 * RP + r]);
+          float zz = 0.f;
+          for (int j = 0; j < nch; ++j) {
+            const float* pj = part + static_cast<size_t>(j) * 2 * RP;
+            zz += pj[RP + r] * ex2_approx(pj[r] - mm);
+          }
+          c2 = mm + lg2_approx(zz);
+        }
+        s_c2[r] = c2;
+      }
+    }
+    epi_bar();
+    const int q4 = warp & 3, cg = warp >> 2;
+    const float s2 = a.s2;
+    const int W = a.W;
+    const int half_cols = RP / 2;                  // multiple of 32
+    const int col0 = cg * half_cols;
+    const int col_end = min(R, col0 + half_cols);
+    const bool is_max = (a.reduce == 2);
+    const float row_scale = (a.reduce == 1) ? 1.f / static_cast<float>(R) : 1.f;
+    const size_t out_base = static_cast<size_t>(a.rq.soff[b]) + static_cast<size_t>(h) * n;
+    for (int t = 0; t < ntiles; ++t) {
+      const int acc = t % nacc, ua = t / nacc;
+      const bool ok = mbar_wait(&accf_bar[acc], ua & 1, &s_abort, a.wc);
+      if (epi_any(!ok)) break;
+      tc_fence_after();
+      const int key = key_begin + t * kTileKeys + q4 * 32 + lane;
+      // causal: row r sees this key iff (r % W) >= key - (n - W)
+      const int wmin = a.causal ? key - (n - W) : -1;
+      float acc_sum = 0.f, acc_max = -INFINITY;
+      const uint32_t trow = tbase + (static_cast<uint32_t>(q4 * 32) << 16) + acc * RP;
+      for (int c0 = col0; c0 < col_end; c0 += 64) {
+        float v[64];
+        const int cnt = min(64, col_end - c0);   // warp-uniform
+        tmem_ld32(trow + c0, v);
+        if (cnt > 32) tmem_ld32(trow + c0 + 32, v + 32);
+        tmem_ld_wait();
+        if (wmin <= 0 && cnt == 64) {
+          if (is_max) {
+#pragma unroll
+            for (int j = 0; j < 64; ++j) acc_max = fmaxf(acc_max, fmaf(v[j], s2, -s_c2[c0 + j]));
+          } else {
+            float p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
+#pragma unroll
+            for (int j = 0; j < 64; j += 4) {
+              p0 += ex2_approx(fmaf(v[j + 0], s2, -s_c2[c0 + j + 0]));
+              p1 += ex2_approx(fmaf(v[j + 1], s2, -s_c2[c0 + j + 1]));
+              p2 += ex2_approx(fmaf(v[j + 2], s2, -s_c2[c0 + j + 2]));
+              p3 += ex2_approx(fmaf(v[j + 3], s2, -s_c2[c0 + j + 3]));
+            }
+            acc_sum += (p0 + p1) + (p2 + p3);
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 64; ++j) {
+            const int r = c0 + j;
+            if (j < cnt && (r % W) >= wmin) {
+              const float y = fmaf(v[j], s2, -s_c2[r]);
+              if (is_max)
+                acc_max = fmaxf(acc_max, y);
+              else
+                acc_sum += ex2_approx(y);
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acce_bar[acc]);
+      float part_v = is_max ? acc_max : acc_sum;
+      if (cg == 1) s_x[q4][lane] = part_v;
+      epi_bar();
+      if (cg == 0 && key < n) {
+        const float o = s_x[q4][lane];
+        float res;
+        if (is_max)
+          res = ex2_approx(fmaxf(part_v, o));
+        else
+          res = (part_v + o) * row_scale;
+        a.s_raw[out_base + key] = res;
+      }
+      epi_bar();
+    }
+  }
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tbase, tmem_cols);
+  }
+}
+
+template <int MT, int NT, int STAGES>
+cudaError_t launch_rowstats_t(const WinScoreArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, cudaStream_t st) {
+  const size_t smem = 1024 + 2 * MT * 128 * 128 + STAGES * NT * 256;
+  cudaError_t e = cudaFuncSetAttribute(win_rowstats_kernel<MT, NT, STAGES>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  win_rowstats_kernel<MT, NT, STAGES><<<a.ck.total, kThreads, smem, st>>>(tq, tk, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_win_rowstats(const WinScoreArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, int mt,
+                                cudaStream_t st) {
+  if (a.ck.total <= 0) return cudaSuccess;
+  switch (mt) {
+    case 1: return launch_rowstats_t<1, 128, 4>(a, tq, tk, st);
+    case 2: return launch_rowstats_t<2, 128, 4>(a, tq, tk, st);
+    default: return launch_rowstats_t<4, 64, 4>(a, tq, tk, st);
+  }
+}
+
+cudaError_t launch_win_keysum(const WinScoreArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, cudaStream_t st) {
+  if (a.ck.total <= 0) return cudaSuccess;
+  const int RP = a.R_pad;
+  const int nacc = (2 * RP <= 512) ? 2 : 1;
+  const uint32_t cols = pow2_cols(static_cast<uint32_t>(nacc * RP));
+  const size_t fixed = 1024 + 2 * static_cast<size_t>(RP) * 128 + static_cast<size_t>(RP) * 4;
+  const size_t budget = 232448 - 4096;  // opt-in limit minus static shared memory
+  int stages = static_cast<int>((budget - fixed) / kKTileBytes);
+  stages = stages > 4 ? 4 : stages;
+  if (stages < 2) return cudaErrorInvalidValue;
+  const size_t smem = fixed + static_cast<size_t>(stages) * kKTileBytes;
+  cudaError_t e =
+      cudaFuncSetAttribute(win_keysum_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  win_keysum_kernel<<<a.ck.total, kThreads, smem, st>>>(tq, tk, a, stages, nacc, cols);
+  return cudaGetLastError();
+}
+
+}  // namespace kvsel

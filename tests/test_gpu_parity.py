@@ -1,0 +1,213 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle on seeded inputs.
+
+Sizes span several key tiles and a ragged tail; full-size layers are checked on every
+score where the oracle is cheap, and on sampled values plus size-independent properties
+where it is not.  Tolerances (tests/gpu_harness.py): scores within 1e-3 relative (plus
+an absolute floor of 1e-7 x the head's max for flushed denormals); kept sets equal
+except entries within 1e-3 of a selection threshold; compacted K/V bit-exact.
+"""
+import math
+
+import numpy as np
+import pytest
+
+from kv_cache_eviction_window_gb300 import datagen
+from oracle import kvsel_oracle as O
+from tests import gpu_harness as GH
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    import __graft_entry__
+
+    __graft_entry__.build()
+    from kv_cache_eviction_window_gb300 import binding
+
+    binding.load()
+    yield
+
+
+def _check_layer(wl, inp, gpu, ora, heads=None):
+    for b, (g, o) in enumerate(zip(gpu, ora)):
+        n = o["n"]
+        assert g["status"] == 0
+        fm = O.forced_mask(n, wl.n_sink, wl.n_recent)
+        H = wl.h_kv
+        hs = range(H) if heads is None else heads
+        for h in hs:
+            GH.assert_scores_close(g["s_attn"][h], o["s_pool"][h], f"s_attn b{b} h{h}")
+            if wl.value_aware:
+                GH.assert_scores_close(g["s_val"][h], o["s_val"][h], f"s_val b{b} h{h}")
+        if wl.budget_mode == "head":
+            B = O.head_budget(n, wl.budget_ratio)
+            for h in hs:
+                if wl.value_aware:
+                    b1 = max(int(math.floor(wl.alpha * B)), int(fm.sum()))
+                    t1 = GH.kth_key(o["s_pool"][h], fm, b1)
+                    keep1 = np.zeros(n, bool)
+                    keep1[O.top_b(o["s_pool"][h], b1, fm)] = True
+                    t2 = GH.kth_key(o["s_val"][h], keep1, B)
+                    th = [(o["s_pool"][h], t1), (o["s_val"][h], t2)]
+                    # the GPU's own scores: stage 1 then stage 2, exactly
+                    k1 = GH.topk_mask(g["s_attn"][h], fm, b1)
+                    GH.check_topk_property(g["s_val"][h], g["idx"][h], k1, B, f"two-stage b{b} h{h}")
+                else:
+                    th = [(o["s_pool"][h], GH.kth_key(o["s_pool"][h], fm, B))]
+                    GH.check_topk_property(g["s_attn"][h], g["idx"][h], fm, B, f"top-B b{b} h{h}")
+                GH.check_selection_near_ties(g["idx"][h], o["idx"][h], fm, n, B, th, f"sel b{b} h{h}")
+        else:
+            BL = int(math.floor(wl.budget_ratio * n * H))
+            fl = int(math.floor(wl.floor_ratio * n))
+            assert sum(len(i) for i in g["idx"]) == BL
+            fh = min(n, max(fl, int(fm.sum())))
+            flat = o["s_pool"].reshape(-1)
+            keep = np.zeros((H, n), bool)
+            ths = []
+            for h in range(H):
+                ths.append((o["s_pool"][h], GH.kth_key(o["s_pool"][h], fm, fh)))
+                keep[h, O.top_b(o["s_pool"][h], fh, fm)] = True
+            tl = GH.kth_key(flat, keep.reshape(-1), BL)
+            for h in range(H):
+                assert len(g["idx"][h]) >= fh
+                GH.check_selection_near_ties(g["idx"][h], o["idx"][h], fm, n, len(g["idx"][h]),
+                                             ths + [(o["s_pool"][h], tl)], f"layer sel b{b} h{h}")
+        # compaction is bit-exact given the GPU's own indices
+        for h in hs:
+            np.testing.assert_array_equal(g["k_out"][h], inp["k"][b][h][g["idx"][h]])
+            np.testing.assert_array_equal(g["v_out"][h], inp["v"][b][h][g["idx"][h]])
+
+
+def test_c1_llama_layer_4k_full():
+    wl = datagen.WORKLOADS[1]
+    inp = datagen.make_layer(wl, 0)
+    ora = O.run_workload_layer(wl, inp)
+    gpu = GH.run_gpu_layer(wl, inp)
+    _check_layer(wl, inp, gpu, ora)
+
+
+@pytest.mark.parametrize("n", [1000, 2085])
+def test_c2_value_aware_ragged(n):
+    wl = datagen.WORKLOADS[2].replace(layers=1)
+    inp = datagen.make_layer(wl, 3, n_ctx=n)
+    ora = O.run_workload_layer(wl, inp)
+    gpu = GH.run_gpu_layer(wl, inp)
+    _check_layer(wl, inp, gpu, ora)
+
+
+def test_c2_per_head_wo_reading():
+    wl = datagen.WORKLOADS[2].replace(layers=1, d_model=1024)
+    inp = datagen.make_layer(wl, 1, n_ctx=777)
+    inp["w_o"] = inp["w_o"]  # [1024][4096]
+    ora = O.run_workload_layer(wl, inp, wo_mode="per_head")
+    gpu = GH.run_gpu_layer(wl, inp, wo_mode="per_head")
+    _check_layer(wl, inp, gpu, ora)
+
+
+@pytest.mark.parametrize("n", [1500, 3333])
+def test_c3_per_layer_budget(n):
+    wl = datagen.WORKLOADS[3].replace(layers=1)
+    inp = datagen.make_layer(wl, 0, n_ctx=n)
+    ora = O.run_workload_layer(wl, inp)
+    gpu = GH.run_gpu_layer(wl, inp)
+    _check_layer(wl, inp, gpu, ora)
+
+
+def test_c4_paged_ragged_batch():
+    wl = datagen.WORKLOADS[4].replace(batch=4, n_min=300, n_ctx=1400)
+    inp = datagen.make_layer(wl, 0)
+    ora = O.run_workload_layer(wl, inp)
+    gpu = GH.run_gpu_layer(wl, inp)
+    _check_layer(wl, inp, gpu, ora)
+    # the same requests from a contiguous (padded) cache give identical results
+    gpu2 = GH.run_gpu_layer(wl, inp, paged=False)
+    for a, b in zip(gpu, gpu2):
+        np.testing.assert_array_equal(a["s_attn"], b["s_attn"])
+        for h in range(wl.h_kv):
+            np.testing.assert_array_equal(a["idx"][h], b["idx"][h])
+
+
+@pytest.mark.parametrize("reduce,pool,causal", [("sum", "none", False), ("max", "max", True),
+                                                 ("mean", "avg", True)])
+def test_reductions_and_pooling(reduce, pool, causal):
+    wl = datagen.WORKLOADS[1].replace(reduce=reduce, pool=pool, pool_kernel=5, causal=causal,
+                                      h_kv=2, n_ctx=1111)
+    inp = datagen.make_layer(wl, 0, n_ctx=1111)
+    ora = O.run_workload_layer(wl, inp)
+    gpu = GH.run_gpu_layer(wl, inp)
+    _check_layer(wl, inp, gpu, ora)
+
+
+def test_budget_equals_n_identity():
+    wl = datagen.WORKLOADS[1].replace(budget_ratio=1.0, h_kv=2)
+    inp = datagen.make_layer(wl, 0, n_ctx=600)
+    gpu = GH.run_gpu_layer(wl, inp)
+    for h in range(2):
+        np.testing.assert_array_equal(gpu[0]["idx"][h], np.arange(600))
+        np.testing.assert_array_equal(gpu[0]["k_out"][h], inp["k"][0][h])
+
+
+def test_minimal_context_equals_window():
+    wl = datagen.WORKLOADS[1].replace(h_kv=1, n_recent=32, n_sink=4, budget_ratio=1.0)
+    inp = datagen.make_layer(wl, 0, n_ctx=32)
+    ora = O.run_workload_layer(wl, inp)
+    gpu = GH.run_gpu_layer(wl, inp)
+    _check_layer(wl, inp, gpu, ora)
+
+
+# ---------------------------------------------------------------------- full size
+def test_c2_full_layer_plain_and_sampled_value_aware():
+    """Llama-3.1-8B layer, n = 32768: plain scores and selection against the full oracle;
+    the value-aware scores on sampled tokens (nu from the oracle per token)."""
+    wl = datagen.WORKLOADS[2]
+    inp = datagen.make_layer(wl, 0)
+    plain = wl.replace(value_aware=False)
+    ora = O.run_workload_layer(plain, inp, compact_out=False)
+    gpu = GH.run_gpu_layer(plain, inp)
+    o = ora[0]
+    _check_layer(plain, inp, gpu, ora)
+    gva = GH.run_gpu_layer(wl, inp)[0]
+    rng = np.random.default_rng(0)
+    w_o = O.bf16_to_f64(inp["w_o"])
+    for h in range(wl.h_kv):
+        GH.assert_scores_close(gva["s_attn"][h], o["s_pool"][h], f"s_attn h{h}")
+        sample = np.concatenate([rng.choice(32768, 256, replace=False), np.arange(8), 32768 - np.arange(1, 9)])
+        v = O.bf16_to_f64(inp["v"][0][h][sample])
+        nu = O.value_norm(v, w_o, h, wl.group)
+        want = O.combine(o["s_pool"][h][sample], nu, wl.eps)
+        GH.assert_scores_close(gva["s_val"][h][sample], want, f"s_val sample h{h}")
+        fm = O.forced_mask(32768, 4, 32)
+        B = O.head_budget(32768, wl.budget_ratio)
+        b1 = max(int(math.floor(wl.alpha * B)), int(fm.sum()))
+        k1 = GH.topk_mask(gva["s_attn"][h], fm, b1)
+        GH.check_topk_property(gva["s_val"][h], gva["idx"][h], k1, B, f"two-stage h{h}")
+        np.testing.assert_array_equal(gva["k_out"][h], inp["k"][0][h][gva["idx"][h]])
+
+
+def test_c3_full_layer():
+    """Qwen2.5-7B layer, n = 131072, 448 window rows per head, per-layer budget."""
+    wl = datagen.WORKLOADS[3]
+    inp = datagen.make_layer(wl, 0)
+    ora = O.run_workload_layer(wl, inp, compact_out=False)
+    gpu = GH.run_gpu_layer(wl, inp)
+    _check_layer(wl, inp, gpu, ora)
+
+
+# ---------------------------------------------------------------------- device status
+def test_bounded_wait_timeout_reports_status():
+    """A wait budget of 0 cycles makes the pipeline waits give up: the kernels end with
+    KVSEL_ETIMEOUT in the status word and the context stays usable."""
+    from kv_cache_eviction_window_gb300 import binding as B
+
+    wl = datagen.WORKLOADS[1].replace(h_kv=2)
+    inp = datagen.make_layer(wl, 0, n_ctx=2048)
+    try:
+        B.kvsel_set_wait_limit(0)
+        out = GH.run_gpu_layer(wl, inp)
+        assert out[0]["status"] == B.KVSEL_ETIMEOUT
+    finally:
+        B.kvsel_set_wait_limit(2_000_000_000)
+    ora = O.run_workload_layer(wl, inp)
+    gpu = GH.run_gpu_layer(wl, inp)
+    _check_layer(wl, inp, gpu, ora)
