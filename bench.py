@@ -1,0 +1,448 @@
+#!/usr/bin/env python
+"""Benchmark of end-of-prefill KV scoring -> selection -> compaction on GB300.
+
+One step = the whole path (window scoring, value norm, pooling, two-stage top-B select,
+K/V compaction) over every layer of the Llama-3.1-8B-shaped 32K stack (32 layers,
+8 KV heads, group 4, d 128, n 32768, window 32, avgpool 5, value-aware, 40% per head),
+synthetic seeded inputs resident in HBM (160 MiB per layer, larger than L2).
+
+Prints ONE JSON line (rank 0).  `--impl reference` times the fp64 CPU oracle instead on
+a bounded sample of the same workload.  Under torchrun each rank runs its own replica of
+the stack (independent requests, no collective on the data path: weak scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "KV entries scored+selected+compacted/s per layer; K/V GB/s vs HBM roofline"
+UNIT = "entries/s"
+WORKLOAD_ID = 2
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-plain", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ------------------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi samples during the timed region (SM clock, reasons)."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.2)
+        self.proc.terminate()
+        self.proc.wait(timeout=10)
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax = float(f[2])
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        os.unlink(self.path)
+        load = [s for s in sm if smax and s > 0.5 * smax] or sm
+        return {"sm_mhz": statistics.median(load) if load else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------------------ dist
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    import torch
+
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------------------ oracle
+def oracle_sample(wl, inputs, heads):
+    """The fp64 oracle on (layer 0, `heads`) of the workload: score, select, compact."""
+    from oracle import kvsel_oracle as O
+
+    q = inputs["q"][0]
+    k = O.bf16_to_f64(inputs["k"][0])
+    w_o = O.bf16_to_f64(inputs["w_o"])
+    n = k.shape[1]
+    fm = O.forced_mask(n, wl.n_sink, wl.n_recent)
+    B = O.head_budget(n, wl.budget_ratio)
+    for h in heads:
+        s_raw = O.window_scores(O.bf16_to_f64(q[h]), k[h], wl.reduce, None, wl.causal)
+        s_pool = O.pool1d(s_raw, wl.pool, wl.pool_kernel)
+        nu = O.value_norm(O.bf16_to_f64(inputs["v"][0][h]), w_o, h, wl.group)
+        s_val = O.combine(s_pool, nu, wl.eps)
+        idx = O.select_two_stage(s_pool, s_val, B, fm, wl.alpha)
+        O.compact(inputs["k"][0][h], idx)
+        O.compact(inputs["v"][0][h], idx)
+    return len(heads) * n
+
+
+def cpu_threads():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+def run_cpu_baseline(wl, inputs, budget_s=10.0):
+    t0 = time.perf_counter()
+    done = 0
+    heads = 0
+    for h in range(wl.h_kv):
+        done += oracle_sample(wl, inputs, [h])
+        heads += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": done / dt, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
+            "sample": f"layer 0, {heads} of {wl.h_kv} KV heads, all {wl.n_ctx} entries each "
+                      f"(fp64 numpy, BLAS threads = host cores); {dt:.1f} s"}
+
+
+def run_reference(args):
+    world, rank, _ = int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")), 0
+    if rank != 0:
+        return 0
+    from kv_cache_eviction_window_gb300 import datagen
+
+    wl = datagen.WORKLOADS[WORKLOAD_ID]
+    inputs = datagen.make_layer(wl, 0)
+    for i in range(args.warmup):
+        oracle_sample(wl, inputs, [i % wl.h_kv])
+    t0 = time.perf_counter()
+    entries = 0
+    for s in range(args.steps):
+        entries += oracle_sample(wl, inputs, [s % wl.h_kv])
+    dt = time.perf_counter() - t0
+    v = entries / dt
+    line = {"metric": METRIC, "value": v, "unit": UNIT, "impl": "reference", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": workload_config(wl),
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
+                             "sample": f"one (layer, KV head) of {wl.n_ctx} entries per step"},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(wl):
+    return {"workload": wl.name, "layers": wl.layers, "h_kv": wl.h_kv, "group": wl.group,
+            "head_dim": wl.head_dim, "n_ctx": wl.n_ctx, "window": wl.window, "d_model": wl.d_model,
+            "pool": f"{wl.pool}{wl.pool_kernel}", "reduce": wl.reduce, "value_aware": wl.value_aware,
+            "alpha": wl.alpha, "budget": f"{wl.budget_ratio:.0%} per KV head",
+            "forced": f"{wl.n_sink} sinks + {wl.n_recent} recent",
+            "l2": "inputs larger than L2 (Q/K/V/W_O 160 MiB per layer, distinct per layer)"}
+
+
+# ------------------------------------------------------------------------------ gb300
+def file_hash(*rel):
+    h = hashlib.sha256()
+    for r in rel:
+        h.update(open(os.path.join(ROOT, r), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def traffic_for(kernel_name):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel source has not
+    changed since the counters were taken."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p)).get(kernel_name)
+    if not d:
+        return None
+    if d.get("source_hash") != file_hash(*d["sources"]):
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+    import numpy as np
+    import torch
+
+    world, rank, local = dist_setup(args)
+    import __graft_entry__
+
+    __graft_entry__.build()
+    from kv_cache_eviction_window_gb300 import binding as B
+    from kv_cache_eviction_window_gb300 import datagen
+
+    B.load()
+    wl = datagen.WORKLOADS[WORKLOAD_ID]
+    L, H, n, d = wl.layers, wl.h_kv, wl.n_ctx, wl.head_dim
+    dev = torch.device("cuda", torch.cuda.current_device())
+
+    # ---- inputs (host, seeded) -> HBM
+    t_gen = time.perf_counter()
+    host = [datagen.make_layer(wl, layer + 100 * rank) for layer in range(L)]
+    t_gen = time.perf_counter() - t_gen
+
+    def to_dev(u16):
+        return torch.from_numpy(u16.view(np.int16)).view(torch.bfloat16).to(dev, non_blocking=False)
+
+    q_d = [to_dev(x["q"]) for x in host]
+    k_d = [to_dev(x["k"][0]) for x in host]
+    v_d = [to_dev(x["v"][0]) for x in host]
+    w_d = [to_dev(x["w_o"]) for x in host]
+    params = B.params_from_workload(wl)
+    bufs = [B.LayerBuffers(params, device=dev) for _ in range(L)]
+    ws = bufs[0].ws
+    kvs = [B.make_kv_contiguous(k_d[i], v_d[i]) for i in range(L)]
+    stream = torch.cuda.current_stream()
+
+    def layer_call(i, p=params, w=None):
+        b = bufs[i]
+        B.kvsel_run_layer(p, q_d[i], kvs[i], w_d[i] if p.value_aware else None, b.s_attn, b.s_val, b.idx,
+                          b.counts, b.offsets, b.k_out, b.v_out, ws, stream)
+
+    # ---- stage events for the live per-kernel timing
+    nst = len(B.STAGES)
+    K, W = args.steps, args.warmup
+    ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(2 * nst)] for _ in range(L)] for _ in range(K)]
+    for s in range(K):
+        for i in range(L):
+            for e in ev[s][i]:
+                e.record(stream)
+    torch.cuda.synchronize()
+    ev_arr = [[(ctypes.c_void_p * (2 * nst))(*[e.cuda_event for e in ev[s][i]]) for i in range(L)] for s in range(K)]
+
+    for _ in range(W):
+        for i in range(L):
+            layer_call(i)
+    torch.cuda.synchronize()
+    st = B.kvsel_get_device_status(ws)
+    assert st == 0, f"device status {st} after warm-up"
+
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for s in range(K):
+        for i in range(L):
+            B.kvsel_set_stage_events(ev_arr[s][i])
+            layer_call(i)
+    B.kvsel_set_stage_events(None)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    ms = t0.elapsed_time(t1)
+    ms = max_over_ranks(ms, world)
+    status = B.kvsel_get_device_status(ws)
+    entries = K * L * H * n * world
+    value = entries / (ms * 1e-3)
+
+    stage_ms = {}
+    for si, name in enumerate(B.STAGES):
+        tot, cnt = 0.0, 0
+        for s in range(K):
+            for i in range(L):
+                a, b = ev[s][i][2 * si], ev[s][i][2 * si + 1]
+                try:
+                    tot += a.elapsed_time(b)
+                    cnt += 1
+                except RuntimeError:
+                    pass
+        stage_ms[name] = tot / cnt if cnt else None
+    pk, pk_src = peaks()
+    dom = max((k for k in stage_ms if stage_ms[k]), key=lambda k: stage_ms[k])
+    Dw = wl.d_model
+    if dom == "vnorm":
+        flops = 2.0 * n * H * Dw * d
+        ach = flops / (stage_ms[dom] * 1e-3) / 1e12
+        peak = pk.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
+        roof = {"kernel": "vnorm_kernel", "bound": "tensor", "achieved": ach, "peak": peak, "unit": "TFLOP/s",
+                "frac": ach / peak, "traffic": traffic_for("vnorm_kernel"),
+                "peak_source": f"{pk_src} bf16_tflops_sustained (kernel timed inside a long step)",
+                "algorithmic": f"2*n*H*D*d = {flops:.3e} flop per launch (one layer)"}
+    else:
+        kb = H * n * d * 2
+        byts = kb
+        ach = byts / (stage_ms[dom] * 1e-3) / 1e9
+        peak = pk.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+        roof = {"kernel": dom, "bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s", "frac": ach / peak,
+                "traffic": traffic_for(dom), "peak_source": f"{pk_src} hbm_gbs"}
+
+    out = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
+           "ms_per_step": ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+           "dtype": "bf16", "data": "synthetic", "config": workload_config(wl), "clocks": clk,
+           "gpu_launches": K * L * 7, "device_status": status, "roofline": roof,
+           "stage_ms_per_layer": {k: (round(v, 5) if v else v) for k, v in stage_ms.items()}}
+
+    # ---- the plain-score path on the same layers (spec HBM target)
+    if not args.no_plain:
+        plain = B.params_from_workload(wl, value_aware=False)
+        for _ in range(W):
+            for i in range(L):
+                layer_call(i, plain)
+        torch.cuda.synchronize()
+        barrier(world)
+        t0.record(stream)
+        for s in range(K):
+            for i in range(L):
+                layer_call(i, plain)
+        t1.record(stream)
+        torch.cuda.synchronize()
+        pms = max_over_ranks(t0.elapsed_time(t1), world) / (K * L)
+        Bh = int(wl.budget_ratio * n)
+        alg = H * n * d * 2 + 3 * H * Bh * d * 2 + int(wl.h_kv * wl.group * wl.window * d * 2) + 2 * H * n * 4
+        gbs = alg / (pms * 1e-3) / 1e9
+        out["hbm_path"] = {"what": "same layers, value_aware=0 (score+select+compact, no W_O pass)",
+                           "ms_per_layer": pms, "entries_per_s": H * n / (pms * 1e-3) * world,
+                           "algorithmic_bytes_per_layer": alg, "achieved_gbs": gbs,
+                           "peak_gbs": pk.get("hbm_gbs"), "frac": gbs / pk.get("hbm_gbs", 6800.0)}
+
+    # ---- end to end through the public API: pinned host -> device each step, results back
+    if not args.no_e2e:
+        pin = []
+        for x in host:
+            t = {}
+            for key, arr in (("q", x["q"]), ("k", x["k"][0]), ("v", x["v"][0]), ("w", x["w_o"])):
+                h = torch.empty(arr.shape, dtype=torch.bfloat16, pin_memory=True)
+                h.view(torch.int16).numpy()[...] = arr.view(np.int16)
+                t[key] = h
+            t["idx"] = torch.empty(bufs[0].idx.shape, dtype=torch.int32, pin_memory=True)
+            t["counts"] = torch.empty(bufs[0].counts.shape, dtype=torch.int32, pin_memory=True)
+            pin.append(t)
+        h2d = sum(t[k].numel() * 2 for t in pin for k in ("q", "k", "v", "w"))
+        d2h = sum(t["idx"].numel() * 4 + t["counts"].numel() * 4 for t in pin)
+        copy = torch.cuda.Stream()
+        c_done = [torch.cuda.Event() for _ in range(L)]
+        x_done = [torch.cuda.Event() for _ in range(L)]
+
+        def e2e_step():
+            for i in range(L):
+                with torch.cuda.stream(copy):
+                    copy.wait_event(c_done[i])
+                    q_d[i].copy_(pin[i]["q"], non_blocking=True)
+                    k_d[i].copy_(pin[i]["k"], non_blocking=True)
+                    v_d[i].copy_(pin[i]["v"], non_blocking=True)
+                    w_d[i].copy_(pin[i]["w"], non_blocking=True)
+                    x_done[i].record(copy)
+                stream.wait_event(x_done[i])
+                layer_call(i)
+                pin[i]["idx"].copy_(bufs[i].idx, non_blocking=True)
+                pin[i]["counts"].copy_(bufs[i].counts, non_blocking=True)
+                c_done[i].record(stream)
+
+        for i in range(L):
+            c_done[i].record(stream)
+        for _ in range(W):
+            e2e_step()
+        torch.cuda.synchronize()
+        barrier(world)
+        w0 = time.perf_counter()
+        t0.record(stream)
+        for _ in range(K):
+            e2e_step()
+        t1.record(stream)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - w0
+        ems = max_over_ranks(max(t0.elapsed_time(t1), wall * 1e3), world)
+        out["e2e"] = {"value": entries / (ems * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                      "d2h_bytes_per_step": d2h, "ms_per_step": ems / K,
+                      "how": "kvsel_run_layer per layer; per-layer H2D of Q/K/V/W_O from pinned host on a copy "
+                             "stream overlapped with the previous layer's compute; idx/counts D2H per layer"}
+
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = run_cpu_baseline(wl, host[0])
+    out["input_generation_s"] = round(t_gen, 2)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -181,6 +181,25 @@ int kvsel_get_device_status(void* ws, void* stream, int* status);
  * to exercise the timeout path.  Host-side setting for subsequent launches. */
 void kvsel_set_wait_limit(uint64_t cycles);
 
+/* Stages of the path, in launch order within one layer. */
+enum {
+  KVSEL_STAGE_ROWSTATS = 0,  /* window scoring pass 1: per-row softmax statistics    */
+  KVSEL_STAGE_KEYSUM = 1,    /* window scoring pass 2: per-key reduced probabilities */
+  KVSEL_STAGE_WBAR = 2,      /* value-aware: W_O slices of each KV head, bf16        */
+  KVSEL_STAGE_VNORM = 3,     /* value-aware: ||W_h v||_1 per token (tensor cores)    */
+  KVSEL_STAGE_FINALIZE = 4,  /* pooling and (s + eps) * nu                           */
+  KVSEL_STAGE_SELECT = 5,    /* top-B selection                                      */
+  KVSEL_STAGE_COMPACT = 6,   /* gather of the kept K/V rows                          */
+  KVSEL_STAGE_COUNT = 7
+};
+
+/* Diagnostics: while `events` is non-NULL, each kernel launched by this thread's
+ * subsequent calls is bracketed by cudaEventRecord(events[2*stage]) and
+ * cudaEventRecord(events[2*stage + 1]) on the launch stream (NULL entries skipped).
+ * `events` is a host array of 2*KVSEL_STAGE_COUNT cudaEvent_t created by the caller and
+ * must stay valid until the hook is cleared with NULL.  No effect on results. */
+void kvsel_set_stage_events(void* const* events);
+
 /* Static description of an error code. */
 const char* kvsel_strerror(int code);
 

@@ -32,7 +32,8 @@ MAX_BATCH = 128
 
 EXPORTS = ("kvsel_workspace_size", "kvsel_output_size", "kvsel_workspace_init", "kvsel_score",
            "kvsel_select", "kvsel_compact", "kvsel_run_layer", "kvsel_get_device_status",
-           "kvsel_set_wait_limit", "kvsel_strerror", "kvsel_version")
+           "kvsel_set_wait_limit", "kvsel_set_stage_events", "kvsel_strerror", "kvsel_version")
+STAGES = ("rowstats", "keysum", "wbar", "vnorm", "finalize", "select", "compact")
 
 
 class KvselUnavailable(RuntimeError):
@@ -95,6 +96,7 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
         "kvsel_run_layer": ([P, vp, K, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp], ctypes.c_int),
         "kvsel_get_device_status": ([vp, vp, ctypes.POINTER(ctypes.c_int)], ctypes.c_int),
         "kvsel_set_wait_limit": ([ctypes.c_uint64], None),
+        "kvsel_set_stage_events": ([ctypes.c_void_p], None),
         "kvsel_strerror": ([ctypes.c_int], ctypes.c_char_p),
         "kvsel_version": ([], ctypes.c_char_p),
     }
@@ -208,6 +210,12 @@ def kvsel_strerror(code: int) -> str:
 
 def kvsel_set_wait_limit(cycles: int) -> None:
     load().kvsel_set_wait_limit(int(cycles))
+
+
+def kvsel_set_stage_events(events) -> None:
+    """events: None, or a ctypes array of 2*len(STAGES) cudaEvent_t handles (kept alive
+    by the caller while set)."""
+    load().kvsel_set_stage_events(None if events is None else ctypes.cast(events, ctypes.c_void_p))
 
 
 def kvsel_workspace_size(params: kvsel_params) -> int:

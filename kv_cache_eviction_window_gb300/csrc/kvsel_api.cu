@@ -20,6 +20,19 @@ std::atomic<unsigned long long> g_wait_limit{2000000000ull};   // ~1 s at the bo
 
 constexpr size_t kStatusBytes = 256;
 
+thread_local void* const* t_stage_events = nullptr;
+
+// Brackets one launch with the caller's diagnostic events (kvsel_set_stage_events).
+struct StageScope {
+  int stage;
+  cudaStream_t st;
+  StageScope(int s, cudaStream_t stream) : stage(s), st(stream) { rec(2 * stage); }
+  ~StageScope() { rec(2 * stage + 1); }
+  void rec(int i) const {
+    if (t_stage_events && t_stage_events[i]) cudaEventRecord(static_cast<cudaEvent_t>(t_stage_events[i]), st);
+  }
+};
+
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 struct Plan {
@@ -290,16 +303,26 @@ int do_score(const kvsel_params* p, const Plan& pl, const void* q, const kvsel_k
   a.part = part;
   a.s_raw = s_raw;
   a.wc = wait_ctl(ws);
-  int rc = launch_rc(launch_win_rowstats(a, tq, tk1, pl.mt, st));
+  int rc;
+  {
+    StageScope sc(KVSEL_STAGE_ROWSTATS, st);
+    rc = launch_rc(launch_win_rowstats(a, tq, tk1, pl.mt, st));
+  }
   if (rc) return rc;
-  rc = launch_rc(launch_win_keysum(a, tq, tk2, st));
+  {
+    StageScope sc(KVSEL_STAGE_KEYSUM, st);
+    rc = launch_rc(launch_win_keysum(a, tq, tk2, st));
+  }
   if (rc) return rc;
 
   float* nu = nullptr;
   if (p->value_aware) {
     nu = reinterpret_cast<float*>(wsb + pl.ws_nu);
     uint16_t* wbar = reinterpret_cast<uint16_t*>(wsb + pl.ws_wbar);
-    rc = launch_rc(launch_wbar(static_cast<const uint16_t*>(w_o), wbar, pl.H, pl.G, pl.D, p->wo_mode, st));
+    {
+      StageScope sc(KVSEL_STAGE_WBAR, st);
+      rc = launch_rc(launch_wbar(static_cast<const uint16_t*>(w_o), wbar, pl.H, pl.G, pl.D, p->wo_mode, st));
+    }
     if (rc) return rc;
     CUtensorMap tv, tw;
     if (!kv_map(&tv, kv->v, kv, pl, kv->layout == KVSEL_LAYOUT_PAGED ? 0 : 128)) return KVSEL_EINVAL;
@@ -318,9 +341,13 @@ int do_score(const kvsel_params* p, const Plan& pl, const void* q, const kvsel_k
     for (int b = 0; b < pl.B; ++b) v.blocks_per_head[b] = pl.blocks_per_head[b];
     v.nu = nu;
     v.wc = wait_ctl(ws);
-    rc = launch_rc(launch_vnorm(v, tv, tw, st));
+    {
+      StageScope sc(KVSEL_STAGE_VNORM, st);
+      rc = launch_rc(launch_vnorm(v, tv, tw, st));
+    }
     if (rc) return rc;
   }
+  StageScope sc(KVSEL_STAGE_FINALIZE, st);
   return launch_rc(launch_finalize(pl.rq, s_raw, nu, s_attn, p->value_aware ? s_val : nullptr, p->pool,
                                    p->pool_kernel, p->eps, st));
 }
@@ -349,6 +376,7 @@ int do_select(const kvsel_params* p, const Plan& pl, const float* s_attn, const 
   int cap = 0;
   const int cs = select_cluster_size(std::max(max_len, 1), &cap);
   if (cs < 0) return KVSEL_EUNSUPPORTED;
+  StageScope sc(KVSEL_STAGE_SELECT, st);
   return launch_rc(launch_select(a, cs, cap, st));
 }
 
@@ -370,6 +398,7 @@ int do_compact(const Plan& pl, const kvsel_kv* kv, const int32_t* idx, const int
   c.status = static_cast<int*>(ws);
   int sms = pl.num_sms;
   if (!sms && device_sms(&sms)) return KVSEL_ECUDA;
+  StageScope sc(KVSEL_STAGE_COMPACT, st);
   return launch_rc(launch_compact(c, pl.max_count, sms, st));
 }
 
@@ -394,6 +423,8 @@ const char* kvsel_strerror(int code) {
 }
 
 void kvsel_set_wait_limit(uint64_t cycles) { g_wait_limit.store(cycles); }
+
+void kvsel_set_stage_events(void* const* events) { t_stage_events = events; }
 
 int kvsel_workspace_size(const kvsel_params* p, size_t* bytes) {
   if (!bytes) return KVSEL_EINVAL;

@@ -1,0 +1,91 @@
+"""Run a few layers of one workload through kvsel_run_layer, for profilers (ncu).
+
+    python -m kv_cache_eviction_window_gb300.profile_case --workload 2 --layers 2 --steps 2
+
+The inputs are the same seeded synthetic tensors as the benchmark (each layer distinct,
+larger than L2 for the 32K stack), so per-launch counters taken here scale to the
+benchmark's full stack.  Prints per-stage CUDA-event times; it is not a benchmark line.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import os
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--workload", type=int, default=2)
+    ap.add_argument("--layers", type=int, default=2)
+    ap.add_argument("--steps", type=int, default=2)
+    ap.add_argument("--plain", action="store_true", help="value_aware=0")
+    args = ap.parse_args()
+    import numpy as np
+    import torch
+
+    import __graft_entry__
+
+    __graft_entry__.build()
+    from kv_cache_eviction_window_gb300 import binding as B
+    from kv_cache_eviction_window_gb300 import datagen
+
+    wl = datagen.WORKLOADS[args.workload]
+    if args.plain:
+        wl = wl.replace(value_aware=False)
+    dev = torch.device("cuda", 0)
+
+    def to_dev(u16):
+        return torch.from_numpy(np.ascontiguousarray(u16).view(np.int16)).view(torch.bfloat16).to(dev)
+
+    layers = []
+    for layer in range(args.layers):
+        x = datagen.make_layer(wl, layer)
+        lens = x["n_ctx"]
+        p = B.params_from_workload(wl, n_ctx_per_req=lens if len(lens) > 1 else None, n_ctx=lens[0])
+        if wl.paged:
+            pg = x["paged"]
+            kt, vt = to_dev(pg["k_pool"]), to_dev(pg["v_pool"])
+            table = torch.from_numpy(pg["block_table"]).to(dev)
+            kv = B.make_kv_paged(kt, vt, table)
+            keep = (kt, vt, table)
+        else:
+            kt, vt = to_dev(np.stack(x["k"])), to_dev(np.stack(x["v"]))
+            kv = B.make_kv_contiguous(kt, vt)
+            keep = (kt, vt)
+        q = to_dev(x["q"])
+        w = to_dev(x["w_o"]) if wl.value_aware else None
+        layers.append((p, q, kv, w, B.LayerBuffers(p, device=dev), keep))
+    nst = len(B.STAGES)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * nst)]
+    for e in ev:
+        e.record()
+    torch.cuda.synchronize()
+    arr = (ctypes.c_void_p * (2 * nst))(*[e.cuda_event for e in ev])
+    tot = [0.0] * nst
+    cnt = 0
+    for _ in range(args.steps):
+        for (p, q, kv, w, b, _k) in layers:
+            B.kvsel_set_stage_events(arr)
+            B.kvsel_run_layer(p, q, kv, w, b.s_attn, b.s_val, b.idx, b.counts, b.offsets, b.k_out, b.v_out, b.ws)
+            B.kvsel_set_stage_events(None)
+            torch.cuda.synchronize()
+            for i in range(nst):
+                try:
+                    tot[i] += ev[2 * i].elapsed_time(ev[2 * i + 1])
+                except RuntimeError:
+                    pass
+            cnt += 1
+    st = B.kvsel_get_device_status(layers[0][4].ws)
+    print(f"workload {wl.name} (value_aware={wl.value_aware}), {args.layers} layers x {args.steps} steps, "
+          f"device status {st}")
+    for i, name in enumerate(B.STAGES):
+        print(f"  {name:9s} {tot[i] / cnt * 1e3:9.2f} us/layer (event-timed, includes launch gaps)")
+    return 0 if st == 0 else 1
+
+
+if __name__ == "__main__":
+    sys.exit(main())
