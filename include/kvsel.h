@@ -170,6 +170,29 @@ int kvsel_run_layer(const kvsel_params* p, const void* q, const kvsel_kv* kv, co
                     float* s_val, int32_t* idx, int32_t* counts, int64_t* offsets, void* k_out, void* v_out,
                     void* ws, size_t ws_bytes, void* stream);
 
+/* ---- scoring without a caller-provided workspace --------------------------------------- */
+
+/* Size of the library's built-in scratch buffer used by kvsel_score_noalloc (16 MiB:
+ * enough for one layer of the 32K Llama-3.1-8B or 128K Qwen2.5-7B shapes). */
+#define KVSEL_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+/* kvsel_score for callers that cannot allocate device memory.  The pages have no
+ * counterpart to this call: it exists for processes whose device memory belongs to an
+ * arena or caching allocator (a serving engine that reserved its KV-cache pool up front)
+ * and for code that must not call cudaMalloc/cudaFree because they can synchronise the
+ * device.  Same arguments and results as kvsel_score minus the workspace: the scratch is
+ * a fixed KVSEL_NOALLOC_SCRATCH_BYTES buffer inside the library, held on every GPU that
+ * loads the library until the process exits.  No allocation of any kind is made.
+ *   Returns KVSEL_EWORKSPACE when the request needs more scratch than that buffer
+ *   (kvsel_workspace_size > KVSEL_NOALLOC_SCRATCH_BYTES), before any launch.
+ *   All calls share the buffer, which keeps the last call's contents (each call clears
+ *   the status word it needs at zero): calls whose GPU work overlaps race; serialise
+ *   them.  The first call on a device resolves the buffer's device address with that
+ *   device current; make it before any stream capture.  The device status word of these
+ *   calls is internal (not readable through kvsel_get_device_status). */
+int kvsel_score_noalloc(const kvsel_params* p, const void* q, const kvsel_kv* kv, const void* w_o, float* s_attn,
+                        float* s_val, void* stream);
+
 /* ---- diagnostics --------------------------------------------------------------------- */
 
 /* Synchronise `stream`, read and clear the workspace's device status word.  *status is

@@ -32,7 +32,9 @@ MAX_BATCH = 128
 
 EXPORTS = ("kvsel_workspace_size", "kvsel_output_size", "kvsel_workspace_init", "kvsel_score",
            "kvsel_select", "kvsel_compact", "kvsel_run_layer", "kvsel_get_device_status",
-           "kvsel_set_wait_limit", "kvsel_set_stage_events", "kvsel_strerror", "kvsel_version")
+           "kvsel_set_wait_limit", "kvsel_set_stage_events", "kvsel_strerror", "kvsel_version",
+           "kvsel_score_noalloc")
+NOALLOC_SCRATCH_BYTES = 16 << 20
 STAGES = ("rowstats", "keysum", "wbar", "vnorm", "finalize", "select", "compact")
 
 
@@ -97,6 +99,7 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
         "kvsel_get_device_status": ([vp, vp, ctypes.POINTER(ctypes.c_int)], ctypes.c_int),
         "kvsel_set_wait_limit": ([ctypes.c_uint64], None),
         "kvsel_set_stage_events": ([ctypes.c_void_p], None),
+        "kvsel_score_noalloc": ([P, vp, K, vp, vp, vp, vp], ctypes.c_int),
         "kvsel_strerror": ([ctypes.c_int], ctypes.c_char_p),
         "kvsel_version": ([], ctypes.c_char_p),
     }
@@ -240,6 +243,13 @@ def kvsel_score(params, q, kv: kvsel_kv, w_o, s_attn, s_val, ws, stream=None) ->
     _check(load().kvsel_score(ctypes.byref(params), _ptr(q), ctypes.byref(kv), _ptr(w_o), _ptr(s_attn),
                               _ptr(s_val), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)),
            "kvsel_score")
+
+
+def kvsel_score_noalloc(params, q, kv: kvsel_kv, w_o, s_attn, s_val, stream=None) -> None:
+    """kvsel_score with the library's built-in scratch buffer instead of a workspace, for
+    callers that cannot allocate device memory (see include/kvsel.h)."""
+    _check(load().kvsel_score_noalloc(ctypes.byref(params), _ptr(q), ctypes.byref(kv), _ptr(w_o), _ptr(s_attn),
+                                      _ptr(s_val), _stream(stream)), "kvsel_score_noalloc")
 
 
 def kvsel_select(params, s_attn, s_val, idx, counts, offsets, ws=None, stream=None) -> None:
