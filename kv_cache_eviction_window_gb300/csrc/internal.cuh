@@ -38,7 +38,12 @@ struct ChunkTable {
   int total;                      // chunks over all requests and heads
   int base[kMaxBatch + 1];        // first chunk id of request b
   int per_head[kMaxBatch];        // chunks per head of request b
+  int pbase[kMaxBatch + 1];       // first partial slot of request b (per head: per_head rounded up to 4)
 };
+
+// Row-statistics partials of (b, h): [2][R_pad][nch_pad] floats (max, sum), chunk index
+// fastest so that a row's partials are contiguous.
+__host__ __device__ inline int chunk_pad(int per_head) { return (per_head + 3) & ~3; }
 
 struct WinScoreArgs {
   ReqTable rq;
@@ -48,7 +53,7 @@ struct WinScoreArgs {
   int causal;
   int reduce;                     // KVSEL_REDUCE_*
   float s2;                       // logit scale * log2(e)
-  float* part;                    // [ck.total][2][R_pad]: row max (log2 units) and sum
+  float* part;                    // per (b, h): [2][R_pad][chunk_pad]: row max (log2 units) and sum
   float* s_raw;                   // packed [sum_b H*n_b] reduced scores
   WaitCtl wc;
 };
@@ -64,6 +69,9 @@ struct VnormArgs {
   float* nu;                      // packed [sum_b H*n_b]
   WaitCtl wc;
 };
+
+// Raise a kernel's dynamic shared-memory limit once per device (cached).
+cudaError_t ensure_smem(const void* func, size_t bytes);
 
 // Host-side launchers (return cudaError_t of the launch).
 cudaError_t launch_win_rowstats(const WinScoreArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, int mt,
@@ -96,7 +104,7 @@ struct SelectArgs {
   long long seg_out[kMaxBatch];   // output offset of request b's first segment
 };
 cudaError_t launch_select(const SelectArgs& a, int cluster, int chunk_cap, cudaStream_t st);
-int select_cluster_size(int max_len, int* chunk_cap);
+int select_cluster_size(int max_len, int segments, int* chunk_cap);
 
 struct CompactArgs {
   ReqTable rq;

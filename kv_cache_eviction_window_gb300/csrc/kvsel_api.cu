@@ -7,12 +7,34 @@
 #include <atomic>
 #include <cmath>
 #include <cstring>
+#include <map>
 #include <mutex>
 
 #include "../../include/kvsel.h"
 #include "internal.cuh"
 
 using namespace kvsel;
+
+namespace kvsel {
+cudaError_t ensure_smem(const void* func, size_t bytes) {
+  static std::mutex mu;
+  static std::map<std::pair<const void*, int>, size_t> done;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  size_t& cur = done[std::make_pair(func, dev)];
+  if (cur >= bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+  if (e == cudaSuccess) cur = bytes;
+  if (e == cudaSuccess && func != nullptr) {
+    // non-portable cluster sizes (16 CTAs) are allowed for every kernel that asks
+    cudaFuncSetAttribute(func, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    cudaGetLastError();
+  }
+  return e;
+}
+}  // namespace kvsel
 
 namespace {
 
@@ -148,14 +170,20 @@ int make_plan(const kvsel_params* p, Plan& pl, bool need_device) {
   for (int b = 0; b < pl.B; ++b) t256 += static_cast<long long>(pl.H) * ((pl.rq.n[b] + 255) / 256);
   long long tpc = (t256 + pl.num_sms - 1) / std::max(pl.num_sms, 1);
   if (tpc < 1) tpc = 1;
+  // at most 64 chunks per head (the pass-2 merge reads a row's partials in one sweep)
+  const long long min_tpc = (static_cast<long long>((pl.n_max + 255) / 256) + 63) / 64;
+  if (tpc < min_tpc) tpc = min_tpc;
   pl.ck.chunk_len = static_cast<int>(256 * tpc);
-  int cb = 0;
+  int cb = 0, pb = 0;
   for (int b = 0; b < pl.B; ++b) {
     pl.ck.base[b] = cb;
+    pl.ck.pbase[b] = pb;
     pl.ck.per_head[b] = (pl.rq.n[b] + pl.ck.chunk_len - 1) / pl.ck.chunk_len;
     cb += pl.H * pl.ck.per_head[b];
+    pb += pl.H * chunk_pad(pl.ck.per_head[b]);
   }
   pl.ck.base[pl.B] = cb;
+  pl.ck.pbase[pl.B] = pb;
   pl.ck.total = cb;
 
   const int tb = vnorm_token_block();
@@ -170,7 +198,7 @@ int make_plan(const kvsel_params* p, Plan& pl, bool need_device) {
 
   size_t off = kStatusBytes;
   pl.ws_part = off;
-  off = align256(off + static_cast<size_t>(pl.ck.total) * 2 * pl.R_pad * sizeof(float));
+  off = align256(off + static_cast<size_t>(pl.ck.pbase[pl.B]) * 2 * pl.R_pad * sizeof(float));
   pl.ws_sraw = off;
   off = align256(off + static_cast<size_t>(pl.n_scores) * sizeof(float));
   if (p->value_aware) {
@@ -374,7 +402,8 @@ int do_select(const kvsel_params* p, const Plan& pl, const float* s_attn, const 
   a.offsets = offsets;
   const int max_len = p->budget_mode == KVSEL_BUDGET_PER_LAYER ? pl.H * pl.n_max : pl.n_max;
   int cap = 0;
-  const int cs = select_cluster_size(std::max(max_len, 1), &cap);
+  const int segs = p->budget_mode == KVSEL_BUDGET_PER_LAYER ? pl.B : pl.B * pl.H;
+  const int cs = select_cluster_size(std::max(max_len, 1), segs, &cap);
   if (cs < 0) return KVSEL_EUNSUPPORTED;
   StageScope sc(KVSEL_STAGE_SELECT, st);
   return launch_rc(launch_select(a, cs, cap, st));

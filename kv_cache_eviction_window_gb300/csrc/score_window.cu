@@ -28,7 +28,6 @@ constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr int kThreads = 320;
 constexpr float kNegBig = -1.0e30f;   // finite "minus infinity" for running maxima
-constexpr float kLog2e = 1.4426950408889634f;
 
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
@@ -265,15 +264,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     epi_bar();
     if (cg == 0) {
-      float* part = a.part + static_cast<size_t>(blockIdx.x) * 2 * a.R_pad;
+      const int nch = a.ck.per_head[b], ncp = chunk_pad(nch);
+      float* part = a.part + (static_cast<size_t>(a.ck.pbase[b]) + static_cast<size_t>(h) * ncp) * 2 * a.R_pad;
+      float* pz = part + static_cast<size_t>(a.R_pad) * ncp;
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt) {
         const int r = mt * 128 + q4 * 32 + lane;
         if (r < R) {
           const float m1 = s_xm[mt][q4][lane], z1 = s_xz[mt][q4][lane];
           const float mm = fmaxf(m[mt], m1);
-          part[r] = mm;
-          part[a.R_pad + r] = z[mt] * ex2_approx(m[mt] - mm) + z1 * ex2_approx(m1 - mm);
+          part[static_cast<size_t>(r) * ncp + c] = mm;
+          pz[static_cast<size_t>(r) * ncp + c] = z[mt] * ex2_approx(m[mt] - mm) + z1 * ex2_approx(m1 - mm);
+          if (c == nch - 1)   // neutral padding after the last chunk
+            for (int j = nch; j < ncp; ++j) {
+              part[static_cast<size_t>(r) * ncp + j] = kNegBig;
+              pz[static_cast<size_t>(r) * ncp + j] = 0.f;
+            }
         }
       }
     }
@@ -390,19 +396,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ---------------- epilogue: warps 0-7 ----------------
-    // merged row statistics c2[r] = m_r + log2 Z_r  (log2 units)
+    // merged row statistics c2[r] = m_r + log2 Z_r  (log2 units); a row's chunk
+    // partials are contiguous, read as float4
     {
-      const int nch = a.ck.per_head[b];
-      const float* part = a.part + static_cast<size_t>(a.ck.base[b] + h * nch) * 2 * RP;
+      const int ncp = chunk_pad(a.ck.per_head[b]);
+      const float* pm = a.part + (static_cast<size_t>(a.ck.pbase[b]) + static_cast<size_t>(h) * ncp) * 2 * RP;
+      const float* pz = pm + static_cast<size_t>(RP) * ncp;
       for (int r = threadIdx.x; r < RP; r += kEpiWarps * 32) {
         float c2 = 0.f;
         if (r < R) {
+          const float4* m4 = reinterpret_cast<const float4*>(pm + static_cast<size_t>(r) * ncp);
+          const float4* z4 = reinterpret_cast<const float4*>(pz + static_cast<size_t>(r) * ncp);
           float mm = kNegBig;
-          for (int j = 0; j < nch; ++j) mm = fmaxf(mm, part[static_cast<size_t>(j) * 2 * RP + r]);
+#pragma unroll 4
+          for (int j = 0; j < ncp / 4; ++j) {
+            const float4 v = m4[j];
+            mm = fmaxf(mm, fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)));
+          }
           float zz = 0.f;
-          for (int j = 0; j < nch; ++j) {
-            const float* pj = part + static_cast<size_t>(j) * 2 * RP;
-            zz += pj[RP + r] * ex2_approx(pj[r] - mm);
+#pragma unroll 4
+          for (int j = 0; j < ncp / 4; ++j) {
+            const float4 v = m4[j], w = z4[j];
+            zz += w.x * ex2_approx(v.x - mm) + w.y * ex2_approx(v.y - mm) + w.z * ex2_approx(v.z - mm) +
+                  w.w * ex2_approx(v.w - mm);
           }
           c2 = mm + lg2_approx(zz);
         }
@@ -494,8 +510,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int MT, int NT, int STAGES>
 cudaError_t launch_rowstats_t(const WinScoreArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, cudaStream_t st) {
   const size_t smem = 1024 + 2 * MT * 128 * 128 + STAGES * NT * 256;
-  cudaError_t e = cudaFuncSetAttribute(win_rowstats_kernel<MT, NT, STAGES>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  cudaError_t e = ensure_smem(reinterpret_cast<const void*>(win_rowstats_kernel<MT, NT, STAGES>), smem);
   if (e != cudaSuccess) return e;
   win_rowstats_kernel<MT, NT, STAGES><<<a.ck.total, kThreads, smem, st>>>(tq, tk, a);
   return cudaGetLastError();
@@ -524,8 +539,7 @@ cudaError_t launch_win_keysum(const WinScoreArgs& a, const CUtensorMap& tq, cons
   stages = stages > 4 ? 4 : stages;
   if (stages < 2) return cudaErrorInvalidValue;
   const size_t smem = fixed + static_cast<size_t>(stages) * kKTileBytes;
-  cudaError_t e =
-      cudaFuncSetAttribute(win_keysum_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  cudaError_t e = ensure_smem(reinterpret_cast<const void*>(win_keysum_kernel), smem);
   if (e != cudaSuccess) return e;
   win_keysum_kernel<<<a.ck.total, kThreads, smem, st>>>(tq, tk, a, stages, nacc, cols);
   return cudaGetLastError();

@@ -15,6 +15,10 @@
 // scan gives each kept entry its output slot, so indices come out ascending.
 #include <cooperative_groups.h>
 
+#include <map>
+#include <mutex>
+#include <tuple>
+
 #include "internal.cuh"
 
 namespace cgx = cooperative_groups;
@@ -27,6 +31,7 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kBins = 2048;
 constexpr uint32_t kKeyMax = 0xFFFFFFFFu;
 constexpr int kMaxHeads = 64;
+static_assert(kBins == 4 * kThreads, "digit search: four bins per thread");
 
 __device__ __forceinline__ uint32_t f2key(float f) {
   const uint32_t u = __float_as_uint(f);
@@ -34,14 +39,26 @@ __device__ __forceinline__ uint32_t f2key(float f) {
 }
 
 struct SelShared {
-  uint32_t hist[kBins];       // local histogram of the current pass
-  uint32_t mslice[kBins];     // merged bins owned by this CTA (first kBins / cluster)
-  uint32_t slice_total;
-  uint32_t cnt_gt, cnt_eq;    // local counts for the current selection
+  uint32_t hist[kBins];       // this CTA's histogram of the current pass
+  uint32_t merged[3][kBins];  // cluster-wide histogram, pushed by every CTA; one buffer per pass mod 3
+  uint32_t cnt[2][16][2];     // (greater, equal) counts of every CTA, pushed by each; one buffer per selection mod 2
   uint32_t res_prefix, res_krem;
   uint32_t wsum_gt[kWarps], wsum_eq[kWarps];
   uint32_t head_cnt[kMaxHeads];
 };
+
+// Address of `p` (this CTA's shared memory) in the shared memory of cluster CTA `rank`.
+__device__ __forceinline__ uint32_t cluster_addr(const void* p, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void red_add_cluster(uint32_t addr, uint32_t v) {
+  asm volatile("red.relaxed.cluster.shared::cluster.add.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ void st_cluster(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
 
 // Block-wide exclusive scan of two counters (one pair per thread).
 __device__ __forceinline__ void block_excl_scan2(SelShared& S, uint32_t a, uint32_t b, uint32_t& ea, uint32_t& eb,
@@ -78,22 +95,34 @@ __device__ __forceinline__ void block_excl_scan2(SelShared& S, uint32_t a, uint3
   __syncthreads();
 }
 
-// Find the key T of the K-th largest candidate among elements [lo, hi) of the segment
-// (local chunk positions given by my_lo/my_hi, already intersected), and how many keys
-// equal to T are taken (krem).  Candidates: keys[] in shared memory.
-__device__ void radix_select(cgx::cluster_group& cl, SelShared& S, const uint32_t* keys, int cnt_local, uint32_t K,
-                            uint32_t& T, uint32_t& krem_out) {
+// Per-kernel pass / selection counters (identical in every CTA of the cluster), used to
+// rotate the shared-memory buffers that other CTAs write or read.
+struct SelState {
+  int pass = 0;
+  int sel = 0;
+};
+
+// Key T of the K-th largest candidate among keys[0, cnt_local) of every CTA, and the
+// number of keys equal to T that are taken (krem).  Each pass: a local histogram, then
+// every CTA adds its non-empty bins into every CTA's copy of the cluster histogram with
+// cluster-scope reductions; after one cluster barrier each CTA finds the digit in its
+// own shared memory.
+__device__ void radix_select(cgx::cluster_group& cl, SelShared& S, SelState& st, const uint32_t* keys,
+                             int cnt_local, uint32_t K, uint32_t& T, uint32_t& krem_out) {
   const unsigned CS = cl.num_blocks();
-  const unsigned rank = cl.block_rank();
-  const int slice = kBins / static_cast<int>(CS);
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   uint32_t prefix = 0, mask = 0, krem = K;
   const int shifts[3] = {21, 10, 0};
   const int widths[3] = {11, 11, 10};
-  for (int pass = 0; pass < 3; ++pass) {
+  for (int pass = 0; pass < 3; ++pass, ++st.pass) {
+    const int buf = st.pass % 3, nxt = (st.pass + 1) % 3;
     const int sh = shifts[pass];
     const uint32_t dmask = (1u << widths[pass]) - 1u;
-    for (int i = threadIdx.x; i < kBins; i += kThreads) S.hist[i] = 0;
+    // the next pass's buffer was last read two barriers ago
+    for (int i = threadIdx.x; i < kBins; i += kThreads) {
+      S.merged[nxt][i] = 0;
+      S.hist[i] = 0;
+    }
     __syncthreads();
     const int trips = (cnt_local + kThreads - 1) / kThreads;
     for (int j = 0; j < trips; ++j) {
@@ -106,152 +135,127 @@ __device__ void radix_select(cgx::cluster_group& cl, SelShared& S, const uint32_
       const unsigned peers = __match_any_sync(0xffffffffu, dig);
       if (dig != 0xFFFFFFFFu && lane == __ffs(peers) - 1) atomicAdd(&S.hist[dig], static_cast<uint32_t>(__popc(peers)));
     }
-    cl.sync();
-    // reduce my slice of bins over the cluster
-    uint32_t my_tot = 0;
-    for (int i = threadIdx.x; i < slice; i += kThreads) {
-      const int bin = static_cast<int>(rank) * slice + i;
-      uint32_t s = 0;
-      for (unsigned c = 0; c < CS; ++c) s += cl.map_shared_rank(&S.hist[0], c)[bin];
-      S.mslice[i] = s;
-      my_tot += s;
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) my_tot += __shfl_xor_sync(0xffffffffu, my_tot, o);
-    if (threadIdx.x == 0) S.slice_total = 0;
     __syncthreads();
-    if (lane == 0 && my_tot) atomicAdd(&S.slice_total, my_tot);
+    for (int bin = threadIdx.x; bin < kBins; bin += kThreads) {
+      const uint32_t c = S.hist[bin];
+      if (c)
+        for (unsigned r = 0; r < CS; ++r) red_add_cluster(cluster_addr(&S.merged[buf][bin], r), c);
+    }
     cl.sync();
-    // every CTA locates the digit (warp 0)
-    if (w == 0) {
-      // slice totals, highest slice first
-      uint32_t tot = (lane < static_cast<int>(CS)) ? cl.map_shared_rank(&S.slice_total, lane)[0] : 0u;
-      // suffix sums over slices: sum of totals of slices > lane
-      uint32_t incl = tot;
+    {
+      // thread t owns bins [4t, 4t + 4) (one 16-byte load, conflict-free); a block-wide
+      // suffix scan of the 512 group sums finds the group holding the krem-th largest
+      const uint4 hv = reinterpret_cast<const uint4*>(S.merged[buf])[threadIdx.x];
+      const uint32_t gsum = hv.x + hv.y + hv.z + hv.w;
+      // exclusive prefix from the top: sum over groups with a larger index
+      uint32_t incl = gsum;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const uint32_t x = __shfl_down_sync(0xffffffffu, incl, o);
         if (lane + o < 32) incl += x;
       }
-      const uint32_t above = incl - tot;  // sum over slices with index > lane
-      const bool hit = (lane < static_cast<int>(CS)) && above < krem && krem <= incl;
-      const unsigned hm = __ballot_sync(0xffffffffu, hit);
-      const int cs = __ffs(hm) - 1;       // exactly one slice qualifies
-      const uint32_t above_s = __shfl_sync(0xffffffffu, above, cs < 0 ? 0 : cs);
-      uint32_t kr = krem - above_s;
-      // bins of slice cs, highest first: lane l holds bins [l*per, (l+1)*per)
-      const int per = slice / 32;
-      const uint32_t* rb = cl.map_shared_rank(&S.mslice[0], cs < 0 ? 0 : cs);
-      uint32_t loc[8];
-      uint32_t lsum = 0;
-      for (int i = 0; i < per; ++i) {
-        loc[i] = rb[lane * per + i];
-        lsum += loc[i];
-      }
-      uint32_t lincl = lsum;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t x = __shfl_down_sync(0xffffffffu, lincl, o);
-        if (lane + o < 32) lincl += x;
-      }
-      const uint32_t labove = lincl - lsum;
-      const bool lhit = labove < kr && kr <= lincl;
-      const unsigned lm = __ballot_sync(0xffffffffu, lhit);
-      const int ls = __ffs(lm) - 1;
-      if (lane == ls) {
-        uint32_t cum = labove;
-        int digit = lane * per;
-        for (int i = per - 1; i >= 0; --i) {
-          if (cum + loc[i] >= kr) {
-            digit = lane * per + i;
+      if (lane == 0) S.wsum_gt[w] = incl;   // warp total
+      __syncthreads();
+      uint32_t above_w = 0;
+      for (int i = w + 1; i < kWarps; ++i) above_w += S.wsum_gt[i];
+      const uint32_t above = above_w + incl - gsum;
+      if (above < krem && krem <= above + gsum) {
+        const uint32_t b4[4] = {hv.x, hv.y, hv.z, hv.w};
+        uint32_t cum = above;
+        int digit = threadIdx.x * 4;
+        for (int i = 3; i >= 0; --i) {
+          if (cum + b4[i] >= krem) {
+            digit = threadIdx.x * 4 + i;
             break;
           }
-          cum += loc[i];
+          cum += b4[i];
         }
-        S.res_prefix = prefix | (static_cast<uint32_t>(cs * slice + digit) << sh);
-        S.res_krem = kr - cum;
+        S.res_prefix = prefix | (static_cast<uint32_t>(digit) << sh);
+        S.res_krem = krem - cum;
       }
     }
     __syncthreads();
     prefix = S.res_prefix;
     krem = S.res_krem;
     mask |= dmask << sh;
-    __syncthreads();
   }
   T = prefix;
   krem_out = krem;
 }
 
-// Walk the local chunk in index order and visit every kept entry with its slot in the
-// segment-wide ascending order.  Returns nothing; `visit(e_local, slot)`.
+// Walk the local chunk [lo_local, hi_local) in index order and visit every kept entry
+// with its slot in the segment-wide ascending order: `visit(e_local, slot)`.  Each warp
+// owns a contiguous run of the chunk and reads it lane-interleaved; ranks come from
+// ballots, so shared-memory reads are conflict-free and slots are assigned in order.
 template <typename Visit>
-__device__ void apply_selection(cgx::cluster_group& cl, SelShared& S, const uint32_t* keys, int lo_local,
-                                int hi_local, uint32_t T, uint32_t krem, Visit visit) {
+__device__ void apply_selection(cgx::cluster_group& cl, SelShared& S, SelState& st, const uint32_t* keys,
+                                int lo_local, int hi_local, uint32_t T, uint32_t krem, Visit visit) {
   const unsigned CS = cl.num_blocks();
   const unsigned rank = cl.block_rank();
-  const int lane = threadIdx.x & 31;
-  const int cnt = hi_local - lo_local;
-  const int per = cnt > 0 ? (cnt + kThreads - 1) / kThreads : 0;
-  const int a = lo_local + min(cnt, static_cast<int>(threadIdx.x) * per);
-  const int b = lo_local + min(cnt, static_cast<int>(threadIdx.x + 1) * per);
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const unsigned lt = (1u << lane) - 1u;
+  const int sb = st.sel & 1;
+  ++st.sel;
+  const int cnt = max(hi_local - lo_local, 0);
+  const int per_w = ((cnt + kWarps - 1) / kWarps + 31) & ~31;
+  const int wa = lo_local + min(cnt, w * per_w);
+  const int wb = lo_local + min(cnt, (w + 1) * per_w);
   uint32_t ngt = 0, neq = 0;
-  for (int e = a; e < b; ++e) {
-    const uint32_t k = keys[e];
-    ngt += (k > T);
-    neq += (k == T);
+  for (int e0 = wa; e0 < wb; e0 += 32) {
+    const int e = e0 + lane;
+    const uint32_t k = e < wb ? keys[e] : 0u;
+    ngt += __popc(__ballot_sync(0xffffffffu, e < wb && k > T));
+    neq += __popc(__ballot_sync(0xffffffffu, e < wb && k == T));
   }
+  // per-warp totals -> exclusive prefix over warps (lane 0 of each warp contributes)
   uint32_t egt, eeq, tgt, teq;
-  block_excl_scan2(S, ngt, neq, egt, eeq, tgt, teq);
-  if (threadIdx.x == 0) {
-    S.cnt_gt = tgt;
-    S.cnt_eq = teq;
+  block_excl_scan2(S, lane == 0 ? ngt : 0u, lane == 0 ? neq : 0u, egt, eeq, tgt, teq);
+  egt = __shfl_sync(0xffffffffu, egt, 0);
+  eeq = __shfl_sync(0xffffffffu, eeq, 0);
+  if (threadIdx.x < CS) {
+    st_cluster(cluster_addr(&S.cnt[sb][rank][0], threadIdx.x), tgt);
+    st_cluster(cluster_addr(&S.cnt[sb][rank][1], threadIdx.x), teq);
   }
   cl.sync();
-  // cluster exclusive prefix over CTA ranks
-  uint32_t base_out = 0, eq_base = 0;
-  {
-    uint32_t g = 0, q = 0;
-    if (lane < static_cast<int>(CS) && lane < static_cast<int>(rank)) {
-      g = cl.map_shared_rank(&S.cnt_gt, lane)[0];
-      q = cl.map_shared_rank(&S.cnt_eq, lane)[0];
-    }
-    // eq_base of each lower CTA is needed to know how many of its equals were taken;
-    // compute prefix of q across lanes
-    uint32_t qincl = q;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t x = __shfl_up_sync(0xffffffffu, qincl, o);
-      if (lane >= o) qincl += x;
-    }
-    const uint32_t qexcl = qincl - q;
-    const uint32_t avail = krem > qexcl ? krem - qexcl : 0u;
-    const uint32_t take = q < avail ? q : avail;
-    uint32_t sel = g + take;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) sel += __shfl_xor_sync(0xffffffffu, sel, o);
-    uint32_t qs = q;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) qs += __shfl_xor_sync(0xffffffffu, qs, o);
-    base_out = sel;
-    eq_base = qs;
+  // exclusive prefix over lower-ranked CTAs (lane c holds CTA c's counts)
+  uint32_t g = 0, q = 0;
+  if (lane < static_cast<int>(rank)) {
+    g = S.cnt[sb][lane][0];
+    q = S.cnt[sb][lane][1];
   }
-  // equals taken before this thread
-  const uint32_t avail_cta = krem > eq_base ? krem - eq_base : 0u;
-  const uint32_t taken_before = eeq < avail_cta ? eeq : avail_cta;
-  uint32_t slot = base_out + egt + taken_before;
-  uint32_t eq_rank = eq_base + eeq;
-  for (int e = a; e < b; ++e) {
-    const uint32_t k = keys[e];
-    bool take = false;
-    if (k > T) {
-      take = true;
-    } else if (k == T) {
-      take = eq_rank < krem;
-      ++eq_rank;
-    }
-    if (take) visit(e, slot++);
+  uint32_t qincl = q;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t x = __shfl_up_sync(0xffffffffu, qincl, o);
+    if (lane >= o) qincl += x;
   }
-  cl.sync();   // counters are reused by the next selection
+  const uint32_t qexcl = qincl - q;
+  const uint32_t avail = krem > qexcl ? krem - qexcl : 0u;
+  uint32_t sel = g + (q < avail ? q : avail);
+  uint32_t qs = q;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    sel += __shfl_xor_sync(0xffffffffu, sel, o);
+    qs += __shfl_xor_sync(0xffffffffu, qs, o);
+  }
+  (void)CS;
+  // equals of earlier CTAs and earlier warps come first
+  uint32_t eq_rank = qs + eeq;
+  const uint32_t avail_w = krem > qs ? krem - qs : 0u;
+  uint32_t slot = sel + egt + (eeq < avail_w ? eeq : avail_w);
+  for (int e0 = wa; e0 < wb; e0 += 32) {
+    const int e = e0 + lane;
+    const uint32_t k = e < wb ? keys[e] : 0u;
+    const bool gt = e < wb && k > T;
+    const bool eq = e < wb && k == T;
+    const unsigned meq = __ballot_sync(0xffffffffu, eq);
+    const bool take = gt || (eq && eq_rank + __popc(meq & lt) < krem);
+    const unsigned mtake = __ballot_sync(0xffffffffu, take);
+    if (take) visit(e, slot + __popc(mtake & lt));
+    slot += __popc(mtake);
+    eq_rank += __popc(meq);
+  }
+  __syncthreads();   // visits (flags, counters) are complete before the caller reads them
 }
 
 __global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelectArgs a, int chunk_cap) {
@@ -279,31 +283,56 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelectArgs a,
   const int nforced = min(n, ns + nr);
 
   // stage-1 keys (forced entries at the top)
-  for (int e = threadIdx.x; e < cnt; e += kThreads) {
-    const int g = c_lo + e;
-    const int i = per_layer ? g % n : g;
-    const bool forced = (i < ns) || (i >= n - nr);
-    keys[e] = forced ? kKeyMax : f2key(__ldg(a.s1 + sbase + g));
-    flag[e] = 0;
+  for (int e0 = 0; e0 < cnt; e0 += 4 * kThreads) {
+    float v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int e = e0 + u * kThreads + threadIdx.x;
+      v[u] = e < cnt ? __ldg(a.s1 + sbase + c_lo + e) : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int e = e0 + u * kThreads + threadIdx.x;
+      if (e < cnt) {
+        const int g = c_lo + e;
+        const int i = per_layer ? g % n : g;
+        const bool forced = (i < ns) || (i >= n - nr);
+        keys[e] = forced ? kKeyMax : f2key(v[u]);
+        flag[e] = 0;
+      }
+    }
   }
   if (threadIdx.x < kMaxHeads) S.head_cnt[threadIdx.x] = 0;
-  __syncthreads();
+  for (int i = threadIdx.x; i < 3 * kBins; i += kThreads) (&S.merged[0][0])[i] = 0;
+  SelState sst;
+  cl.sync();   // every CTA's buffers are zero before any remote reduction lands
 
   uint32_t T, krem;
   if (!per_layer) {
     const uint32_t B = static_cast<uint32_t>(a.budget[b]);
     if (a.two_stage) {
       // stage 1: b' = max(floor(alpha*B), |F|) entries by the attention score
-      radix_select(cl, S, keys, cnt, static_cast<uint32_t>(a.budget1[b]), T, krem);
-      apply_selection(cl, S, keys, 0, cnt, T, krem, [&](int e, uint32_t) { flag[e] = 1; });
+      radix_select(cl, S, sst, keys, cnt, static_cast<uint32_t>(a.budget1[b]), T, krem);
+      apply_selection(cl, S, sst, keys, 0, cnt, T, krem, [&](int e, uint32_t) { flag[e] = 1; });
       // stage 2: the remaining B - b' by the value-aware score, stage-1 picks forced in
-      for (int e = threadIdx.x; e < cnt; e += kThreads)
-        keys[e] = flag[e] ? kKeyMax : f2key(__ldg(a.s2 + sbase + c_lo + e));
+      for (int e0 = 0; e0 < cnt; e0 += 4 * kThreads) {
+        float v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int e = e0 + u * kThreads + threadIdx.x;
+          v[u] = e < cnt ? __ldg(a.s2 + sbase + c_lo + e) : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int e = e0 + u * kThreads + threadIdx.x;
+          if (e < cnt) keys[e] = flag[e] ? kKeyMax : f2key(v[u]);
+        }
+      }
       __syncthreads();
     }
-    radix_select(cl, S, keys, cnt, B, T, krem);
+    radix_select(cl, S, sst, keys, cnt, B, T, krem);
     const long long out0 = a.seg_out[b] + static_cast<long long>(h0) * B;
-    apply_selection(cl, S, keys, 0, cnt, T, krem, [&](int e, uint32_t slot) {
+    apply_selection(cl, S, sst, keys, 0, cnt, T, krem, [&](int e, uint32_t slot) {
       if (slot < B) a.idx[out0 + slot] = c_lo + e;
     });
     if (rank == 0 && threadIdx.x == 0) {
@@ -318,19 +347,19 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelectArgs a,
       for (int hh = 0; hh < H; ++hh) {
         const int lo = min(max(hh * n - c_lo, 0), cnt);
         const int hi = min(max((hh + 1) * n - c_lo, 0), cnt);
-        radix_select(cl, S, keys + lo, hi - lo, static_cast<uint32_t>(fh), T, krem);
-        apply_selection(cl, S, keys, lo, hi, T, krem, [&](int e, uint32_t) { flag[e] = 1; });
+        radix_select(cl, S, sst, keys + lo, hi - lo, static_cast<uint32_t>(fh), T, krem);
+        apply_selection(cl, S, sst, keys, lo, hi, T, krem, [&](int e, uint32_t) { flag[e] = 1; });
       }
       for (int e = threadIdx.x; e < cnt; e += kThreads)
         if (flag[e]) keys[e] = kKeyMax;
       __syncthreads();
     }
     const uint32_t BL = static_cast<uint32_t>(a.budget[b]);
-    radix_select(cl, S, keys, cnt, BL, T, krem);
+    radix_select(cl, S, sst, keys, cnt, BL, T, krem);
     const long long out0 = a.seg_out[b];
     int cur_h = -1;
     uint32_t cur_c = 0;
-    apply_selection(cl, S, keys, 0, cnt, T, krem, [&](int e, uint32_t slot) {
+    apply_selection(cl, S, sst, keys, 0, cnt, T, krem, [&](int e, uint32_t slot) {
       const int g = c_lo + e;
       const int hh = g / n;
       if (slot < BL) a.idx[out0 + slot] = g - hh * n;
@@ -364,14 +393,44 @@ size_t select_smem(int chunk_cap) {
 
 }  // namespace
 
-int select_cluster_size(int max_len, int* chunk_cap) {
+// Cluster size for `segments` segments of at most `max_len` entries: the largest of
+// 16 / 8 CTAs whose clusters all fit on the device at once (a cluster must sit inside one
+// GPC), else the one that keeps the most CTAs busy in the first wave.
+int select_cluster_size_uncached(int max_len, int segments, int* chunk_cap);
+
+int select_cluster_size(int max_len, int segments, int* chunk_cap) {
+  static std::mutex mu;
+  static std::map<std::tuple<int, int, int>, std::pair<int, int>> cache;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const auto key = std::make_tuple(dev, max_len, segments);
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = cache.find(key);
+    if (it != cache.end()) {
+      *chunk_cap = it->second.second;
+      return it->second.first;
+    }
+  }
+  int cap = 0;
+  const int cs = select_cluster_size_uncached(max_len, segments, &cap);
+  if (cs > 0) {
+    std::lock_guard<std::mutex> lock(mu);
+    cache[key] = std::make_pair(cs, cap);
+    *chunk_cap = cap;
+  }
+  return cs;
+}
+
+int select_cluster_size_uncached(int max_len, int segments, int* chunk_cap) {
   const size_t limit = 232448 - 1024;
+  int best_cs = -1, best_cap = 0;
+  long long best_busy = -1;
   for (int cs = 16; cs >= 8; cs >>= 1) {
     const int cap = (max_len + cs - 1) / cs;
     const int cap16 = ((cap + 15) & ~15) > 16 ? ((cap + 15) & ~15) : 16;
     const size_t smem = select_smem(cap16);
     if (smem > limit) continue;
-    // the cluster must be schedulable on this device with that much shared memory
     if (cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
         cudaSuccess)
       continue;
@@ -388,25 +447,30 @@ int select_cluster_size(int max_len, int* chunk_cap) {
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    int nclusters = 0;
-    if (cudaOccupancyMaxActiveClusters(&nclusters, select_kernel, &cfg) != cudaSuccess || nclusters < 1) {
+    int active = 0;
+    if (cudaOccupancyMaxActiveClusters(&active, select_kernel, &cfg) != cudaSuccess || active < 1) {
       cudaGetLastError();
       continue;
     }
-    *chunk_cap = cap16;
-    return cs;
+    if (active >= segments) {   // all segments at once: take the largest such cluster
+      *chunk_cap = cap16;
+      return cs;
+    }
+    const long long busy = static_cast<long long>(active) * cs;
+    if (busy > best_busy) {
+      best_busy = busy;
+      best_cs = cs;
+      best_cap = cap16;
+    }
   }
-  return -1;
+  if (best_cs > 0) *chunk_cap = best_cap;
+  return best_cs;
 }
 
 cudaError_t launch_select(const SelectArgs& a, int cluster, int chunk_cap, cudaStream_t st) {
   const size_t smem = select_smem(chunk_cap);
-  cudaError_t e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  cudaError_t e = ensure_smem(reinterpret_cast<const void*>(select_kernel), smem);
   if (e != cudaSuccess) return e;
-  if (cluster > 8) {
-    e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    if (e != cudaSuccess) return e;
-  }
   const int segs = (a.mode == 1) ? a.rq.B : a.rq.B * a.rq.H;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(cluster, segs, 1);

@@ -291,7 +291,7 @@ cudaError_t launch_wbar(const uint16_t* w_o, uint16_t* wbar, int H, int G, int D
 cudaError_t launch_vnorm(const VnormArgs& a, const CUtensorMap& tv, const CUtensorMap& tw, cudaStream_t st) {
   if (a.units_total <= 0) return cudaSuccess;
   const size_t smem = 1024 + kVBuf * kVTile + kWStages * kWTile;
-  cudaError_t e = cudaFuncSetAttribute(vnorm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  cudaError_t e = ensure_smem(reinterpret_cast<const void*>(vnorm_kernel), smem);
   if (e != cudaSuccess) return e;
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
