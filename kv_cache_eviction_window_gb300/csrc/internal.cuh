@@ -58,6 +58,24 @@ struct WinScoreArgs {
   WaitCtl wc;
 };
 
+// Query-agnostic scoring (all G*n query rows of a KV head, non-causal, max reduction).
+struct QaArgs {
+  int H;                          // KV heads
+  int n;                          // keys (context length)
+  int GN;                         // query rows per head (G * n)
+  int row_blocks;                 // pass 1: blocks of 512 query rows per head
+  int key_blocks;                 // pass 2: blocks of 512 keys per head
+  int row_splits;                 // pass 2: query-row slices per key block
+  float s2;                       // logit scale * log2(e)
+  float* c2;                      // [H][GN] row log-sum-exp, log2 units
+  uint32_t* tmax;                 // [H][n] order-preserving keys of max_r (l*s2 - c2_r)
+  float* s_raw;                   // [H][n] exp2 of that max
+  WaitCtl wc;
+};
+cudaError_t launch_qa_rowlse(const QaArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, cudaStream_t st);
+cudaError_t launch_qa_keymax(const QaArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, cudaStream_t st);
+int qa_block_rows();
+
 struct VnormArgs {
   ReqTable rq;
   KvSource src;

@@ -70,6 +70,8 @@ struct Plan {
   int units_total = 0, unit_base[kMaxBatch + 1]{}, blocks_per_head[kMaxBatch]{};
   int num_sms = 0;
   size_t ws_part = 0, ws_sraw = 0, ws_nu = 0, ws_wbar = 0, ws_total = 0;
+  size_t ws_c2 = 0, ws_tmax = 0;   // query-agnostic scoring
+  int qa_row_blocks = 0, qa_key_blocks = 0, qa_row_splits = 0;
 };
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -120,14 +122,21 @@ int make_plan(const kvsel_params* p, Plan& pl, bool need_device) {
   pl.n_scores = so;
   if (so > (1ll << 31) - 1) return KVSEL_EUNSUPPORTED;
   if (pl.qa) {
-    return KVSEL_EUNSUPPORTED;   // query-agnostic scoring is served by its own entry (not in this build)
+    // KVzip's query-agnostic score: one request, all G*n positions as queries, no causal
+    // mask, max over queries and group heads
+    if (pl.B != 1 || p->causal || p->reduce != KVSEL_REDUCE_MAX || p->value_aware || p->q_chunk < 0)
+      return KVSEL_EUNSUPPORTED;
+    if (static_cast<long long>(pl.G) * pl.n_max > (1ll << 30)) return KVSEL_EUNSUPPORTED;
+    pl.R = 0;
+    pl.R_pad = 64;
+  } else {
+    for (int b = 0; b < pl.B; ++b)
+      if (pl.rq.n[b] > 0 && pl.W > pl.rq.n[b]) return KVSEL_EINVAL;
+    pl.R = pl.G * pl.W;
+    if (pl.R > 512 || pl.R % 32 != 0) return KVSEL_EUNSUPPORTED;
+    pl.R_pad = (pl.R + 63) / 64 * 64;
+    pl.mt = pl.R <= 128 ? 1 : (pl.R <= 256 ? 2 : 4);
   }
-  for (int b = 0; b < pl.B; ++b)
-    if (pl.rq.n[b] > 0 && pl.W > pl.rq.n[b]) return KVSEL_EINVAL;
-  pl.R = pl.G * pl.W;
-  if (pl.R > 512 || pl.R % 32 != 0) return KVSEL_EUNSUPPORTED;
-  pl.R_pad = (pl.R + 63) / 64 * 64;
-  pl.mt = pl.R <= 128 ? 1 : (pl.R <= 256 ? 2 : 4);
   pl.Dw = p->value_aware ? (p->wo_mode == KVSEL_WO_PER_HEAD ? pl.G * pl.D : pl.D) : 0;
 
   // budgets and output layout
@@ -197,6 +206,24 @@ int make_plan(const kvsel_params* p, Plan& pl, bool need_device) {
   pl.units_total = p->value_aware ? ub : 0;
 
   size_t off = kStatusBytes;
+  if (pl.qa) {
+    const int n = pl.rq.n[0];
+    const long long GN = static_cast<long long>(pl.G) * n;
+    const int br = qa_block_rows();
+    pl.qa_row_blocks = static_cast<int>((GN + br - 1) / br);
+    pl.qa_key_blocks = (n + br - 1) / br;
+    const long long want = 8ll * pl.num_sms;
+    const long long base = static_cast<long long>(pl.H) * std::max(pl.qa_key_blocks, 1);
+    pl.qa_row_splits = static_cast<int>(std::min<long long>(64, std::max<long long>(1, (want + base - 1) / base)));
+    pl.ws_c2 = off;
+    off = align256(off + static_cast<size_t>(pl.H) * GN * sizeof(float));
+    pl.ws_tmax = off;
+    off = align256(off + static_cast<size_t>(pl.n_scores) * sizeof(uint32_t));
+    pl.ws_sraw = off;
+    off = align256(off + static_cast<size_t>(pl.n_scores) * sizeof(float));
+    pl.ws_total = off;
+    return KVSEL_OK;
+  }
   pl.ws_part = off;
   off = align256(off + static_cast<size_t>(pl.ck.pbase[pl.B]) * 2 * pl.R_pad * sizeof(float));
   pl.ws_sraw = off;
@@ -304,6 +331,41 @@ int do_score(const kvsel_params* p, const Plan& pl, const void* q, const kvsel_k
   float* part = reinterpret_cast<float*>(wsb + pl.ws_part);
   float* s_raw = reinterpret_cast<float*>(wsb + pl.ws_sraw);
   if (pl.n_scores == 0) return KVSEL_OK;
+  const float scale = p->scale > 0.f ? p->scale : 1.f / std::sqrt(static_cast<float>(kHeadDim));
+  if (pl.qa) {
+    const int n = pl.rq.n[0];
+    CUtensorMap tq, tk64, tk128;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(pl.H) * pl.G * n};
+    const cuuint64_t strides[1] = {kHeadDim * 2};
+    const cuuint32_t box[2] = {64, 64};
+    if (!encode(&tq, q, 2, dims, strides, box)) return KVSEL_EINVAL;
+    if (!kv_map(&tk64, kv->k, kv, pl, 64) || !kv_map(&tk128, kv->k, kv, pl, 128)) return KVSEL_EINVAL;
+    QaArgs a{};
+    a.H = pl.H;
+    a.n = n;
+    a.GN = pl.G * n;
+    a.row_blocks = pl.qa_row_blocks;
+    a.key_blocks = pl.qa_key_blocks;
+    a.row_splits = pl.qa_row_splits;
+    a.s2 = scale * 1.4426950408889634f;
+    a.c2 = reinterpret_cast<float*>(wsb + pl.ws_c2);
+    a.tmax = reinterpret_cast<uint32_t*>(wsb + pl.ws_tmax);
+    a.s_raw = s_raw;
+    a.wc = wait_ctl(ws);
+    int rc;
+    {
+      StageScope sc(KVSEL_STAGE_ROWSTATS, st);
+      rc = launch_rc(launch_qa_rowlse(a, tq, tk64, st));
+    }
+    if (rc) return rc;
+    {
+      StageScope sc(KVSEL_STAGE_KEYSUM, st);
+      rc = launch_rc(launch_qa_keymax(a, tq, tk128, st));
+    }
+    if (rc) return rc;
+    StageScope sc(KVSEL_STAGE_FINALIZE, st);
+    return launch_rc(launch_finalize(pl.rq, s_raw, nullptr, s_attn, nullptr, p->pool, p->pool_kernel, p->eps, st));
+  }
 
   CUtensorMap tq, tk1, tk2;
   {
@@ -326,7 +388,6 @@ int do_score(const kvsel_params* p, const Plan& pl, const void* q, const kvsel_k
   a.R_pad = pl.R_pad;
   a.causal = p->causal ? 1 : 0;
   a.reduce = p->reduce;
-  const float scale = p->scale > 0.f ? p->scale : 1.f / std::sqrt(static_cast<float>(kHeadDim));
   a.s2 = scale * 1.4426950408889634f;
   a.part = part;
   a.s_raw = s_raw;
@@ -487,6 +548,7 @@ int kvsel_score(const kvsel_params* p, const void* q, const kvsel_kv* kv, const 
   if (!q || !aligned16(q) || !s_attn) return KVSEL_EINVAL;
   if (p->value_aware && (!w_o || !aligned16(w_o) || !s_val)) return KVSEL_EINVAL;
   if ((rc = check_kv(kv, pl, p->value_aware != 0))) return rc;
+  if (pl.qa && kv->layout != KVSEL_LAYOUT_CONTIGUOUS) return KVSEL_EUNSUPPORTED;
   if ((rc = check_ws(pl, ws, ws_bytes))) return rc;
   return do_score(p, pl, q, kv, w_o, s_attn, s_val, ws, static_cast<cudaStream_t>(stream));
 }
@@ -525,6 +587,7 @@ int kvsel_run_layer(const kvsel_params* p, const void* q, const kvsel_kv* kv, co
   if (!aligned16(k_out) || !aligned16(v_out)) return KVSEL_EINVAL;
   if (p->value_aware && (!w_o || !aligned16(w_o) || !s_val)) return KVSEL_EINVAL;
   if ((rc = check_kv(kv, pl, true))) return rc;
+  if (pl.qa && kv->layout != KVSEL_LAYOUT_CONTIGUOUS) return KVSEL_EUNSUPPORTED;
   if ((rc = check_ws(pl, ws, ws_bytes))) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (pl.n_scores == 0) return KVSEL_OK;

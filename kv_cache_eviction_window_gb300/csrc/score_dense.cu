@@ -1,0 +1,415 @@
+// Query-agnostic scoring on tcgen05 tensor cores ("KVzip: Query-Agnostic KV Cache
+// Compression with Context Reconstruction", §3.2: each key's importance is its maximum
+// softmax weight over all queries and group heads; §3.4: queries are processed in chunks
+// and the per-chunk maxima combined — max is associative, so the chunk size only bounds
+// memory and does not change the result).
+//
+// Per KV head the queries are the G*n rows of Q[h] (all positions of all group heads),
+// non-causal over all n keys:  S_i = max_r exp(l_ri - c_r),  c_r = log sum_j exp(l_rj).
+//
+//   qa_rowlse_kernel: A = a block of 512 query rows (4 M tiles), B = 64-key tiles
+//     streamed over all n keys; every epilogue thread keeps an online (max, sum) for its
+//     rows; writes c2_r = (m_r + log2 Z_r) in log2 units.
+//   qa_keymax_kernel: A = a block of 512 keys (4 M tiles, resident), B = 64-row query
+//     tiles streamed over a slice of the rows; every thread keeps max_r (l_ri*s2 - c2_r)
+//     for its keys; slices merge with an order-preserving atomicMax in global memory.
+//   qa_finish_kernel: s_raw_i = exp2(max).
+// Both passes are tensor-core bound at this shape (2*G*n*n*d flop each).
+#include "internal.cuh"
+
+namespace kvsel {
+namespace {
+
+constexpr int kEpiWarps = 8;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kThreads = 320;
+constexpr float kNegBig = -1.0e30f;
+constexpr int kMT = 4;                 // 128-row M tiles per CTA (512 rows or keys)
+constexpr int kNT = 64;                // streamed tile rows (keys in pass 1, queries in pass 2)
+constexpr int kStages = 4;
+constexpr int kAcc = 2;
+constexpr uint32_t kAccCols = kMT * kNT;      // 256
+constexpr uint32_t kTmemCols = kAcc * kAccCols;
+constexpr int kBlockHalf = kMT * 128 * 128;   // bytes of one column half of the resident block
+constexpr int kTile = kNT * 256;              // bytes of one streamed tile
+
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~static_cast<uintptr_t>(1023));
+}
+
+__device__ __forceinline__ uint32_t f2key(float f) {
+  const uint32_t u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key2f(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
+// ------------------------------------------------------------------------------------
+// pass 1: log-sum-exp of every query row over all keys
+// ------------------------------------------------------------------------------------
+__global__ void __launch_bounds__(kThreads, 1)
+    qa_rowlse_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                     const QaArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  uint8_t* sQ = smem;                      // [2 halves][512 rows][128 B]
+  uint8_t* sK = smem + 2 * kBlockHalf;     // [stages][2 halves][64 keys][128 B]
+
+  __shared__ __align__(8) uint64_t full_bar[kStages], empty_bar[kStages], accf_bar[kAcc], acce_bar[kAcc];
+  __shared__ __align__(8) uint64_t q_bar, done_bar;
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_abort;
+  __shared__ float s_xm[kMT][4][32], s_xz[kMT][4][32];
+
+  const int warp = warp_id(), lane = lane_id();
+  const int h = blockIdx.x / a.row_blocks;
+  const int row0 = (blockIdx.x % a.row_blocks) * kMT * 128;
+  const int n = a.n, GN = a.GN;
+  const int ntiles = (n + kNT - 1) / kNT;
+  int* status = a.wc.status;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    for (int s = 0; s < kAcc; ++s) {
+      mbar_init(&accf_bar[s], 1);
+      mbar_init(&acce_bar[s], kEpiWarps);
+    }
+    mbar_init(&q_bar, 1);
+    mbar_init(&done_bar, 1);
+    s_abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(&s_tmem, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = s_tmem;
+
+  if (warp == kProducerWarp) {
+    if (lane == 0) {
+      tma_prefetch_desc(&tq);
+      tma_prefetch_desc(&tk);
+      mbar_arrive_expect_tx(&q_bar, 2 * kBlockHalf);
+      const int qrow0 = h * GN + row0;
+      for (int rb = 0; rb < kMT * 128; rb += 64) {
+        tma_load_2d(sQ + rb * 128, &tq, &q_bar, 0, qrow0 + rb);
+        tma_load_2d(sQ + kBlockHalf + rb * 128, &tq, &q_bar, 64, qrow0 + rb);
+      }
+      int t = 0;
+      for (; t < ntiles; ++t) {
+        const int s = t % kStages, u = t / kStages;
+        if (!mbar_wait(&empty_bar[s], (u & 1) ^ 1, &s_abort, a.wc)) break;
+        mbar_arrive_expect_tx(&full_bar[s], kTile);
+        tma_load_4d(sK + s * kTile, &tk, &full_bar[s], 0, t * kNT, h, 0);
+        tma_load_4d(sK + s * kTile + kNT * 128, &tk, &full_bar[s], 64, t * kNT, h, 0);
+      }
+      for (int tt = max(0, t - kStages); tt < t; ++tt) mbar_drain(&full_bar[tt % kStages], (tt / kStages) & 1, status);
+      mbar_drain(&q_bar, 0, status);
+    }
+  } else if (warp == kMmaWarp) {
+    if (lane == 0) {
+      bool ok = mbar_wait(&q_bar, 0, &s_abort, a.wc);
+      constexpr uint32_t idesc = idesc_bf16_f32(128, kNT);
+      for (int t = 0; ok && t < ntiles; ++t) {
+        const int s = t % kStages, u = t / kStages;
+        const int acc = t % kAcc, ua = t / kAcc;
+        if (!mbar_wait(&full_bar[s], u & 1, &s_abort, a.wc)) break;
+        if (!mbar_wait(&acce_bar[acc], (ua & 1) ^ 1, &s_abort, a.wc)) break;
+        tc_fence_after();
+        const uint32_t kb = smem_u32(sK + s * kTile);
+        const uint32_t qb = smem_u32(sQ);
+#pragma unroll
+        for (int mt = 0; mt < kMT; ++mt) {
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const uint32_t koff = (k & 3) * 32;
+            const uint64_t da = sdesc_kmajor_sw128(qb + (k >> 2) * kBlockHalf + mt * 16384 + koff);
+            const uint64_t db = sdesc_kmajor_sw128(kb + (k >> 2) * (kNT * 128) + koff);
+            umma_bf16(tbase + acc * kAccCols + mt * kNT, da, db, idesc, k > 0 ? 1u : 0u);
+          }
+        }
+        umma_commit(&empty_bar[s]);
+        umma_commit(&accf_bar[acc]);
+      }
+      umma_commit(&done_bar);
+      mbar_drain(&done_bar, 0, status);
+    }
+  } else {
+    const int q4 = warp & 3, cg = warp >> 2;
+    const float s2 = a.s2;
+    float m[kMT], z[kMT];
+#pragma unroll
+    for (int mt = 0; mt < kMT; ++mt) {
+      m[mt] = kNegBig;
+      z[mt] = 0.f;
+    }
+    for (int t = 0; t < ntiles; ++t) {
+      const int acc = t % kAcc, ua = t / kAcc;
+      bool ok = mbar_wait(&accf_bar[acc], ua & 1, &s_abort, a.wc);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      const int key0 = t * kNT + cg * 32;
+      const bool tail = key0 + 32 > n;
+#pragma unroll
+      for (int mt = 0; mt < kMT; ++mt) {
+        float v[32];
+        tmem_ld32(tbase + (static_cast<uint32_t>(q4 * 32) << 16) + acc * kAccCols + mt * kNT + cg * 32, v);
+        tmem_ld_wait();
+        if (tail) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (key0 + j >= n) v[j] = -INFINITY;
+        }
+        float cmax = v[0];
+#pragma unroll
+        for (int j = 1; j < 32; ++j) cmax = fmaxf(cmax, v[j]);
+        const float mn = fmaxf(m[mt], cmax * s2);
+        float p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
+#pragma unroll
+        for (int j = 0; j < 32; j += 4) {
+          p0 += ex2_approx(fmaf(v[j + 0], s2, -mn));
+          p1 += ex2_approx(fmaf(v[j + 1], s2, -mn));
+          p2 += ex2_approx(fmaf(v[j + 2], s2, -mn));
+          p3 += ex2_approx(fmaf(v[j + 3], s2, -mn));
+        }
+        z[mt] = z[mt] * ex2_approx(m[mt] - mn) + ((p0 + p1) + (p2 + p3));
+        m[mt] = mn;
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acce_bar[acc]);
+    }
+    if (cg == 1) {
+#pragma unroll
+      for (int mt = 0; mt < kMT; ++mt) {
+        s_xm[mt][q4][lane] = m[mt];
+        s_xz[mt][q4][lane] = z[mt];
+      }
+    }
+    epi_bar();
+    if (cg == 0) {
+#pragma unroll
+      for (int mt = 0; mt < kMT; ++mt) {
+        const int r = row0 + mt * 128 + q4 * 32 + lane;
+        if (r < GN) {
+          const float m1 = s_xm[mt][q4][lane], z1 = s_xz[mt][q4][lane];
+          const float mm = fmaxf(m[mt], m1);
+          const float zz = z[mt] * ex2_approx(m[mt] - mm) + z1 * ex2_approx(m1 - mm);
+          a.c2[static_cast<size_t>(h) * GN + r] = mm + lg2_approx(zz);
+        }
+      }
+    }
+  }
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tbase, kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------------------------------
+// pass 2: per key, max over a slice of query rows of (l * s2 - c2_row)
+// ------------------------------------------------------------------------------------
+__global__ void __launch_bounds__(kThreads, 1)
+    qa_keymax_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                     const QaArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  uint8_t* sK = smem;                      // [4 M tiles][2 halves][128 keys][128 B]
+  uint8_t* sQ = smem + 2 * kBlockHalf;     // [stages][2 halves][64 rows][128 B]
+
+  __shared__ __align__(8) uint64_t full_bar[kStages], empty_bar[kStages], accf_bar[kAcc], acce_bar[kAcc];
+  __shared__ __align__(8) uint64_t k_bar, done_bar;
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_abort;
+  __shared__ float s_x[kMT][4][32];
+
+  const int warp = warp_id(), lane = lane_id();
+  const int per_head = a.key_blocks * a.row_splits;
+  const int h = blockIdx.x / per_head;
+  const int rem = blockIdx.x % per_head;
+  const int kb = rem / a.row_splits, rs = rem % a.row_splits;
+  const int key0 = kb * kMT * 128;
+  const int n = a.n, GN = a.GN;
+  const int rows_per = (GN + a.row_splits - 1) / a.row_splits;
+  const int r_begin = rs * rows_per, r_end = min(GN, r_begin + rows_per);
+  const int ntiles = r_end > r_begin ? (r_end - r_begin + kNT - 1) / kNT : 0;
+  int* status = a.wc.status;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    for (int s = 0; s < kAcc; ++s) {
+      mbar_init(&accf_bar[s], 1);
+      mbar_init(&acce_bar[s], kEpiWarps);
+    }
+    mbar_init(&k_bar, 1);
+    mbar_init(&done_bar, 1);
+    s_abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(&s_tmem, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = s_tmem;
+
+  if (warp == kProducerWarp) {
+    if (lane == 0 && ntiles > 0) {
+      tma_prefetch_desc(&tq);
+      tma_prefetch_desc(&tk);
+      mbar_arrive_expect_tx(&k_bar, 2 * kBlockHalf);
+      for (int mt = 0; mt < kMT; ++mt) {
+        tma_load_4d(sK + mt * 32768, &tk, &k_bar, 0, key0 + mt * 128, h, 0);
+        tma_load_4d(sK + mt * 32768 + 16384, &tk, &k_bar, 64, key0 + mt * 128, h, 0);
+      }
+      int t = 0;
+      for (; t < ntiles; ++t) {
+        const int s = t % kStages, u = t / kStages;
+        if (!mbar_wait(&empty_bar[s], (u & 1) ^ 1, &s_abort, a.wc)) break;
+        mbar_arrive_expect_tx(&full_bar[s], kTile);
+        const int qrow = h * GN + r_begin + t * kNT;
+        tma_load_2d(sQ + s * kTile, &tq, &full_bar[s], 0, qrow);
+        tma_load_2d(sQ + s * kTile + kNT * 128, &tq, &full_bar[s], 64, qrow);
+      }
+      for (int tt = max(0, t - kStages); tt < t; ++tt) mbar_drain(&full_bar[tt % kStages], (tt / kStages) & 1, status);
+      mbar_drain(&k_bar, 0, status);
+    }
+  } else if (warp == kMmaWarp) {
+    if (lane == 0 && ntiles > 0) {
+      bool ok = mbar_wait(&k_bar, 0, &s_abort, a.wc);
+      constexpr uint32_t idesc = idesc_bf16_f32(128, kNT);
+      for (int t = 0; ok && t < ntiles; ++t) {
+        const int s = t % kStages, u = t / kStages;
+        const int acc = t % kAcc, ua = t / kAcc;
+        if (!mbar_wait(&full_bar[s], u & 1, &s_abort, a.wc)) break;
+        if (!mbar_wait(&acce_bar[acc], (ua & 1) ^ 1, &s_abort, a.wc)) break;
+        tc_fence_after();
+        const uint32_t kbase = smem_u32(sK);
+        const uint32_t qbase = smem_u32(sQ + s * kTile);
+#pragma unroll
+        for (int mt = 0; mt < kMT; ++mt) {
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const uint32_t koff = (k & 3) * 32;
+            const uint64_t da = sdesc_kmajor_sw128(kbase + mt * 32768 + (k >> 2) * 16384 + koff);
+            const uint64_t db = sdesc_kmajor_sw128(qbase + (k >> 2) * (kNT * 128) + koff);
+            umma_bf16(tbase + acc * kAccCols + mt * kNT, da, db, idesc, k > 0 ? 1u : 0u);
+          }
+        }
+        umma_commit(&empty_bar[s]);
+        umma_commit(&accf_bar[acc]);
+      }
+      umma_commit(&done_bar);
+      mbar_drain(&done_bar, 0, status);
+    }
+  } else {
+    const int q4 = warp & 3, cg = warp >> 2;
+    const float s2 = a.s2;
+    float best[kMT];
+#pragma unroll
+    for (int mt = 0; mt < kMT; ++mt) best[mt] = -INFINITY;
+    for (int t = 0; t < ntiles; ++t) {
+      const int acc = t % kAcc, ua = t / kAcc;
+      bool ok = mbar_wait(&accf_bar[acc], ua & 1, &s_abort, a.wc);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      // c2 of this thread's 32 query rows: one coalesced load, broadcast by shuffles
+      const int rrow = r_begin + t * kNT + cg * 32 + lane;
+      const float myc2 = rrow < r_end ? __ldg(a.c2 + static_cast<size_t>(h) * GN + rrow) : INFINITY;
+      float nc[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) nc[j] = -__shfl_sync(0xffffffffu, myc2, j);
+#pragma unroll
+      for (int mt = 0; mt < kMT; ++mt) {
+        float v[32];
+        tmem_ld32(tbase + (static_cast<uint32_t>(q4 * 32) << 16) + acc * kAccCols + mt * kNT + cg * 32, v);
+        tmem_ld_wait();
+        float b0 = best[mt], b1 = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < 32; j += 2) {
+          b0 = fmaxf(b0, fmaf(v[j], s2, nc[j]));
+          b1 = fmaxf(b1, fmaf(v[j + 1], s2, nc[j + 1]));
+        }
+        best[mt] = fmaxf(b0, b1);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acce_bar[acc]);
+    }
+    if (cg == 1) {
+#pragma unroll
+      for (int mt = 0; mt < kMT; ++mt) s_x[mt][q4][lane] = best[mt];
+    }
+    epi_bar();
+    if (cg == 0) {
+#pragma unroll
+      for (int mt = 0; mt < kMT; ++mt) {
+        const int key = key0 + mt * 128 + q4 * 32 + lane;
+        const float bm = fmaxf(best[mt], s_x[mt][q4][lane]);
+        if (key < n && ntiles > 0) atomicMax(a.tmax + static_cast<size_t>(h) * n + key, f2key(bm));
+      }
+    }
+  }
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tbase, kTmemCols);
+  }
+}
+
+__global__ void qa_finish_kernel(const uint32_t* __restrict__ tmax, float* __restrict__ s_raw, long long total) {
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<long long>(gridDim.x) * blockDim.x)
+    s_raw[i] = ex2_approx(key2f(tmax[i]));
+}
+
+}  // namespace
+
+cudaError_t launch_qa_rowlse(const QaArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, cudaStream_t st) {
+  const size_t smem = 1024 + 2 * kBlockHalf + kStages * kTile;
+  cudaError_t e = ensure_smem(reinterpret_cast<const void*>(qa_rowlse_kernel), smem);
+  if (e != cudaSuccess) return e;
+  qa_rowlse_kernel<<<a.H * a.row_blocks, kThreads, smem, st>>>(tq, tk, a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_qa_keymax(const QaArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, cudaStream_t st) {
+  const size_t smem = 1024 + 2 * kBlockHalf + kStages * kTile;
+  cudaError_t e = ensure_smem(reinterpret_cast<const void*>(qa_keymax_kernel), smem);
+  if (e != cudaSuccess) return e;
+  e = cudaMemsetAsync(a.tmax, 0, static_cast<size_t>(a.H) * a.n * sizeof(uint32_t), st);
+  if (e != cudaSuccess) return e;
+  qa_keymax_kernel<<<a.H * a.key_blocks * a.row_splits, kThreads, smem, st>>>(tq, tk, a);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const long long total = static_cast<long long>(a.H) * a.n;
+  const int blocks = static_cast<int>((total + 255) / 256 < 4096 ? (total + 255) / 256 : 4096);
+  qa_finish_kernel<<<blocks, 256, 0, st>>>(a.tmax, a.s_raw, total);
+  return cudaGetLastError();
+}
+
+int qa_block_rows() { return kMT * 128; }
+
+}  // namespace kvsel

@@ -91,7 +91,9 @@ def _p(B, **kw):
     (dict(pool="max", pool_kernel=4), -1),
     (dict(budget_ratio=0.005), -2),            # 20 slots < 36 forced entries
     (dict(budget_ratio=1.5), -1),
-    (dict(window=0, causal=False, reduce="max"), -3),
+    (dict(window=0, causal=True, reduce="max"), -3),     # query-agnostic scoring is non-causal
+    (dict(window=0, causal=False, reduce="mean"), -3),   # ... and takes the max over queries
+    (dict(window=0, causal=False, reduce="max", value_aware=True, d_model=4096), -3),
     (dict(group=3, window=10), -3),             # 30 window rows: not a multiple of 32
     (dict(window=8192), -1),                    # window longer than the context
     (dict(value_aware=True, d_model=4096, budget_mode="layer"), -3),
@@ -115,3 +117,10 @@ def test_select_rejects_null_pointers(B):
 def test_empty_request_is_a_no_op(B):
     p = _p(B, n_ctx=0, n_recent=0, n_sink=0, window=32)
     assert B.kvsel_output_size(p) == (0, 0, 8)
+
+
+def test_query_agnostic_sizes(B):
+    p = _p(B, window=0, causal=False, reduce="max", pool="none", n_recent=0,
+           budget_mode="layer", budget_ratio=0.3, n_ctx=32768)
+    n_scores, n_kept, n_seg = B.kvsel_output_size(p)
+    assert (n_scores, n_kept, n_seg) == (8 * 32768, math.floor(0.3 * 32768 * 8), 8)

@@ -156,6 +156,17 @@ def test_minimal_context_equals_window():
     _check_layer(wl, inp, gpu, ora)
 
 
+@pytest.mark.parametrize("n", [1000, 2048])
+def test_c5_query_agnostic(n):
+    """KVzip maximum cross-attention score: all G*n positions as queries, non-causal,
+    max over queries and group heads, one budget per layer."""
+    wl = datagen.WORKLOADS[5].replace(h_kv=4)
+    inp = datagen.make_layer(wl, 0, n_ctx=n)
+    ora = O.run_workload_layer(wl, inp)
+    gpu = GH.run_gpu_layer(wl, inp)
+    _check_layer(wl, inp, gpu, ora)
+
+
 # ---------------------------------------------------------------------- full size
 def test_c2_full_layer_plain_and_sampled_value_aware():
     """Llama-3.1-8B layer, n = 32768: plain scores and selection against the full oracle;
@@ -211,3 +222,28 @@ def test_bounded_wait_timeout_reports_status():
     ora = O.run_workload_layer(wl, inp)
     gpu = GH.run_gpu_layer(wl, inp)
     _check_layer(wl, inp, gpu, ora)
+
+
+def test_c5_full_layer_sampled_rows():
+    """Llama-3.1-70B layer shape, n = 32768 (262144 query rows per KV head).  The oracle
+    cannot form every row's normaliser at this size, so: every score is a probability,
+    it is at least the oracle's score over a sample of 48 query rows per head (a max over
+    a subset), and the kept set is exactly the layer top-B of the GPU's own scores."""
+    wl = datagen.WORKLOADS[5]
+    inp = datagen.make_layer(wl, 0)
+    gpu = GH.run_gpu_layer(wl, inp)[0]
+    n, H = wl.n_ctx, wl.h_kv
+    rng = np.random.default_rng(5)
+    k = O.bf16_to_f64(inp["k"][0])
+    for h in range(H):
+        s = gpu["s_attn"][h].astype(np.float64)
+        assert np.all(s > 0) and np.all(s <= 1.0 + 1e-6)
+        pos = rng.choice(n, size=6, replace=False)
+        qs = O.bf16_to_f64(inp["q"][0][h][:, pos, :])          # [G][6][d]
+        lower = O.query_agnostic_scores(qs, k[h])
+        assert np.all(s >= lower * (1 - GH.RTOL) - GH.ATOL_FRAC * lower.max()), f"head {h}"
+    fm = O.forced_mask(n, wl.n_sink, wl.n_recent)
+    BL = int(math.floor(wl.budget_ratio * n * H))
+    flat = np.concatenate([gpu["s_attn"][h] for h in range(H)])
+    kept = np.concatenate([np.asarray(gpu["idx"][h]) + h * n for h in range(H)])
+    GH.check_topk_property(flat, np.sort(kept), np.tile(fm, H), BL, "C5 layer top-B")
