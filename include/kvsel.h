@@ -206,7 +206,8 @@ void kvsel_set_wait_limit(uint64_t cycles);
 
 /* Stages of the path, in launch order within one layer. */
 enum {
-  KVSEL_STAGE_ROWSTATS = 0,  /* window scoring pass 1: per-row softmax statistics    */
+  KVSEL_STAGE_ROWSTATS = 0,  /* scoring pass 1 (row softmax statistics), or both    
+                                passes when they run as one cooperative launch        */
   KVSEL_STAGE_KEYSUM = 1,    /* window scoring pass 2: per-key reduced probabilities */
   KVSEL_STAGE_WBAR = 2,      /* value-aware: W_O slices of each KV head, bf16        */
   KVSEL_STAGE_VNORM = 3,     /* value-aware: ||W_h v||_1 per token (tensor cores)    */

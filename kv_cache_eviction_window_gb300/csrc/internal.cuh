@@ -95,6 +95,8 @@ cudaError_t ensure_smem(const void* func, size_t bytes);
 cudaError_t launch_win_rowstats(const WinScoreArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, int mt,
                                 cudaStream_t st);
 cudaError_t launch_win_keysum(const WinScoreArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, cudaStream_t st);
+cudaError_t launch_win_fused(const WinScoreArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
+                             unsigned int* grid_count, cudaStream_t st);
 
 cudaError_t launch_wbar(const uint16_t* w_o, uint16_t* wbar, int H, int G, int D, int wo_mode, cudaStream_t st);
 cudaError_t launch_vnorm(const VnormArgs& a, const CUtensorMap& tv, const CUtensorMap& tw, cudaStream_t st);

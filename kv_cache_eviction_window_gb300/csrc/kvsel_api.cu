@@ -41,6 +41,7 @@ namespace {
 std::atomic<unsigned long long> g_wait_limit{2000000000ull};   // ~1 s at the boost clock
 
 constexpr size_t kStatusBytes = 256;
+constexpr size_t kCounterBytes = 4 * kMaxBatch * 64;   // grid-barrier counters, one per (request, head)
 
 thread_local void* const* t_stage_events = nullptr;
 
@@ -51,7 +52,14 @@ struct StageScope {
   StageScope(int s, cudaStream_t stream) : stage(s), st(stream) { rec(2 * stage); }
   ~StageScope() { rec(2 * stage + 1); }
   void rec(int i) const {
-    if (t_stage_events && t_stage_events[i]) cudaEventRecord(static_cast<cudaEvent_t>(t_stage_events[i]), st);
+    if (!t_stage_events || !t_stage_events[i]) return;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    cudaStreamIsCapturing(st, &cs);
+    // under stream capture the record must become an external event node to time replays
+    if (cs == cudaStreamCaptureStatusActive)
+      cudaEventRecordWithFlags(static_cast<cudaEvent_t>(t_stage_events[i]), st, cudaEventRecordExternal);
+    else
+      cudaEventRecord(static_cast<cudaEvent_t>(t_stage_events[i]), st);
   }
 };
 
@@ -205,7 +213,7 @@ int make_plan(const kvsel_params* p, Plan& pl, bool need_device) {
   pl.unit_base[pl.B] = ub;
   pl.units_total = p->value_aware ? ub : 0;
 
-  size_t off = kStatusBytes;
+  size_t off = kStatusBytes + kCounterBytes;
   if (pl.qa) {
     const int n = pl.rq.n[0];
     const long long GN = static_cast<long long>(pl.G) * n;
@@ -393,16 +401,26 @@ int do_score(const kvsel_params* p, const Plan& pl, const void* q, const kvsel_k
   a.s_raw = s_raw;
   a.wc = wait_ctl(ws);
   int rc;
-  {
+  cudaError_t fe = cudaErrorNotSupported;
+  if (pl.mt <= 2) {
+    // both passes in one cooperative launch when every chunk fits on the device at once
     StageScope sc(KVSEL_STAGE_ROWSTATS, st);
-    rc = launch_rc(launch_win_rowstats(a, tq, tk1, pl.mt, st));
+    fe = launch_win_fused(a, tq, tk2, reinterpret_cast<unsigned int*>(wsb + kStatusBytes), st);
+    if (fe != cudaSuccess && fe != cudaErrorNotSupported) return KVSEL_ECUDA;
   }
-  if (rc) return rc;
-  {
-    StageScope sc(KVSEL_STAGE_KEYSUM, st);
-    rc = launch_rc(launch_win_keysum(a, tq, tk2, st));
+  if (fe == cudaSuccess) StageScope sc(KVSEL_STAGE_KEYSUM, st);   // pass 2 ran inside the fused launch
+  if (fe == cudaErrorNotSupported) {
+    {
+      StageScope sc(KVSEL_STAGE_ROWSTATS, st);
+      rc = launch_rc(launch_win_rowstats(a, tq, tk1, pl.mt, st));
+    }
+    if (rc) return rc;
+    {
+      StageScope sc(KVSEL_STAGE_KEYSUM, st);
+      rc = launch_rc(launch_win_keysum(a, tq, tk2, st));
+    }
+    if (rc) return rc;
   }
-  if (rc) return rc;
 
   float* nu = nullptr;
   if (p->value_aware) {

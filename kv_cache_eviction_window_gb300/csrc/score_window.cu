@@ -46,6 +46,29 @@ __device__ __forceinline__ bool epi_any(bool pred) {
   return r != 0;
 }
 
+// max of v[0..N) as a balanced tree (short dependency chain)
+template <int N>
+__device__ __forceinline__ float tree_max(const float* v) {
+  float t[N / 2];
+#pragma unroll
+  for (int i = 0; i < N / 2; ++i) t[i] = fmaxf(v[2 * i], v[2 * i + 1]);
+#pragma unroll
+  for (int w = N / 4; w >= 1; w >>= 1) {
+#pragma unroll
+    for (int i = 0; i < w; ++i) t[i] = fmaxf(t[2 * i], t[2 * i + 1]);
+  }
+  return t[0];
+}
+
+// sum of exp2(v[j] * s2 - mn) over j < N, in eight independent accumulators
+template <int N>
+__device__ __forceinline__ float exp2_sum(const float* v, float s2, float mn) {
+  float p[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int j = 0; j < N; ++j) p[j & 7] += ex2_approx(fmaf(v[j], s2, -mn));
+  return ((p[0] + p[1]) + (p[2] + p[3])) + ((p[4] + p[5]) + (p[6] + p[7]));
+}
+
 __host__ __device__ constexpr uint32_t pow2_cols(uint32_t c) {
   return c <= 32 ? 32 : c <= 64 ? 64 : c <= 128 ? 128 : c <= 256 ? 256 : 512;
 }
@@ -235,19 +258,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j = 0; j < kCh; ++j)
             if (kcol0 + j > lim_r) v[j] = -INFINITY;
         }
-        float cmax = v[0];
-#pragma unroll
-        for (int j = 1; j < kCh; ++j) cmax = fmaxf(cmax, v[j]);
-        const float mn = fmaxf(m[mt], cmax * s2);
-        float p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
-#pragma unroll
-        for (int j = 0; j < kCh; j += 4) {
-          p0 += ex2_approx(fmaf(v[j + 0], s2, -mn));
-          p1 += ex2_approx(fmaf(v[j + 1], s2, -mn));
-          p2 += ex2_approx(fmaf(v[j + 2], s2, -mn));
-          p3 += ex2_approx(fmaf(v[j + 3], s2, -mn));
-        }
-        z[mt] = z[mt] * ex2_approx(m[mt] - mn) + ((p0 + p1) + (p2 + p3));
+        const float mn = fmaxf(m[mt], tree_max<kCh>(v) * s2);
+        z[mt] = z[mt] * ex2_approx(m[mt] - mn) + exp2_sum<kCh>(v, s2, mn);
         m[mt] = mn;
       }
       tc_fence_before();
@@ -507,6 +519,343 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// ------------------------------------------------------------------------------------
+// both passes in one cooperative launch (one key chunk per CTA, all CTAs co-resident)
+// ------------------------------------------------------------------------------------
+// pass 1 as win_rowstats_kernel; then a bounded grid barrier (the row partials of every
+// chunk are written); then pass 2 over the CTA's own chunk, whose K tiles are still in
+// L2.  The TMA producer and the UMMA warp run straight on into pass 2 (K and Q do not
+// depend on the barrier); only the epilogue waits.  In pass 2 the two epilogue warp
+// groups take alternate tiles and each thread owns one key over all R rows.
+template <int MT>
+__global__ void __launch_bounds__(kThreads, 1)
+    win_fused_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                     const WinScoreArgs a, unsigned int* grid_count) {
+  constexpr int NT = 128, STAGES = (MT == 1) ? 5 : 4, kAcc = 2;
+  constexpr int kAcc2 = (MT == 1) ? 4 : 2;           // pass-2 accumulators (R <= MT*128 columns each)
+  constexpr uint32_t kAccCols = MT * 128;
+  constexpr uint32_t kTmemCols = 512;
+  constexpr int kQHalf = MT * 128 * 128;
+  constexpr int kKStage = NT * 256;
+  constexpr int kCh = NT / 2;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  uint8_t* sQ = smem;
+  uint8_t* sK = smem + 2 * kQHalf;
+
+  __shared__ __align__(8) uint64_t full_bar[STAGES], empty_bar[STAGES];
+  __shared__ __align__(8) uint64_t accf1[kAcc], acce1[kAcc], accf2[kAcc2], acce2[kAcc2];
+  __shared__ __align__(8) uint64_t q_bar, done_bar;
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_abort;
+  __shared__ float s_xm[MT][4][32], s_xz[MT][4][32];
+  __shared__ __align__(16) float s_c2[MT * 128];
+
+  const int warp = warp_id(), lane = lane_id();
+  int b, h, c;
+  chunk_coords(a.ck, a.rq.B, blockIdx.x, b, h, c);
+  const int n = a.rq.n[b];
+  const int key_begin = c * a.ck.chunk_len;
+  const int key_end = min(n, key_begin + a.ck.chunk_len);
+  const int ntiles = key_end > key_begin ? (key_end - key_begin + NT - 1) / NT : 0;
+  int* status = a.wc.status;
+  const int R = a.R, RP = a.R_pad;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    for (int s = 0; s < kAcc; ++s) {
+      mbar_init(&accf1[s], 1);
+      mbar_init(&acce1[s], kEpiWarps);
+    }
+    for (int s = 0; s < kAcc2; ++s) {
+      mbar_init(&accf2[s], 1);
+      mbar_init(&acce2[s], kEpiWarps / 2);
+    }
+    mbar_init(&q_bar, 1);
+    mbar_init(&done_bar, 1);
+    s_abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(&s_tmem, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = s_tmem;
+
+  if (warp == kProducerWarp) {
+    if (lane == 0 && ntiles > 0) {
+      tma_prefetch_desc(&tq);
+      tma_prefetch_desc(&tk);
+      mbar_arrive_expect_tx(&q_bar, R * 256);
+      load_q_rows(&tq, (b * a.rq.H + h) * R, R, kQHalf, sQ, &q_bar);
+      int T = 0;
+      for (; T < 2 * ntiles; ++T) {   // pass 1 tiles, then the same tiles again for pass 2
+        const int s = T % STAGES, u = T / STAGES;
+        if (!mbar_wait(&empty_bar[s], (u & 1) ^ 1, &s_abort, a.wc)) break;
+        mbar_arrive_expect_tx(&full_bar[s], kKStage);
+        const int t = T < ntiles ? T : T - ntiles;
+        load_kv_tile(&tk, a.src, b, h, n, key_begin + t * NT, NT, sK + s * kKStage, &full_bar[s], status);
+      }
+      for (int tt = max(0, T - STAGES); tt < T; ++tt) mbar_drain(&full_bar[tt % STAGES], (tt / STAGES) & 1, status);
+      mbar_drain(&q_bar, 0, status);
+    }
+  } else if (warp == kMmaWarp) {
+    if (lane == 0 && ntiles > 0) {
+      bool ok = mbar_wait(&q_bar, 0, &s_abort, a.wc);
+      const uint32_t qbase = smem_u32(sQ);
+      // pass 1: A = window rows, B = keys
+      constexpr uint32_t idesc1 = idesc_bf16_f32(128, NT);
+      for (int t = 0; ok && t < ntiles; ++t) {
+        const int s = t % STAGES, u = t / STAGES;
+        const int acc = t % kAcc, ua = t / kAcc;
+        if (!mbar_wait(&full_bar[s], u & 1, &s_abort, a.wc) ||
+            !mbar_wait(&acce1[acc], (ua & 1) ^ 1, &s_abort, a.wc)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t kbase = smem_u32(sK + s * kKStage);
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const uint32_t koff = (k & 3) * 32;
+            umma_bf16(tbase + acc * kAccCols + mt * NT,
+                      sdesc_kmajor_sw128(qbase + (k >> 2) * kQHalf + mt * 16384 + koff),
+                      sdesc_kmajor_sw128(kbase + (k >> 2) * (NT * 128) + koff), idesc1, k > 0 ? 1u : 0u);
+          }
+        }
+        umma_commit(&empty_bar[s]);
+        umma_commit(&accf1[acc]);
+      }
+      // pass 2: A = keys (M = 128), B = window rows (N = R in chunks of <= 256)
+      for (int t = 0; ok && t < ntiles; ++t) {
+        const int T = ntiles + t;
+        const int s = T % STAGES, u = T / STAGES;
+        const int acc = t % kAcc2, ua = t / kAcc2;
+        if (!mbar_wait(&full_bar[s], u & 1, &s_abort, a.wc)) {
+          ok = false;
+          break;
+        }
+        if (t < kAcc2) {
+          // first pass-2 use of these columns: pass 1's last use of them is released
+          if (acc < kAcc) {
+            const int last1 = ((ntiles - 1 - acc) >= 0) ? ntiles - 1 - ((ntiles - 1 - acc) % kAcc) : -1;
+            if (last1 >= 0 && !mbar_wait(&acce1[acc], (last1 / kAcc) & 1, &s_abort, a.wc)) {
+              ok = false;
+              break;
+            }
+          }
+        } else if (!mbar_wait(&acce2[acc], (ua & 1) ^ 1, &s_abort, a.wc)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t kbase = smem_u32(sK + s * kKStage);
+        for (int n0 = 0; n0 < R; n0 += 256) {
+          const int nc = min(256, R - n0);
+          const uint32_t idesc = idesc_bf16_f32(128, nc);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const uint32_t koff = (k & 3) * 32;
+            umma_bf16(tbase + acc * kAccCols + n0, sdesc_kmajor_sw128(kbase + (k >> 2) * (NT * 128) + koff),
+                      sdesc_kmajor_sw128(qbase + (k >> 2) * kQHalf + n0 * 128 + koff), idesc, k > 0 ? 1u : 0u);
+          }
+        }
+        umma_commit(&empty_bar[s]);
+        umma_commit(&accf2[acc]);
+      }
+      umma_commit(&done_bar);
+      mbar_drain(&done_bar, 0, status);
+    }
+  } else {
+    // ---------------- epilogue, pass 1 (column halves, as win_rowstats_kernel) ----------------
+    const int q4 = warp & 3, cg = warp >> 2;
+    const float s2 = a.s2;
+    const int W = a.W;
+    const int lim_all = a.causal ? (n - W + 1) : n;
+    float m[MT], z[MT];
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+      m[mt] = kNegBig;
+      z[mt] = 0.f;
+    }
+    bool alive = true;
+    for (int t = 0; t < ntiles; ++t) {
+      const int acc = t % kAcc, ua = t / kAcc;
+      bool ok = mbar_wait(&accf1[acc], ua & 1, &s_abort, a.wc);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) {
+        alive = false;
+        break;
+      }
+      tc_fence_after();
+      const int kcol0 = key_begin + t * NT + cg * kCh;
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+        float v[kCh];
+        const uint32_t taddr = tbase + (static_cast<uint32_t>(q4 * 32) << 16) + acc * kAccCols + mt * NT + cg * kCh;
+#pragma unroll
+        for (int j = 0; j < kCh / 32; ++j) tmem_ld32(taddr + j * 32, v + j * 32);
+        tmem_ld_wait();
+        const int r = mt * 128 + q4 * 32 + lane;
+        if (!(kcol0 + kCh <= lim_all) || r >= R) {
+          const int lim_r = (r >= R) ? -1 : (a.causal ? min(n - 1, n - W + (r % W)) : n - 1);
+#pragma unroll
+          for (int j = 0; j < kCh; ++j)
+            if (kcol0 + j > lim_r) v[j] = -INFINITY;
+        }
+        const float mn = fmaxf(m[mt], tree_max<kCh>(v) * s2);
+        z[mt] = z[mt] * ex2_approx(m[mt] - mn) + exp2_sum<kCh>(v, s2, mn);
+        m[mt] = mn;
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acce1[acc]);
+    }
+    if (cg == 1) {
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+        s_xm[mt][q4][lane] = m[mt];
+        s_xz[mt][q4][lane] = z[mt];
+      }
+    }
+    epi_bar();
+    const int nch = a.ck.per_head[b], ncp = chunk_pad(nch);
+    float* pm = a.part + (static_cast<size_t>(a.ck.pbase[b]) + static_cast<size_t>(h) * ncp) * 2 * RP;
+    float* pz = pm + static_cast<size_t>(RP) * ncp;
+    if (cg == 0) {
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+        const int r = mt * 128 + q4 * 32 + lane;
+        if (r < R) {
+          const float m1 = s_xm[mt][q4][lane], z1 = s_xz[mt][q4][lane];
+          const float mm = fmaxf(m[mt], m1);
+          pm[static_cast<size_t>(r) * ncp + c] = mm;
+          pz[static_cast<size_t>(r) * ncp + c] = z[mt] * ex2_approx(m[mt] - mm) + z1 * ex2_approx(m1 - mm);
+          if (c == nch - 1)
+            for (int j = nch; j < ncp; ++j) {
+              pm[static_cast<size_t>(r) * ncp + j] = kNegBig;
+              pz[static_cast<size_t>(r) * ncp + j] = 0.f;
+            }
+        }
+      }
+    }
+    // ---------------- grid barrier: every chunk's partials are in memory ----------------
+    epi_bar();
+    if (threadIdx.x == 0) {
+      // only the chunks of this (request, head) are needed: one counter per head
+      unsigned int* cnt = grid_count + b * a.rq.H + h;
+      __threadfence();
+      atomicAdd(cnt, 1u);
+      const long long t0 = clock64();
+      while (true) {
+        const unsigned int v = *reinterpret_cast<volatile unsigned int*>(cnt);
+        if (v >= static_cast<unsigned int>(nch)) break;
+        if (*reinterpret_cast<volatile int*>(&s_abort) ||
+            static_cast<unsigned long long>(clock64() - t0) > a.wc.limit) {
+          s_abort = 1;
+          atomicOr(status, DEV_TIMEOUT_PIPE);
+          break;
+        }
+      }
+      __threadfence();
+    }
+    if (epi_any(!alive || *reinterpret_cast<volatile int*>(&s_abort) != 0)) alive = false;
+    if (alive) {
+      // merged row statistics c2[r] = m_r + log2 Z_r (log2 units)
+      for (int r = threadIdx.x; r < RP; r += kEpiWarps * 32) {
+        float c2v = 0.f;
+        if (r < R) {
+          const float4* m4 = reinterpret_cast<const float4*>(pm + static_cast<size_t>(r) * ncp);
+          const float4* z4 = reinterpret_cast<const float4*>(pz + static_cast<size_t>(r) * ncp);
+          float mm = kNegBig;
+#pragma unroll 4
+          for (int j = 0; j < ncp / 4; ++j) {
+            const float4 v = __ldcg(m4 + j);
+            mm = fmaxf(mm, fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)));
+          }
+          float zz = 0.f;
+#pragma unroll 4
+          for (int j = 0; j < ncp / 4; ++j) {
+            const float4 v = __ldcg(m4 + j), w = __ldcg(z4 + j);
+            zz += w.x * ex2_approx(v.x - mm) + w.y * ex2_approx(v.y - mm) + w.z * ex2_approx(v.z - mm) +
+                  w.w * ex2_approx(v.w - mm);
+          }
+          c2v = mm + lg2_approx(zz);
+        }
+        s_c2[r] = c2v;
+      }
+      epi_bar();
+      // ---------------- epilogue, pass 2: group g takes tiles g, g+2, ... ----------------
+      const int grp = cg;
+      const bool is_max = (a.reduce == 2);
+      const float row_scale = (a.reduce == 1) ? 1.f / static_cast<float>(R) : 1.f;
+      const size_t out_base = static_cast<size_t>(a.rq.soff[b]) + static_cast<size_t>(h) * n;
+      for (int t = grp; t < ntiles; t += 2) {
+        const int acc = t % kAcc2, ua = t / kAcc2;
+        bool ok = mbar_wait(&accf2[acc], ua & 1, &s_abort, a.wc);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc_fence_after();
+        const int key = key_begin + t * NT + q4 * 32 + lane;
+        const int wmin = a.causal ? key - (n - W) : -1;
+        float acc_sum = 0.f, acc_max = -INFINITY;
+        const uint32_t trow = tbase + (static_cast<uint32_t>(q4 * 32) << 16) + acc * kAccCols;
+#pragma unroll 1
+        for (int c0 = 0; c0 < R; c0 += 64) {
+          float v[64];
+          tmem_ld32(trow + c0, v);
+          tmem_ld32(trow + c0 + 32, v + 32);   // R is a multiple of 64 here (R_pad == R)
+          tmem_ld_wait();
+          if (wmin > 0) {
+            // causal tail: rows whose window position precedes the key do not see it
+            int w = c0 % W;
+#pragma unroll
+            for (int j = 0; j < 64; ++j) {
+              if (w < wmin) v[j] = -INFINITY;
+              w = (w + 1 == W) ? 0 : w + 1;
+            }
+          }
+          if (is_max) {
+            float y[64];
+#pragma unroll
+            for (int j = 0; j < 64; ++j) y[j] = fmaf(v[j], s2, -s_c2[c0 + j]);
+            acc_max = fmaxf(acc_max, tree_max<64>(y));
+          } else {
+            float p[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int j = 0; j < 64; j += 4) {
+              const float4 cc = *reinterpret_cast<const float4*>(&s_c2[c0 + j]);
+              p[(j >> 2) & 7] += ex2_approx(fmaf(v[j + 0], s2, -cc.x)) + ex2_approx(fmaf(v[j + 1], s2, -cc.y)) +
+                                 ex2_approx(fmaf(v[j + 2], s2, -cc.z)) + ex2_approx(fmaf(v[j + 3], s2, -cc.w));
+            }
+            acc_sum += ((p[0] + p[1]) + (p[2] + p[3])) + ((p[4] + p[5]) + (p[6] + p[7]));
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acce2[acc]);
+        if (key < n) a.s_raw[out_base + key] = is_max ? ex2_approx(acc_max) : acc_sum * row_scale;
+      }
+    }
+  }
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tbase, kTmemCols);
+  }
+}
+
 template <int MT, int NT, int STAGES>
 cudaError_t launch_rowstats_t(const WinScoreArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, cudaStream_t st) {
   const size_t smem = 1024 + 2 * MT * 128 * 128 + STAGES * NT * 256;
@@ -526,6 +875,40 @@ cudaError_t launch_win_rowstats(const WinScoreArgs& a, const CUtensorMap& tq, co
     case 2: return launch_rowstats_t<2, 128, 4>(a, tq, tk, st);
     default: return launch_rowstats_t<4, 64, 4>(a, tq, tk, st);
   }
+}
+
+// One cooperative launch for both passes when every chunk's CTA fits on the device at
+// once (R <= 256, one CTA per SM); returns cudaErrorNotSupported otherwise.
+cudaError_t launch_win_fused(const WinScoreArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
+                             unsigned int* grid_count, cudaStream_t st) {
+  if (a.ck.total <= 0) return cudaSuccess;
+  if (a.R > 256 || a.R_pad != a.R) return cudaErrorNotSupported;   // 64-column epilogue chunks
+  const int mt = a.R <= 128 ? 1 : 2;
+  const void* fn = mt == 1 ? reinterpret_cast<const void*>(win_fused_kernel<1>)
+                           : reinterpret_cast<const void*>(win_fused_kernel<2>);
+  const size_t smem = 1024 + 2 * static_cast<size_t>(mt) * 128 * 128 + (mt == 1 ? 5 : 4) * 128 * 256;
+  cudaError_t e = ensure_smem(fn, smem);
+  if (e != cudaSuccess) return e;
+  int dev = 0, sms = 0, per_sm = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kThreads, smem);
+  if (e != cudaSuccess) return e;
+  if (per_sm < 1 || a.ck.total > per_sm * sms) return cudaErrorNotSupported;
+  e = cudaMemsetAsync(grid_count, 0, sizeof(unsigned int) * a.rq.B * a.rq.H, st);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.ck.total, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (mt == 1) return cudaLaunchKernelEx(&cfg, win_fused_kernel<1>, tq, tk, a, grid_count);
+  return cudaLaunchKernelEx(&cfg, win_fused_kernel<2>, tq, tk, a, grid_count);
 }
 
 cudaError_t launch_win_keysum(const WinScoreArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, cudaStream_t st) {
