@@ -101,6 +101,7 @@ cudaError_t launch_win_fused(const WinScoreArgs& a, const CUtensorMap& tq, const
 cudaError_t launch_wbar(const uint16_t* w_o, uint16_t* wbar, int H, int G, int D, int wo_mode, cudaStream_t st);
 cudaError_t launch_vnorm(const VnormArgs& a, const CUtensorMap& tv, const CUtensorMap& tw, cudaStream_t st);
 int vnorm_token_block();
+int vnorm_w_tile_rows();
 
 cudaError_t launch_finalize(const ReqTable& rq, const float* s_raw, const float* nu, float* s_attn, float* s_val,
                             int pool, int pool_kernel, float eps, cudaStream_t st);
@@ -118,6 +119,14 @@ struct SelectArgs {
   int floor_h[kMaxBatch];         // per-layer mode: per-head floor
   const float* s1;                // stage-1 scores (s_attn)
   const float* s2;                // stage-2 scores (s_val) or null
+  // pooling fused into the selection (kvsel_run_layer): when raw != null the kernel pools
+  // raw (and combines with nu), writes out_attn / out_val, and selects on those values
+  const float* raw;
+  const float* nu;
+  float* out_attn;
+  float* out_val;
+  int pool, pool_kernel;
+  float eps;
   int32_t* idx;
   int32_t* counts;
   int64_t* offsets;               // written for every segment

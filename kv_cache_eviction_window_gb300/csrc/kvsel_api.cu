@@ -334,7 +334,7 @@ int check_ws(const Plan& pl, void* ws, size_t ws_bytes) {
 WaitCtl wait_ctl(void* ws) { return WaitCtl{g_wait_limit.load(), static_cast<int*>(ws)}; }
 
 int do_score(const kvsel_params* p, const Plan& pl, const void* q, const kvsel_kv* kv, const void* w_o, float* s_attn,
-             float* s_val, void* ws, cudaStream_t st) {
+             float* s_val, void* ws, cudaStream_t st, bool finalize = true) {
   uint8_t* wsb = static_cast<uint8_t*>(ws);
   float* part = reinterpret_cast<float*>(wsb + pl.ws_part);
   float* s_raw = reinterpret_cast<float*>(wsb + pl.ws_sraw);
@@ -372,6 +372,7 @@ int do_score(const kvsel_params* p, const Plan& pl, const void* q, const kvsel_k
     }
     if (rc) return rc;
     StageScope sc(KVSEL_STAGE_FINALIZE, st);
+    if (!finalize) return KVSEL_OK;   // pooling happens inside the selection (kvsel_run_layer)
     return launch_rc(launch_finalize(pl.rq, s_raw, nullptr, s_attn, nullptr, p->pool, p->pool_kernel, p->eps, st));
   }
 
@@ -436,7 +437,7 @@ int do_score(const kvsel_params* p, const Plan& pl, const void* q, const kvsel_k
     const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(pl.Dw),
                                 static_cast<cuuint64_t>(pl.H)};
     const cuuint64_t strides[2] = {kHeadDim * 2, static_cast<cuuint64_t>(pl.Dw) * kHeadDim * 2};
-    const cuuint32_t box[3] = {64, 128, 1};
+    const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(vnorm_w_tile_rows()), 1};
     if (!encode(&tw, wbar, 3, dims, strides, box)) return KVSEL_EINVAL;
     VnormArgs v{};
     v.rq = pl.rq;
@@ -455,13 +456,22 @@ int do_score(const kvsel_params* p, const Plan& pl, const void* q, const kvsel_k
     if (rc) return rc;
   }
   StageScope sc(KVSEL_STAGE_FINALIZE, st);
+  if (!finalize) return KVSEL_OK;   // pooling happens inside the selection (kvsel_run_layer)
   return launch_rc(launch_finalize(pl.rq, s_raw, nu, s_attn, p->value_aware ? s_val : nullptr, p->pool,
                                    p->pool_kernel, p->eps, st));
 }
 
 int do_select(const kvsel_params* p, const Plan& pl, const float* s_attn, const float* s_val, int32_t* idx,
-              int32_t* counts, int64_t* offsets, cudaStream_t st) {
+              int32_t* counts, int64_t* offsets, cudaStream_t st, const float* raw = nullptr,
+              const float* nu = nullptr, float* out_attn = nullptr, float* out_val = nullptr) {
   SelectArgs a{};
+  a.raw = raw;
+  a.nu = nu;
+  a.out_attn = out_attn;
+  a.out_val = out_val;
+  a.pool = p->pool;
+  a.pool_kernel = p->pool_kernel;
+  a.eps = p->eps;
   a.rq = pl.rq;
   a.mode = p->budget_mode;
   a.two_stage = p->value_aware ? 1 : 0;
@@ -609,8 +619,19 @@ int kvsel_run_layer(const kvsel_params* p, const void* q, const kvsel_kv* kv, co
   if ((rc = check_ws(pl, ws, ws_bytes))) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (pl.n_scores == 0) return KVSEL_OK;
-  if ((rc = do_score(p, pl, q, kv, w_o, s_attn, s_val, ws, st))) return rc;
-  if ((rc = do_select(p, pl, s_attn, s_val, idx, counts, offsets, st))) return rc;
+  // pooling and the value combination run inside the selection kernel when possible
+  const bool fuse_pool = (!p->pool || p->pool_kernel / 2 <= 32);
+  if ((rc = do_score(p, pl, q, kv, w_o, s_attn, s_val, ws, st, !fuse_pool))) return rc;
+  if (fuse_pool) {
+    uint8_t* wsb = static_cast<uint8_t*>(ws);
+    const float* raw = reinterpret_cast<const float*>(wsb + pl.ws_sraw);
+    const float* nu = p->value_aware ? reinterpret_cast<const float*>(wsb + pl.ws_nu) : nullptr;
+    if ((rc = do_select(p, pl, s_attn, s_val, idx, counts, offsets, st, raw, nu, s_attn,
+                        p->value_aware ? s_val : nullptr)))
+      return rc;
+  } else if ((rc = do_select(p, pl, s_attn, s_val, idx, counts, offsets, st))) {
+    return rc;
+  }
   if (pl.n_kept == 0) return KVSEL_OK;
   return do_compact(pl, kv, idx, counts, offsets, k_out, v_out, ws, st);
 }

@@ -31,6 +31,7 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kBins = 2048;
 constexpr uint32_t kKeyMax = 0xFFFFFFFFu;
 constexpr int kMaxHeads = 64;
+constexpr int kMaxHalo = 64;   // room for 2 * (pool_kernel / 2) staged neighbours of a chunk
 static_assert(kBins == 4 * kThreads, "digit search: four bins per thread");
 
 __device__ __forceinline__ uint32_t f2key(float f) {
@@ -263,7 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelectArgs a,
   extern __shared__ uint8_t smem_raw[];
   SelShared& S = *reinterpret_cast<SelShared*>(smem_raw);
   uint32_t* keys = reinterpret_cast<uint32_t*>(smem_raw + ((sizeof(SelShared) + 15) & ~static_cast<size_t>(15)));
-  uint8_t* flag = reinterpret_cast<uint8_t*>(keys + chunk_cap);
+  uint8_t* flag = reinterpret_cast<uint8_t*>(keys + chunk_cap + kMaxHalo);
 
   const unsigned CS = cl.num_blocks();
   const unsigned rank = cl.block_rank();
@@ -282,13 +283,46 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelectArgs a,
   const int ns = a.n_sink, nr = a.n_recent;
   const int nforced = min(n, ns + nr);
 
-  // stage-1 keys (forced entries at the top)
+  const bool pool_mode = a.raw != nullptr;
+  if (pool_mode) {
+    // stage the raw scores of [c_lo - half, c_hi + half) in the key array, pool each of
+    // this CTA's entries inside its own head, combine with nu, write the API outputs
+    const int half = a.pool != 0 ? a.pool_kernel / 2 : 0;
+    const int lo = max(0, c_lo - half), hi = min(L, c_hi + half);
+    float* stage = reinterpret_cast<float*>(keys);
+    for (int e = threadIdx.x; e < hi - lo; e += kThreads) stage[e] = __ldg(a.raw + sbase + lo + e);
+    __syncthreads();
+    for (int e = threadIdx.x; e < cnt; e += kThreads) {
+      const int g = c_lo + e;
+      const int i = per_layer ? g % n : g;
+      const int wlo = max(0, i - half) - i, whi = min(n - 1, i + half) - i;   // window offsets
+      float p;
+      if (a.pool == 1) {
+        p = stage[g - lo];
+        for (int d = wlo; d <= whi; ++d) p = fmaxf(p, stage[g + d - lo]);
+      } else if (a.pool == 2) {
+        float acc = 0.f;
+        for (int d = wlo; d <= whi; ++d) acc += stage[g + d - lo];
+        p = acc / static_cast<float>(a.pool_kernel);
+      } else {
+        p = stage[g - lo];
+      }
+      a.out_attn[sbase + g] = p;
+      if (a.out_val) a.out_val[sbase + g] = (p + a.eps) * __ldg(a.nu + sbase + g);
+    }
+    __syncthreads();   // the staged raw scores are no longer read
+  }
+  const float* s1 = pool_mode ? a.out_attn : a.s1;
+  const float* s2 = pool_mode ? a.out_val : a.s2;
+
+  // stage-1 keys (forced entries at the top); in pooling mode each thread reads back the
+  // values it wrote itself (same strided assignment), so plain loads suffice
   for (int e0 = 0; e0 < cnt; e0 += 4 * kThreads) {
     float v[4];
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int e = e0 + u * kThreads + threadIdx.x;
-      v[u] = e < cnt ? __ldg(a.s1 + sbase + c_lo + e) : 0.f;
+      v[u] = e < cnt ? (pool_mode ? s1[sbase + c_lo + e] : __ldg(s1 + sbase + c_lo + e)) : 0.f;
     }
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
@@ -320,7 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelectArgs a,
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           const int e = e0 + u * kThreads + threadIdx.x;
-          v[u] = e < cnt ? __ldg(a.s2 + sbase + c_lo + e) : 0.f;
+          v[u] = e < cnt ? (pool_mode ? s2[sbase + c_lo + e] : __ldg(s2 + sbase + c_lo + e)) : 0.f;
         }
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
@@ -388,7 +422,7 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelectArgs a,
 }
 
 size_t select_smem(int chunk_cap) {
-  return ((sizeof(SelShared) + 15) & ~static_cast<size_t>(15)) + static_cast<size_t>(chunk_cap) * 5 + 16;
+  return ((sizeof(SelShared) + 15) & ~static_cast<size_t>(15)) + static_cast<size_t>(chunk_cap + kMaxHalo) * 5 + 16;
 }
 
 }  // namespace

@@ -278,6 +278,7 @@ __global__ void wbar_kernel(const uint16_t* __restrict__ w_o, uint16_t* __restri
 }  // namespace
 
 int vnorm_token_block() { return kTokBlock; }
+int vnorm_w_tile_rows() { return kNT; }
 
 cudaError_t launch_wbar(const uint16_t* w_o, uint16_t* wbar, int H, int G, int D, int wo_mode, cudaStream_t st) {
   const long long total = static_cast<long long>(H) * D * 16;

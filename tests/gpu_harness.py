@@ -19,8 +19,10 @@ def torch_bf16(u16, device="cuda"):
     return torch.from_numpy(np.ascontiguousarray(u16).view(np.int16)).view(torch.bfloat16).to(device)
 
 
-def run_gpu_layer(wl, inp, paged=None, ws_pad=0, **override):
-    """Run kvsel_run_layer on one layer of seeded inputs; return numpy outputs per request."""
+def run_gpu_layer(wl, inp, paged=None, ws_pad=0, split=False, **override):
+    """Run kvsel_run_layer on one layer of seeded inputs; return numpy outputs per request.
+    With split=True the three stages are called one by one (kvsel_score, kvsel_select,
+    kvsel_compact) instead, which pools in its own kernel rather than inside the selection."""
     import torch
     from kv_cache_eviction_window_gb300 import binding as B
 
@@ -49,8 +51,13 @@ def run_gpu_layer(wl, inp, paged=None, ws_pad=0, **override):
         keep = (kt, vt)
     w_o = torch_bf16(inp["w_o"]) if inp["w_o"] is not None and p.value_aware else None
     buf = B.LayerBuffers(p)
-    B.kvsel_run_layer(p, q, kv, w_o, buf.s_attn, buf.s_val, buf.idx, buf.counts, buf.offsets, buf.k_out,
-                      buf.v_out, buf.ws)
+    if split:
+        B.kvsel_score(p, q, kv, w_o, buf.s_attn, buf.s_val, buf.ws)
+        B.kvsel_select(p, buf.s_attn, buf.s_val, buf.idx, buf.counts, buf.offsets, buf.ws)
+        B.kvsel_compact(p, kv, buf.idx, buf.counts, buf.offsets, buf.k_out, buf.v_out, buf.ws)
+    else:
+        B.kvsel_run_layer(p, q, kv, w_o, buf.s_attn, buf.s_val, buf.idx, buf.counts, buf.offsets, buf.k_out,
+                          buf.v_out, buf.ws)
     torch.cuda.synchronize()
     status = B.kvsel_get_device_status(buf.ws)
     del keep

@@ -139,6 +139,33 @@ def test_reductions_and_pooling(reduce, pool, causal):
     _check_layer(wl, inp, gpu, ora)
 
 
+@pytest.mark.parametrize("cid,n,kw", [
+    (1, 1111, dict(pool="max", pool_kernel=7)),
+    (2, 1500, dict()),                                   # value-aware, two-stage, avg pooling
+    (3, 1333, dict()),                                   # per-layer budget with floors
+    (1, 1111, dict(pool="avg", pool_kernel=67)),         # halo wider than the fused staging
+])
+def test_split_calls_match_run_layer(cid, n, kw):
+    """kvsel_score + kvsel_select + kvsel_compact give exactly what kvsel_run_layer gives
+    (the latter pools inside the selection), and both match the oracle."""
+    wl = datagen.WORKLOADS[cid].replace(**kw)
+    if cid == 2:
+        wl = wl.replace(layers=1, h_kv=2, d_model=1024)
+    inp = datagen.make_layer(wl, 0, n_ctx=n)
+    ora = O.run_workload_layer(wl, inp)
+    fused = GH.run_gpu_layer(wl, inp)
+    split = GH.run_gpu_layer(wl, inp, split=True)
+    _check_layer(wl, inp, fused, ora)
+    for a, b in zip(fused, split):
+        np.testing.assert_array_equal(a["s_attn"], b["s_attn"])
+        if a["s_val"] is not None:
+            np.testing.assert_array_equal(a["s_val"], b["s_val"])
+        for h in range(wl.h_kv):
+            np.testing.assert_array_equal(a["idx"][h], b["idx"][h])
+            np.testing.assert_array_equal(a["k_out"][h], b["k_out"][h])
+            np.testing.assert_array_equal(a["v_out"][h], b["v_out"][h])
+
+
 def test_budget_equals_n_identity():
     wl = datagen.WORKLOADS[1].replace(budget_ratio=1.0, h_kv=2)
     inp = datagen.make_layer(wl, 0, n_ctx=600)
