@@ -211,7 +211,8 @@ enum {
   KVSEL_STAGE_KEYSUM = 1,    /* window scoring pass 2: per-key reduced probabilities */
   KVSEL_STAGE_WBAR = 2,      /* value-aware: W_O slices of each KV head, bf16        */
   KVSEL_STAGE_VNORM = 3,     /* value-aware: ||W_h v||_1 per token (tensor cores)    */
-  KVSEL_STAGE_FINALIZE = 4,  /* pooling and (s + eps) * nu                           */
+  KVSEL_STAGE_FINALIZE = 4,  /* pooling and (s + eps) * nu (inside the selection     
+                                launch on the kvsel_run_layer path)                   */
   KVSEL_STAGE_SELECT = 5,    /* top-B selection                                      */
   KVSEL_STAGE_COMPACT = 6,   /* gather of the kept K/V rows                          */
   KVSEL_STAGE_COUNT = 7
@@ -223,6 +224,11 @@ enum {
  * `events` is a host array of 2*KVSEL_STAGE_COUNT cudaEvent_t created by the caller and
  * must stay valid until the hook is cleared with NULL.  No effect on results. */
 void kvsel_set_stage_events(void* const* events);
+
+/* Number of kernels this library has launched in this process so far (all devices and
+ * threads; a launch recorded into a CUDA graph under stream capture counts once, at
+ * capture).  The difference across a call is that call's kernel count.  Never fails. */
+uint64_t kvsel_launch_count(void);
 
 /* Static description of an error code. */
 const char* kvsel_strerror(int code);

@@ -33,7 +33,7 @@ MAX_BATCH = 128
 EXPORTS = ("kvsel_workspace_size", "kvsel_output_size", "kvsel_workspace_init", "kvsel_score",
            "kvsel_select", "kvsel_compact", "kvsel_run_layer", "kvsel_get_device_status",
            "kvsel_set_wait_limit", "kvsel_set_stage_events", "kvsel_strerror", "kvsel_version",
-           "kvsel_score_noalloc")
+           "kvsel_score_noalloc", "kvsel_launch_count")
 NOALLOC_SCRATCH_BYTES = 16 << 20
 STAGES = ("rowstats", "keysum", "wbar", "vnorm", "finalize", "select", "compact")
 
@@ -102,6 +102,7 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
         "kvsel_score_noalloc": ([P, vp, K, vp, vp, vp, vp], ctypes.c_int),
         "kvsel_strerror": ([ctypes.c_int], ctypes.c_char_p),
         "kvsel_version": ([], ctypes.c_char_p),
+        "kvsel_launch_count": ([], ctypes.c_uint64),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -209,6 +210,10 @@ def kvsel_version() -> str:
 
 def kvsel_strerror(code: int) -> str:
     return load().kvsel_strerror(code).decode()
+
+
+def kvsel_launch_count() -> int:
+    return int(load().kvsel_launch_count())
 
 
 def kvsel_set_wait_limit(cycles: int) -> None:

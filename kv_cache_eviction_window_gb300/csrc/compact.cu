@@ -84,6 +84,7 @@ cudaError_t launch_compact(const CompactArgs& a, int max_count, int num_sms, cud
   const int want = (num_sms * 8 + segs - 1) / segs;
   if (gx > want) gx = want > 0 ? want : 1;
   compact_kernel<<<dim3(gx, segs), kThreads, 0, st>>>(a);
+  note_launch();
   return cudaGetLastError();
 }
 

@@ -49,6 +49,7 @@ cudaError_t launch_finalize(const ReqTable& rq, const float* s_raw, const float*
   int gx = (nmax + threads - 1) / threads;
   if (gx > 1024) gx = 1024;
   finalize_kernel<<<dim3(gx, rq.B * rq.H), threads, 0, st>>>(rq, s_raw, nu, s_attn, s_val, pool, pool_kernel, eps);
+  note_launch();
   return cudaGetLastError();
 }
 

@@ -12,6 +12,13 @@ namespace kvsel {
 
 constexpr int kMaxBatch = 128;
 constexpr int kHeadDim = 128;
+// workspace layout: device status word, then the fused scoring kernel's grid-barrier
+// counters (an arrival and a departure count per (request, head)), then the plan's buffers
+constexpr size_t kStatusBytes = 256;
+// counts every kernel launch (or graph capture of one) made by this library
+void note_launch();
+
+constexpr size_t kCounterBytes = 2 * 4 * static_cast<size_t>(kMaxBatch) * 64;
 
 // Per-request table passed by value to kernels.
 struct ReqTable {

@@ -34,14 +34,14 @@ cudaError_t ensure_smem(const void* func, size_t bytes) {
   }
   return e;
 }
+
+std::atomic<unsigned long long> g_launches{0};
+void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 }  // namespace kvsel
 
 namespace {
 
 std::atomic<unsigned long long> g_wait_limit{2000000000ull};   // ~1 s at the boost clock
-
-constexpr size_t kStatusBytes = 256;
-constexpr size_t kCounterBytes = 4 * kMaxBatch * 64;   // grid-barrier counters, one per (request, head)
 
 thread_local void* const* t_stage_events = nullptr;
 
@@ -524,6 +524,8 @@ int do_compact(const Plan& pl, const kvsel_kv* kv, const int32_t* idx, const int
 
 extern "C" {
 
+uint64_t kvsel_launch_count(void) { return kvsel::g_launches.load(std::memory_order_relaxed); }
+
 const char* kvsel_version(void) { return "kvsel 0.1 (sm_103a)"; }
 
 const char* kvsel_strerror(int code) {
@@ -565,7 +567,10 @@ int kvsel_output_size(const kvsel_params* p, int64_t* n_scores, int64_t* n_kept,
 
 int kvsel_workspace_init(void* ws, size_t ws_bytes, void* stream) {
   if (!ws || ws_bytes < kStatusBytes) return KVSEL_EWORKSPACE;
-  return launch_rc(cudaMemsetAsync(ws, 0, kStatusBytes, static_cast<cudaStream_t>(stream)));
+  // status word and, when the workspace holds them, the grid-barrier counters (they reset
+  // themselves after every use, so one zeroing at allocation is enough)
+  const size_t n = ws_bytes >= kStatusBytes + kCounterBytes ? kStatusBytes + kCounterBytes : kStatusBytes;
+  return launch_rc(cudaMemsetAsync(ws, 0, n, static_cast<cudaStream_t>(stream)));
 }
 
 int kvsel_score(const kvsel_params* p, const void* q, const kvsel_kv* kv, const void* w_o, float* s_attn,

@@ -54,7 +54,10 @@ extern "C" int kvsel_score_noalloc(const kvsel_params* p, const void* q, const k
   if (need > KVSEL_NOALLOC_SCRATCH_BYTES) return KVSEL_EWORKSPACE;
   void* scratch = nullptr;
   if ((rc = scratch_address(&scratch))) return rc;
-  // the status word must start at zero for this call; everything else is rewritten
-  if (cudaMemsetAsync(scratch, 0, 256, static_cast<cudaStream_t>(stream)) != cudaSuccess) return KVSEL_ECUDA;
+  // the status word and the barrier counters start at zero for this call; everything else
+  // is rewritten
+  if (cudaMemsetAsync(scratch, 0, kvsel::kStatusBytes + kvsel::kCounterBytes, static_cast<cudaStream_t>(stream)) !=
+      cudaSuccess)
+    return KVSEL_ECUDA;
   return kvsel_score(p, q, kv, w_o, s_attn, s_val, scratch, KVSEL_NOALLOC_SCRATCH_BYTES, stream);
 }

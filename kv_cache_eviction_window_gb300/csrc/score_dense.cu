@@ -392,6 +392,7 @@ cudaError_t launch_qa_rowlse(const QaArgs& a, const CUtensorMap& tq, const CUten
   cudaError_t e = ensure_smem(reinterpret_cast<const void*>(qa_rowlse_kernel), smem);
   if (e != cudaSuccess) return e;
   qa_rowlse_kernel<<<a.H * a.row_blocks, kThreads, smem, st>>>(tq, tk, a);
+  note_launch();
   return cudaGetLastError();
 }
 
@@ -402,11 +403,13 @@ cudaError_t launch_qa_keymax(const QaArgs& a, const CUtensorMap& tq, const CUten
   e = cudaMemsetAsync(a.tmax, 0, static_cast<size_t>(a.H) * a.n * sizeof(uint32_t), st);
   if (e != cudaSuccess) return e;
   qa_keymax_kernel<<<a.H * a.key_blocks * a.row_splits, kThreads, smem, st>>>(tq, tk, a);
+  note_launch();
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const long long total = static_cast<long long>(a.H) * a.n;
   const int blocks = static_cast<int>((total + 255) / 256 < 4096 ? (total + 255) / 256 : 4096);
   qa_finish_kernel<<<blocks, 256, 0, st>>>(a.tmax, a.s_raw, total);
+  note_launch();
   return cudaGetLastError();
 }
 

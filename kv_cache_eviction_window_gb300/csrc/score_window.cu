@@ -46,27 +46,35 @@ __device__ __forceinline__ bool epi_any(bool pred) {
   return r != 0;
 }
 
-// max of v[0..N) as a balanced tree (short dependency chain)
+// max of v[0..N): four independent chains of three-input max
 template <int N>
 __device__ __forceinline__ float tree_max(const float* v) {
-  float t[N / 2];
+  static_assert(N % 8 == 0, "N must be a multiple of 8");
+  float t[4] = {v[0], v[1], v[2], v[3]};
 #pragma unroll
-  for (int i = 0; i < N / 2; ++i) t[i] = fmaxf(v[2 * i], v[2 * i + 1]);
+  for (int j = 4; j < N - 4; j += 8) {
 #pragma unroll
-  for (int w = N / 4; w >= 1; w >>= 1) {
-#pragma unroll
-    for (int i = 0; i < w; ++i) t[i] = fmaxf(t[2 * i], t[2 * i + 1]);
+    for (int c = 0; c < 4; ++c) t[c] = fmax3(t[c], v[j + 2 * c], v[j + 2 * c + 1]);
   }
-  return t[0];
+  // the loop above covers v[4 .. N-4); the last four values close the chains
+  return fmax3(fmax3(t[0], t[1], v[N - 4]), fmax3(t[2], t[3], v[N - 3]), fmaxf(v[N - 2], v[N - 1]));
 }
 
-// sum of exp2(v[j] * s2 - mn) over j < N, in eight independent accumulators
+// sum of exp2(v[j] * s2 + c) over j < N: packed two-lane FMA and add, four accumulators
 template <int N>
 __device__ __forceinline__ float exp2_sum(const float* v, float s2, float mn) {
-  float p[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  static_assert(N % 8 == 0, "N must be a multiple of 8");
+  const uint64_t s2p = pack2(s2, s2), nm = pack2(-mn, -mn);
+  uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
-  for (int j = 0; j < N; ++j) p[j & 7] += ex2_approx(fmaf(v[j], s2, -mn));
-  return ((p[0] + p[1]) + (p[2] + p[3])) + ((p[4] + p[5]) + (p[6] + p[7]));
+  for (int j = 0; j < N; j += 2) {
+    float x0, x1;
+    unpack2(ffma2(pack2(v[j], v[j + 1]), s2p, nm), x0, x1);
+    acc[(j >> 1) & 3] = fadd2(acc[(j >> 1) & 3], pack2(ex2_approx(x0), ex2_approx(x1)));
+  }
+  float a0, a1;
+  unpack2(fadd2(fadd2(acc[0], acc[1]), fadd2(acc[2], acc[3])), a0, a1);
+  return a0 + a1;
 }
 
 __host__ __device__ constexpr uint32_t pow2_cols(uint32_t c) {
@@ -522,13 +530,53 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ------------------------------------------------------------------------------------
 // both passes in one cooperative launch (one key chunk per CTA, all CTAs co-resident)
 // ------------------------------------------------------------------------------------
-// pass 1 as win_rowstats_kernel; then a bounded grid barrier (the row partials of every
-// chunk are written); then pass 2 over the CTA's own chunk, whose K tiles are still in
-// L2.  The TMA producer and the UMMA warp run straight on into pass 2 (K and Q do not
-// depend on the barrier); only the epilogue waits.  In pass 2 the two epilogue warp
-// groups take alternate tiles and each thread owns one key over all R rows.
+// Pass 1 as win_rowstats_kernel; then a bounded grid barrier (the row partials of every
+// chunk of this (request, head) are written); then pass 2 over the CTA's own chunk, whose
+// K tiles are still in L2.  The TMA producer and the UMMA warp run straight on into
+// pass 2 (K and Q do not depend on the barrier); only the epilogue waits.
+//
+// The epilogue has 16 warps, four per TMEM lane quadrant, so that every SM sub-partition
+// keeps four warps of exponentials in flight.  Pass 1: each warp takes a 32-key column
+// group of every tile.  Pass 2: two groups of eight warps take alternate tiles; in a
+// group the two warps of a lane quadrant split the window rows in halves and add their
+// partial sums through shared memory.
+constexpr int kFEpiWarps = 16;
+constexpr int kFProducerWarp = 16;
+constexpr int kFMmaWarp = 17;
+constexpr int kFThreads = 576;
+
+__device__ __forceinline__ void fused_epi_bar() { asm volatile("bar.sync 1, 512;" ::: "memory"); }
+
+__device__ __forceinline__ bool fused_epi_any(bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, 1, 512, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(pred))
+      : "memory");
+  return r != 0;
+}
+
+// barrier over the 256 threads of pass-2 group `grp` that ANDs a predicate across them
+__device__ __forceinline__ bool group_all(int grp, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, %2, 256, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(pred)), "r"(2 + grp)
+      : "memory");
+  return r != 0;
+}
+__device__ __forceinline__ void group_bar(int grp) { asm volatile("bar.sync %0, 256;" ::"r"(4 + grp) : "memory"); }
+
 template <int MT>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kFThreads, 1)
     win_fused_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                      const WinScoreArgs a, unsigned int* grid_count) {
   constexpr int NT = 128, STAGES = (MT == 1) ? 5 : 4, kAcc = 2;
@@ -537,7 +585,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr uint32_t kTmemCols = 512;
   constexpr int kQHalf = MT * 128 * 128;
   constexpr int kKStage = NT * 256;
-  constexpr int kCh = NT / 2;
+  constexpr int kCg = 32;                            // pass-1 keys per warp and tile
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
@@ -549,8 +597,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ __align__(8) uint64_t q_bar, done_bar;
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
-  __shared__ float s_xm[MT][4][32], s_xz[MT][4][32];
-  __shared__ __align__(16) float s_c2[MT * 128];
+  __shared__ float s_xm[MT][4][128], s_xz[MT][4][128];   // pass-1 partials per column group
+  __shared__ __align__(16) float s_nc2[MT * 128];          // -(m_r + log2 Z_r) per window row
+  __shared__ float s_part[2][128];                         // pass-2 half sums per group
 
   const int warp = warp_id(), lane = lane_id();
   int b, h, c;
@@ -569,18 +618,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int s = 0; s < kAcc; ++s) {
       mbar_init(&accf1[s], 1);
-      mbar_init(&acce1[s], kEpiWarps);
+      mbar_init(&acce1[s], kFEpiWarps);
     }
     for (int s = 0; s < kAcc2; ++s) {
       mbar_init(&accf2[s], 1);
-      mbar_init(&acce2[s], kEpiWarps / 2);
+      mbar_init(&acce2[s], kFEpiWarps / 2);
     }
     mbar_init(&q_bar, 1);
     mbar_init(&done_bar, 1);
     s_abort = 0;
     fence_mbar_init();
   }
-  if (warp == kMmaWarp) {
+  if (warp == kFMmaWarp) {
     tmem_alloc(&s_tmem, kTmemCols);
     tmem_relinquish();
   }
@@ -589,7 +638,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tbase = s_tmem;
 
-  if (warp == kProducerWarp) {
+  if (warp == kFProducerWarp) {
     if (lane == 0 && ntiles > 0) {
       tma_prefetch_desc(&tq);
       tma_prefetch_desc(&tk);
@@ -606,7 +655,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int tt = max(0, T - STAGES); tt < T; ++tt) mbar_drain(&full_bar[tt % STAGES], (tt / STAGES) & 1, status);
       mbar_drain(&q_bar, 0, status);
     }
-  } else if (warp == kMmaWarp) {
+  } else if (warp == kFMmaWarp) {
     if (lane == 0 && ntiles > 0) {
       bool ok = mbar_wait(&q_bar, 0, &s_abort, a.wc);
       const uint32_t qbase = smem_u32(sQ);
@@ -676,7 +725,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_drain(&done_bar, 0, status);
     }
   } else {
-    // ---------------- epilogue, pass 1 (column halves, as win_rowstats_kernel) ----------------
+    // ---------------- epilogue, pass 1: warp (q4, cg) takes keys [32cg, 32cg + 32) of a tile ----------------
     const int q4 = warp & 3, cg = warp >> 2;
     const float s2 = a.s2;
     const int W = a.W;
@@ -697,49 +746,52 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       tc_fence_after();
-      const int kcol0 = key_begin + t * NT + cg * kCh;
+      float v[MT][kCg];
+      const uint32_t taddr = tbase + (static_cast<uint32_t>(q4 * 32) << 16) + acc * kAccCols + cg * kCg;
 #pragma unroll
-      for (int mt = 0; mt < MT; ++mt) {
-        float v[kCh];
-        const uint32_t taddr = tbase + (static_cast<uint32_t>(q4 * 32) << 16) + acc * kAccCols + mt * NT + cg * kCh;
-#pragma unroll
-        for (int j = 0; j < kCh / 32; ++j) tmem_ld32(taddr + j * 32, v + j * 32);
-        tmem_ld_wait();
-        const int r = mt * 128 + q4 * 32 + lane;
-        if (!(kcol0 + kCh <= lim_all) || r >= R) {
-          const int lim_r = (r >= R) ? -1 : (a.causal ? min(n - 1, n - W + (r % W)) : n - 1);
-#pragma unroll
-          for (int j = 0; j < kCh; ++j)
-            if (kcol0 + j > lim_r) v[j] = -INFINITY;
-        }
-        const float mn = fmaxf(m[mt], tree_max<kCh>(v) * s2);
-        z[mt] = z[mt] * ex2_approx(m[mt] - mn) + exp2_sum<kCh>(v, s2, mn);
-        m[mt] = mn;
-      }
+      for (int mt = 0; mt < MT; ++mt) tmem_ld32(taddr + mt * NT, v[mt]);
+      tmem_ld_wait();
+      // the logits are in registers: hand the accumulator back to the UMMA warp now
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&acce1[acc]);
-    }
-    if (cg == 1) {
+      const int kcol0 = key_begin + t * NT + cg * kCg;
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt) {
-        s_xm[mt][q4][lane] = m[mt];
-        s_xz[mt][q4][lane] = z[mt];
+        const int r = mt * 128 + q4 * 32 + lane;
+        if (!(kcol0 + kCg <= lim_all) || r >= R) {
+          const int lim_r = (r >= R) ? -1 : (a.causal ? min(n - 1, n - W + (r % W)) : n - 1);
+#pragma unroll
+          for (int j = 0; j < kCg; ++j)
+            if (kcol0 + j > lim_r) v[mt][j] = -INFINITY;
+        }
+        const float mn = fmaxf(m[mt], tree_max<kCg>(v[mt]) * s2);
+        z[mt] = z[mt] * ex2_approx(m[mt] - mn) + exp2_sum<kCg>(v[mt], s2, mn);
+        m[mt] = mn;
       }
     }
-    epi_bar();
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+      s_xm[mt][cg][q4 * 32 + lane] = m[mt];
+      s_xz[mt][cg][q4 * 32 + lane] = z[mt];
+    }
+    fused_epi_bar();
     const int nch = a.ck.per_head[b], ncp = chunk_pad(nch);
     float* pm = a.part + (static_cast<size_t>(a.ck.pbase[b]) + static_cast<size_t>(h) * ncp) * 2 * RP;
     float* pz = pm + static_cast<size_t>(RP) * ncp;
     if (cg == 0) {
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt) {
-        const int r = mt * 128 + q4 * 32 + lane;
+        const int rl = q4 * 32 + lane, r = mt * 128 + rl;
         if (r < R) {
-          const float m1 = s_xm[mt][q4][lane], z1 = s_xz[mt][q4][lane];
-          const float mm = fmaxf(m[mt], m1);
+          float mm = s_xm[mt][0][rl];
+#pragma unroll
+          for (int g = 1; g < 4; ++g) mm = fmaxf(mm, s_xm[mt][g][rl]);
+          float zz = 0.f;
+#pragma unroll
+          for (int g = 0; g < 4; ++g) zz += s_xz[mt][g][rl] * ex2_approx(s_xm[mt][g][rl] - mm);
           pm[static_cast<size_t>(r) * ncp + c] = mm;
-          pz[static_cast<size_t>(r) * ncp + c] = z[mt] * ex2_approx(m[mt] - mm) + z1 * ex2_approx(m1 - mm);
+          pz[static_cast<size_t>(r) * ncp + c] = zz;
           if (c == nch - 1)
             for (int j = nch; j < ncp; ++j) {
               pm[static_cast<size_t>(r) * ncp + j] = kNegBig;
@@ -749,15 +801,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     // ---------------- grid barrier: every chunk's partials are in memory ----------------
-    epi_bar();
+    fused_epi_bar();
     if (threadIdx.x == 0) {
-      // only the chunks of this (request, head) are needed: one counter per head
-      unsigned int* cnt = grid_count + b * a.rq.H + h;
+      // only the chunks of this (request, head) are needed: an arrival and a departure
+      // count per head.  Every CTA arrives and departs exactly once (also after a timeout),
+      // and the last to depart zeroes both, so the counters are ready for the next launch
+      // without a memset.
+      unsigned int* arrive = grid_count + 2 * (b * a.rq.H + h);
+      unsigned int* depart = arrive + 1;
       __threadfence();
-      atomicAdd(cnt, 1u);
+      atomicAdd(arrive, 1u);
       const long long t0 = clock64();
       while (true) {
-        const unsigned int v = *reinterpret_cast<volatile unsigned int*>(cnt);
+        const unsigned int v = *reinterpret_cast<volatile unsigned int*>(arrive);
         if (v >= static_cast<unsigned int>(nch)) break;
         if (*reinterpret_cast<volatile int*>(&s_abort) ||
             static_cast<unsigned long long>(clock64() - t0) > a.wc.limit) {
@@ -767,57 +823,70 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       __threadfence();
-    }
-    if (epi_any(!alive || *reinterpret_cast<volatile int*>(&s_abort) != 0)) alive = false;
-    if (alive) {
-      // merged row statistics c2[r] = m_r + log2 Z_r (log2 units)
-      for (int r = threadIdx.x; r < RP; r += kEpiWarps * 32) {
-        float c2v = 0.f;
-        if (r < R) {
-          const float4* m4 = reinterpret_cast<const float4*>(pm + static_cast<size_t>(r) * ncp);
-          const float4* z4 = reinterpret_cast<const float4*>(pz + static_cast<size_t>(r) * ncp);
-          float mm = kNegBig;
-#pragma unroll 4
-          for (int j = 0; j < ncp / 4; ++j) {
-            const float4 v = __ldcg(m4 + j);
-            mm = fmaxf(mm, fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)));
-          }
-          float zz = 0.f;
-#pragma unroll 4
-          for (int j = 0; j < ncp / 4; ++j) {
-            const float4 v = __ldcg(m4 + j), w = __ldcg(z4 + j);
-            zz += w.x * ex2_approx(v.x - mm) + w.y * ex2_approx(v.y - mm) + w.z * ex2_approx(v.z - mm) +
-                  w.w * ex2_approx(v.w - mm);
-          }
-          c2v = mm + lg2_approx(zz);
-        }
-        s_c2[r] = c2v;
+      if (atomicAdd(depart, 1u) == static_cast<unsigned int>(nch) - 1u) {
+        atomicExch(arrive, 0u);
+        atomicExch(depart, 0u);
       }
-      epi_bar();
-      // ---------------- epilogue, pass 2: group g takes tiles g, g+2, ... ----------------
-      const int grp = cg;
+    }
+    if (fused_epi_any(!alive || *reinterpret_cast<volatile int*>(&s_abort) != 0)) alive = false;
+    if (alive) {
+      // merged row statistics c2[r] = m_r + log2 Z_r (log2 units): warp w takes rows w, w+16, ...,
+      // lanes over chunks; every load is issued before the first reduction
+      constexpr int kRowsPerWarp = MT * 128 / kFEpiWarps;
+      float lm[kRowsPerWarp][2], lz[kRowsPerWarp][2];
+#pragma unroll
+      for (int k = 0; k < kRowsPerWarp; ++k) {
+        const int r = warp + k * kFEpiWarps;
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int j = lane + 32 * u;
+          const bool in = r < R && j < ncp;
+          lm[k][u] = in ? __ldcg(pm + static_cast<size_t>(r) * ncp + j) : kNegBig;
+          lz[k][u] = in ? __ldcg(pz + static_cast<size_t>(r) * ncp + j) : 0.f;
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < kRowsPerWarp; ++k) {
+        const int r = warp + k * kFEpiWarps;
+        float mm = fmaxf(lm[k][0], lm[k][1]);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mm = fmaxf(mm, __shfl_xor_sync(0xffffffffu, mm, o));
+        float zz = lz[k][0] * ex2_approx(lm[k][0] - mm) + lz[k][1] * ex2_approx(lm[k][1] - mm);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) zz += __shfl_xor_sync(0xffffffffu, zz, o);
+        if (lane == 0 && r < RP) s_nc2[r] = r < R ? -(mm + lg2_approx(zz)) : 0.f;
+      }
+      fused_epi_bar();
+      // ---------------- epilogue, pass 2: group g takes tiles g, g+2, ...; halves split the rows ----------------
+      const int grp = cg >> 1, hf = cg & 1;
+      const int Rh = R / 2;   // a multiple of 32
       const bool is_max = (a.reduce == 2);
       const float row_scale = (a.reduce == 1) ? 1.f / static_cast<float>(R) : 1.f;
       const size_t out_base = static_cast<size_t>(a.rq.soff[b]) + static_cast<size_t>(h) * n;
       for (int t = grp; t < ntiles; t += 2) {
         const int acc = t % kAcc2, ua = t / kAcc2;
-        bool ok = mbar_wait(&accf2[acc], ua & 1, &s_abort, a.wc);
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok) break;
+        const bool ok = mbar_wait(&accf2[acc], ua & 1, &s_abort, a.wc);
+        if (!group_all(grp, ok)) break;   // the eight warps of the group leave together
         tc_fence_after();
         const int key = key_begin + t * NT + q4 * 32 + lane;
         const int wmin = a.causal ? key - (n - W) : -1;
         float acc_sum = 0.f, acc_max = -INFINITY;
-        const uint32_t trow = tbase + (static_cast<uint32_t>(q4 * 32) << 16) + acc * kAccCols;
+        const uint32_t trow = tbase + (static_cast<uint32_t>(q4 * 32) << 16) + acc * kAccCols + hf * Rh;
 #pragma unroll 1
-        for (int c0 = 0; c0 < R; c0 += 64) {
+        for (int c0 = 0; c0 < Rh; c0 += 64) {
+          const int ca = hf * Rh + c0;   // window row of column 0 of this chunk
+          const bool two = c0 + 32 < Rh;
           float v[64];
           tmem_ld32(trow + c0, v);
-          tmem_ld32(trow + c0 + 32, v + 32);   // R is a multiple of 64 here (R_pad == R)
+          if (two) tmem_ld32(trow + c0 + 32, v + 32);
           tmem_ld_wait();
+          if (!two) {
+#pragma unroll
+            for (int j = 32; j < 64; ++j) v[j] = -INFINITY;
+          }
           if (wmin > 0) {
             // causal tail: rows whose window position precedes the key do not see it
-            int w = c0 % W;
+            int w = ca % W;
 #pragma unroll
             for (int j = 0; j < 64; ++j) {
               if (w < wmin) v[j] = -INFINITY;
@@ -825,32 +894,43 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           if (is_max) {
-            float y[64];
 #pragma unroll
-            for (int j = 0; j < 64; ++j) y[j] = fmaf(v[j], s2, -s_c2[c0 + j]);
-            acc_max = fmaxf(acc_max, tree_max<64>(y));
+            for (int j = 0; j < 64; ++j) v[j] = fmaf(v[j], s2, s_nc2[min(ca + j, R - 1)]);
+            acc_max = fmaxf(acc_max, tree_max<64>(v));
           } else {
-            float p[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            // exp2(l * s2 - c2_r): packed FMA with the row constants read as pairs
+            const uint64_t s2p = pack2(s2, s2);
+            uint64_t p2[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
             for (int j = 0; j < 64; j += 4) {
-              const float4 cc = *reinterpret_cast<const float4*>(&s_c2[c0 + j]);
-              p[(j >> 2) & 7] += ex2_approx(fmaf(v[j + 0], s2, -cc.x)) + ex2_approx(fmaf(v[j + 1], s2, -cc.y)) +
-                                 ex2_approx(fmaf(v[j + 2], s2, -cc.z)) + ex2_approx(fmaf(v[j + 3], s2, -cc.w));
+              const float4 cc = *reinterpret_cast<const float4*>(&s_nc2[min(ca + j, RP - 4)]);
+              float x0, x1, x2, x3;
+              unpack2(ffma2(pack2(v[j + 0], v[j + 1]), s2p, pack2(cc.x, cc.y)), x0, x1);
+              unpack2(ffma2(pack2(v[j + 2], v[j + 3]), s2p, pack2(cc.z, cc.w)), x2, x3);
+              p2[(j >> 2) & 3] = fadd2(p2[(j >> 2) & 3], pack2(ex2_approx(x0), ex2_approx(x1)));
+              p2[(j >> 2) & 3] = fadd2(p2[(j >> 2) & 3], pack2(ex2_approx(x2), ex2_approx(x3)));
             }
-            acc_sum += ((p[0] + p[1]) + (p[2] + p[3])) + ((p[4] + p[5]) + (p[6] + p[7]));
+            float q0, q1;
+            unpack2(fadd2(fadd2(p2[0], p2[1]), fadd2(p2[2], p2[3])), q0, q1);
+            acc_sum += q0 + q1;
           }
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&acce2[acc]);
-        if (key < n) a.s_raw[out_base + key] = is_max ? ex2_approx(acc_max) : acc_sum * row_scale;
+        if (hf == 1) s_part[grp][q4 * 32 + lane] = is_max ? acc_max : acc_sum;
+        group_bar(grp);
+        if (hf == 0 && key < n) {
+          const float o = s_part[grp][q4 * 32 + lane];
+          a.s_raw[out_base + key] = is_max ? ex2_approx(fmaxf(acc_max, o)) : (acc_sum + o) * row_scale;
+        }
       }
     }
   }
   __syncwarp();
   tc_fence_before();
   __syncthreads();
-  if (warp == kMmaWarp) {
+  if (warp == kFMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tbase, kTmemCols);
   }
@@ -862,6 +942,7 @@ cudaError_t launch_rowstats_t(const WinScoreArgs& a, const CUtensorMap& tq, cons
   cudaError_t e = ensure_smem(reinterpret_cast<const void*>(win_rowstats_kernel<MT, NT, STAGES>), smem);
   if (e != cudaSuccess) return e;
   win_rowstats_kernel<MT, NT, STAGES><<<a.ck.total, kThreads, smem, st>>>(tq, tk, a);
+  note_launch();
   return cudaGetLastError();
 }
 
@@ -882,7 +963,7 @@ cudaError_t launch_win_rowstats(const WinScoreArgs& a, const CUtensorMap& tq, co
 cudaError_t launch_win_fused(const WinScoreArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
                              unsigned int* grid_count, cudaStream_t st) {
   if (a.ck.total <= 0) return cudaSuccess;
-  if (a.R > 256 || a.R_pad != a.R) return cudaErrorNotSupported;   // 64-column epilogue chunks
+  if (a.R > 256 || a.R_pad != a.R || a.R % 64 != 0) return cudaErrorNotSupported;   // 32-row halves
   const int mt = a.R <= 128 ? 1 : 2;
   const void* fn = mt == 1 ? reinterpret_cast<const void*>(win_fused_kernel<1>)
                            : reinterpret_cast<const void*>(win_fused_kernel<2>);
@@ -892,14 +973,12 @@ cudaError_t launch_win_fused(const WinScoreArgs& a, const CUtensorMap& tq, const
   int dev = 0, sms = 0, per_sm = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kThreads, smem);
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kFThreads, smem);
   if (e != cudaSuccess) return e;
   if (per_sm < 1 || a.ck.total > per_sm * sms) return cudaErrorNotSupported;
-  e = cudaMemsetAsync(grid_count, 0, sizeof(unsigned int) * a.rq.B * a.rq.H, st);
-  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.ck.total, 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.blockDim = dim3(kFThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
@@ -907,8 +986,10 @@ cudaError_t launch_win_fused(const WinScoreArgs& a, const CUtensorMap& tq, const
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (mt == 1) return cudaLaunchKernelEx(&cfg, win_fused_kernel<1>, tq, tk, a, grid_count);
-  return cudaLaunchKernelEx(&cfg, win_fused_kernel<2>, tq, tk, a, grid_count);
+  e = mt == 1 ? cudaLaunchKernelEx(&cfg, win_fused_kernel<1>, tq, tk, a, grid_count)
+              : cudaLaunchKernelEx(&cfg, win_fused_kernel<2>, tq, tk, a, grid_count);
+  if (e == cudaSuccess) note_launch();
+  return e;
 }
 
 cudaError_t launch_win_keysum(const WinScoreArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, cudaStream_t st) {
@@ -925,6 +1006,7 @@ cudaError_t launch_win_keysum(const WinScoreArgs& a, const CUtensorMap& tq, cons
   cudaError_t e = ensure_smem(reinterpret_cast<const void*>(win_keysum_kernel), smem);
   if (e != cudaSuccess) return e;
   win_keysum_kernel<<<a.ck.total, kThreads, smem, st>>>(tq, tk, a, stages, nacc, cols);
+  note_launch();
   return cudaGetLastError();
 }
 

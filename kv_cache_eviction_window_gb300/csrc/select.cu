@@ -519,6 +519,7 @@ cudaError_t launch_select(const SelectArgs& a, int cluster, int chunk_cap, cudaS
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   e = cudaLaunchKernelEx(&cfg, select_kernel, a, chunk_cap);
+  if (e == cudaSuccess) note_launch();
   return e;
 }
 

@@ -286,6 +286,7 @@ cudaError_t launch_wbar(const uint16_t* w_o, uint16_t* wbar, int H, int G, int D
   const long long blocks = (total + threads - 1) / threads;
   wbar_kernel<<<static_cast<unsigned>(blocks < 65535 * 8 ? blocks : 65535 * 8), threads, 0, st>>>(w_o, wbar, H, G, D,
                                                                                                   wo_mode);
+  note_launch();
   return cudaGetLastError();
 }
 
@@ -299,6 +300,7 @@ cudaError_t launch_vnorm(const VnormArgs& a, const CUtensorMap& tv, const CUtens
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int grid = a.units_total < sms ? a.units_total : sms;
   vnorm_kernel<<<grid, kThreads, smem, st>>>(tv, tw, a);
+  note_launch();
   return cudaGetLastError();
 }
 
