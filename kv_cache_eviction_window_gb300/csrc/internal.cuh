@@ -86,6 +86,8 @@ int qa_block_rows();
 struct VnormArgs {
   ReqTable rq;
   KvSource src;
+  const uint16_t* v;              // value cache (contiguous) or value block pool (paged)
+  long long stride_req, stride_head, stride_tok;   // contiguous layout, in elements
   int D;                          // rows of W_O (output features)
   int Dw;                         // rows of the combined weight per head (D or G*D)
   int units_total;                // (b, h, token block) work units
@@ -106,7 +108,7 @@ cudaError_t launch_win_fused(const WinScoreArgs& a, const CUtensorMap& tq, const
                              unsigned int* grid_count, cudaStream_t st);
 
 cudaError_t launch_wbar(const uint16_t* w_o, uint16_t* wbar, int H, int G, int D, int wo_mode, cudaStream_t st);
-cudaError_t launch_vnorm(const VnormArgs& a, const CUtensorMap& tv, const CUtensorMap& tw, cudaStream_t st);
+cudaError_t launch_vnorm(const VnormArgs& a, const CUtensorMap& tw, cudaStream_t st);
 int vnorm_token_block();
 int vnorm_w_tile_rows();
 

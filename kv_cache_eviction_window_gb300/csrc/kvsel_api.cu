@@ -432,8 +432,7 @@ int do_score(const kvsel_params* p, const Plan& pl, const void* q, const kvsel_k
       rc = launch_rc(launch_wbar(static_cast<const uint16_t*>(w_o), wbar, pl.H, pl.G, pl.D, p->wo_mode, st));
     }
     if (rc) return rc;
-    CUtensorMap tv, tw;
-    if (!kv_map(&tv, kv->v, kv, pl, kv->layout == KVSEL_LAYOUT_PAGED ? 0 : 128)) return KVSEL_EINVAL;
+    CUtensorMap tw;
     const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(pl.Dw),
                                 static_cast<cuuint64_t>(pl.H)};
     const cuuint64_t strides[2] = {kHeadDim * 2, static_cast<cuuint64_t>(pl.Dw) * kHeadDim * 2};
@@ -442,6 +441,10 @@ int do_score(const kvsel_params* p, const Plan& pl, const void* q, const kvsel_k
     VnormArgs v{};
     v.rq = pl.rq;
     v.src = kv_source(kv);
+    v.v = static_cast<const uint16_t*>(kv->v);
+    v.stride_req = kv->stride_req;
+    v.stride_head = kv->stride_head;
+    v.stride_tok = kv->stride_tok;
     v.D = pl.D;
     v.Dw = pl.Dw;
     v.units_total = pl.units_total;
@@ -451,7 +454,7 @@ int do_score(const kvsel_params* p, const Plan& pl, const void* q, const kvsel_k
     v.wc = wait_ctl(ws);
     {
       StageScope sc(KVSEL_STAGE_VNORM, st);
-      rc = launch_rc(launch_vnorm(v, tv, tw, st));
+      rc = launch_rc(launch_vnorm(v, tw, st));
     }
     if (rc) return rc;
   }

@@ -8,10 +8,21 @@
 // reading, the G slices stacked (G*D rows, giving sum_g ||W_O^(h,g) v||_1).
 //
 //   wbar_kernel: W_h rows in bf16, [H][Dw][d] (sum taken in fp32, rounded once).
-//   vnorm_kernel: persistent UMMA GEMM.  A = a block of MSUB*128 value rows (resident in
-//     shared memory, double-buffered), B = W_h tiles of NT rows streamed through a TMA
-//     ring; accumulators in TMEM are drained by 8 epilogue warps that add |.| along the
-//     row, so each thread ends with the L1 norm of one token's projected value.
+//   vnorm_kernel: persistent UMMA GEMM, M = 128 value rows (a subtile), N = 256 W_h rows,
+//     K = d = 128.  A work unit is 256 tokens of one (request, head): its two subtiles
+//     stay in shared memory while all W_h tiles stream through a two-stage TMA ring, and
+//     each round (W tile j, subtile m) accumulates into TMEM accumulator m.  Eight
+//     epilogue warps drain the accumulators adding |.| along the row, so each thread ends
+//     with half the L1 norm of one token's projected value; the halves meet in shared
+//     memory.
+//
+// With K = 128 every round is only eight UMMAs; the tensor pipe queues just a few, so the
+// issuing thread's barrier waits and commits between rounds are hidden only when each
+// UMMA is long: hence N = 256 (128 cycles per UMMA) rather than 128.  The shared memory
+// this takes leaves room for a single value buffer, which the epilogue threads refill:
+// each holds the next unit's row of one token in registers (loaded early with plain
+// loads) and writes it, 128-byte swizzled, as soon as the last round reading that subtile
+// has completed.
 #include "internal.cuh"
 
 namespace kvsel {
@@ -24,41 +35,17 @@ constexpr int kThreads = 320;
 
 constexpr int kMsub = 2;                  // 128-token subtiles per work unit
 constexpr int kTokBlock = kMsub * 128;    // tokens per work unit
-constexpr int kNT = 128;                  // W_h rows per B tile
-constexpr int kWStages = 3;
-constexpr int kVBuf = 2;
-constexpr int kAcc = 2;
-constexpr uint32_t kAccCols = kMsub * kNT;        // 256
-constexpr uint32_t kTmemCols = kAcc * kAccCols;   // 512
+constexpr int kNT = 256;                  // W_h rows per B tile (UMMA N)
+constexpr int kWStages = 2;
+constexpr uint32_t kAccCols = kNT;                // accumulator of one subtile
+constexpr uint32_t kTmemCols = kMsub * kAccCols;  // 512
 constexpr int kVSub = 128 * 256;                  // bytes of one 128-token subtile
 constexpr int kVTile = kMsub * kVSub;
 constexpr int kWTile = kNT * 256;
+constexpr int kEpiCols = kNT / 2;                 // accumulator columns per epilogue warp
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~static_cast<uintptr_t>(1023));
-}
-
-__device__ __forceinline__ void load_v_rows(const CUtensorMap* map, const KvSource& src, int b, int h, int n,
-                                            int tok0, uint8_t* dst, uint64_t* bar, int* status) {
-  const int half = 128 * 128;
-  if (!src.paged) {
-    tma_load_4d(dst, map, bar, 0, tok0, h, b);
-    tma_load_4d(dst + half, map, bar, 64, tok0, h, b);
-  } else {
-    const int bs = src.block_size;
-    const int nblk_req = (n + bs - 1) / bs;
-    for (int j = 0; j < 128 / bs; ++j) {
-      const int lb = tok0 / bs + j;
-      int pb = -1;
-      if (lb < nblk_req && lb < src.max_blocks) pb = __ldg(src.block_table + (size_t)b * src.max_blocks + lb);
-      if (pb < 0 || pb >= src.num_blocks) {
-        if (lb < nblk_req) atomicOr(status, DEV_BAD_INDEX);
-        pb = 0;
-      }
-      tma_load_4d(dst + j * bs * 128, map, bar, 0, h, 0, pb);
-      tma_load_4d(dst + half + j * bs * 128, map, bar, 64, h, 0, pb);
-    }
-  }
 }
 
 __device__ __forceinline__ void unit_coords(const VnormArgs& a, int u, int& b, int& h, int& blk) {
@@ -69,34 +56,85 @@ __device__ __forceinline__ void unit_coords(const VnormArgs& a, int u, int& b, i
   blk = rem - h * a.blocks_per_head[b];
 }
 
+// One token's value row (128 bf16) of unit u, subtile m, row r into registers; zeros past
+// the request's end or for a block-table entry out of range (flagged).
+__device__ __forceinline__ void load_v_row(const VnormArgs& a, int u, int m, int r, uint4 (&row)[16]) {
+  int b, h, blk;
+  unit_coords(a, u, b, h, blk);
+  const int n = a.rq.n[b];
+  const int tok = blk * kTokBlock + m * 128 + r;
+  const uint4* src = nullptr;
+  if (tok < n) {
+    if (!a.src.paged) {
+      src = reinterpret_cast<const uint4*>(a.v + b * a.stride_req + h * a.stride_head +
+                                           static_cast<long long>(tok) * a.stride_tok);
+    } else {
+      const int bs = a.src.block_size;
+      const int pb = __ldg(a.src.block_table + static_cast<size_t>(b) * a.src.max_blocks + tok / bs);
+      if (pb >= 0 && pb < a.src.num_blocks)
+        src = reinterpret_cast<const uint4*>(a.v + ((static_cast<long long>(pb) * bs + tok % bs) * a.rq.H + h) *
+                                                       kHeadDim);
+      else if (a.wc.status)
+        atomicOr(a.wc.status, DEV_BAD_INDEX);
+    }
+  }
+#pragma unroll
+  for (int q = 0; q < 16; ++q) row[q] = src ? __ldcs(src + q) : make_uint4(0, 0, 0, 0);
+}
+
+// The row into a K-major, 128-byte-swizzled subtile [2 K halves][128 rows][128 B]: the
+// 16-byte chunk c of row r sits at chunk c ^ (r % 8) of the row (the TMA SWIZZLE_128B
+// pattern, which the UMMA descriptor expects).
+__device__ __forceinline__ void store_v_row(uint8_t* sub, int r, const uint4 (&row)[16]) {
+#pragma unroll
+  for (int q = 0; q < 16; ++q) {
+    const int kh = q >> 3, c = q & 7;
+    *reinterpret_cast<uint4*>(sub + kh * (128 * 128) + r * 128 + ((c ^ (r & 7)) << 4)) = row[q];
+  }
+}
+
+__device__ __forceinline__ bool epi_vote_any(bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, 1, 256, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(pred))
+      : "memory");
+  return r != 0;
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
-    vnorm_kernel(const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tw, const VnormArgs a) {
+    vnorm_kernel(const __grid_constant__ CUtensorMap tw, const VnormArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
-  uint8_t* sV = smem;                       // [kVBuf][kMsub][2 halves][128][128 B]
-  uint8_t* sW = smem + kVBuf * kVTile;      // [kWStages][2 halves][kNT][128 B]
+  uint8_t* sV = smem;                // [kMsub][2 K halves][128 rows][128 B]
+  uint8_t* sW = smem + kVTile;       // [kWStages][2 K halves][kNT rows][128 B]
 
-  __shared__ __align__(8) uint64_t wfull[kWStages], wempty[kWStages], vfull[kVBuf], vempty[kVBuf];
-  __shared__ __align__(8) uint64_t accf[kAcc], acce[kAcc], done_bar;
+  __shared__ __align__(8) uint64_t wfull[kWStages], wempty[kWStages], vfull[kMsub];
+  __shared__ __align__(8) uint64_t accf[kMsub], acce[kMsub], done_bar;
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
+  __shared__ float s_half[kMsub][128];
 
   const int warp = warp_id(), lane = lane_id();
   int* status = a.wc.status;
-  const int nwt = a.Dw / kNT;   // W tiles per unit
+  const int nwt = (a.Dw + kNT - 1) / kNT;   // W tiles per unit (rows past Dw read as zeros)
+  const int my_units = static_cast<int>(blockIdx.x) < a.units_total
+                           ? (a.units_total - 1 - static_cast<int>(blockIdx.x)) / static_cast<int>(gridDim.x) + 1
+                           : 0;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kWStages; ++s) {
       mbar_init(&wfull[s], 1);
       mbar_init(&wempty[s], 1);
     }
-    for (int s = 0; s < kVBuf; ++s) {
-      mbar_init(&vfull[s], 1);
-      mbar_init(&vempty[s], 1);
-    }
-    for (int s = 0; s < kAcc; ++s) {
-      mbar_init(&accf[s], 1);
-      mbar_init(&acce[s], kEpiWarps);
+    for (int m = 0; m < kMsub; ++m) {
+      mbar_init(&vfull[m], 128);
+      mbar_init(&accf[m], 1);
+      mbar_init(&acce[m], kEpiWarps);
     }
     mbar_init(&done_bar, 1);
     s_abort = 0;
@@ -112,24 +150,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tbase = s_tmem;
 
   if (warp == kProducerWarp) {
-    if (lane == 0) {
-      tma_prefetch_desc(&tv);
+    if (lane == 0 && my_units > 0) {
       tma_prefetch_desc(&tw);
-      int wt = 0;     // W tiles issued so far (global across units)
-      int iu = 0;     // units processed by this CTA
+      int wt = 0;
       bool ok = true;
-      int last_v = -1;
-      for (int u = blockIdx.x; ok && u < a.units_total; u += gridDim.x, ++iu) {
+      for (int iu = 0; ok && iu < my_units; ++iu) {
         int b, h, blk;
-        unit_coords(a, u, b, h, blk);
-        const int n = a.rq.n[b];
-        const int vb = iu % kVBuf, vu = iu / kVBuf;
-        if (!mbar_wait(&vempty[vb], (vu & 1) ^ 1, &s_abort, a.wc)) break;
-        mbar_arrive_expect_tx(&vfull[vb], kVTile);
-        for (int m = 0; m < kMsub; ++m)
-          load_v_rows(&tv, a.src, b, h, n, blk * kTokBlock + m * 128, sV + vb * kVTile + m * kVSub, &vfull[vb],
-                      status);
-        last_v = iu;
+        unit_coords(a, blockIdx.x + iu * gridDim.x, b, h, blk);
         for (int j = 0; j < nwt; ++j, ++wt) {
           const int s = wt % kWStages, us = wt / kWStages;
           if (!mbar_wait(&wempty[s], (us & 1) ^ 1, &s_abort, a.wc)) {
@@ -142,87 +169,123 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       for (int tt = max(0, wt - kWStages); tt < wt; ++tt) mbar_drain(&wfull[tt % kWStages], (tt / kWStages) & 1, status);
-      for (int vv = max(0, last_v - kVBuf + 1); vv <= last_v; ++vv)
-        mbar_drain(&vfull[vv % kVBuf], (vv / kVBuf) & 1, status);
     }
   } else if (warp == kMmaWarp) {
-    if (lane == 0) {
+    if (lane == 0 && my_units > 0) {
       constexpr uint32_t idesc = idesc_bf16_f32(128, kNT);
-      int wt = 0, t = 0, iu = 0;
+      const uint64_t vdesc = sdesc_kmajor_sw128(smem_u32(sV));
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < a.units_total; u += gridDim.x, ++iu) {
-        const int vb = iu % kVBuf, vu = iu / kVBuf;
-        if (!mbar_wait(&vfull[vb], vu & 1, &s_abort, a.wc)) break;
-        const uint32_t vbase = smem_u32(sV + vb * kVTile);
-        for (int j = 0; j < nwt; ++j, ++wt, ++t) {
+      int wt = 0;
+      for (int iu = 0; ok && iu < my_units; ++iu) {
+        for (int j = 0; ok && j < nwt; ++j, ++wt) {
           const int s = wt % kWStages, us = wt / kWStages;
-          const int acc = t % kAcc, ua = t / kAcc;
-          if (!mbar_wait(&wfull[s], us & 1, &s_abort, a.wc) ||
-              !mbar_wait(&acce[acc], (ua & 1) ^ 1, &s_abort, a.wc)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t wbase = smem_u32(sW + s * kWTile);
+          const uint64_t wdesc = sdesc_kmajor_sw128(smem_u32(sW + s * kWTile));
 #pragma unroll
           for (int m = 0; m < kMsub; ++m) {
+            const int uses = iu * nwt + j;   // earlier rounds on accumulator m
+            if ((m == 0 && !mbar_wait(&wfull[s], us & 1, &s_abort, a.wc)) ||
+                (j == 0 && !mbar_wait(&vfull[m], iu & 1, &s_abort, a.wc)) ||
+                !mbar_wait(&acce[m], (uses & 1) ^ 1, &s_abort, a.wc)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
-              const uint32_t koff = (k & 3) * 32;
-              const uint64_t da = sdesc_kmajor_sw128(vbase + m * kVSub + (k >> 2) * (128 * 128) + koff);
-              const uint64_t db = sdesc_kmajor_sw128(wbase + (k >> 2) * (kNT * 128) + koff);
-              umma_bf16(tbase + acc * kAccCols + m * kNT, da, db, idesc, k > 0 ? 1u : 0u);
+              // descriptor start addresses advance in 16-byte units
+              const uint32_t aoff = (m * kVSub + (k >> 2) * (128 * 128) + (k & 3) * 32) >> 4;
+              const uint32_t boff = ((k >> 2) * (kNT * 128) + (k & 3) * 32) >> 4;
+              umma_bf16(tbase + m * kAccCols, vdesc + aoff, wdesc + boff, idesc, k > 0 ? 1u : 0u);
             }
+            umma_commit(&accf[m]);
           }
-          umma_commit(&wempty[s]);
-          umma_commit(&accf[acc]);
+          if (ok) umma_commit(&wempty[s]);
         }
-        if (ok) umma_commit(&vempty[vb]);
       }
       umma_commit(&done_bar);
       mbar_drain(&done_bar, 0, status);
     }
   } else {
-    // epilogue: warp e owns TMEM lane quadrant e%4 of subtile e/4
-    const int q4 = warp & 3, m = warp >> 2;
-    int t = 0;
+    // epilogue: warp (q4, hf) reads TMEM lane quadrant q4, columns [hf*128, hf*128 + 128)
+    // of every round, and owns the value row of token q4*32 + lane of subtile hf
+    const int q4 = warp & 3, hf = warp >> 2;
+    const int vr = q4 * 32 + lane;
+    uint8_t* my_sub = sV + hf * kVSub;
+    uint4 row[16];
+    if (my_units > 0) {
+      load_v_row(a, blockIdx.x, hf, vr, row);
+      store_v_row(my_sub, vr, row);
+      fence_proxy_async_smem();
+      mbar_arrive(&vfull[hf]);
+      if (my_units > 1) load_v_row(a, blockIdx.x + gridDim.x, hf, vr, row);
+    }
     bool ok = true;
-    for (int u = blockIdx.x; ok && u < a.units_total; u += gridDim.x) {
-      int b, h, blk;
-      unit_coords(a, u, b, h, blk);
-      const int n = a.rq.n[b];
-      float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
-      for (int j = 0; j < nwt; ++j, ++t) {
-        const int acc = t % kAcc, ua = t / kAcc;
-        bool w = mbar_wait(&accf[acc], ua & 1, &s_abort, a.wc);
-        w = __all_sync(0xffffffffu, w);
-        if (!w) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t taddr = tbase + (static_cast<uint32_t>(q4 * 32) << 16) + acc * kAccCols + m * kNT;
+    for (int iu = 0; iu < my_units; ++iu) {
+      const int u = blockIdx.x + iu * gridDim.x;
+      float sm[kMsub][2];
 #pragma unroll
-        for (int c0 = 0; c0 < kNT; c0 += 64) {
-          float v[64];
-          tmem_ld32(taddr + c0, v);
-          tmem_ld32(taddr + c0 + 32, v + 32);
-          tmem_ld_wait();
+      for (int m = 0; m < kMsub; ++m) sm[m][0] = sm[m][1] = 0.f;
+      for (int j = 0; j < nwt; ++j) {
 #pragma unroll
-          for (int i = 0; i < 64; i += 4) {
-            s0 += fabsf(v[i + 0]);
-            s1 += fabsf(v[i + 1]);
-            s2 += fabsf(v[i + 2]);
-            s3 += fabsf(v[i + 3]);
+        for (int m = 0; m < kMsub; ++m) {
+          if (!ok) continue;   // after an abort: fall through to the unit's vote
+          const int uses = iu * nwt + j;
+          const bool w = mbar_wait(&accf[m], uses & 1, &s_abort, a.wc);
+          ok = __all_sync(0xffffffffu, w);
+          if (!ok) continue;
+          tc_fence_after();
+          const uint32_t taddr = tbase + (static_cast<uint32_t>(q4 * 32) << 16) + m * kAccCols + hf * kEpiCols;
+          float p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
+#pragma unroll
+          for (int c0 = 0; c0 < kEpiCols; c0 += 64) {
+            float v[64];
+            tmem_ld32(taddr + c0, v);
+            tmem_ld32(taddr + c0 + 32, v + 32);
+            tmem_ld_wait();
+            if (c0 + 64 == kEpiCols) {
+              // every column of this round is in registers: release the accumulator
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&acce[m]);
+            }
+#pragma unroll
+            for (int i = 0; i < 64; i += 4) {
+              p0 += fabsf(v[i + 0]);
+              p1 += fabsf(v[i + 1]);
+              p2 += fabsf(v[i + 2]);
+              p3 += fabsf(v[i + 3]);
+            }
+          }
+          sm[m][0] += p0 + p1;
+          sm[m][1] += p2 + p3;
+          if (j == nwt - 1 && m == hf && iu + 1 < my_units) {
+            // every UMMA reading subtile hf of this unit has completed: refill it with the
+            // next unit's rows, then fetch the rows of the unit after that
+            store_v_row(my_sub, vr, row);
+            fence_proxy_async_smem();
+            mbar_arrive(&vfull[hf]);
+            if (iu + 2 < my_units) load_v_row(a, u + 2 * gridDim.x, hf, vr, row);
           }
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&acce[acc]);
       }
-      if (!ok) break;
-      const int tok = blk * kTokBlock + m * 128 + q4 * 32 + lane;
-      if (tok < n) a.nu[a.rq.soff[b] + static_cast<size_t>(h) * n + tok] = (s0 + s1) + (s2 + s3);
+      // the two column halves of every token meet in shared memory; the barrier also
+      // tells all eight warps whether any of them gave up
+      if (hf == 1 && ok) {
+#pragma unroll
+        for (int m = 0; m < kMsub; ++m) s_half[m][vr] = sm[m][0] + sm[m][1];
+      }
+      if (epi_vote_any(!ok)) break;
+      if (hf == 0) {
+        int b, h, blk;
+        unit_coords(a, u, b, h, blk);
+        const int n = a.rq.n[b];
+#pragma unroll
+        for (int m = 0; m < kMsub; ++m) {
+          const int tok = blk * kTokBlock + m * 128 + vr;
+          if (tok < n) a.nu[a.rq.soff[b] + static_cast<size_t>(h) * n + tok] = (sm[m][0] + sm[m][1]) + s_half[m][vr];
+        }
+      }
+      asm volatile("bar.sync 1, 256;" ::: "memory");   // s_half is read before the next unit writes it
     }
   }
   __syncwarp();
@@ -290,16 +353,16 @@ cudaError_t launch_wbar(const uint16_t* w_o, uint16_t* wbar, int H, int G, int D
   return cudaGetLastError();
 }
 
-cudaError_t launch_vnorm(const VnormArgs& a, const CUtensorMap& tv, const CUtensorMap& tw, cudaStream_t st) {
+cudaError_t launch_vnorm(const VnormArgs& a, const CUtensorMap& tw, cudaStream_t st) {
   if (a.units_total <= 0) return cudaSuccess;
-  const size_t smem = 1024 + kVBuf * kVTile + kWStages * kWTile;
+  const size_t smem = 1024 + kVTile + kWStages * kWTile;
   cudaError_t e = ensure_smem(reinterpret_cast<const void*>(vnorm_kernel), smem);
   if (e != cudaSuccess) return e;
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int grid = a.units_total < sms ? a.units_total : sms;
-  vnorm_kernel<<<grid, kThreads, smem, st>>>(tv, tw, a);
+  vnorm_kernel<<<grid, kThreads, smem, st>>>(tw, a);
   note_launch();
   return cudaGetLastError();
 }
