@@ -103,7 +103,11 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------------------ dist
-def dist_setup(args):
+# One process per GPU; every rank runs its own replica of the layer stack on its own
+# seeded inputs (weak scaling: no data-path collective), then the ranks meet only for a
+# barrier around the timed region and the max of their times.  With CUDA the process
+# group uses NCCL; without it (the CPU tests) gloo.
+def dist_setup(args=None):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
@@ -112,8 +116,11 @@ def dist_setup(args):
     if world > 1:
         import torch.distributed as dist
 
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl")
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+            dist.init_process_group("nccl")
+        else:
+            dist.init_process_group("gloo")
     elif torch.cuda.is_available():
         torch.cuda.set_device(0)
     return world, rank, local
@@ -132,9 +139,20 @@ def max_over_ranks(x, world):
     import torch
     import torch.distributed as dist
 
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def rank_layer_ids(rank, layers):
+    """Seeds of the synthetic layers rank `rank` processes: distinct across ranks."""
+    return [layer + 100 * rank for layer in range(layers)]
+
+
+def job_value(entries_per_rank, ms_max, world):
+    """Whole-job throughput: the entries all ranks processed over the slowest rank's time."""
+    return entries_per_rank * world / (ms_max * 1e-3)
 
 
 # ------------------------------------------------------------------------------ oracle
@@ -260,7 +278,7 @@ def main():
 
     # ---- inputs (host, seeded) -> HBM
     t_gen = time.perf_counter()
-    host = [datagen.make_layer(wl, layer + 100 * rank) for layer in range(L)]
+    host = [datagen.make_layer(wl, seed) for seed in rank_layer_ids(rank, L)]
     t_gen = time.perf_counter() - t_gen
 
     def to_dev(u16):
@@ -362,8 +380,7 @@ def main():
     ms = t0.elapsed_time(t1)
     ms = max_over_ranks(ms, world)
     status = B.kvsel_get_device_status(ws)
-    entries = K * L * H * n * world
-    value = entries / (ms * 1e-3)
+    value = job_value(K * L * H * n, ms, world)
     if egraph is not None:
         egraph.replay()
         torch.cuda.synchronize()
@@ -488,7 +505,7 @@ def main():
         torch.cuda.synchronize()
         wall = time.perf_counter() - w0
         ems = max_over_ranks(max(t0.elapsed_time(t1), wall * 1e3), world)
-        out["e2e"] = {"value": entries / (ems * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+        out["e2e"] = {"value": job_value(K * L * H * n, ems, world), "unit": UNIT, "h2d_bytes_per_step": h2d,
                       "d2h_bytes_per_step": d2h, "ms_per_step": ems / K,
                       "how": "kvsel_run_layer per layer; per-layer H2D of Q/K/V/W_O from pinned host on a copy "
                              "stream overlapped with the previous layer's compute; idx/counts D2H per layer"}
