@@ -7,8 +7,8 @@
 // A segment is one (request, KV head) in per-head mode, or all heads of one request
 // flattened head-major in per-layer mode.  The CTAs of a cluster split the segment into
 // contiguous chunks held in shared memory as order-preserving 32-bit keys (forced
-// entries get the largest key).  The B-th largest key T is found by a three-pass radix
-// select (11/11/10-bit digits): each pass builds per-CTA histograms of the candidates,
+// entries get the largest key).  The B-th largest key T is found by a four-pass radix
+// select (8-bit digits): each pass builds per-CTA histograms of the candidates,
 // the cluster reduces them through distributed shared memory, and every CTA finds the
 // same digit.  Entries with key > T, and the first (B - #greater) entries equal to T in
 // index order, are kept; a cluster-wide exclusive scan of per-CTA counts plus a block
@@ -28,11 +28,11 @@ namespace {
 
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
-constexpr int kBins = 2048;
+constexpr int kBins = 256;        // 8-bit digits, four passes
 constexpr uint32_t kKeyMax = 0xFFFFFFFFu;
 constexpr int kMaxHeads = 64;
 constexpr int kMaxHalo = 64;   // room for 2 * (pool_kernel / 2) staged neighbours of a chunk
-static_assert(kBins == 4 * kThreads, "digit search: four bins per thread");
+static_assert(kBins <= kThreads && kBins % 32 == 0, "digit search: one bin per thread");
 
 __device__ __forceinline__ uint32_t f2key(float f) {
   const uint32_t u = __float_as_uint(f);
@@ -40,8 +40,8 @@ __device__ __forceinline__ uint32_t f2key(float f) {
 }
 
 struct SelShared {
-  uint32_t hist[kBins];       // this CTA's histogram of the current pass
-  uint32_t merged[3][kBins];  // cluster-wide histogram, pushed by every CTA; one buffer per pass mod 3
+  uint32_t whist[kWarps][kBins];  // per-warp histograms of the current pass (no cross-warp atomics)
+  uint32_t merged[3][kBins];      // cluster-wide histogram, pushed by every CTA; one buffer per pass mod 3
   uint32_t cnt[2][16][2];     // (greater, equal) counts of every CTA, pushed by each; one buffer per selection mod 2
   uint32_t res_prefix, res_krem;
   uint32_t wsum_gt[kWarps], wsum_eq[kWarps];
@@ -104,81 +104,73 @@ struct SelState {
 };
 
 // Key T of the K-th largest candidate among keys[0, cnt_local) of every CTA, and the
-// number of keys equal to T that are taken (krem).  Each pass: a local histogram, then
-// every CTA adds its non-empty bins into every CTA's copy of the cluster histogram with
-// cluster-scope reductions; after one cluster barrier each CTA finds the digit in its
-// own shared memory.
+// number of keys equal to T that are taken (krem).  Each pass: per-warp histograms of the
+// keys that match the digits found so far (plain shared atomics, contention only inside a
+// warp), summed per bin; every CTA adds its non-empty bins into every CTA's copy of the
+// cluster histogram with cluster-scope reductions (at most 256 per CTA and pass); after
+// one cluster barrier each CTA finds the same digit in its own shared memory.
 __device__ void radix_select(cgx::cluster_group& cl, SelShared& S, SelState& st, const uint32_t* keys,
                              int cnt_local, uint32_t K, uint32_t& T, uint32_t& krem_out) {
   const unsigned CS = cl.num_blocks();
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   uint32_t prefix = 0, mask = 0, krem = K;
-  const int shifts[3] = {21, 10, 0};
-  const int widths[3] = {11, 11, 10};
-  for (int pass = 0; pass < 3; ++pass, ++st.pass) {
+  uint32_t* my_hist = S.whist[w];
+  for (int pass = 0; pass < 4; ++pass, ++st.pass) {
     const int buf = st.pass % 3, nxt = (st.pass + 1) % 3;
-    const int sh = shifts[pass];
-    const uint32_t dmask = (1u << widths[pass]) - 1u;
+    const int sh = 24 - 8 * pass;
     // the next pass's buffer was last read two barriers ago
-    for (int i = threadIdx.x; i < kBins; i += kThreads) {
-      S.merged[nxt][i] = 0;
-      S.hist[i] = 0;
-    }
+    for (int i = threadIdx.x; i < kWarps * kBins; i += kThreads) (&S.whist[0][0])[i] = 0;
+    if (threadIdx.x < kBins) S.merged[nxt][threadIdx.x] = 0;
     __syncthreads();
     const int trips = (cnt_local + kThreads - 1) / kThreads;
     for (int j = 0; j < trips; ++j) {
       const int e = j * kThreads + threadIdx.x;
-      uint32_t dig = 0xFFFFFFFFu;
       if (e < cnt_local) {
         const uint32_t k = keys[e];
-        if ((k & mask) == prefix) dig = (k >> sh) & dmask;
+        if ((k & mask) == prefix) atomicAdd(&my_hist[(k >> sh) & 0xFFu], 1u);
       }
-      const unsigned peers = __match_any_sync(0xffffffffu, dig);
-      if (dig != 0xFFFFFFFFu && lane == __ffs(peers) - 1) atomicAdd(&S.hist[dig], static_cast<uint32_t>(__popc(peers)));
     }
     __syncthreads();
-    for (int bin = threadIdx.x; bin < kBins; bin += kThreads) {
-      const uint32_t c = S.hist[bin];
+    if (threadIdx.x < kBins) {
+      uint32_t c = 0;
+#pragma unroll
+      for (int ww = 0; ww < kWarps; ++ww) c += S.whist[ww][threadIdx.x];
       if (c)
-        for (unsigned r = 0; r < CS; ++r) red_add_cluster(cluster_addr(&S.merged[buf][bin], r), c);
+        for (unsigned r = 0; r < CS; ++r) red_add_cluster(cluster_addr(&S.merged[buf][threadIdx.x], r), c);
     }
     cl.sync();
-    {
-      // thread t owns bins [4t, 4t + 4) (one 16-byte load, conflict-free); a block-wide
-      // suffix scan of the 512 group sums finds the group holding the krem-th largest
-      const uint4 hv = reinterpret_cast<const uint4*>(S.merged[buf])[threadIdx.x];
-      const uint32_t gsum = hv.x + hv.y + hv.z + hv.w;
-      // exclusive prefix from the top: sum over groups with a larger index
-      uint32_t incl = gsum;
+    if (threadIdx.x < kBins) {
+      // bin t = thread t; suffix sums from the top find the bin holding the krem-th largest
+      const uint32_t v = S.merged[buf][threadIdx.x];
+      uint32_t incl = v;   // sum over bins [t, warp end)
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const uint32_t x = __shfl_down_sync(0xffffffffu, incl, o);
         if (lane + o < 32) incl += x;
       }
       if (lane == 0) S.wsum_gt[w] = incl;   // warp total
-      __syncthreads();
+    }
+    __syncthreads();
+    if (threadIdx.x < kBins) {
+      const uint32_t v = S.merged[buf][threadIdx.x];
+      uint32_t incl = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t x = __shfl_down_sync(0xffffffffu, incl, o);
+        if (lane + o < 32) incl += x;
+      }
       uint32_t above_w = 0;
-      for (int i = w + 1; i < kWarps; ++i) above_w += S.wsum_gt[i];
-      const uint32_t above = above_w + incl - gsum;
-      if (above < krem && krem <= above + gsum) {
-        const uint32_t b4[4] = {hv.x, hv.y, hv.z, hv.w};
-        uint32_t cum = above;
-        int digit = threadIdx.x * 4;
-        for (int i = 3; i >= 0; --i) {
-          if (cum + b4[i] >= krem) {
-            digit = threadIdx.x * 4 + i;
-            break;
-          }
-          cum += b4[i];
-        }
-        S.res_prefix = prefix | (static_cast<uint32_t>(digit) << sh);
-        S.res_krem = krem - cum;
+      for (int i = w + 1; i < kBins / 32; ++i) above_w += S.wsum_gt[i];
+      const uint32_t above = above_w + incl - v;   // keys in bins above this one
+      if (above < krem && krem <= above + v) {
+        S.res_prefix = prefix | (static_cast<uint32_t>(threadIdx.x) << sh);
+        S.res_krem = krem - above;
       }
     }
     __syncthreads();
     prefix = S.res_prefix;
     krem = S.res_krem;
-    mask |= dmask << sh;
+    mask |= 0xFFu << sh;
   }
   T = prefix;
   krem_out = krem;
