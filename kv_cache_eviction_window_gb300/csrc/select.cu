@@ -43,7 +43,7 @@ struct SelShared {
   uint32_t whist[kWarps][kBins];  // per-warp histograms of the current pass (no cross-warp atomics)
   uint32_t merged[3][kBins];      // cluster-wide histogram, pushed by every CTA; one buffer per pass mod 3
   uint32_t cnt[2][16][2];     // (greater, equal) counts of every CTA, pushed by each; one buffer per selection mod 2
-  uint32_t res_prefix, res_krem;
+  uint32_t res_prefix, res_krem, res_bin;
   uint32_t wsum_gt[kWarps], wsum_eq[kWarps];
   uint32_t head_cnt[kMaxHeads];
 };
@@ -114,6 +114,11 @@ __device__ void radix_select(cgx::cluster_group& cl, SelShared& S, SelState& st,
   const unsigned CS = cl.num_blocks();
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   uint32_t prefix = 0, mask = 0, krem = K;
+  if (K == 0) {   // nothing to take (same in every CTA of the cluster)
+    T = kKeyMax;
+    krem_out = 0;
+    return;
+  }
   uint32_t* my_hist = S.whist[w];
   for (int pass = 0; pass < 4; ++pass, ++st.pass) {
     const int buf = st.pass % 3, nxt = (st.pass + 1) % 3;
@@ -122,12 +127,18 @@ __device__ void radix_select(cgx::cluster_group& cl, SelShared& S, SelState& st,
     for (int i = threadIdx.x; i < kWarps * kBins; i += kThreads) (&S.whist[0][0])[i] = 0;
     if (threadIdx.x < kBins) S.merged[nxt][threadIdx.x] = 0;
     __syncthreads();
-    const int trips = (cnt_local + kThreads - 1) / kThreads;
-    for (int j = 0; j < trips; ++j) {
-      const int e = j * kThreads + threadIdx.x;
-      if (e < cnt_local) {
-        const uint32_t k = keys[e];
-        if ((k & mask) == prefix) atomicAdd(&my_hist[(k >> sh) & 0xFFu], 1u);
+    // four keys loaded before their four atomics, so the loads overlap
+    for (int e0 = 0; e0 < cnt_local; e0 += 4 * kThreads) {
+      uint32_t k[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int e = e0 + u * kThreads + threadIdx.x;
+        k[u] = e < cnt_local ? keys[e] : 0u;   // out-of-range slots are skipped below
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int e = e0 + u * kThreads + threadIdx.x;
+        if (e < cnt_local && (k[u] & mask) == prefix) atomicAdd(&my_hist[(k[u] >> sh) & 0xFFu], 1u);
       }
     }
     __syncthreads();
@@ -165,12 +176,21 @@ __device__ void radix_select(cgx::cluster_group& cl, SelShared& S, SelState& st,
       if (above < krem && krem <= above + v) {
         S.res_prefix = prefix | (static_cast<uint32_t>(threadIdx.x) << sh);
         S.res_krem = krem - above;
+        S.res_bin = v;
       }
     }
     __syncthreads();
     prefix = S.res_prefix;
     krem = S.res_krem;
     mask |= 0xFFu << sh;
+    if (krem == S.res_bin && prefix != 0u && pass < 3) {
+      // every key of the threshold bin is taken: the selection is all keys >= prefix,
+      // i.e. keys > prefix - 1 with no ties to resolve (the same decision in every CTA)
+      ++st.pass;
+      T = prefix - 1u;
+      krem_out = 0;
+      return;
+    }
   }
   T = prefix;
   krem_out = krem;

@@ -166,6 +166,20 @@ def test_split_calls_match_run_layer(cid, n, kw):
             np.testing.assert_array_equal(a["v_out"][h], b["v_out"][h])
 
 
+def test_two_stage_with_empty_first_stage():
+    """floor(alpha * B) = 0 and no forced entries: stage 1 takes nothing, so the single
+    kept entry per head is the value-aware argmax (radix selection of zero entries)."""
+    wl = datagen.WORKLOADS[2].replace(layers=1, h_kv=2, d_model=512, n_sink=0, n_recent=0, budget_ratio=0.001)
+    inp = datagen.make_layer(wl, 0, n_ctx=1000)
+    ora = O.run_workload_layer(wl, inp)
+    gpu = GH.run_gpu_layer(wl, inp)
+    for h in range(2):
+        GH.assert_scores_close(gpu[0]["s_val"][h], ora[0]["s_val"][h], f"s_val h{h}")
+        assert len(gpu[0]["idx"][h]) == 1 and len(ora[0]["idx"][h]) == 1
+        sv = ora[0]["s_val"][h]
+        assert sv[gpu[0]["idx"][h][0]] >= sv.max() * (1 - GH.SEL_RTOL)
+
+
 def test_budget_equals_n_identity():
     wl = datagen.WORKLOADS[1].replace(budget_ratio=1.0, h_kv=2)
     inp = datagen.make_layer(wl, 0, n_ctx=600)
