@@ -107,7 +107,9 @@ cudaError_t launch_win_keysum(const WinScoreArgs& a, const CUtensorMap& tq, cons
 cudaError_t launch_win_fused(const WinScoreArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
                              unsigned int* grid_count, cudaStream_t st);
 
-cudaError_t launch_wbar(const uint16_t* w_o, uint16_t* wbar, int H, int G, int D, int wo_mode, cudaStream_t st);
+// Also zeroes nu[0, nu_count), which launch_vnorm (next on the stream) accumulates into.
+cudaError_t launch_wbar(const uint16_t* w_o, uint16_t* wbar, int H, int G, int D, int wo_mode, float* nu,
+                        long long nu_count, cudaStream_t st);
 cudaError_t launch_vnorm(const VnormArgs& a, const CUtensorMap& tw, cudaStream_t st);
 int vnorm_token_block();
 int vnorm_w_tile_rows();

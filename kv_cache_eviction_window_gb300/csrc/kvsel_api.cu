@@ -429,7 +429,8 @@ int do_score(const kvsel_params* p, const Plan& pl, const void* q, const kvsel_k
     uint16_t* wbar = reinterpret_cast<uint16_t*>(wsb + pl.ws_wbar);
     {
       StageScope sc(KVSEL_STAGE_WBAR, st);
-      rc = launch_rc(launch_wbar(static_cast<const uint16_t*>(w_o), wbar, pl.H, pl.G, pl.D, p->wo_mode, st));
+      rc = launch_rc(launch_wbar(static_cast<const uint16_t*>(w_o), wbar, pl.H, pl.G, pl.D, p->wo_mode, nu,
+                                 pl.n_scores, st));
     }
     if (rc) return rc;
     CUtensorMap tw;

@@ -56,6 +56,28 @@ __device__ __forceinline__ void unit_coords(const VnormArgs& a, int u, int& b, i
   blk = rem - h * a.blocks_per_head[b];
 }
 
+// Work balance: the items (unit, W tile) of the whole launch, unit-major, are cut into
+// gridDim.x equal contiguous ranges.  A CTA's range splits into segments, one per unit
+// it touches; a unit shared by two CTAs gets its L1 norm in two parts, added atomically
+// into nu (zeroed beforehand; with two terms the sum does not depend on their order).
+struct Seg {
+  int u, j0, j1;
+};
+__device__ __forceinline__ void cta_items(int total, int& lo, int& hi) {
+  lo = static_cast<int>(static_cast<long long>(blockIdx.x) * total / gridDim.x);
+  hi = static_cast<int>(static_cast<long long>(blockIdx.x + 1) * total / gridDim.x);
+}
+__device__ __forceinline__ int seg_count(int lo, int hi, int nwt) {
+  return hi > lo ? (hi - 1) / nwt - lo / nwt + 1 : 0;
+}
+__device__ __forceinline__ Seg seg_at(int lo, int hi, int nwt, int q) {
+  Seg g;
+  g.u = lo / nwt + q;
+  g.j0 = max(lo - g.u * nwt, 0);
+  g.j1 = min(hi - g.u * nwt, nwt);
+  return g;
+}
+
 // One token's value row (128 bf16) of unit u, subtile m, row r into registers; zeros past
 // the request's end or for a block-table entry out of range (flagged).
 __device__ __forceinline__ void load_v_row(const VnormArgs& a, int u, int m, int r, uint4 (&row)[16]) {
@@ -122,9 +144,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = warp_id(), lane = lane_id();
   int* status = a.wc.status;
   const int nwt = (a.Dw + kNT - 1) / kNT;   // W tiles per unit (rows past Dw read as zeros)
-  const int my_units = static_cast<int>(blockIdx.x) < a.units_total
-                           ? (a.units_total - 1 - static_cast<int>(blockIdx.x)) / static_cast<int>(gridDim.x) + 1
-                           : 0;
+  int lo, hi;
+  cta_items(a.units_total * nwt, lo, hi);
+  const int nseg = seg_count(lo, hi, nwt);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kWStages; ++s) {
@@ -150,14 +172,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tbase = s_tmem;
 
   if (warp == kProducerWarp) {
-    if (lane == 0 && my_units > 0) {
+    if (lane == 0 && nseg > 0) {
       tma_prefetch_desc(&tw);
       int wt = 0;
       bool ok = true;
-      for (int iu = 0; ok && iu < my_units; ++iu) {
+      for (int q = 0; ok && q < nseg; ++q) {
+        const Seg sg = seg_at(lo, hi, nwt, q);
         int b, h, blk;
-        unit_coords(a, blockIdx.x + iu * gridDim.x, b, h, blk);
-        for (int j = 0; j < nwt; ++j, ++wt) {
+        unit_coords(a, sg.u, b, h, blk);
+        for (int j = sg.j0; j < sg.j1; ++j, ++wt) {
           const int s = wt % kWStages, us = wt / kWStages;
           if (!mbar_wait(&wempty[s], (us & 1) ^ 1, &s_abort, a.wc)) {
             ok = false;
@@ -171,20 +194,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int tt = max(0, wt - kWStages); tt < wt; ++tt) mbar_drain(&wfull[tt % kWStages], (tt / kWStages) & 1, status);
     }
   } else if (warp == kMmaWarp) {
-    if (lane == 0 && my_units > 0) {
+    if (lane == 0 && nseg > 0) {
       constexpr uint32_t idesc = idesc_bf16_f32(128, kNT);
       const uint64_t vdesc = sdesc_kmajor_sw128(smem_u32(sV));
       bool ok = true;
-      int wt = 0;
-      for (int iu = 0; ok && iu < my_units; ++iu) {
-        for (int j = 0; ok && j < nwt; ++j, ++wt) {
+      int wt = 0;   // W tiles (= rounds per accumulator) so far
+      for (int q = 0; ok && q < nseg; ++q) {
+        const Seg sg = seg_at(lo, hi, nwt, q);
+        for (int j = sg.j0; ok && j < sg.j1; ++j, ++wt) {
           const int s = wt % kWStages, us = wt / kWStages;
           const uint64_t wdesc = sdesc_kmajor_sw128(smem_u32(sW + s * kWTile));
 #pragma unroll
           for (int m = 0; m < kMsub; ++m) {
-            const int uses = iu * nwt + j;   // earlier rounds on accumulator m
+            const int uses = wt;   // earlier rounds on accumulator m
             if ((m == 0 && !mbar_wait(&wfull[s], us & 1, &s_abort, a.wc)) ||
-                (j == 0 && !mbar_wait(&vfull[m], iu & 1, &s_abort, a.wc)) ||
+                (j == sg.j0 && !mbar_wait(&vfull[m], q & 1, &s_abort, a.wc)) ||
                 !mbar_wait(&acce[m], (uses & 1) ^ 1, &s_abort, a.wc)) {
               ok = false;
               break;
@@ -212,24 +236,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int vr = q4 * 32 + lane;
     uint8_t* my_sub = sV + hf * kVSub;
     uint4 row[16];
-    if (my_units > 0) {
-      load_v_row(a, blockIdx.x, hf, vr, row);
+    if (nseg > 0) {
+      load_v_row(a, seg_at(lo, hi, nwt, 0).u, hf, vr, row);
       store_v_row(my_sub, vr, row);
       fence_proxy_async_smem();
       mbar_arrive(&vfull[hf]);
-      if (my_units > 1) load_v_row(a, blockIdx.x + gridDim.x, hf, vr, row);
+      if (nseg > 1) load_v_row(a, seg_at(lo, hi, nwt, 1).u, hf, vr, row);
     }
     bool ok = true;
-    for (int iu = 0; iu < my_units; ++iu) {
-      const int u = blockIdx.x + iu * gridDim.x;
+    int wt = 0;
+    for (int q = 0; q < nseg; ++q) {
+      const Seg sg = seg_at(lo, hi, nwt, q);
+      const int u = sg.u;
       float sm[kMsub][2];
 #pragma unroll
       for (int m = 0; m < kMsub; ++m) sm[m][0] = sm[m][1] = 0.f;
-      for (int j = 0; j < nwt; ++j) {
+      for (int j = sg.j0; j < sg.j1; ++j, ++wt) {
 #pragma unroll
         for (int m = 0; m < kMsub; ++m) {
-          if (!ok) continue;   // after an abort: fall through to the unit's vote
-          const int uses = iu * nwt + j;
+          if (!ok) continue;   // after an abort: fall through to the segment's vote
+          const int uses = wt;
           const bool w = mbar_wait(&accf[m], uses & 1, &s_abort, a.wc);
           ok = __all_sync(0xffffffffu, w);
           if (!ok) continue;
@@ -258,13 +284,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           sm[m][0] += p0 + p1;
           sm[m][1] += p2 + p3;
-          if (j == nwt - 1 && m == hf && iu + 1 < my_units) {
-            // every UMMA reading subtile hf of this unit has completed: refill it with the
-            // next unit's rows, then fetch the rows of the unit after that
+          if (j == sg.j1 - 1 && m == hf && q + 1 < nseg) {
+            // every UMMA reading subtile hf of this segment has completed: refill it with
+            // the next segment's rows, then fetch the rows of the segment after that
             store_v_row(my_sub, vr, row);
             fence_proxy_async_smem();
             mbar_arrive(&vfull[hf]);
-            if (iu + 2 < my_units) load_v_row(a, u + 2 * gridDim.x, hf, vr, row);
+            if (q + 2 < nseg) load_v_row(a, seg_at(lo, hi, nwt, q + 2).u, hf, vr, row);
           }
         }
       }
@@ -282,7 +308,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int m = 0; m < kMsub; ++m) {
           const int tok = blk * kTokBlock + m * 128 + vr;
-          if (tok < n) a.nu[a.rq.soff[b] + static_cast<size_t>(h) * n + tok] = (sm[m][0] + sm[m][1]) + s_half[m][vr];
+          if (tok < n) atomicAdd(a.nu + a.rq.soff[b] + static_cast<size_t>(h) * n + tok, (sm[m][0] + sm[m][1]) + s_half[m][vr]);
         }
       }
       asm volatile("bar.sync 1, 256;" ::: "memory");   // s_half is read before the next unit writes it
@@ -300,9 +326,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 // W_h[h][j][c]: group sum of W_O[j][(h*G+g)*d + c] (wo_mode 0) or the stacked slices
 // W_h[h][g*D + j][c] = W_O[j][(h*G+g)*d + c] (wo_mode 1).  One thread per 8 columns.
 __global__ void wbar_kernel(const uint16_t* __restrict__ w_o, uint16_t* __restrict__ wbar, int H, int G, int D,
-                            int wo_mode) {
+                            int wo_mode, float* __restrict__ nu, long long nu_count) {
   const long long total = static_cast<long long>(H) * D * 16;
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  // nu is accumulated atomically by vnorm_kernel, which runs next on the stream
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < nu_count; i += stride) nu[i] = 0.f;
   const long long row_len = static_cast<long long>(H) * G * kHeadDim;
   for (long long t = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; t < total; t += stride) {
     const int c8 = static_cast<int>(t % 16);
@@ -343,12 +371,13 @@ __global__ void wbar_kernel(const uint16_t* __restrict__ w_o, uint16_t* __restri
 int vnorm_token_block() { return kTokBlock; }
 int vnorm_w_tile_rows() { return kNT; }
 
-cudaError_t launch_wbar(const uint16_t* w_o, uint16_t* wbar, int H, int G, int D, int wo_mode, cudaStream_t st) {
+cudaError_t launch_wbar(const uint16_t* w_o, uint16_t* wbar, int H, int G, int D, int wo_mode, float* nu,
+                        long long nu_count, cudaStream_t st) {
   const long long total = static_cast<long long>(H) * D * 16;
   const int threads = 256;
   const long long blocks = (total + threads - 1) / threads;
   wbar_kernel<<<static_cast<unsigned>(blocks < 65535 * 8 ? blocks : 65535 * 8), threads, 0, st>>>(w_o, wbar, H, G, D,
-                                                                                                  wo_mode);
+                                                                                                  wo_mode, nu, nu_count);
   note_launch();
   return cudaGetLastError();
 }
