@@ -830,31 +830,36 @@ __global__ void __launch_bounds__(kFThreads, 1)
     }
     if (fused_epi_any(!alive || *reinterpret_cast<volatile int*>(&s_abort) != 0)) alive = false;
     if (alive) {
-      // merged row statistics c2[r] = m_r + log2 Z_r (log2 units): warp w takes rows w, w+16, ...,
-      // lanes over chunks; every load is issued before the first reduction
-      constexpr int kRowsPerWarp = MT * 128 / kFEpiWarps;
-      float lm[kRowsPerWarp][2], lz[kRowsPerWarp][2];
+      // merged row statistics c2[r] = m_r + log2 Z_r (log2 units): kTpr threads per row
+      // split its chunk partials (float4 groups, all loads issued first), then combine
+      {
+        constexpr int kTpr = (kFEpiWarps * 32) / (MT * 128);   // 4 (R <= 128) or 2
+        constexpr int kMaxG = 64 / 4 / kTpr;                   // float4 groups per thread (ncp <= 64)
+        const int r = threadIdx.x / kTpr, part = threadIdx.x % kTpr;
+        const int ng = ncp / 4;
+        float4 m4[kMaxG], z4[kMaxG];
 #pragma unroll
-      for (int k = 0; k < kRowsPerWarp; ++k) {
-        const int r = warp + k * kFEpiWarps;
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int j = lane + 32 * u;
-          const bool in = r < R && j < ncp;
-          lm[k][u] = in ? __ldcg(pm + static_cast<size_t>(r) * ncp + j) : kNegBig;
-          lz[k][u] = in ? __ldcg(pz + static_cast<size_t>(r) * ncp + j) : 0.f;
+        for (int i = 0; i < kMaxG; ++i) {
+          const int gi = part + kTpr * i;
+          const bool in = r < R && gi < ng;
+          m4[i] = in ? __ldcg(reinterpret_cast<const float4*>(pm + static_cast<size_t>(r) * ncp) + gi)
+                     : make_float4(kNegBig, kNegBig, kNegBig, kNegBig);
+          z4[i] = in ? __ldcg(reinterpret_cast<const float4*>(pz + static_cast<size_t>(r) * ncp) + gi)
+                     : make_float4(0.f, 0.f, 0.f, 0.f);
         }
-      }
+        float mm = kNegBig;
 #pragma unroll
-      for (int k = 0; k < kRowsPerWarp; ++k) {
-        const int r = warp + k * kFEpiWarps;
-        float mm = fmaxf(lm[k][0], lm[k][1]);
+        for (int i = 0; i < kMaxG; ++i) mm = fmaxf(mm, fmaxf(fmaxf(m4[i].x, m4[i].y), fmaxf(m4[i].z, m4[i].w)));
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) mm = fmaxf(mm, __shfl_xor_sync(0xffffffffu, mm, o));
-        float zz = lz[k][0] * ex2_approx(lm[k][0] - mm) + lz[k][1] * ex2_approx(lm[k][1] - mm);
+        for (int o = 1; o < kTpr; o <<= 1) mm = fmaxf(mm, __shfl_xor_sync(0xffffffffu, mm, o));
+        float zz = 0.f;
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) zz += __shfl_xor_sync(0xffffffffu, zz, o);
-        if (lane == 0 && r < RP) s_nc2[r] = r < R ? -(mm + lg2_approx(zz)) : 0.f;
+        for (int i = 0; i < kMaxG; ++i)
+          zz += z4[i].x * ex2_approx(m4[i].x - mm) + z4[i].y * ex2_approx(m4[i].y - mm) +
+                z4[i].z * ex2_approx(m4[i].z - mm) + z4[i].w * ex2_approx(m4[i].w - mm);
+#pragma unroll
+        for (int o = 1; o < kTpr; o <<= 1) zz += __shfl_xor_sync(0xffffffffu, zz, o);
+        if (part == 0 && r < RP) s_nc2[r] = r < R ? -(mm + lg2_approx(zz)) : 0.f;
       }
       fused_epi_bar();
       // ---------------- epilogue, pass 2: group g takes tiles g, g+2, ...; halves split the rows ----------------
