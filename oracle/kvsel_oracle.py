@@ -14,8 +14,10 @@ Sources (cited by page title and section):
          App. C.4 Theorem C.1, App. D.4, and the kvpress notes (section 3 of the add-on).
   [KVZ]  "KVzip: Query-Agnostic KV Cache Compression with Context Reconstruction":
          §2.2 (GQA cache structure), §3.2 (maximum cross-attention score), §3.4 (chunked
-         scoring), §4.2 (non-uniform head budget, kept system prompt, eviction on the
-         un-replicated cache), §7.1 (variable-length decode).
+         scoring; head-level score as the maximum over the sequence), §3.6 (head-level
+         eviction), §4.2 (non-uniform head budget, kept system prompt, eviction on the
+         un-replicated cache), §6.5 (softmax-free variant, KVzip-logit), §7.1
+         (variable-length decode).
   [VKV]  "VestigeKV: The NoPE-MLA KV Cache Carries Its Own Eviction Signal in a Vestigial
          Branch": §4.1 (4 sinks + recent window are always kept).
   [AKV]  "AnchorKV: Anchor-Residual KV Cache Compression": §3.2 (recent window always
@@ -189,6 +191,28 @@ def query_agnostic_scores(q: np.ndarray, k: np.ndarray, scale: Optional[float] =
     return S
 
 
+def query_agnostic_logit_scores(q: np.ndarray, k: np.ndarray, scale: Optional[float] = None,
+                                q_chunk: int = 0) -> np.ndarray:
+    """KVzip-logit, the softmax-free variant ([KVZ] §6.5): S[i] = max over group heads g
+    and query positions j of the scaled dot product q[g][j] . k[i] / sqrt(d) itself,
+    without softmax normalisation.  Chunks combine with max as in §3.4."""
+    G, m, d = q.shape
+    if scale is None or scale == 0.0:
+        scale = 1.0 / math.sqrt(d)
+    step = m if q_chunk <= 0 else q_chunk
+    S = np.full(k.shape[0], -np.inf)
+    for a in range(0, m, step):
+        qa = q[:, a:a + step, :].reshape(-1, d)
+        S = np.maximum(S, ((qa @ k.T) * scale).max(axis=0))
+    return S
+
+
+def head_scores(S: np.ndarray) -> np.ndarray:
+    """Head-level importance ([KVZ] §3.4, §3.6): S_head = max over the sequence of the
+    per-key score of that head.  S: [H][n] -> [H]."""
+    return S.max(axis=1)
+
+
 # ---------------------------------------------------------------------------------------
 # forced entries and selection
 # ---------------------------------------------------------------------------------------
@@ -296,6 +320,8 @@ def run_layer(q_bits: np.ndarray, k_bits: Sequence[np.ndarray], v_bits: Sequence
             qh = bf16_to_f64(q_bits[b][h])
             if window > 0:
                 s_raw[h] = window_scores(qh, k[h], reduce, scale, causal)
+            elif reduce == "max_logit":
+                s_raw[h] = query_agnostic_logit_scores(qh, k[h], scale, q_chunk)
             else:
                 s_raw[h] = query_agnostic_scores(qh, k[h], scale, q_chunk)
         s_pool = np.stack([pool1d(s_raw[h], pool, pool_kernel) for h in range(H)])

@@ -101,6 +101,18 @@ def _per_layer_ignores_floor(scores, budget, forced, floor_per_head):
     return ORIG["select_per_layer"](scores, budget, forced, 0)
 
 
+def _logit_no_scale(q, k, scale=None, q_chunk=0):
+    return ORIG["query_agnostic_logit_scores"](q, k, 1.0, q_chunk)
+
+
+def _logit_first_group_head_only(q, k, scale=None, q_chunk=0):
+    return ORIG["query_agnostic_logit_scores"](q[:1], k, scale, q_chunk)
+
+
+def _head_scores_mean(S):
+    return S.mean(axis=1)
+
+
 MUTANTS = {
     "no_scale": ("window_logits", _logits_no_scale),
     "causal_off_by_one": ("window_logits", _logits_causal_off_by_one),
@@ -115,6 +127,9 @@ MUTANTS = {
     "forced_recent_off_by_one": ("forced_mask", _forced_recent_off_by_one),
     "query_agnostic_mean": ("query_agnostic_scores", _query_agnostic_mean),
     "per_layer_ignores_floor": ("select_per_layer", _per_layer_ignores_floor),
+    "logit_no_scale": ("query_agnostic_logit_scores", _logit_no_scale),
+    "logit_first_group_head": ("query_agnostic_logit_scores", _logit_first_group_head_only),
+    "head_scores_mean": ("head_scores", _head_scores_mean),
 }
 
 

@@ -404,6 +404,43 @@ def test_max_trick_identity():
                                O.query_agnostic_scores(q, k), rtol=1e-13)
 
 
+def test_logit_score_brute_force_and_chunks():
+    """KVzip-logit: max over group heads and positions of the scaled dot product, by
+    plain loops; chunking does not change it."""
+    rng = np.random.default_rng(21)
+    G, m, d, n = 3, 5, 4, 8
+    q = rng.standard_normal((G, m, d))
+    k = rng.standard_normal((n, d))
+    S = O.query_agnostic_logit_scores(q, k)
+    for i in range(n):
+        best = -math.inf
+        for g in range(G):
+            for j in range(m):
+                best = max(best, sum(float(q[g, j, c]) * float(k[i, c]) for c in range(d)) / math.sqrt(d))
+        assert abs(S[i] - best) < 1e-14
+    np.testing.assert_array_equal(O.query_agnostic_logit_scores(q, k, q_chunk=2), S)
+    np.testing.assert_allclose(O.query_agnostic_logit_scores(q, k, scale=0.5), S * math.sqrt(d) * 0.5, rtol=1e-14)
+
+
+def test_logit_and_softmax_scores_rank_alike_for_one_query():
+    """With a single query row the softmax weight is exp(logit - logsumexp): a monotone
+    function of the logit, so the two scores order the keys identically."""
+    rng = np.random.default_rng(22)
+    q = rng.standard_normal((1, 1, 16))
+    k = rng.standard_normal((40, 16))
+    sl = O.query_agnostic_logit_scores(q, k)
+    ss = O.query_agnostic_scores(q, k)
+    np.testing.assert_allclose(ss, np.exp(sl - scipy.special.logsumexp(sl)), rtol=1e-13)
+    np.testing.assert_array_equal(np.argsort(-sl, kind="stable"), np.argsort(-ss, kind="stable"))
+
+
+def test_head_scores():
+    S = np.array([[1.0, 5.0, 3.0], [-2.0, -1.0, -7.0], [0.25, 0.25, 0.5]])
+    np.testing.assert_array_equal(O.head_scores(S), [5.0, -1.0, 0.5])
+    # a head whose keys all score the same has that score as its head score
+    assert O.head_scores(np.full((1, 9), 0.125))[0] == 0.125
+
+
 # --------------------------------------------------------------------- compaction
 def test_compact_and_paging():
     wl = datagen.WORKLOADS[4].replace(batch=3, n_min=40, n_ctx=90)
