@@ -10,9 +10,10 @@
  *     SnapKV kernel 7 / window 32 per its §4.1).
  *   - Value-aware criterion (A + eps) * ||W_O v||_1 and two-stage selection with
  *     alpha = 0.5 (same page, §3.3 Theorem 3.3, §3.4 Algorithm 1, §3.5, footnote 3).
- *   - Query-agnostic maximum cross-attention score and a budget shared by the heads of a
- *     layer ("KVzip: Query-Agnostic KV Cache Compression with Context Reconstruction",
- *     §3.2, §3.4, §4.2).
+ *   - Query-agnostic maximum cross-attention score, its softmax-free variant
+ *     (KVzip-logit) and head-level scores, and a budget shared by the heads of a layer
+ *     ("KVzip: Query-Agnostic KV Cache Compression with Context Reconstruction", §3.2,
+ *     §3.4, §3.6, §4.2, §6.5).
  *   - Attention sinks and the recent window are always kept ("VestigeKV: The NoPE-MLA KV
  *     Cache Carries Its Own Eviction Signal in a Vestigial Branch", §4.1; "AnchorKV:
  *     Anchor-Residual KV Cache Compression", §3.2).
@@ -69,7 +70,9 @@ extern "C" {
 #define KVSEL_EDEVICE (-7)       /* other device-side error recorded in the status word  */
 
 /* ---- enumerations ------------------------------------------------------------------- */
-enum { KVSEL_REDUCE_SUM = 0, KVSEL_REDUCE_MEAN = 1, KVSEL_REDUCE_MAX = 2 };
+/* MAX_LOGIT: query-agnostic only — the maximum scaled dot product itself, without
+ * softmax normalisation (KVzip §6.5, "KVzip-logit"). */
+enum { KVSEL_REDUCE_SUM = 0, KVSEL_REDUCE_MEAN = 1, KVSEL_REDUCE_MAX = 2, KVSEL_REDUCE_MAX_LOGIT = 3 };
 enum { KVSEL_POOL_NONE = 0, KVSEL_POOL_MAX = 1, KVSEL_POOL_AVG = 2 };
 enum { KVSEL_BUDGET_PER_HEAD = 0, KVSEL_BUDGET_PER_LAYER = 1 };
 enum { KVSEL_WO_GROUP_SUM = 0, KVSEL_WO_PER_HEAD = 1 };
@@ -143,7 +146,8 @@ int kvsel_workspace_init(void* ws, size_t ws_bytes, void* stream);
  *   s_attn  device fp32 [n_scores]: pooled attention score
  *   s_val   device fp32 [n_scores]: (s_attn + eps) * nu, or NULL unless value_aware
  *   ws      device workspace of ws_bytes >= kvsel_workspace_size
- * Query-agnostic scoring (window == 0) supports batch 1, non-causal, reduce MAX. */
+ * Query-agnostic scoring (window == 0) supports batch 1, non-causal, reduce MAX (maximum
+ * softmax weight) or MAX_LOGIT (maximum logit, no softmax: one pass instead of two). */
 int kvsel_score(const kvsel_params* p, const void* q, const kvsel_kv* kv, const void* w_o, float* s_attn,
                 float* s_val, void* ws, size_t ws_bytes, void* stream);
 
@@ -229,6 +233,12 @@ void kvsel_set_stage_events(void* const* events);
  * threads; a launch recorded into a CUDA graph under stream capture counts once, at
  * capture).  The difference across a call is that call's kernel count.  Never fails. */
 uint64_t kvsel_launch_count(void);
+
+/* Head-level scores (KVzip §3.4, §3.6): head_out[b*h_kv + h] = the maximum over the
+ * sequence of request b, head h of `scores` (packed as kvsel_score writes them, device fp32
+ * [n_scores]); -inf for an empty request.  head_out: device fp32 [batch*h_kv].  Asynchronous
+ * on `stream`; errors as kvsel_output_size. */
+int kvsel_head_scores(const kvsel_params* p, const float* scores, float* head_out, void* stream);
 
 /* Static description of an error code. */
 const char* kvsel_strerror(int code);

@@ -23,7 +23,7 @@ KVSEL_ECUDA = -5
 KVSEL_ETIMEOUT = -6
 KVSEL_EDEVICE = -7
 
-REDUCE = {"sum": 0, "mean": 1, "max": 2}
+REDUCE = {"sum": 0, "mean": 1, "max": 2, "max_logit": 3}
 POOL = {"none": 0, "max": 1, "avg": 2}
 BUDGET = {"head": 0, "layer": 1}
 WO_MODE = {"group_sum": 0, "per_head": 1}
@@ -33,7 +33,7 @@ MAX_BATCH = 128
 EXPORTS = ("kvsel_workspace_size", "kvsel_output_size", "kvsel_workspace_init", "kvsel_score",
            "kvsel_select", "kvsel_compact", "kvsel_run_layer", "kvsel_get_device_status",
            "kvsel_set_wait_limit", "kvsel_set_stage_events", "kvsel_strerror", "kvsel_version",
-           "kvsel_score_noalloc", "kvsel_launch_count")
+           "kvsel_score_noalloc", "kvsel_launch_count", "kvsel_head_scores")
 NOALLOC_SCRATCH_BYTES = 16 << 20
 STAGES = ("rowstats", "keysum", "wbar", "vnorm", "finalize", "select", "compact")
 
@@ -103,6 +103,7 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
         "kvsel_strerror": ([ctypes.c_int], ctypes.c_char_p),
         "kvsel_version": ([], ctypes.c_char_p),
         "kvsel_launch_count": ([], ctypes.c_uint64),
+        "kvsel_head_scores": ([P, vp, vp, vp], ctypes.c_int),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -214,6 +215,12 @@ def kvsel_strerror(code: int) -> str:
 
 def kvsel_launch_count() -> int:
     return int(load().kvsel_launch_count())
+
+
+def kvsel_head_scores(params, scores, head_out, stream=None) -> None:
+    """head_out[b*h_kv + h] = max over the sequence of request b, head h of `scores`."""
+    _check(load().kvsel_head_scores(ctypes.byref(params), _ptr(scores), _ptr(head_out), _stream(stream)),
+           "kvsel_head_scores")
 
 
 def kvsel_set_wait_limit(cycles: int) -> None:

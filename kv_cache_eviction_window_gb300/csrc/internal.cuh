@@ -76,7 +76,8 @@ struct QaArgs {
   float s2;                       // logit scale * log2(e)
   float* c2;                      // [H][GN] row log-sum-exp, log2 units
   uint32_t* tmax;                 // [H][n] order-preserving keys of max_r (l*s2 - c2_r)
-  float* s_raw;                   // [H][n] exp2 of that max
+  float* s_raw;                   // [H][n] exp2 of that max (softmax), or the max logit itself
+  int logit;                      // softmax-free score: no row log-sum-exp, s2 = scale, c2 = 0
   WaitCtl wc;
 };
 cudaError_t launch_qa_rowlse(const QaArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, cudaStream_t st);
@@ -113,6 +114,10 @@ cudaError_t launch_wbar(const uint16_t* w_o, uint16_t* wbar, int H, int G, int D
 cudaError_t launch_vnorm(const VnormArgs& a, const CUtensorMap& tw, cudaStream_t st);
 int vnorm_token_block();
 int vnorm_w_tile_rows();
+
+// Per-segment maximum of a packed score array: out[b*H + h] = max_i s[soff[b] + h*n_b + i]
+// (-inf for an empty request).
+cudaError_t launch_head_max(const ReqTable& rq, const float* s, float* out, cudaStream_t st);
 
 cudaError_t launch_finalize(const ReqTable& rq, const float* s_raw, const float* nu, float* s_attn, float* s_val,
                             int pool, int pool_kernel, float eps, cudaStream_t st);

@@ -97,7 +97,8 @@ int make_plan(const kvsel_params* p, Plan& pl, bool need_device) {
   if (!p) return KVSEL_EINVAL;
   if (p->head_dim != kHeadDim) return KVSEL_EUNSUPPORTED;
   if (p->h_kv < 1 || p->h_kv > 64 || p->group < 1 || p->batch < 1 || p->batch > kMaxBatch) return KVSEL_EINVAL;
-  if (p->reduce < 0 || p->reduce > 2 || p->pool < 0 || p->pool > 2) return KVSEL_EINVAL;
+  if (p->reduce < 0 || p->reduce > 3 || p->pool < 0 || p->pool > 2) return KVSEL_EINVAL;
+  if (p->reduce == KVSEL_REDUCE_MAX_LOGIT && p->window != 0) return KVSEL_EUNSUPPORTED;   // query-agnostic only
   if (p->pool != KVSEL_POOL_NONE && (p->pool_kernel < 1 || (p->pool_kernel & 1) == 0)) return KVSEL_EINVAL;
   if (p->budget_mode != KVSEL_BUDGET_PER_HEAD && p->budget_mode != KVSEL_BUDGET_PER_LAYER) return KVSEL_EINVAL;
   if (!(p->budget_ratio >= 0.0 && p->budget_ratio <= 1.0) || !(p->floor_ratio >= 0.0 && p->floor_ratio <= 1.0))
@@ -132,7 +133,8 @@ int make_plan(const kvsel_params* p, Plan& pl, bool need_device) {
   if (pl.qa) {
     // KVzip's query-agnostic score: one request, all G*n positions as queries, no causal
     // mask, max over queries and group heads
-    if (pl.B != 1 || p->causal || p->reduce != KVSEL_REDUCE_MAX || p->value_aware || p->q_chunk < 0)
+    if (pl.B != 1 || p->causal || (p->reduce != KVSEL_REDUCE_MAX && p->reduce != KVSEL_REDUCE_MAX_LOGIT) ||
+        p->value_aware || p->q_chunk < 0)
       return KVSEL_EUNSUPPORTED;
     if (static_cast<long long>(pl.G) * pl.n_max > (1ll << 30)) return KVSEL_EUNSUPPORTED;
     pl.R = 0;
@@ -355,17 +357,18 @@ int do_score(const kvsel_params* p, const Plan& pl, const void* q, const kvsel_k
     a.row_blocks = pl.qa_row_blocks;
     a.key_blocks = pl.qa_key_blocks;
     a.row_splits = pl.qa_row_splits;
-    a.s2 = scale * 1.4426950408889634f;
+    a.logit = p->reduce == KVSEL_REDUCE_MAX_LOGIT ? 1 : 0;
+    a.s2 = a.logit ? scale : scale * 1.4426950408889634f;
     a.c2 = reinterpret_cast<float*>(wsb + pl.ws_c2);
     a.tmax = reinterpret_cast<uint32_t*>(wsb + pl.ws_tmax);
     a.s_raw = s_raw;
     a.wc = wait_ctl(ws);
     int rc;
-    {
+    if (!a.logit) {
       StageScope sc(KVSEL_STAGE_ROWSTATS, st);
       rc = launch_rc(launch_qa_rowlse(a, tq, tk64, st));
+      if (rc) return rc;
     }
-    if (rc) return rc;
     {
       StageScope sc(KVSEL_STAGE_KEYSUM, st);
       rc = launch_rc(launch_qa_keymax(a, tq, tk128, st));
@@ -529,6 +532,15 @@ int do_compact(const Plan& pl, const kvsel_kv* kv, const int32_t* idx, const int
 extern "C" {
 
 uint64_t kvsel_launch_count(void) { return kvsel::g_launches.load(std::memory_order_relaxed); }
+
+int kvsel_head_scores(const kvsel_params* p, const float* scores, float* head_out, void* stream) {
+  Plan pl;
+  const int rc = make_plan(p, pl, false);
+  if (rc) return rc;
+  if (!scores || !head_out) return KVSEL_EINVAL;
+  if (pl.n_scores == 0 && pl.B * pl.H == 0) return KVSEL_OK;
+  return launch_rc(launch_head_max(pl.rq, scores, head_out, static_cast<cudaStream_t>(stream)));
+}
 
 const char* kvsel_version(void) { return "kvsel 0.1 (sm_103a)"; }
 

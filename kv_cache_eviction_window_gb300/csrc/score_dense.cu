@@ -14,6 +14,8 @@
 //     tiles streamed over a slice of the rows; every thread keeps max_r (l_ri*s2 - c2_r)
 //     for its keys; slices merge with an order-preserving atomicMax in global memory.
 //   qa_finish_kernel: s_raw_i = exp2(max).
+// The softmax-free variant (KVzip §6.5, "KVzip-logit") skips the first pass: c2 = 0 and
+// s2 = the logit scale, so the second pass keeps max_r l_ri itself and s_raw is that max.
 // Both passes are tensor-core bound at this shape (2*G*n*n*d flop each).
 #include "internal.cuh"
 
@@ -335,7 +337,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       // c2 of this thread's 32 query rows: one coalesced load, broadcast by shuffles
       const int rrow = r_begin + t * kNT + cg * 32 + lane;
-      const float myc2 = rrow < r_end ? __ldg(a.c2 + static_cast<size_t>(h) * GN + rrow) : INFINITY;
+      const float myc2 = rrow < r_end ? (a.logit ? 0.f : __ldg(a.c2 + static_cast<size_t>(h) * GN + rrow)) : INFINITY;
       float nc[32];
 #pragma unroll
       for (int j = 0; j < 32; ++j) nc[j] = -__shfl_sync(0xffffffffu, myc2, j);
@@ -379,10 +381,34 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-__global__ void qa_finish_kernel(const uint32_t* __restrict__ tmax, float* __restrict__ s_raw, long long total) {
+__global__ void qa_finish_kernel(const uint32_t* __restrict__ tmax, float* __restrict__ s_raw, long long total,
+                                 int logit) {
   for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
-       i += static_cast<long long>(gridDim.x) * blockDim.x)
-    s_raw[i] = ex2_approx(key2f(tmax[i]));
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const float m = key2f(tmax[i]);
+    s_raw[i] = logit ? m : ex2_approx(m);
+  }
+}
+
+// One block per (request, head): maximum of the head's scores.
+__global__ void head_max_kernel(const ReqTable rq, const float* __restrict__ s, float* __restrict__ out) {
+  const int seg = blockIdx.x;
+  const int b = seg / rq.H, h = seg - (seg / rq.H) * rq.H;
+  const int n = rq.n[b];
+  const float* src = s + rq.soff[b] + static_cast<long long>(h) * n;
+  float m = -INFINITY;
+  for (int i = threadIdx.x; i < n; i += blockDim.x) m = fmaxf(m, __ldg(src + i));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  __shared__ float wm[32];
+  if ((threadIdx.x & 31) == 0) wm[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    m = threadIdx.x < blockDim.x / 32 ? wm[threadIdx.x] : -INFINITY;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if (threadIdx.x == 0) out[seg] = m;
+  }
 }
 
 }  // namespace
@@ -408,11 +434,18 @@ cudaError_t launch_qa_keymax(const QaArgs& a, const CUtensorMap& tq, const CUten
   if (e != cudaSuccess) return e;
   const long long total = static_cast<long long>(a.H) * a.n;
   const int blocks = static_cast<int>((total + 255) / 256 < 4096 ? (total + 255) / 256 : 4096);
-  qa_finish_kernel<<<blocks, 256, 0, st>>>(a.tmax, a.s_raw, total);
+  qa_finish_kernel<<<blocks, 256, 0, st>>>(a.tmax, a.s_raw, total, a.logit);
   note_launch();
   return cudaGetLastError();
 }
 
 int qa_block_rows() { return kMT * 128; }
+
+cudaError_t launch_head_max(const ReqTable& rq, const float* s, float* out, cudaStream_t st) {
+  if (rq.B * rq.H <= 0) return cudaSuccess;
+  head_max_kernel<<<rq.B * rq.H, 512, 0, st>>>(rq, s, out);
+  note_launch();
+  return cudaGetLastError();
+}
 
 }  // namespace kvsel

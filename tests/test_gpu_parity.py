@@ -208,6 +208,44 @@ def test_c5_query_agnostic(n):
     _check_layer(wl, inp, gpu, ora)
 
 
+@pytest.mark.parametrize("n", [1000, 2048])
+def test_c5_logit_scores_and_head_scores(n):
+    """KVzip-logit (softmax-free): the maximum scaled dot product over all G*n query rows,
+    one budget per layer; and head-level scores (max over the sequence) of those scores."""
+    import torch
+    from kv_cache_eviction_window_gb300 import binding as B
+
+    wl = datagen.WORKLOADS[5].replace(h_kv=4, reduce="max_logit")
+    inp = datagen.make_layer(wl, 0, n_ctx=n)
+    ora = O.run_workload_layer(wl, inp)
+    gpu = GH.run_gpu_layer(wl, inp)
+    _check_layer(wl, inp, gpu, ora)
+    p = B.params_from_workload(wl, n_ctx=n)
+    s = torch.from_numpy(np.concatenate([gpu[0]["s_attn"][h] for h in range(wl.h_kv)])).cuda()
+    hs = torch.empty(wl.h_kv, dtype=torch.float32, device="cuda")
+    B.kvsel_head_scores(p, s, hs)
+    hs = hs.cpu().numpy()
+    np.testing.assert_array_equal(hs, [gpu[0]["s_attn"][h].max() for h in range(wl.h_kv)])
+    GH.assert_scores_close(hs, O.head_scores(ora[0]["s_pool"]), "head scores")
+
+
+def test_head_scores_ragged_batch():
+    """Head scores over a packed ragged batch (per request and head)."""
+    import torch
+    from kv_cache_eviction_window_gb300 import binding as B
+
+    wl = datagen.WORKLOADS[4].replace(batch=5, n_min=100, n_ctx=700)
+    lens = datagen.context_lengths(wl)
+    p = B.params_from_workload(wl, n_ctx_per_req=lens)
+    rng = np.random.default_rng(3)
+    parts = [rng.standard_normal((wl.h_kv, n)).astype(np.float32) for n in lens]
+    s = torch.from_numpy(np.concatenate([x.reshape(-1) for x in parts])).cuda()
+    hs = torch.empty(len(lens) * wl.h_kv, dtype=torch.float32, device="cuda")
+    B.kvsel_head_scores(p, s, hs)
+    want = np.concatenate([x.max(axis=1) for x in parts])
+    np.testing.assert_array_equal(hs.cpu().numpy(), want)
+
+
 # ---------------------------------------------------------------------- full size
 def test_c2_full_layer_plain_and_sampled_value_aware():
     """Llama-3.1-8B layer, n = 32768: plain scores and selection against the full oracle;
@@ -263,6 +301,32 @@ def test_bounded_wait_timeout_reports_status():
     ora = O.run_workload_layer(wl, inp)
     gpu = GH.run_gpu_layer(wl, inp)
     _check_layer(wl, inp, gpu, ora)
+
+
+def test_c5_logit_full_layer_sampled_keys():
+    """KVzip-logit at n = 32768: 12 keys per head checked exactly against the maximum over
+    all 262144 query rows, every key against a sampled-row lower bound, and the kept set
+    is exactly the layer top-B of the GPU's own scores."""
+    wl = datagen.WORKLOADS[5].replace(reduce="max_logit")
+    inp = datagen.make_layer(wl, 0)
+    gpu = GH.run_gpu_layer(wl, inp)[0]
+    n, H = wl.n_ctx, wl.h_kv
+    rng = np.random.default_rng(6)
+    k = O.bf16_to_f64(inp["k"][0])
+    for h in range(H):
+        s = gpu["s_attn"][h].astype(np.float64)
+        q = O.bf16_to_f64(inp["q"][0][h])                        # [G][n][d]
+        keys = rng.choice(n, size=12, replace=False)
+        exact = O.query_agnostic_logit_scores(q, k[h][keys])
+        GH.assert_scores_close(s[keys], exact, f"head {h} sampled keys")
+        pos = rng.choice(n, size=6, replace=False)
+        lower = O.query_agnostic_logit_scores(q[:, pos, :], k[h])
+        assert np.all(s >= lower - 1e-4 * np.abs(lower).max()), f"head {h}"
+    fm = O.forced_mask(n, wl.n_sink, wl.n_recent)
+    BL = int(math.floor(wl.budget_ratio * n * H))
+    flat = np.concatenate([gpu["s_attn"][h] for h in range(H)])
+    kept = np.concatenate([np.asarray(gpu["idx"][h]) + h * n for h in range(H)])
+    GH.check_topk_property(flat, np.sort(kept), np.tile(fm, H), BL, "C5-logit layer top-B")
 
 
 def test_c5_full_layer_sampled_rows():
