@@ -48,7 +48,7 @@ class Workload:
     n_ctx: int            # context length (max length for the ragged batch)
     window: int           # observation-window queries per group head; 0 = all n positions
     causal: bool
-    reduce: str           # "sum" | "mean" | "max"
+    reduce: str           # "sum" | "mean" | "max" | "max_logit" (query-agnostic, no softmax)
     pool: str             # "none" | "max" | "avg"
     pool_kernel: int
     value_aware: bool
@@ -65,6 +65,7 @@ class Workload:
     block_size: int = 16
     q_chunk: int = 0      # query-agnostic scoring: query rows per chunk (per group head)
     key_structure: str = "plain"  # "heavy" | "lognormal" | "zipf" | "plain"
+    value_norm: str = "l1"        # value-aware: "l1" (default) | "l2" (norm of W_h v)
 
     def replace(self, **kw) -> "Workload":
         return dataclasses.replace(self, **kw)

@@ -136,9 +136,11 @@ def wo_slices(w_o: np.ndarray, h: int, group: int, d: int) -> List[np.ndarray]:
 
 
 def value_norm(v: np.ndarray, w_o: np.ndarray, h: int, group: int,
-               mode: str = "group_sum", row_block: int = 4096) -> np.ndarray:
+               mode: str = "group_sum", row_block: int = 4096, norm: str = "l1") -> np.ndarray:
     """nu[i] = L1 norm of the value state v[i] projected through W_O ([CKV] Algorithm 1,
-    Theorem 3.3; kvpress notes: L1 norm of V @ Wo[head]).
+    Theorem 3.3; kvpress notes: L1 norm of V @ Wo[head]); with norm="l2" the Euclidean
+    norm, the other distance [CKV] App. C.3 compares (reading of the garbled symbols:
+    the paper adopts L1 for simplicity and reports L2 as giving similar gains).
 
     v: [n][d] values of KV head h.  GQA reading ("group_sum", default): the value is
     replicated over the G query heads of the group, so its projected contribution is
@@ -149,17 +151,25 @@ def value_norm(v: np.ndarray, w_o: np.ndarray, h: int, group: int,
     n, d = v.shape
     sl = wo_slices(w_o, h, group, d)
     out = np.empty(n)
+    if norm == "l1":
+        def rownorm(x):
+            return np.abs(x).sum(axis=1)
+    elif norm == "l2":
+        def rownorm(x):
+            return np.sqrt((x * x).sum(axis=1))
+    else:
+        raise ValueError(norm)
     if mode == "group_sum":
         wbar = np.zeros_like(sl[0])
         for s in sl:
             wbar = wbar + s
         for a in range(0, n, row_block):
-            out[a:a + row_block] = np.abs(v[a:a + row_block] @ wbar.T).sum(axis=1)
+            out[a:a + row_block] = rownorm(v[a:a + row_block] @ wbar.T)
     elif mode == "per_head":
         out[:] = 0.0
         for s in sl:
             for a in range(0, n, row_block):
-                out[a:a + row_block] += np.abs(v[a:a + row_block] @ s.T).sum(axis=1)
+                out[a:a + row_block] += rownorm(v[a:a + row_block] @ s.T)
     else:
         raise ValueError(mode)
     return out
@@ -300,7 +310,7 @@ def run_layer(q_bits: np.ndarray, k_bits: Sequence[np.ndarray], v_bits: Sequence
               alpha: float, n_sink: int, n_recent: int, budget_mode: str,
               budget_ratio: float, floor_ratio: float = 0.0, scale: Optional[float] = None,
               q_chunk: int = 0, wo_mode: str = "group_sum", heads: Optional[Sequence[int]] = None,
-              compact_out: bool = True) -> List[dict]:
+              compact_out: bool = True, value_norm_kind: str = "l1") -> List[dict]:
     """Score -> select -> compact for every request of one layer.
 
     q_bits: [B][H][G][W][d] bf16 bits (W = n for query-agnostic scoring), k_bits/v_bits:
@@ -330,7 +340,7 @@ def run_layer(q_bits: np.ndarray, k_bits: Sequence[np.ndarray], v_bits: Sequence
             v = bf16_to_f64(v_bits[b])
             nu = np.zeros((H, n))
             for h in hs:
-                nu[h] = value_norm(v[h], w_o, h, group, wo_mode)
+                nu[h] = value_norm(v[h], w_o, h, group, wo_mode, norm=value_norm_kind)
             s_val = combine(s_pool, nu, eps)
         fm = forced_mask(n, n_sink, n_recent)
         if budget_mode == "head":
@@ -362,4 +372,5 @@ def run_workload_layer(wl, inputs: dict, **kw) -> List[dict]:
                      pool_kernel=wl.pool_kernel, value_aware=wl.value_aware, eps=wl.eps,
                      alpha=wl.alpha, n_sink=wl.n_sink, n_recent=wl.n_recent,
                      budget_mode=wl.budget_mode, budget_ratio=wl.budget_ratio,
-                     floor_ratio=wl.floor_ratio, q_chunk=wl.q_chunk, **kw)
+                     floor_ratio=wl.floor_ratio, q_chunk=wl.q_chunk,
+                     value_norm_kind=wl.value_norm, **kw)

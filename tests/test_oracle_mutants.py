@@ -49,15 +49,16 @@ def _avgpool_divides_by_count(s, kind, kernel):
     return out
 
 
-def _value_norm_l2(v, w_o, h, group, mode="group_sum", row_block=4096):
+def _value_norm_l2(v, w_o, h, group, mode="group_sum", row_block=4096, norm="l1"):
     sl = O.wo_slices(w_o, h, group, v.shape[1])
     wbar = sum(sl)
     return np.sqrt(((v @ wbar.T) ** 2).sum(1))
 
 
-def _value_norm_first_slice_only(v, w_o, h, group, mode="group_sum", row_block=4096):
+def _value_norm_first_slice_only(v, w_o, h, group, mode="group_sum", row_block=4096, norm="l1"):
     sl = O.wo_slices(w_o, h, group, v.shape[1])
-    return np.abs(v @ (group * sl[0]).T).sum(1)
+    x = v @ (group * sl[0]).T
+    return np.abs(x).sum(1) if norm == "l1" else np.sqrt((x * x).sum(1))
 
 
 def _combine_no_eps(s_pool, nu, eps=1e-4):
@@ -113,6 +114,11 @@ def _head_scores_mean(S):
     return S.mean(axis=1)
 
 
+def _value_norm_l2_no_sqrt(v, w_o, h, group, mode="group_sum", row_block=4096, norm="l1"):
+    r = ORIG["value_norm"](v, w_o, h, group, mode, row_block, norm)
+    return r * r if norm == "l2" else r
+
+
 MUTANTS = {
     "no_scale": ("window_logits", _logits_no_scale),
     "causal_off_by_one": ("window_logits", _logits_causal_off_by_one),
@@ -130,6 +136,7 @@ MUTANTS = {
     "logit_no_scale": ("query_agnostic_logit_scores", _logit_no_scale),
     "logit_first_group_head": ("query_agnostic_logit_scores", _logit_first_group_head_only),
     "head_scores_mean": ("head_scores", _head_scores_mean),
+    "value_norm_l2_no_sqrt": ("value_norm", _value_norm_l2_no_sqrt),
 }
 
 

@@ -181,6 +181,47 @@ def test_value_norm_identity_slices_closed_form():
                                    G * np.abs(v).sum(1), rtol=1e-14)
 
 
+def test_value_norm_l2_closed_forms():
+    """L2 reading: identity slices give G*||v||_2; an orthogonal group sum Q (Q^T Q = I)
+    preserves the Euclidean norm; one 3-4-5 row by hand."""
+    rng = np.random.default_rng(23)
+    H, G, d, D, n = 2, 3, 4, 6, 9
+    w_o = np.zeros((D, H * G * d))
+    for q in range(H * G):
+        w_o[:d, q * d:(q + 1) * d] = np.eye(d)
+    v = rng.standard_normal((n, d))
+    for h in range(H):
+        np.testing.assert_allclose(O.value_norm(v, w_o, h, G, norm="l2"), G * np.sqrt((v * v).sum(1)), rtol=1e-14)
+    # orthogonal W_h (one query head per KV head): ||Q v||_2 = ||v||_2
+    Q, _ = np.linalg.qr(rng.standard_normal((d, d)))
+    w1 = np.zeros((d, d))
+    w1[:, :] = Q
+    np.testing.assert_allclose(O.value_norm(v, w1, 0, 1, norm="l2"), np.linalg.norm(v, axis=1), rtol=1e-13)
+    # hand: W_h = diag(1, 1), v = (3, 4) -> 5 (L1 would give 7)
+    w2 = np.eye(2)
+    vv = np.array([[3.0, 4.0]])
+    assert O.value_norm(vv, w2, 0, 1, norm="l2")[0] == 5.0
+    assert O.value_norm(vv, w2, 0, 1, norm="l1")[0] == 7.0
+
+
+def test_value_norm_l2_brute_force():
+    rng = np.random.default_rng(24)
+    H, G, d, D, n = 2, 2, 3, 5, 4
+    w_o = rng.standard_normal((D, H * G * d))
+    v = rng.standard_normal((n, d))
+    for h in range(H):
+        got = O.value_norm(v, w_o, h, G, norm="l2")
+        for i in range(n):
+            tot = 0.0
+            for j in range(D):
+                x = 0.0
+                for g in range(G):
+                    for c in range(d):
+                        x += w_o[j, (h * G + g) * d + c] * v[i, c]
+                tot += x * x
+            assert abs(got[i] - math.sqrt(tot)) < 1e-12 * max(1.0, math.sqrt(tot))
+
+
 def test_value_norm_readings_differ_on_opposite_slices():
     d, D, G = 3, 3, 2
     w_o = np.concatenate([np.eye(d), -np.eye(d)], axis=1)   # head 0: +I, head 1: -I
