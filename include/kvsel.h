@@ -76,6 +76,10 @@ enum { KVSEL_REDUCE_SUM = 0, KVSEL_REDUCE_MEAN = 1, KVSEL_REDUCE_MAX = 2, KVSEL_
 enum { KVSEL_POOL_NONE = 0, KVSEL_POOL_MAX = 1, KVSEL_POOL_AVG = 2 };
 enum { KVSEL_BUDGET_PER_HEAD = 0, KVSEL_BUDGET_PER_LAYER = 1 };
 enum { KVSEL_WO_GROUP_SUM = 0, KVSEL_WO_PER_HEAD = 1 };
+/* Value norm of the value-aware criterion: L1 (CriticalKV's choice) or L2, the other
+ * distance its App. C.3 compares.  L2 is computed through the d x d Gram matrix
+ * W_h^T W_h (32x fewer flops at D = 4096); group-sum W_O reading only. */
+enum { KVSEL_NORM_L1 = 0, KVSEL_NORM_L2 = 1 };
 enum { KVSEL_LAYOUT_CONTIGUOUS = 0, KVSEL_LAYOUT_PAGED = 1 };
 
 #define KVSEL_MAX_BATCH 128
@@ -107,6 +111,7 @@ typedef struct kvsel_params {
   double floor_ratio;   /* per layer: each head keeps at least floor(floor_ratio*n)      */
   int32_t batch;        /* requests in the call (<= KVSEL_MAX_BATCH)                      */
   const int32_t* n_ctx_per_req; /* host [batch] context lengths, or NULL                  */
+  int32_t value_norm;   /* KVSEL_NORM_*: ||W_h v||_1 (default) or ||W_h v||_2            */
 } kvsel_params;
 
 /* K/V cache view, contiguous or paged (block_size tokens per block). */
@@ -145,6 +150,7 @@ int kvsel_workspace_init(void* ws, size_t ws_bytes, void* stream);
  *   w_o     device bf16 [d_model][h_kv*group*head_dim], or NULL unless value_aware
  *   s_attn  device fp32 [n_scores]: pooled attention score
  *   s_val   device fp32 [n_scores]: (s_attn + eps) * nu, or NULL unless value_aware
+ *           (nu = ||W_h v||_1, or ||W_h v||_2 with value_norm = KVSEL_NORM_L2)
  *   ws      device workspace of ws_bytes >= kvsel_workspace_size
  * Query-agnostic scoring (window == 0) supports batch 1, non-causal, reduce MAX (maximum
  * softmax weight) or MAX_LOGIT (maximum logit, no softmax: one pass instead of two). */

@@ -27,6 +27,7 @@ REDUCE = {"sum": 0, "mean": 1, "max": 2, "max_logit": 3}
 POOL = {"none": 0, "max": 1, "avg": 2}
 BUDGET = {"head": 0, "layer": 1}
 WO_MODE = {"group_sum": 0, "per_head": 1}
+VALUE_NORM = {"l1": 0, "l2": 1}
 LAYOUT_CONTIGUOUS, LAYOUT_PAGED = 0, 1
 MAX_BATCH = 128
 
@@ -58,7 +59,7 @@ class kvsel_params(ctypes.Structure):
         ("alpha", ctypes.c_float), ("n_sink", ctypes.c_int32), ("n_recent", ctypes.c_int32),
         ("budget_mode", ctypes.c_int32), ("budget_ratio", ctypes.c_double),
         ("floor_ratio", ctypes.c_double), ("batch", ctypes.c_int32),
-        ("n_ctx_per_req", ctypes.POINTER(ctypes.c_int32)),
+        ("n_ctx_per_req", ctypes.POINTER(ctypes.c_int32)), ("value_norm", ctypes.c_int32),
     ]
 
 
@@ -121,7 +122,7 @@ def make_params(*, h_kv: int, group: int, n_ctx: int, window: int, head_dim: int
                 value_aware: bool = False, wo_mode: str = "group_sum", eps: float = 1e-4,
                 alpha: float = 0.5, n_sink: int = 4, n_recent: int = 32,
                 budget_mode: str = "head", budget_ratio: float = 0.2, floor_ratio: float = 0.0,
-                n_ctx_per_req: Optional[Sequence[int]] = None) -> kvsel_params:
+                n_ctx_per_req: Optional[Sequence[int]] = None, value_norm: str = "l1") -> kvsel_params:
     p = kvsel_params()
     p.h_kv, p.group, p.head_dim, p.d_model = h_kv, group, head_dim, d_model
     p.n_ctx, p.window, p.q_chunk, p.causal = n_ctx, window, q_chunk, int(bool(causal))
@@ -130,6 +131,7 @@ def make_params(*, h_kv: int, group: int, n_ctx: int, window: int, head_dim: int
     p.value_aware, p.wo_mode, p.eps, p.alpha = int(bool(value_aware)), WO_MODE[wo_mode], eps, alpha
     p.n_sink, p.n_recent = n_sink, n_recent
     p.budget_mode, p.budget_ratio, p.floor_ratio = BUDGET[budget_mode], budget_ratio, floor_ratio
+    p.value_norm = VALUE_NORM[value_norm]
     if n_ctx_per_req is not None:
         arr = (ctypes.c_int32 * len(n_ctx_per_req))(*[int(x) for x in n_ctx_per_req])
         p._n_arr = arr  # keep alive
@@ -146,7 +148,7 @@ def params_from_workload(wl, n_ctx_per_req: Optional[Sequence[int]] = None, **ov
               reduce=wl.reduce, pool=wl.pool, pool_kernel=wl.pool_kernel, value_aware=wl.value_aware,
               eps=wl.eps, alpha=wl.alpha, n_sink=wl.n_sink, n_recent=wl.n_recent,
               budget_mode=wl.budget_mode, budget_ratio=wl.budget_ratio, floor_ratio=wl.floor_ratio,
-              n_ctx_per_req=n_ctx_per_req)
+              n_ctx_per_req=n_ctx_per_req, value_norm=wl.value_norm)
     kw.update(override)
     return make_params(**kw)
 

@@ -38,6 +38,31 @@ struct KvSource {
   const int* block_table;   // device [B][max_blocks]
 };
 
+// TMA loads of `rows` tokens [tok0, tok0 + rows) of KV head h of request b into a
+// K-major 128B-swizzled tile [2 column halves][rows][128 B].
+__device__ __forceinline__ void load_kv_tile(const CUtensorMap* map, const KvSource& src, int b, int h, int n,
+                                             int tok0, int rows, uint8_t* dst, uint64_t* bar, int* status) {
+  const int half = rows * 128;
+  if (!src.paged) {
+    tma_load_4d(dst, map, bar, 0, tok0, h, b);
+    tma_load_4d(dst + half, map, bar, 64, tok0, h, b);
+  } else {
+    const int bs = src.block_size;
+    const int nblk_req = (n + bs - 1) / bs;
+    for (int j = 0; j < rows / bs; ++j) {
+      const int lb = tok0 / bs + j;
+      int pb = -1;
+      if (lb < nblk_req && lb < src.max_blocks) pb = __ldg(src.block_table + (size_t)b * src.max_blocks + lb);
+      if (pb < 0 || pb >= src.num_blocks) {
+        if (lb < nblk_req) atomicOr(status, DEV_BAD_INDEX);
+        pb = 0;  // tokens past the request (masked by the epilogue) or a bad entry
+      }
+      tma_load_4d(dst + j * bs * 128, map, bar, 0, h, 0, pb);
+      tma_load_4d(dst + half + j * bs * 128, map, bar, 64, h, 0, pb);
+    }
+  }
+}
+
 // Key-range decomposition shared by the two window-scoring passes: every (b, h) is cut
 // into chunks of `chunk_len` keys; chunk ids run request-major, then head, then chunk.
 struct ChunkTable {
@@ -97,6 +122,26 @@ struct VnormArgs {
   float* nu;                      // packed [sum_b H*n_b]
   WaitCtl wc;
 };
+
+// L2 value norm through the Gram matrix Gamma_h = W_h^T W_h.  Units are (request, head,
+// 128-token block), request-major then head, as VnormArgs with 128-token blocks.
+struct VgramArgs {
+  ReqTable rq;
+  KvSource src;
+  int units_total;
+  int unit_base[kMaxBatch + 1];
+  int blocks_per_head[kMaxBatch];
+  float* nu;                      // packed [sum_b H*n_b]
+  WaitCtl wc;
+};
+// Dw-slices of the Gram partials (workspace: H * slices * 128 * 128 fp32).
+int gram_slices(int Dw);
+// W_h^T (wt: [H][d][D] bf16), Gamma partials (part), Gamma hi/lo (gam: [H][2][d][d] bf16).
+// twt: 2-D map over wt (D, H*d rows), box 64 x 128.
+cudaError_t launch_value_gram(const uint16_t* w_o, uint16_t* wt, float* part, uint16_t* gam, int H, int G, int D,
+                              const CUtensorMap& twt, WaitCtl wc, cudaStream_t st);
+// tv: V tiles of 128 tokens (kv_map); tg: 2-D map over gam (d, H*2*d rows), box 64 x 128.
+cudaError_t launch_vgram(const VgramArgs& a, const CUtensorMap& tv, const CUtensorMap& tg, cudaStream_t st);
 
 // Raise a kernel's dynamic shared-memory limit once per device (cached).
 cudaError_t ensure_smem(const void* func, size_t bytes);

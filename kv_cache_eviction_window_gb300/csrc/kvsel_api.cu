@@ -76,9 +76,12 @@ struct Plan {
   int max_count = 0;
   ChunkTable ck{};
   int units_total = 0, unit_base[kMaxBatch + 1]{}, blocks_per_head[kMaxBatch]{};
+  bool l2 = false;     // value norm through the Gram matrix (KVSEL_NORM_L2)
+  int g_units = 0, g_unit_base[kMaxBatch + 1]{}, g_blocks_per_head[kMaxBatch]{};   // 128-token tiles
   int num_sms = 0;
   size_t ws_part = 0, ws_sraw = 0, ws_nu = 0, ws_wbar = 0, ws_total = 0;
   size_t ws_c2 = 0, ws_tmax = 0;   // query-agnostic scoring
+  size_t ws_gpart = 0, ws_gam = 0;  // L2 value norm: Gram partials and Gamma hi/lo
   int qa_row_blocks = 0, qa_key_blocks = 0, qa_row_splits = 0;
 };
 
@@ -110,6 +113,10 @@ int make_plan(const kvsel_params* p, Plan& pl, bool need_device) {
     if (p->d_model < 128 || p->d_model % 128 != 0) return KVSEL_EUNSUPPORTED;
     if (!(p->alpha >= 0.f && p->alpha <= 1.f) || !(p->eps >= 0.f)) return KVSEL_EINVAL;
     if (p->budget_mode != KVSEL_BUDGET_PER_HEAD) return KVSEL_EUNSUPPORTED;
+    if (p->value_norm != KVSEL_NORM_L1 && p->value_norm != KVSEL_NORM_L2) return KVSEL_EINVAL;
+    // the Gram identity holds for one projection per token: the group-sum reading only
+    if (p->value_norm == KVSEL_NORM_L2 && p->wo_mode != KVSEL_WO_GROUP_SUM) return KVSEL_EUNSUPPORTED;
+    pl.l2 = p->value_norm == KVSEL_NORM_L2;
   }
   pl.B = p->batch;
   pl.H = p->h_kv;
@@ -214,6 +221,14 @@ int make_plan(const kvsel_params* p, Plan& pl, bool need_device) {
   }
   pl.unit_base[pl.B] = ub;
   pl.units_total = p->value_aware ? ub : 0;
+  int gu = 0;
+  for (int b = 0; b < pl.B; ++b) {
+    pl.g_unit_base[b] = gu;
+    pl.g_blocks_per_head[b] = (pl.rq.n[b] + 127) / 128;
+    gu += pl.H * pl.g_blocks_per_head[b];
+  }
+  pl.g_unit_base[pl.B] = gu;
+  pl.g_units = pl.l2 ? gu : 0;
 
   size_t off = kStatusBytes + kCounterBytes;
   if (pl.qa) {
@@ -241,8 +256,14 @@ int make_plan(const kvsel_params* p, Plan& pl, bool need_device) {
   if (p->value_aware) {
     pl.ws_nu = off;
     off = align256(off + static_cast<size_t>(pl.n_scores) * sizeof(float));
-    pl.ws_wbar = off;
+    pl.ws_wbar = off;   // W_h (L1) or W_h^T (L2), same size
     off = align256(off + static_cast<size_t>(pl.H) * pl.Dw * kHeadDim * 2);
+    if (pl.l2) {
+      pl.ws_gpart = off;
+      off = align256(off + static_cast<size_t>(pl.H) * gram_slices(pl.Dw) * kHeadDim * kHeadDim * sizeof(float));
+      pl.ws_gam = off;
+      off = align256(off + static_cast<size_t>(pl.H) * 2 * kHeadDim * kHeadDim * 2);
+    }
   }
   pl.ws_total = off;
   return KVSEL_OK;
@@ -427,7 +448,46 @@ int do_score(const kvsel_params* p, const Plan& pl, const void* q, const kvsel_k
   }
 
   float* nu = nullptr;
-  if (p->value_aware) {
+  if (p->value_aware && pl.l2) {
+    // nu = ||W_h v||_2 = sqrt(v^T Gamma_h v) with Gamma_h = W_h^T W_h (d x d)
+    nu = reinterpret_cast<float*>(wsb + pl.ws_nu);
+    uint16_t* wt = reinterpret_cast<uint16_t*>(wsb + pl.ws_wbar);
+    float* gpart = reinterpret_cast<float*>(wsb + pl.ws_gpart);
+    uint16_t* gam = reinterpret_cast<uint16_t*>(wsb + pl.ws_gam);
+    CUtensorMap twt, tg, tv;
+    {
+      const cuuint64_t dims[2] = {static_cast<cuuint64_t>(pl.Dw), static_cast<cuuint64_t>(pl.H) * kHeadDim};
+      const cuuint64_t strides[1] = {static_cast<cuuint64_t>(pl.Dw) * 2};
+      const cuuint32_t box[2] = {64, 128};
+      if (!encode(&twt, wt, 2, dims, strides, box)) return KVSEL_EINVAL;
+    }
+    {
+      const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(pl.H) * 2 * kHeadDim};
+      const cuuint64_t strides[1] = {kHeadDim * 2};
+      const cuuint32_t box[2] = {64, 128};
+      if (!encode(&tg, gam, 2, dims, strides, box)) return KVSEL_EINVAL;
+    }
+    if (!kv_map(&tv, kv->v, kv, pl, kv->layout == KVSEL_LAYOUT_PAGED ? 0 : 128)) return KVSEL_EINVAL;
+    {
+      StageScope sc(KVSEL_STAGE_WBAR, st);
+      rc = launch_rc(launch_value_gram(static_cast<const uint16_t*>(w_o), wt, gpart, gam, pl.H, pl.G, pl.D, twt,
+                                       wait_ctl(ws), st));
+    }
+    if (rc) return rc;
+    VgramArgs v{};
+    v.rq = pl.rq;
+    v.src = kv_source(kv);
+    v.units_total = pl.g_units;
+    for (int b = 0; b <= pl.B; ++b) v.unit_base[b] = pl.g_unit_base[b];
+    for (int b = 0; b < pl.B; ++b) v.blocks_per_head[b] = pl.g_blocks_per_head[b];
+    v.nu = nu;
+    v.wc = wait_ctl(ws);
+    {
+      StageScope sc(KVSEL_STAGE_VNORM, st);
+      rc = launch_rc(launch_vgram(v, tv, tg, st));
+    }
+    if (rc) return rc;
+  } else if (p->value_aware) {
     nu = reinterpret_cast<float*>(wsb + pl.ws_nu);
     uint16_t* wbar = reinterpret_cast<uint16_t*>(wsb + pl.ws_wbar);
     {

@@ -93,31 +93,6 @@ __device__ __forceinline__ void chunk_coords(const ChunkTable& ck, int B, int id
   c = rem - h * ck.per_head[b];
 }
 
-// TMA loads of `rows` tokens [tok0, tok0 + rows) of KV head h of request b into a
-// K-major 128B-swizzled tile [2 column halves][rows][128 B].
-__device__ __forceinline__ void load_kv_tile(const CUtensorMap* map, const KvSource& src, int b, int h, int n,
-                                             int tok0, int rows, uint8_t* dst, uint64_t* bar, int* status) {
-  const int half = rows * 128;
-  if (!src.paged) {
-    tma_load_4d(dst, map, bar, 0, tok0, h, b);
-    tma_load_4d(dst + half, map, bar, 64, tok0, h, b);
-  } else {
-    const int bs = src.block_size;
-    const int nblk_req = (n + bs - 1) / bs;
-    for (int j = 0; j < rows / bs; ++j) {
-      const int lb = tok0 / bs + j;
-      int pb = -1;
-      if (lb < nblk_req && lb < src.max_blocks) pb = __ldg(src.block_table + (size_t)b * src.max_blocks + lb);
-      if (pb < 0 || pb >= src.num_blocks) {
-        if (lb < nblk_req) atomicOr(status, DEV_BAD_INDEX);
-        pb = 0;  // tokens past the request (masked by the epilogue) or a bad entry
-      }
-      tma_load_4d(dst + j * bs * 128, map, bar, 0, h, 0, pb);
-      tma_load_4d(dst + half + j * bs * 128, map, bar, 64, h, 0, pb);
-    }
-  }
-}
-
 // Window rows [0, R) of (b, h) from the 2-D query map (d, B*H*R rows), 32-row boxes,
 // into [2 halves][R_pad rows][128 B].
 __device__ __forceinline__ void load_q_rows(const CUtensorMap* map, int row0, int R, int half_bytes, uint8_t* dst,

@@ -1,0 +1,391 @@
+// L2 value norm through the d x d Gram matrix of the output projection
+// ("CriticalKV: 출력 섭동 관점에서 KV 캐시 축출을 최적화하기", App. C.3: the Euclidean
+//  distance as the alternative to L1; same page §3.3 Theorem 3.3 for the projected value).
+//
+// ||W_h v||_2^2 = v^T (W_h^T W_h) v, so with the d x d Gram matrix Gamma_h = W_h^T W_h the
+// per-token cost drops from 2*D*d to 2*d*d flop (D / d = 32x for a 4096-wide model):
+//
+//   wbar_t_kernel:     W_h^T [H][d][Dw] bf16: the group sum of the W_O slices in fp32,
+//                      rounded once (the same values wbar_kernel writes), transposed
+//                      through shared memory.
+//   gram_kernel:       Gamma_h partials over K slices of Dw on tcgen05 (A = B = a W_h^T
+//                      tile, M = N = 128), fp32 to the workspace.
+//   gram_finish_kernel: Gamma_h = sum of the partials (fixed order), split into a bf16 high
+//                      part and a bf16 remainder so the tensor cores see it to ~2^-16.
+//   vgram_kernel:      persistent: per 128-token tile, Y = V (Gamma_hi + Gamma_lo) on tcgen05
+//                      (16 UMMAs into one TMEM accumulator), then each epilogue thread
+//                      forms nu = sqrt(sum_c Y[c] v[c]) for its token, reading v from the
+//                      same shared-memory tile.
+#include "internal.cuh"
+
+namespace kvsel {
+namespace {
+
+constexpr int kGramSliceMax = 512;          // Dw elements per gram_kernel CTA
+constexpr int kGramChunk = 64;              // K elements per 128-byte swizzle atom column
+constexpr int kGramChunkBytes = 128 * 128;  // 128 rows x 128 B
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~static_cast<uintptr_t>(1023));
+}
+
+// ------------------------------------------------------------------------------------
+// W_h^T from W_O
+// ------------------------------------------------------------------------------------
+// Block (64-row block of W_h, head h): the G slices of 64 rows x 128 columns are summed in
+// fp32 into shared memory, then written column-major as 128 rows of 64 bf16.
+__global__ void __launch_bounds__(256) wbar_t_kernel(const uint16_t* __restrict__ w_o, uint16_t* __restrict__ wt,
+                                                      int H, int G, int D) {
+  __shared__ float tile[64][129];
+  const int h = blockIdx.y, j0 = blockIdx.x * 64;
+  const long long row_len = static_cast<long long>(H) * G * kHeadDim;
+  for (int item = threadIdx.x; item < 64 * 16; item += 256) {
+    const int r = item / 16, c8 = item % 16, j = j0 + r;
+    float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    if (j < D) {
+      const uint16_t* src = w_o + j * row_len + static_cast<long long>(h) * G * kHeadDim + c8 * 8;
+      for (int g = 0; g < G; ++g) {
+        const uint4 p = __ldg(reinterpret_cast<const uint4*>(src + g * kHeadDim));
+        const uint32_t w[4] = {p.x, p.y, p.z, p.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          acc[2 * e] += __uint_as_float(w[e] << 16);
+          acc[2 * e + 1] += __uint_as_float(w[e] & 0xFFFF0000u);
+        }
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) tile[r][c8 * 8 + e] = acc[e];
+  }
+  __syncthreads();
+  // thread t writes column c = t / 2, rows [32 * (t % 2), +32): four 16-byte stores
+  const int c = threadIdx.x / 2, half = threadIdx.x % 2;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int r0 = half * 32 + q * 8;
+    if (j0 + r0 >= D) break;
+    uint32_t o[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const __nv_bfloat162 v2 = __floats2bfloat162_rn(tile[r0 + 2 * e][c], tile[r0 + 2 * e + 1][c]);
+      o[e] = *reinterpret_cast<const uint32_t*>(&v2);
+    }
+    *reinterpret_cast<uint4*>(wt + (static_cast<long long>(h) * kHeadDim + c) * D + j0 + r0) =
+        make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+// ------------------------------------------------------------------------------------
+// Gamma partials
+// ------------------------------------------------------------------------------------
+// Block (slice s, head h): W_h^T[:, s*slice : (s+1)*slice] arrives as 64-element chunks
+// (TMA, 128-byte swizzle); D[m][n] = sum_k Wt[m][k] Wt[n][k] accumulates in TMEM; four
+// epilogue warps write the 128 x 128 fp32 partial.  Warp 4 allocates TMEM and issues.
+__global__ void __launch_bounds__(160, 1) gram_kernel(const __grid_constant__ CUtensorMap twt, float* part,
+                                                      int D, int slice, WaitCtl wc) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  __shared__ __align__(8) uint64_t full_bar, done_bar;
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_abort;
+  const int warp = warp_id(), lane = lane_id();
+  const int s = blockIdx.x, h = blockIdx.y;
+  const int k0 = s * slice;
+  const int nchunks = (min(slice, D - k0) + kGramChunk - 1) / kGramChunk;
+  if (threadIdx.x == 0) {
+    mbar_init(&full_bar, 1);
+    mbar_init(&done_bar, 1);
+    s_abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 4) {
+    tmem_alloc(&s_tmem, 128);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = s_tmem;
+  if (warp == 4) {
+    if (lane == 0) {
+      tma_prefetch_desc(&twt);
+      mbar_arrive_expect_tx(&full_bar, nchunks * kGramChunkBytes);
+      for (int c = 0; c < nchunks; ++c) tma_load_2d(smem + c * kGramChunkBytes, &twt, &full_bar, k0 + c * kGramChunk, h * 128);
+      if (mbar_wait(&full_bar, 0, &s_abort, wc)) {
+        tc_fence_after();
+        constexpr uint32_t idesc = idesc_bf16_f32(128, 128);
+        for (int c = 0; c < nchunks; ++c) {
+          const uint64_t desc = sdesc_kmajor_sw128(smem_u32(smem + c * kGramChunkBytes));
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            umma_bf16(tbase, desc + ((k * 32) >> 4), desc + ((k * 32) >> 4), idesc, (c | k) ? 1u : 0u);
+        }
+      } else {
+        mbar_drain(&full_bar, 0, wc.status);
+      }
+      umma_commit(&done_bar);
+    }
+    __syncwarp();
+  } else {
+    const bool ok = __all_sync(0xffffffffu, mbar_wait(&done_bar, 0, &s_abort, wc));
+    tc_fence_after();
+    if (ok) {
+      float* dst = part + ((static_cast<size_t>(h) * gridDim.x + s) * 128 + warp * 32 + lane) * 128;
+      for (int c0 = 0; c0 < 128; c0 += 32) {
+        float v[32];
+        tmem_ld32(tbase + (static_cast<uint32_t>(warp * 32) << 16) + c0, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 32; j += 4) *reinterpret_cast<float4*>(dst + c0 + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 4) {
+    tc_fence_after();
+    tmem_dealloc(tbase, 128);
+  }
+}
+
+// Gamma_h = sum_s partial[h][s] (in order), split: hi = bf16(Gamma), lo = bf16(Gamma - hi).
+// Output [H][2][128][128] bf16; row n of either matrix is the K-major B operand row n.
+__global__ void __launch_bounds__(256) gram_finish_kernel(const float* __restrict__ part, uint16_t* __restrict__ gam,
+                                                          int S) {
+  const int h = blockIdx.x;
+  for (int e = threadIdx.x; e < 128 * 128; e += 256) {
+    float g = 0.f;
+    for (int s = 0; s < S; ++s) g += part[(static_cast<size_t>(h) * S + s) * 128 * 128 + e];
+    const __nv_bfloat16 hi = __float2bfloat16_rn(g);
+    const __nv_bfloat16 lo = __float2bfloat16_rn(g - __bfloat162float(hi));
+    gam[(static_cast<size_t>(h) * 2 + 0) * 128 * 128 + e] = *reinterpret_cast<const uint16_t*>(&hi);
+    gam[(static_cast<size_t>(h) * 2 + 1) * 128 * 128 + e] = *reinterpret_cast<const uint16_t*>(&lo);
+  }
+}
+
+// ------------------------------------------------------------------------------------
+// nu = sqrt(v^T Gamma v)
+// ------------------------------------------------------------------------------------
+constexpr int kVgEpiWarps = 4;
+constexpr int kVgProducer = 4;
+constexpr int kVgMma = 5;
+constexpr int kVgThreads = 192;
+constexpr int kVgStages = 4;
+constexpr int kVgTile = 128 * 256;     // 128 tokens x 128 bf16
+constexpr int kVgGamma = 128 * 256;    // one 128 x 128 bf16 matrix
+constexpr int kVgAcc = 2;
+
+__device__ __forceinline__ void vg_unit(const VgramArgs& a, int u, int& b, int& h, int& blk) {
+  b = 0;
+  while (b + 1 < a.rq.B && a.unit_base[b + 1] <= u) ++b;
+  const int rem = u - a.unit_base[b];
+  h = rem / a.blocks_per_head[b];
+  blk = rem - h * a.blocks_per_head[b];
+}
+
+__global__ void __launch_bounds__(kVgThreads, 1)
+    vgram_kernel(const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tg, const VgramArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  uint8_t* sG = smem;                   // [hi, lo][2 K halves][128 rows][128 B]
+  uint8_t* sV = smem + 2 * kVgGamma;    // [stages][2 K halves][128 tokens][128 B]
+
+  __shared__ __align__(8) uint64_t vfull[kVgStages], vempty[kVgStages], accf[kVgAcc], acce[kVgAcc];
+  __shared__ __align__(8) uint64_t gfull, gempty, done_bar;
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_abort;
+
+  const int warp = warp_id(), lane = lane_id();
+  int* status = a.wc.status;
+  const int lo = static_cast<int>(static_cast<long long>(blockIdx.x) * a.units_total / gridDim.x);
+  const int hi = static_cast<int>(static_cast<long long>(blockIdx.x + 1) * a.units_total / gridDim.x);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kVgStages; ++s) {
+      mbar_init(&vfull[s], 1);
+      mbar_init(&vempty[s], kVgEpiWarps);
+    }
+    for (int s = 0; s < kVgAcc; ++s) {
+      mbar_init(&accf[s], 1);
+      mbar_init(&acce[s], kVgEpiWarps);
+    }
+    mbar_init(&gfull, 1);
+    mbar_init(&gempty, 1);
+    mbar_init(&done_bar, 1);
+    s_abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == kVgMma) {
+    tmem_alloc(&s_tmem, kVgAcc * 128);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = s_tmem;
+
+  if (warp == kVgProducer) {
+    if (lane == 0 && hi > lo) {
+      tma_prefetch_desc(&tv);
+      tma_prefetch_desc(&tg);
+      int cur_h = -1, gl = 0, t = 0;
+      for (int u = lo; u < hi; ++u, ++t) {
+        int b, h, blk;
+        vg_unit(a, u, b, h, blk);
+        if (h != cur_h) {
+          // the previous head's Gamma is released by the UMMA warp after its last tile
+          if (gl > 0 && !mbar_wait(&gempty, (gl - 1) & 1, &s_abort, a.wc)) break;
+          mbar_arrive_expect_tx(&gfull, 2 * kVgGamma);
+          for (int m = 0; m < 2; ++m) {
+            tma_load_2d(sG + m * kVgGamma, &tg, &gfull, 0, (h * 2 + m) * 128);
+            tma_load_2d(sG + m * kVgGamma + 128 * 128, &tg, &gfull, 64, (h * 2 + m) * 128);
+          }
+          cur_h = h;
+          ++gl;
+        }
+        const int s = t % kVgStages, us = t / kVgStages;
+        if (!mbar_wait(&vempty[s], (us & 1) ^ 1, &s_abort, a.wc)) break;
+        mbar_arrive_expect_tx(&vfull[s], kVgTile);
+        load_kv_tile(&tv, a.src, b, h, a.rq.n[b], blk * 128, 128, sV + s * kVgTile, &vfull[s], status);
+      }
+      // drain copies still in flight
+      for (int tt = max(0, t - kVgStages); tt < t; ++tt) mbar_drain(&vfull[tt % kVgStages], (tt / kVgStages) & 1, status);
+      if (gl > 0) mbar_drain(&gfull, (gl - 1) & 1, status);
+    }
+  } else if (warp == kVgMma) {
+    if (lane == 0 && hi > lo) {
+      constexpr uint32_t idesc = idesc_bf16_f32(128, 128);
+      const uint64_t gdesc[2] = {sdesc_kmajor_sw128(smem_u32(sG)), sdesc_kmajor_sw128(smem_u32(sG + kVgGamma))};
+      int cur_h = -1, gl = 0, t = 0;
+      bool ok = true;
+      for (int u = lo; ok && u < hi; ++u, ++t) {
+        int b, h, blk;
+        vg_unit(a, u, b, h, blk);
+        if (h != cur_h) {
+          if (!mbar_wait(&gfull, gl & 1, &s_abort, a.wc)) break;
+          cur_h = h;
+          ++gl;
+        }
+        const int s = t % kVgStages, us = t / kVgStages;
+        const int acc = t % kVgAcc, ua = t / kVgAcc;
+        if (!mbar_wait(&vfull[s], us & 1, &s_abort, a.wc) || !mbar_wait(&acce[acc], (ua & 1) ^ 1, &s_abort, a.wc)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint64_t vdesc = sdesc_kmajor_sw128(smem_u32(sV + s * kVgTile));
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const uint32_t off = ((k >> 2) * (128 * 128) + (k & 3) * 32) >> 4;
+            umma_bf16(tbase + acc * 128, vdesc + off, gdesc[m] + off, idesc, (m | k) ? 1u : 0u);
+          }
+        }
+        umma_commit(&accf[acc]);
+        // the head changes after this tile (or the range ends): its Gamma may be replaced
+        int nb, nh, nblk;
+        if (u + 1 < hi) vg_unit(a, u + 1, nb, nh, nblk);
+        if (u + 1 >= hi || nh != h) umma_commit(&gempty);
+      }
+      umma_commit(&done_bar);
+      mbar_drain(&done_bar, 0, status);
+    }
+  } else {
+    // epilogue: warp q4 owns TMEM lanes / tokens [32 q4, 32 q4 + 32) of each tile
+    const int q4 = warp;
+    const int r = q4 * 32 + lane;
+    int t = 0;
+    for (int u = lo; u < hi; ++u, ++t) {
+      int b, h, blk;
+      vg_unit(a, u, b, h, blk);
+      const int s = t % kVgStages;
+      const int acc = t % kVgAcc, ua = t / kVgAcc;
+      const bool ok = __all_sync(0xffffffffu, mbar_wait(&accf[acc], ua & 1, &s_abort, a.wc));
+      if (!ok) break;
+      tc_fence_after();
+      const uint8_t* vrow = sV + s * kVgTile + r * 128;
+      float dot = 0.f;
+#pragma unroll
+      for (int c0 = 0; c0 < 128; c0 += 64) {
+        float y[64];
+        const uint32_t taddr = tbase + (static_cast<uint32_t>(q4 * 32) << 16) + acc * 128 + c0;
+        tmem_ld32(taddr, y);
+        tmem_ld32(taddr + 32, y + 32);
+        tmem_ld_wait();
+        // columns c0 .. c0+63 pair with v elements c0 .. c0+63: K half c0/64, eight 16-byte
+        // chunks of row r, 128-byte swizzled (chunk q at q ^ (r % 8))
+        const uint8_t* half = vrow + (c0 / 64) * (128 * 128);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const uint4 w = *reinterpret_cast<const uint4*>(half + ((q ^ (r & 7)) << 4));
+          const uint32_t e[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            dot = fmaf(y[q * 8 + 2 * i], __uint_as_float(e[i] << 16), dot);
+            dot = fmaf(y[q * 8 + 2 * i + 1], __uint_as_float(e[i] & 0xFFFF0000u), dot);
+          }
+        }
+      }
+      // accumulator and value stage are both read: hand them back
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&acce[acc]);
+        mbar_arrive(&vempty[s]);
+      }
+      const int n = a.rq.n[b];
+      const int tok = blk * 128 + r;
+      if (tok < n) a.nu[a.rq.soff[b] + static_cast<size_t>(h) * n + tok] = sqrtf(fmaxf(dot, 0.f));
+    }
+  }
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kVgMma) {
+    tc_fence_after();
+    tmem_dealloc(tbase, kVgAcc * 128);
+  }
+}
+
+}  // namespace
+
+// Slices of Dw per head: kGramSliceMax elements each (a multiple of the 64-element chunk,
+// so the slices tile Dw without overlap; the last one reads zeros past Dw).
+int gram_slices(int Dw) { return (Dw + kGramSliceMax - 1) / kGramSliceMax; }
+
+cudaError_t launch_value_gram(const uint16_t* w_o, uint16_t* wt, float* part, uint16_t* gam, int H, int G, int D,
+                              const CUtensorMap& twt, WaitCtl wc, cudaStream_t st) {
+  wbar_t_kernel<<<dim3((D + 63) / 64, H), 256, 0, st>>>(w_o, wt, H, G, D);
+  note_launch();
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int S = gram_slices(D);
+  const int slice = kGramSliceMax;
+  const size_t smem = 1024 + static_cast<size_t>((slice + kGramChunk - 1) / kGramChunk) * kGramChunkBytes;
+  e = ensure_smem(reinterpret_cast<const void*>(gram_kernel), smem);
+  if (e != cudaSuccess) return e;
+  gram_kernel<<<dim3(S, H), 160, smem, st>>>(twt, part, D, slice, wc);
+  note_launch();
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  gram_finish_kernel<<<H, 256, 0, st>>>(part, gam, S);
+  note_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_vgram(const VgramArgs& a, const CUtensorMap& tv, const CUtensorMap& tg, cudaStream_t st) {
+  if (a.units_total <= 0) return cudaSuccess;
+  const size_t smem = 1024 + 2 * kVgGamma + kVgStages * kVgTile;
+  cudaError_t e = ensure_smem(reinterpret_cast<const void*>(vgram_kernel), smem);
+  if (e != cudaSuccess) return e;
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int grid = a.units_total < sms ? a.units_total : sms;
+  vgram_kernel<<<grid, kVgThreads, smem, st>>>(tv, tg, a);
+  note_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace kvsel

@@ -96,6 +96,25 @@ def test_c2_value_aware_ragged(n):
     _check_layer(wl, inp, gpu, ora)
 
 
+@pytest.mark.parametrize("n", [1000, 2085])
+def test_c2_value_aware_l2_norm(n):
+    """nu = ||W_h v||_2 through the d x d Gram matrix (the other distance of CriticalKV
+    App. C.3), two-stage selection on it."""
+    wl = datagen.WORKLOADS[2].replace(layers=1, value_norm="l2")
+    inp = datagen.make_layer(wl, 3, n_ctx=n)
+    ora = O.run_workload_layer(wl, inp)
+    gpu = GH.run_gpu_layer(wl, inp)
+    _check_layer(wl, inp, gpu, ora)
+
+
+def test_c4_paged_l2_norm():
+    wl = datagen.WORKLOADS[4].replace(batch=3, n_min=300, n_ctx=1500, value_norm="l2", d_model=1024)
+    inp = datagen.make_layer(wl, 0)
+    ora = O.run_workload_layer(wl, inp)
+    gpu = GH.run_gpu_layer(wl, inp)
+    _check_layer(wl, inp, gpu, ora)
+
+
 def test_c2_per_head_wo_reading():
     wl = datagen.WORKLOADS[2].replace(layers=1, d_model=1024)
     inp = datagen.make_layer(wl, 1, n_ctx=777)
