@@ -290,7 +290,11 @@ def main():
     w_d = [to_dev(x["w_o"]) for x in host]
     params = B.params_from_workload(wl)
     bufs = [B.LayerBuffers(params, device=dev) for _ in range(L)]
-    ws = bufs[0].ws
+    # one workspace for every variant timed below (the L2 path needs Gram scratch too)
+    ws_bytes = max(B.kvsel_workspace_size(x) for x in
+                   (params, B.params_from_workload(wl, value_aware=False), B.params_from_workload(wl, value_norm="l2")))
+    ws = torch.empty(ws_bytes // 4 + 64, dtype=torch.int32, device=dev)
+    B.kvsel_workspace_init(ws)
     kvs = [B.make_kv_contiguous(k_d[i], v_d[i]) for i in range(L)]
     stream = torch.cuda.current_stream()
 
@@ -424,39 +428,52 @@ def main():
            "gpu_launches": K * launches_per_step, "device_status": status, "roofline": roof, "launch": launch_mode,
            "stage_ms_per_layer": {k: (round(v, 5) if v else v) for k, v in stage_ms.items()}}
 
-    # ---- the plain-score path on the same layers (spec HBM target)
-    if not args.no_plain:
-        plain = B.params_from_workload(wl, value_aware=False)
+    def time_variant(p):
+        """ms per layer of the same layers under parameters p (graph replay when possible)."""
         for _ in range(W):
             for i in range(L):
-                layer_call(i, plain)
+                layer_call(i, p)
         torch.cuda.synchronize()
-        pgraph = None
+        vgraph = None
         if graph is not None:
             try:
-                pgraph = capture(plain)
-                pgraph.replay()
+                vgraph = capture(p)
+                vgraph.replay()
                 torch.cuda.synchronize()
             except Exception:  # pragma: no cover
-                pgraph = None
+                vgraph = None
         barrier(world)
         t0.record(stream)
         for s in range(K):
-            if pgraph is not None:
-                pgraph.replay()
+            if vgraph is not None:
+                vgraph.replay()
             else:
                 for i in range(L):
-                    layer_call(i, plain)
+                    layer_call(i, p)
         t1.record(stream)
         torch.cuda.synchronize()
-        pms = max_over_ranks(t0.elapsed_time(t1), world) / (K * L)
-        Bh = int(wl.budget_ratio * n)
-        alg = H * n * d * 2 + 3 * H * Bh * d * 2 + int(wl.h_kv * wl.group * wl.window * d * 2) + 2 * H * n * 4
+        return max_over_ranks(t0.elapsed_time(t1), world) / (K * L)
+
+    Bh = int(wl.budget_ratio * n)
+    kept_rw = 3 * H * Bh * d * 2                       # kept V read (plain) / kept K,V written
+    small = int(wl.h_kv * wl.group * wl.window * d * 2) + 2 * H * n * 4
+    # ---- the plain-score path on the same layers (north-star HBM target)
+    if not args.no_plain:
+        pms = time_variant(B.params_from_workload(wl, value_aware=False))
+        alg = H * n * d * 2 + kept_rw + small
         gbs = alg / (pms * 1e-3) / 1e9
         out["hbm_path"] = {"what": "same layers, value_aware=0 (score+select+compact, no W_O pass)",
                            "ms_per_layer": pms, "entries_per_s": H * n / (pms * 1e-3) * world,
                            "algorithmic_bytes_per_layer": alg, "achieved_gbs": gbs,
                            "peak_gbs": pk.get("hbm_gbs"), "frac": gbs / pk.get("hbm_gbs", 6800.0)}
+        # ---- the L2 value norm through the d x d Gram matrix (CriticalKV App. C.3 distance)
+        lms = time_variant(B.params_from_workload(wl, value_norm="l2"))
+        alg2 = 2 * H * n * d * 2 + wl.d_model * wl.h_kv * wl.group * d * 2 + 2 * H * Bh * d * 2 + small
+        gbs2 = alg2 / (lms * 1e-3) / 1e9
+        out["l2_gram_path"] = {"what": "same layers, value-aware with ||W_h v||_2 via Gamma = W_h^T W_h",
+                               "ms_per_layer": lms, "entries_per_s": H * n / (lms * 1e-3) * world,
+                               "algorithmic_bytes_per_layer": alg2, "achieved_gbs": gbs2,
+                               "peak_gbs": pk.get("hbm_gbs"), "frac": gbs2 / pk.get("hbm_gbs", 6800.0)}
 
     # ---- end to end through the public API: pinned host -> device each step, results back
     if not args.no_e2e:

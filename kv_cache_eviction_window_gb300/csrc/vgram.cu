@@ -152,8 +152,8 @@ __global__ void __launch_bounds__(160, 1) gram_kernel(const __grid_constant__ CU
 // Output [H][2][128][128] bf16; row n of either matrix is the K-major B operand row n.
 __global__ void __launch_bounds__(256) gram_finish_kernel(const float* __restrict__ part, uint16_t* __restrict__ gam,
                                                           int S) {
-  const int h = blockIdx.x;
-  for (int e = threadIdx.x; e < 128 * 128; e += 256) {
+  const int h = blockIdx.y;
+  for (int e = blockIdx.x * 256 + threadIdx.x; e < 128 * 128; e += gridDim.x * 256) {
     float g = 0.f;
     for (int s = 0; s < S; ++s) g += part[(static_cast<size_t>(h) * S + s) * 128 * 128 + e];
     const __nv_bfloat16 hi = __float2bfloat16_rn(g);
@@ -305,7 +305,7 @@ __global__ void __launch_bounds__(kVgThreads, 1)
       if (!ok) break;
       tc_fence_after();
       const uint8_t* vrow = sV + s * kVgTile + r * 128;
-      float dot = 0.f;
+      float dp[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};   // independent partial sums
 #pragma unroll
       for (int c0 = 0; c0 < 128; c0 += 64) {
         float y[64];
@@ -322,11 +322,12 @@ __global__ void __launch_bounds__(kVgThreads, 1)
           const uint32_t e[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
-            dot = fmaf(y[q * 8 + 2 * i], __uint_as_float(e[i] << 16), dot);
-            dot = fmaf(y[q * 8 + 2 * i + 1], __uint_as_float(e[i] & 0xFFFF0000u), dot);
+            dp[2 * i] = fmaf(y[q * 8 + 2 * i], __uint_as_float(e[i] << 16), dp[2 * i]);
+            dp[2 * i + 1] = fmaf(y[q * 8 + 2 * i + 1], __uint_as_float(e[i] & 0xFFFF0000u), dp[2 * i + 1]);
           }
         }
       }
+      const float dot = ((dp[0] + dp[1]) + (dp[2] + dp[3])) + ((dp[4] + dp[5]) + (dp[6] + dp[7]));
       // accumulator and value stage are both read: hand them back
       tc_fence_before();
       __syncwarp();
@@ -369,7 +370,7 @@ cudaError_t launch_value_gram(const uint16_t* w_o, uint16_t* wt, float* part, ui
   note_launch();
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  gram_finish_kernel<<<H, 256, 0, st>>>(part, gam, S);
+  gram_finish_kernel<<<dim3(64, H), 256, 0, st>>>(part, gam, S);
   note_launch();
   return cudaGetLastError();
 }
