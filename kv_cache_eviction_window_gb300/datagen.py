@@ -31,7 +31,7 @@ _CHUNK = 1 << 22
 _THREADS = 16
 
 # tensor tags inside one layer's seed
-_TAG_Q, _TAG_K, _TAG_V, _TAG_WO, _TAG_KSCALE, _TAG_HEAVY, _TAG_CTX, _TAG_BLOCKS = range(8)
+_TAG_Q, _TAG_K, _TAG_V, _TAG_WO, _TAG_KSCALE, _TAG_HEAVY, _TAG_CTX, _TAG_BLOCKS, _TAG_RAND = range(9)
 
 
 @dataclasses.dataclass(frozen=True)
@@ -56,7 +56,7 @@ class Workload:
     eps: float
     n_sink: int
     n_recent: int
-    budget_mode: str      # "head" | "layer"
+    budget_mode: str      # "head" | "layer" | "anchor" (k = budget_ratio*n anchors, rho = alpha)
     budget_ratio: float
     floor_ratio: float
     batch: int = 1
@@ -91,6 +91,11 @@ WORKLOADS: Dict[int, Workload] = {
                 block_size=16, key_structure="plain"),
     5: Workload(5, "llama3.1-70b-query-agnostic-32k", 1, 8, 8, 128, 8192, 32768, 0, False, "max", "none", 1,
                 False, 0.5, 1e-4, 4, 0, "layer", 0.3, 0.0, q_chunk=2048, key_structure="plain"),
+    # AnchorKV anchor selection and nearest-anchor projection on the Llama-3.1-8B 32K
+    # shape: W = 32, k = n/128 anchors, rho = 0.7 (carried in alpha), kappa = 7 (AnchorKV
+    # §4.1); the recent window is the only forced set (§3.2).
+    6: Workload(6, "llama3.1-8b-32k-anchors", 1, 8, 4, 128, 4096, 32768, 32, True, "mean", "max", 7,
+                False, 0.7, 1e-4, 0, 32, "anchor", 1.0 / 128, 0.0, key_structure="lognormal"),
 }
 
 
@@ -158,6 +163,8 @@ def make_layer(wl: Workload, layer: int = 0, n_ctx: Optional[int] = None,
       n_ctx  : list of per-request lengths
       paged  : dict(k_pool, v_pool [num_blocks][block][H][d], block_table [B][max_blocks])
                when the workload is paged
+      rand   : list over requests of [H][n_b] float32 i.i.d. uniform [0, 1) keys (anchor
+               workloads: the random share of the anchors takes the largest keys)
     ``n_ctx`` overrides the context length (single-request workloads only), which the
     tests use for smaller cases of the same recipe.
     """
@@ -171,7 +178,7 @@ def make_layer(wl: Workload, layer: int = 0, n_ctx: Optional[int] = None,
     W = wl.window if wl.window > 0 else None
     B = len(lens)
 
-    qs, ks, vs = [], [], []
+    qs, ks, vs, rs = [], [], [], []
     for b, n in enumerate(lens):
         rows = W if W is not None else n
         sub = seed * 64 + b
@@ -201,9 +208,11 @@ def make_layer(wl: Workload, layer: int = 0, n_ctx: Optional[int] = None,
         ks.append(to_bf16_bits(k))
         vs.append(to_bf16_bits(_normal_f32(sub, _TAG_V, H * n * d, threads).reshape(H, n, d)))
         qs.append(q)
+        if wl.budget_mode == "anchor":
+            rs.append(_rng(sub, _TAG_RAND).random((H, n), dtype=np.float32))
 
     out = dict(q=np.stack(qs) if W is not None else qs[0][None], k=ks, v=vs, n_ctx=lens, w_o=None,
-               paged=None)
+               paged=None, rand=rs if wl.budget_mode == "anchor" else None)
     if wl.value_aware:
         D = wl.d_model
         w = _normal_f32(seed, _TAG_WO, D * H * G * d, threads) * np.float32(0.02)

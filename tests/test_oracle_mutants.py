@@ -11,7 +11,10 @@ import pytest
 from oracle import kvsel_oracle as O
 import tests.test_oracle_pins as P
 
+from oracle import anchor_oracle as AO
+
 ORIG = {name: getattr(O, name) for name in dir(O) if callable(getattr(O, name))}
+A_ORIG = {name: getattr(AO, name) for name in dir(AO) if callable(getattr(AO, name))}
 
 
 def _logits_no_scale(q, k, scale=None, causal=True):
@@ -119,6 +122,63 @@ def _value_norm_l2_no_sqrt(v, w_o, h, group, mode="group_sum", row_block=4096, n
     return r * r if norm == "l2" else r
 
 
+def _anchor_abs_cosine(x, anchors):
+    slot, gamma, cos = A_ORIG["anchor_project"](x, anchors)
+    anchors = np.asarray(anchors, dtype=np.int64)
+    A_ = x[anchors]
+    an2 = (A_ * A_).sum(1)
+    s2 = np.argmax(np.abs(cos), axis=1)
+    g2 = (x @ A_.T)[np.arange(len(x)), s2] / np.where(an2[s2] > 0, an2[s2], 1.0)
+    s2[anchors] = np.arange(len(anchors))
+    g2[anchors] = 1.0
+    return s2, g2, cos
+
+
+def _anchor_gamma_unnormalised(x, anchors):
+    slot, gamma, cos = A_ORIG["anchor_project"](x, anchors)
+    an = np.sqrt((x[np.asarray(anchors, dtype=np.int64)] ** 2).sum(1))
+    return slot, gamma * an[slot], cos
+
+
+def _anchor_no_self(x, anchors):
+    anchors = np.asarray(anchors, dtype=np.int64)
+    slot, gamma, cos = A_ORIG["anchor_project"](x, anchors)
+    best = np.argmax(cos, axis=1)
+    slot[anchors] = best[anchors]
+    return slot, gamma, cos
+
+
+def _anchor_rho_ceil(s_pool, rand_key, k, forced, rho=0.7):
+    nf = int(forced.sum())
+    k1 = nf + int(math.ceil(rho * (k - nf)))
+    s1 = O.top_b(s_pool, k1, forced)
+    keep1 = np.zeros_like(forced)
+    keep1[s1] = True
+    return O.top_b(rand_key, k, keep1)
+
+
+def _anchor_random_share_ignores_stage1(s_pool, rand_key, k, forced, rho=0.7):
+    nf = int(forced.sum())
+    k1 = nf + int(math.floor(rho * (k - nf)))
+    s1 = O.top_b(s_pool, k1, forced)
+    s2 = O.top_b(rand_key, k - k1 + nf, forced)
+    return np.union1d(s1, s2)
+
+
+def _anchor_count_ignores_forced(n, n_forced, div=128):
+    return min(n, n // div)
+
+
+A_MUTANTS = {
+    "anchor_abs_cosine": ("anchor_project", _anchor_abs_cosine),
+    "anchor_gamma_unnormalised": ("anchor_project", _anchor_gamma_unnormalised),
+    "anchor_no_self": ("anchor_project", _anchor_no_self),
+    "anchor_rho_ceil": ("select_anchors", _anchor_rho_ceil),
+    "anchor_random_share_ignores_stage1": ("select_anchors", _anchor_random_share_ignores_stage1),
+    "anchor_count_ignores_forced": ("anchor_count", _anchor_count_ignores_forced),
+}
+
+
 MUTANTS = {
     "no_scale": ("window_logits", _logits_no_scale),
     "causal_off_by_one": ("window_logits", _logits_causal_off_by_one),
@@ -159,10 +219,14 @@ def _pin_calls():
     return calls
 
 
-@pytest.mark.parametrize("mutant", sorted(MUTANTS))
+@pytest.mark.parametrize("mutant", sorted(MUTANTS) + sorted(A_MUTANTS))
 def test_pins_catch_mutant(mutant, monkeypatch):
-    attr, fake = MUTANTS[mutant]
-    monkeypatch.setattr(O, attr, fake)
+    if mutant in A_MUTANTS:
+        attr, fake = A_MUTANTS[mutant]
+        monkeypatch.setattr(AO, attr, fake)
+    else:
+        attr, fake = MUTANTS[mutant]
+        monkeypatch.setattr(O, attr, fake)
     failed = []
     for name, fn, kw in _pin_calls():
         try:

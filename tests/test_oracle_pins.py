@@ -511,3 +511,123 @@ def test_run_layer_small_invariants():
         np.testing.assert_array_equal(r["k_out"][h], inp["k"][0][h][r["idx"][h]])
     assert np.all(r["nu"] > 0)
     np.testing.assert_allclose(r["s_raw"].sum(1), 1.0 * 1, rtol=1e-9)  # mean of prob rows
+
+
+# --------------------------------------------------------------------- AnchorKV anchors
+from oracle import anchor_oracle as A  # noqa: E402
+
+
+def test_anchor_count_closed_form():
+    # AnchorKV §4.1: k = S/128; the recent window counts inside k (§3.2); never above n
+    assert A.anchor_count(32768, 32) == 256
+    assert A.anchor_count(131072, 64) == 1024
+    assert A.anchor_count(1000, 32) == 32       # floor(1000/128) = 7 < |F|
+    assert A.anchor_count(20, 20) == 20
+    assert A.anchor_count(0, 0) == 0
+
+
+def test_select_anchors_hand_example():
+    # n = 12, recent window {10, 11}, k = 7, rho = 0.7: stage 1 = F + floor(0.7 * 5) = 3
+    # picks by score among 0..9: 0.9 (5), then the tie 0.5 at 1 and 3 (index order);
+    # stage 2 = 2 picks by random key among the rest: the 0.99 at 1 is taken already, so
+    # the three-way tie 0.7 at {2, 4, 8} resolves to 2 and 4.
+    s = np.array([0.1, 0.5, 0.3, 0.5, 0.2, 0.9, 0.0, 0.3, 0.4, 0.1, 0.05, 0.01])
+    r = np.array([0.2, 0.99, 0.7, 0.1, 0.7, 0.3, 0.6, 0.05, 0.7, 0.4, 0.8, 0.9])
+    fm = O.forced_mask(12, 0, 2)
+    got = A.select_anchors(s, r, 7, fm, 0.7)
+    assert got.tolist() == [1, 2, 3, 4, 5, 10, 11]
+
+
+def test_select_anchors_rho_extremes():
+    g = np.random.default_rng(5)
+    n, k = 300, 40
+    s = g.random(n)
+    r = g.random(n)
+    fm = O.forced_mask(n, 0, 16)
+    # rho = 1: all free slots by score = the plain top-k with the window forced
+    assert np.array_equal(A.select_anchors(s, r, k, fm, 1.0), O.top_b(s, k, fm))
+    # rho = 0: all free slots by the random keys
+    assert np.array_equal(A.select_anchors(s, r, k, fm, 0.0), O.top_b(r, k, fm))
+
+
+def test_select_anchors_random_share_is_uniform_without_replacement():
+    # n = 40, F = 4 recent, k = 12, rho = 0.5: 4 by score, then 4 drawn from the other 32
+    g = np.random.default_rng(11)
+    n, k, trials = 40, 12, 3000
+    s = np.linspace(1.0, 0.0, n)          # stage 1 is always positions 0..3
+    fm = O.forced_mask(n, 0, 4)
+    counts = np.zeros(n, int)
+    for _ in range(trials):
+        got = A.select_anchors(s, g.random(n), k, fm, 0.5)
+        assert len(got) == k and len(set(got.tolist())) == k
+        counts[got] += 1
+    assert (counts[:4] == trials).all() and (counts[-4:] == trials).all()
+    mid = counts[4:n - 4]                 # 32 positions, 4 draws each trial: 375 expected
+    assert abs(mid.sum() - 4 * trials) == 0
+    assert mid.min() > 375 - 100 and mid.max() < 375 + 100
+
+
+def test_anchor_project_scaled_basis():
+    # anchors c_j e_j: cos(x, a_j) = x_j / |x|, so the slot is the largest coordinate
+    # (signed) and gamma = x_j / c_j
+    c = [2.0, 0.5, 3.0, 1.0]
+    x = np.zeros((6, 4))
+    for j in range(4):
+        x[j, j] = c[j]
+    x[4] = [1.0, -2.0, 0.5, 0.7]
+    x[5] = [-1.0, -2.0, -0.5, -3.0]
+    slot, gamma, _ = A.anchor_project(x, np.arange(4))
+    assert slot.tolist() == [0, 1, 2, 3, 0, 2]
+    assert np.allclose(gamma, [1, 1, 1, 1, 0.5, -0.5 / 3.0], rtol=0, atol=1e-15)
+
+
+def test_anchor_project_parallel_zero_and_duplicates():
+    a = np.array([1.0, 2.0, -2.0])
+    b = np.array([0.0, 1.0, 0.0])
+    x = np.stack([a, a.copy(), b, 2.5 * b, np.zeros(3), -a, a])
+    anchors = np.array([0, 1, 2])           # anchors 0 and 1 hold the same vector
+    slot, gamma, cos = A.anchor_project(x, anchors)
+    assert slot[:3].tolist() == [0, 1, 2] and (gamma[:3] == 1.0).all()   # anchors: themselves
+    assert slot[3] == 2 and gamma[3] == 2.5                              # parallel to b
+    assert slot[4] == 0 and gamma[4] == 0.0                              # zero vector: slot 0
+    # -a: cos -1 with anchors 0, 1 and -2/3 with b: the larger (signed) cosine is b's
+    assert slot[5] == 2 and abs(gamma[5] - (-2.0)) < 1e-15
+    assert slot[6] == 0 and gamma[6] == 1.0                              # tie: first slot
+
+
+def test_anchor_project_residual_orthogonal_and_best():
+    g = np.random.default_rng(3)
+    x = g.standard_normal((200, 16))
+    anchors = np.sort(g.choice(200, 12, replace=False))
+    slot, gamma, cos = A.anchor_project(x, anchors)
+    a = x[anchors][slot]
+    r = x - gamma[:, None] * a
+    # the residual of an orthogonal projection is orthogonal to the anchor
+    assert np.abs((r * a).sum(1)).max() < 1e-12 * np.abs(x).max() ** 2 * 16
+    # and no other anchor has a larger cosine
+    assert (cos[np.arange(200), slot] >= cos.max(1) - 1e-15).all()
+    # |r|^2 = |x|^2 (1 - cos^2) for the chosen anchor (Pythagoras)
+    xn2 = (x * x).sum(1)
+    c = cos[np.arange(200), slot]
+    nonanchor = np.setdiff1d(np.arange(200), anchors)
+    assert np.allclose((r * r).sum(1)[nonanchor], (xn2 * (1 - c * c))[nonanchor], rtol=1e-9, atol=1e-12)
+
+
+def test_run_anchor_layer_invariants():
+    wl = datagen.WORKLOADS[6].replace(h_kv=2, n_ctx=700)
+    inp = datagen.make_layer(wl, 0, n_ctx=700)
+    r = A.run_anchor_workload_layer(wl, inp)[0]
+    assert r["k"] == 32                         # floor(700/128) = 5 < W = 32
+    wl2 = wl.replace(n_ctx=9000)
+    inp2 = datagen.make_layer(wl2, 0, n_ctx=9000)
+    r2 = A.run_anchor_workload_layer(wl2, inp2, heads=[0])[0]
+    assert r2["k"] == 70
+    anc = r2["anchors"][0]
+    assert len(anc) == 70 and np.all(np.diff(anc) > 0)
+    assert set(range(9000 - 32, 9000)) <= set(anc.tolist())
+    # 32 forced + floor(0.7 * 38) = 26 by score: all of them rank above the random ones
+    s = r2["s_pool"][0]
+    free = np.setdiff1d(anc, np.arange(9000 - 32, 9000))
+    top26 = O.top_b(s, 58, O.forced_mask(9000, 0, 32))
+    assert set(top26.tolist()) <= set(anc.tolist())
+    assert len(free) == 38
