@@ -74,7 +74,14 @@ extern "C" {
  * softmax normalisation (KVzip §6.5, "KVzip-logit"). */
 enum { KVSEL_REDUCE_SUM = 0, KVSEL_REDUCE_MEAN = 1, KVSEL_REDUCE_MAX = 2, KVSEL_REDUCE_MAX_LOGIT = 3 };
 enum { KVSEL_POOL_NONE = 0, KVSEL_POOL_MAX = 1, KVSEL_POOL_AVG = 2 };
-enum { KVSEL_BUDGET_PER_HEAD = 0, KVSEL_BUDGET_PER_LAYER = 1 };
+/* ANCHOR: AnchorKV anchors ("AnchorKV: Anchor-Residual KV Cache Compression", §3.2,
+ * §4.1).  Per head k = floor(budget_ratio * n) anchors (1/128 on the page), at least the
+ * forced entries and at most n; the forced entries (the recent window) count inside k;
+ * floor(alpha * (k - |F|)) more go to the highest s_attn (alpha = rho = 0.7), the rest to
+ * the largest of the caller's random keys, which kvsel_select takes in place of s_val:
+ * i.i.d. uniform keys make that share a uniform draw without replacement.  Not with
+ * value_aware; kvsel_run_layer refuses it (use kvsel_run_anchors). */
+enum { KVSEL_BUDGET_PER_HEAD = 0, KVSEL_BUDGET_PER_LAYER = 1, KVSEL_BUDGET_ANCHOR = 2 };
 enum { KVSEL_WO_GROUP_SUM = 0, KVSEL_WO_PER_HEAD = 1 };
 /* Value norm of the value-aware criterion: L1 (CriticalKV's choice) or L2, the other
  * distance its App. C.3 compares.  L2 is computed through the d x d Gram matrix
@@ -225,7 +232,8 @@ enum {
                                 launch on the kvsel_run_layer path)                   */
   KVSEL_STAGE_SELECT = 5,    /* top-B selection                                      */
   KVSEL_STAGE_COMPACT = 6,   /* gather of the kept K/V rows                          */
-  KVSEL_STAGE_COUNT = 7
+  KVSEL_STAGE_PROJECT = 7,   /* anchors: anchor norms and nearest-anchor projection  */
+  KVSEL_STAGE_COUNT = 8
 };
 
 /* Diagnostics: while `events` is non-NULL, each kernel launched by this thread's
@@ -245,6 +253,37 @@ uint64_t kvsel_launch_count(void);
  * [n_scores]); -inf for an empty request.  head_out: device fp32 [batch*h_kv].  Asynchronous
  * on `stream`; errors as kvsel_output_size. */
 int kvsel_head_scores(const kvsel_params* p, const float* scores, float* head_out, void* stream);
+
+/* ---- AnchorKV anchors ---------------------------------------------------------------- */
+
+/* Nearest-anchor representation of every key and value vector ("AnchorKV: Anchor-Residual
+ * KV Cache Compression", §3.1): for every position i of segment (b, h) and each side
+ * (K, V) the anchor slot j whose vector has the largest cosine similarity with x_i (signed;
+ * first slot on ties; cosine 0 against a zero vector) and gamma_i = <x_i, a_j> / |a_j|^2,
+ * the coefficient of the orthogonal projection of x_i onto span(a_j).  Anchor positions
+ * represent themselves (slot = own, gamma = 1).  Dot products run on tcgen05 tensor cores
+ * (bf16 inputs, fp32 accumulation); 1/|a_j| in fp32.
+ *   p        budget_mode must be KVSEL_BUDGET_ANCHOR (sizes: k anchors per head <= 1024,
+ *            else KVSEL_EUNSUPPORTED)
+ *   kv       the vectors to represent (the page projects pre-RoPE keys: pass that view)
+ *   anchor_k, anchor_v  device bf16 [n_kept][head_dim]: the anchors' rows, as
+ *            kvsel_compact writes them for idx/counts/offsets
+ *   idx/counts/offsets  device, the anchors as kvsel_select writes them in ANCHOR mode
+ *   slot_k, slot_v      device int32 [n_scores]; gamma_k, gamma_v device fp32 [n_scores],
+ *            packed like the scores; slots index the segment's anchor list
+ *   ws       workspace of kvsel_workspace_size bytes (holds the anchors' inverse norms) */
+int kvsel_anchor_project(const kvsel_params* p, const kvsel_kv* kv, const void* anchor_k, const void* anchor_v,
+                         const int32_t* idx, const int32_t* counts, const int64_t* offsets, int32_t* slot_k,
+                         float* gamma_k, int32_t* slot_v, float* gamma_v, void* ws, size_t ws_bytes, void* stream);
+
+/* AnchorKV compression front end for one layer, enqueued back to back on `stream`:
+ * window scoring (s_attn = the pooled SnapKV score), anchor selection (ANCHOR mode,
+ * rand_keys: device fp32 [n_scores] i.i.d. uniform keys), gather of the anchor rows into
+ * anchor_k / anchor_v, and kvsel_anchor_project.  Arguments as in those calls. */
+int kvsel_run_anchors(const kvsel_params* p, const void* q, const kvsel_kv* kv, const float* rand_keys,
+                      float* s_attn, int32_t* idx, int32_t* counts, int64_t* offsets, void* anchor_k, void* anchor_v,
+                      int32_t* slot_k, float* gamma_k, int32_t* slot_v, float* gamma_v, void* ws, size_t ws_bytes,
+                      void* stream);
 
 /* Static description of an error code. */
 const char* kvsel_strerror(int code);

@@ -25,7 +25,7 @@ KVSEL_EDEVICE = -7
 
 REDUCE = {"sum": 0, "mean": 1, "max": 2, "max_logit": 3}
 POOL = {"none": 0, "max": 1, "avg": 2}
-BUDGET = {"head": 0, "layer": 1}
+BUDGET = {"head": 0, "layer": 1, "anchor": 2}
 WO_MODE = {"group_sum": 0, "per_head": 1}
 VALUE_NORM = {"l1": 0, "l2": 1}
 LAYOUT_CONTIGUOUS, LAYOUT_PAGED = 0, 1
@@ -34,9 +34,10 @@ MAX_BATCH = 128
 EXPORTS = ("kvsel_workspace_size", "kvsel_output_size", "kvsel_workspace_init", "kvsel_score",
            "kvsel_select", "kvsel_compact", "kvsel_run_layer", "kvsel_get_device_status",
            "kvsel_set_wait_limit", "kvsel_set_stage_events", "kvsel_strerror", "kvsel_version",
-           "kvsel_score_noalloc", "kvsel_launch_count", "kvsel_head_scores")
+           "kvsel_score_noalloc", "kvsel_launch_count", "kvsel_head_scores", "kvsel_anchor_project",
+           "kvsel_run_anchors")
 NOALLOC_SCRATCH_BYTES = 16 << 20
-STAGES = ("rowstats", "keysum", "wbar", "vnorm", "finalize", "select", "compact")
+STAGES = ("rowstats", "keysum", "wbar", "vnorm", "finalize", "select", "compact", "project")
 
 
 class KvselUnavailable(RuntimeError):
@@ -105,6 +106,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
         "kvsel_version": ([], ctypes.c_char_p),
         "kvsel_launch_count": ([], ctypes.c_uint64),
         "kvsel_head_scores": ([P, vp, vp, vp], ctypes.c_int),
+        "kvsel_anchor_project": ([P, K] + [vp] * 10 + [sz, vp], ctypes.c_int),
+        "kvsel_run_anchors": ([P, vp, K] + [vp] * 12 + [sz, vp], ctypes.c_int),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -286,6 +289,23 @@ def kvsel_run_layer(params, q, kv: kvsel_kv, w_o, s_attn, s_val, idx, counts, of
            "kvsel_run_layer")
 
 
+def kvsel_anchor_project(params, kv: kvsel_kv, anchor_k, anchor_v, idx, counts, offsets, slot_k, gamma_k,
+                         slot_v, gamma_v, ws, stream=None) -> None:
+    _check(load().kvsel_anchor_project(ctypes.byref(params), ctypes.byref(kv), _ptr(anchor_k), _ptr(anchor_v),
+                                       _ptr(idx), _ptr(counts), _ptr(offsets), _ptr(slot_k), _ptr(gamma_k),
+                                       _ptr(slot_v), _ptr(gamma_v), _ptr(ws), ws.numel() * ws.element_size(),
+                                       _stream(stream)), "kvsel_anchor_project")
+
+
+def kvsel_run_anchors(params, q, kv: kvsel_kv, rand_keys, s_attn, idx, counts, offsets, anchor_k, anchor_v,
+                      slot_k, gamma_k, slot_v, gamma_v, ws, stream=None) -> None:
+    _check(load().kvsel_run_anchors(ctypes.byref(params), _ptr(q), ctypes.byref(kv), _ptr(rand_keys),
+                                    _ptr(s_attn), _ptr(idx), _ptr(counts), _ptr(offsets), _ptr(anchor_k),
+                                    _ptr(anchor_v), _ptr(slot_k), _ptr(gamma_k), _ptr(slot_v), _ptr(gamma_v),
+                                    _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)),
+           "kvsel_run_anchors")
+
+
 def kvsel_get_device_status(ws, stream=None) -> int:
     st = ctypes.c_int()
     _check(load().kvsel_get_device_status(_ptr(ws), _stream(stream), ctypes.byref(st)), "kvsel_get_device_status")
@@ -309,5 +329,11 @@ class LayerBuffers:
         self.k_out = torch.empty((max(n_kept, 1), params.head_dim), dtype=torch.bfloat16, device=device)
         self.v_out = torch.empty((max(n_kept, 1), params.head_dim), dtype=torch.bfloat16, device=device)
         self.ws = torch.empty(max(ws_bytes, 256) // 4 + 64, dtype=torch.int32, device=device)
+        if params.budget_mode == BUDGET["anchor"]:
+            # anchors: per-position slot and gamma for K and V (k_out / v_out hold the anchors)
+            self.slot_k = torch.empty(max(n_scores, 1), dtype=torch.int32, device=device)
+            self.slot_v = torch.empty(max(n_scores, 1), dtype=torch.int32, device=device)
+            self.gamma_k = torch.empty(max(n_scores, 1), dtype=torch.float32, device=device)
+            self.gamma_v = torch.empty(max(n_scores, 1), dtype=torch.float32, device=device)
         kvsel_workspace_init(self.ws)
         self.n_scores, self.n_kept, self.n_seg = n_scores, n_kept, n_seg

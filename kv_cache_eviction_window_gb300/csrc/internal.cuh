@@ -143,6 +143,28 @@ cudaError_t launch_value_gram(const uint16_t* w_o, uint16_t* wt, float* part, ui
 // tv: V tiles of 128 tokens (kv_map); tg: 2-D map over gam (d, H*2*d rows), box 64 x 128.
 cudaError_t launch_vgram(const VgramArgs& a, const CUtensorMap& tv, const CUtensorMap& tg, cudaStream_t st);
 
+// AnchorKV nearest-anchor projection.  Units are (request, head, side, 128-token tile):
+// request-major, then head, then side (K = 0, V = 1), then tile.
+struct AnchorArgs {
+  ReqTable rq;
+  KvSource src;
+  int units_total;
+  int unit_base[kMaxBatch + 1];
+  int tiles[kMaxBatch];            // 128-token tiles per head of request b
+  const int32_t* idx;              // anchor positions, ascending within each segment
+  const int32_t* counts;           // anchors per segment (b, h)
+  const int64_t* offsets;          // first anchor row of each segment
+  long long n_rows;                // rows of the compacted anchor buffers
+  const float* inv;                // [2][n_rows]: 1 / |a| of the K and V anchor rows
+  int32_t* slot[2];                // K, V: anchor slot per position (packed like scores)
+  float* gamma[2];                 // K, V: projection coefficient per position
+  WaitCtl wc;
+};
+int anchor_max();
+cudaError_t launch_anchor_norms(const uint16_t* ak, const uint16_t* av, long long rows, float* inv, cudaStream_t st);
+cudaError_t launch_anchor_project(const AnchorArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
+                                  const CUtensorMap& tak, const CUtensorMap& tav, cudaStream_t st);
+
 // Raise a kernel's dynamic shared-memory limit once per device (cached).
 cudaError_t ensure_smem(const void* func, size_t bytes);
 

@@ -77,6 +77,9 @@ struct Plan {
   ChunkTable ck{};
   int units_total = 0, unit_base[kMaxBatch + 1]{}, blocks_per_head[kMaxBatch]{};
   bool l2 = false;     // value norm through the Gram matrix (KVSEL_NORM_L2)
+  bool anchor = false; // AnchorKV anchors (KVSEL_BUDGET_ANCHOR)
+  int ap_units = 0, ap_unit_base[kMaxBatch + 1]{}, ap_tiles[kMaxBatch]{};   // (b, h, side, 128-token tile)
+  size_t ws_ainv = 0;  // anchors: 1/|a| of the K and V anchor rows
   int g_units = 0, g_unit_base[kMaxBatch + 1]{}, g_blocks_per_head[kMaxBatch]{};   // 128-token tiles
   int num_sms = 0;
   size_t ws_part = 0, ws_sraw = 0, ws_nu = 0, ws_wbar = 0, ws_total = 0;
@@ -103,7 +106,11 @@ int make_plan(const kvsel_params* p, Plan& pl, bool need_device) {
   if (p->reduce < 0 || p->reduce > 3 || p->pool < 0 || p->pool > 2) return KVSEL_EINVAL;
   if (p->reduce == KVSEL_REDUCE_MAX_LOGIT && p->window != 0) return KVSEL_EUNSUPPORTED;   // query-agnostic only
   if (p->pool != KVSEL_POOL_NONE && (p->pool_kernel < 1 || (p->pool_kernel & 1) == 0)) return KVSEL_EINVAL;
-  if (p->budget_mode != KVSEL_BUDGET_PER_HEAD && p->budget_mode != KVSEL_BUDGET_PER_LAYER) return KVSEL_EINVAL;
+  if (p->budget_mode != KVSEL_BUDGET_PER_HEAD && p->budget_mode != KVSEL_BUDGET_PER_LAYER &&
+      p->budget_mode != KVSEL_BUDGET_ANCHOR)
+    return KVSEL_EINVAL;
+  pl.anchor = p->budget_mode == KVSEL_BUDGET_ANCHOR;
+  if (pl.anchor && !(p->alpha >= 0.f && p->alpha <= 1.f)) return KVSEL_EINVAL;
   if (!(p->budget_ratio >= 0.0 && p->budget_ratio <= 1.0) || !(p->floor_ratio >= 0.0 && p->floor_ratio <= 1.0))
     return KVSEL_EINVAL;
   if (p->n_sink < 0 || p->n_recent < 0 || p->window < 0 || !(p->scale >= 0.f) || std::isinf(p->scale))
@@ -163,7 +170,17 @@ int make_plan(const kvsel_params* p, Plan& pl, bool need_device) {
     const int nf = static_cast<int>(std::min<long long>(n, static_cast<long long>(p->n_sink) + p->n_recent));
     pl.nforced[b] = nf;
     pl.seg_out[b] = out;
-    if (p->budget_mode == KVSEL_BUDGET_PER_HEAD) {
+    if (pl.anchor) {
+      // AnchorKV: k = floor(ratio * n) anchors, at least the forced window, at most n;
+      // floor(rho * (k - |F|)) of the free slots by score, the rest by the random keys
+      long long k = static_cast<long long>(std::floor(p->budget_ratio * static_cast<double>(n)));
+      k = std::min<long long>(std::max<long long>(k, nf), n);
+      pl.budget[b] = static_cast<int>(k);
+      pl.budget1[b] =
+          nf + static_cast<int>(std::floor(static_cast<double>(p->alpha) * static_cast<double>(k - nf)));
+      out += static_cast<long long>(pl.H) * k;
+      pl.max_count = std::max(pl.max_count, static_cast<int>(k));
+    } else if (p->budget_mode == KVSEL_BUDGET_PER_HEAD) {
       const long long B = static_cast<long long>(std::floor(p->budget_ratio * static_cast<double>(n)));
       if (B < nf || B > n) return KVSEL_EBUDGET;
       pl.budget[b] = static_cast<int>(B);
@@ -229,6 +246,14 @@ int make_plan(const kvsel_params* p, Plan& pl, bool need_device) {
   }
   pl.g_unit_base[pl.B] = gu;
   pl.g_units = pl.l2 ? gu : 0;
+  int au = 0;
+  for (int b = 0; b < pl.B; ++b) {
+    pl.ap_unit_base[b] = au;
+    pl.ap_tiles[b] = (pl.rq.n[b] + 127) / 128;
+    au += pl.H * 2 * pl.ap_tiles[b];
+  }
+  pl.ap_unit_base[pl.B] = au;
+  pl.ap_units = pl.anchor ? au : 0;
 
   size_t off = kStatusBytes + kCounterBytes;
   if (pl.qa) {
@@ -246,6 +271,10 @@ int make_plan(const kvsel_params* p, Plan& pl, bool need_device) {
     off = align256(off + static_cast<size_t>(pl.n_scores) * sizeof(uint32_t));
     pl.ws_sraw = off;
     off = align256(off + static_cast<size_t>(pl.n_scores) * sizeof(float));
+    if (pl.anchor) {
+      pl.ws_ainv = off;
+      off = align256(off + 2 * static_cast<size_t>(pl.n_kept) * sizeof(float));
+    }
     pl.ws_total = off;
     return KVSEL_OK;
   }
@@ -264,6 +293,10 @@ int make_plan(const kvsel_params* p, Plan& pl, bool need_device) {
       pl.ws_gam = off;
       off = align256(off + static_cast<size_t>(pl.H) * 2 * kHeadDim * kHeadDim * 2);
     }
+  }
+  if (pl.anchor) {
+    pl.ws_ainv = off;
+    off = align256(off + 2 * static_cast<size_t>(pl.n_kept) * sizeof(float));
   }
   pl.ws_total = off;
   return KVSEL_OK;
@@ -541,7 +574,9 @@ int do_select(const kvsel_params* p, const Plan& pl, const float* s_attn, const 
   a.eps = p->eps;
   a.rq = pl.rq;
   a.mode = p->budget_mode;
-  a.two_stage = p->value_aware ? 1 : 0;
+  // two stages: value-aware (CriticalKV Algorithm 1), or anchors (AnchorKV §3.2: the
+  // second stage ranks by the caller's random keys, passed as s_val)
+  a.two_stage = (p->value_aware || pl.anchor) ? 1 : 0;
   a.alpha = p->alpha;
   a.n_sink = p->n_sink;
   a.n_recent = p->n_recent;
@@ -587,9 +622,105 @@ int do_compact(const Plan& pl, const kvsel_kv* kv, const int32_t* idx, const int
   return launch_rc(launch_compact(c, pl.max_count, sms, st));
 }
 
+int do_anchor_project(const Plan& pl, const kvsel_kv* kv, const void* anchor_k, const void* anchor_v,
+                      const int32_t* idx, const int32_t* counts, const int64_t* offsets, int32_t* slot_k,
+                      float* gamma_k, int32_t* slot_v, float* gamma_v, void* ws, cudaStream_t st) {
+  if (pl.n_scores == 0) return KVSEL_OK;
+  uint8_t* wsb = static_cast<uint8_t*>(ws);
+  float* inv = reinterpret_cast<float*>(wsb + pl.ws_ainv);
+  CUtensorMap tk, tv, tak, tav;
+  const int rows = kv->layout == KVSEL_LAYOUT_PAGED ? 0 : 128;
+  if (!kv_map(&tk, kv->k, kv, pl, rows) || !kv_map(&tv, kv->v, kv, pl, rows)) return KVSEL_EINVAL;
+  const long long nr = std::max<long long>(pl.n_kept, 1);
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(nr)};
+  const cuuint64_t strides[1] = {kHeadDim * 2};
+  const cuuint32_t box[2] = {64, 256};
+  if (!encode(&tak, anchor_k, 2, dims, strides, box) || !encode(&tav, anchor_v, 2, dims, strides, box))
+    return KVSEL_EINVAL;
+  StageScope sc(KVSEL_STAGE_PROJECT, st);
+  int rc = launch_rc(launch_anchor_norms(static_cast<const uint16_t*>(anchor_k), static_cast<const uint16_t*>(anchor_v),
+                                         pl.n_kept, inv, st));
+  if (rc) return rc;
+  AnchorArgs a{};
+  a.rq = pl.rq;
+  a.src = kv_source(kv);
+  a.units_total = pl.ap_units;
+  for (int b = 0; b <= pl.B; ++b) a.unit_base[b] = pl.ap_unit_base[b];
+  for (int b = 0; b < pl.B; ++b) a.tiles[b] = pl.ap_tiles[b];
+  a.idx = idx;
+  a.counts = counts;
+  a.offsets = offsets;
+  a.n_rows = pl.n_kept;
+  a.inv = inv;
+  a.slot[0] = slot_k;
+  a.slot[1] = slot_v;
+  a.gamma[0] = gamma_k;
+  a.gamma[1] = gamma_v;
+  a.wc = wait_ctl(ws);
+  return launch_rc(launch_anchor_project(a, tk, tv, tak, tav, st));
+}
+
+int check_anchor_args(const Plan& pl, const kvsel_kv* kv, const void* anchor_k, const void* anchor_v,
+                      const int32_t* idx, const int32_t* counts, const int64_t* offsets, const int32_t* slot_k,
+                      const float* gamma_k, const int32_t* slot_v, const float* gamma_v, void* ws, size_t ws_bytes) {
+  if (!pl.anchor) return KVSEL_EINVAL;
+  if (pl.max_count > anchor_max()) return KVSEL_EUNSUPPORTED;
+  if (!anchor_k || !anchor_v || !aligned16(anchor_k) || !aligned16(anchor_v) || !idx || !counts || !offsets)
+    return KVSEL_EINVAL;
+  if (!slot_k || !gamma_k || !slot_v || !gamma_v) return KVSEL_EINVAL;
+  int rc = check_kv(kv, pl, true);
+  if (rc) return rc;
+  return check_ws(pl, ws, ws_bytes);
+}
+
 }  // namespace
 
 extern "C" {
+
+int kvsel_anchor_project(const kvsel_params* p, const kvsel_kv* kv, const void* anchor_k, const void* anchor_v,
+                         const int32_t* idx, const int32_t* counts, const int64_t* offsets, int32_t* slot_k,
+                         float* gamma_k, int32_t* slot_v, float* gamma_v, void* ws, size_t ws_bytes, void* stream) {
+  Plan pl;
+  int rc = make_plan(p, pl, true);
+  if (rc) return rc;
+  if ((rc = check_anchor_args(pl, kv, anchor_k, anchor_v, idx, counts, offsets, slot_k, gamma_k, slot_v, gamma_v, ws,
+                              ws_bytes)))
+    return rc;
+  return do_anchor_project(pl, kv, anchor_k, anchor_v, idx, counts, offsets, slot_k, gamma_k, slot_v, gamma_v, ws,
+                           static_cast<cudaStream_t>(stream));
+}
+
+int kvsel_run_anchors(const kvsel_params* p, const void* q, const kvsel_kv* kv, const float* rand_keys,
+                      float* s_attn, int32_t* idx, int32_t* counts, int64_t* offsets, void* anchor_k, void* anchor_v,
+                      int32_t* slot_k, float* gamma_k, int32_t* slot_v, float* gamma_v, void* ws, size_t ws_bytes,
+                      void* stream) {
+  Plan pl;
+  int rc = make_plan(p, pl, true);
+  if (rc) return rc;
+  if (!q || !aligned16(q) || !s_attn || !rand_keys) return KVSEL_EINVAL;
+  if (pl.qa && kv && kv->layout != KVSEL_LAYOUT_CONTIGUOUS) return KVSEL_EUNSUPPORTED;
+  if ((rc = check_anchor_args(pl, kv, anchor_k, anchor_v, idx, counts, offsets, slot_k, gamma_k, slot_v, gamma_v, ws,
+                              ws_bytes)))
+    return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (pl.n_scores == 0) return KVSEL_OK;
+  // pooling runs inside the selection kernel when the halo fits (as in kvsel_run_layer)
+  const bool fuse_pool = (!p->pool || p->pool_kernel / 2 <= 32);
+  if ((rc = do_score(p, pl, q, kv, nullptr, s_attn, nullptr, ws, st, !fuse_pool))) return rc;
+  {
+    StageScope sc(KVSEL_STAGE_SELECT, st);
+    if (fuse_pool) {
+      const float* raw = reinterpret_cast<const float*>(static_cast<uint8_t*>(ws) + pl.ws_sraw);
+      rc = do_select(p, pl, s_attn, rand_keys, idx, counts, offsets, st, raw, nullptr, s_attn, nullptr);
+    } else {
+      rc = do_select(p, pl, s_attn, rand_keys, idx, counts, offsets, st);
+    }
+  }
+  if (rc) return rc;
+  if (pl.n_kept > 0 && (rc = do_compact(pl, kv, idx, counts, offsets, anchor_k, anchor_v, ws, st))) return rc;
+  return do_anchor_project(pl, kv, anchor_k, anchor_v, idx, counts, offsets, slot_k, gamma_k, slot_v, gamma_v, ws, st);
+}
+
 
 uint64_t kvsel_launch_count(void) { return kvsel::g_launches.load(std::memory_order_relaxed); }
 
@@ -669,7 +800,7 @@ int kvsel_select(const kvsel_params* p, const float* s_attn, const float* s_val,
   Plan pl;
   const int rc = make_plan(p, pl, false);
   if (rc) return rc;
-  if (!s_attn || !idx || !counts || !offsets || (p->value_aware && !s_val)) return KVSEL_EINVAL;
+  if (!s_attn || !idx || !counts || !offsets || ((p->value_aware || pl.anchor) && !s_val)) return KVSEL_EINVAL;
   if (pl.n_scores == 0) return KVSEL_OK;
   return do_select(p, pl, s_attn, s_val, idx, counts, offsets, static_cast<cudaStream_t>(stream));
 }
@@ -692,6 +823,7 @@ int kvsel_run_layer(const kvsel_params* p, const void* q, const kvsel_kv* kv, co
   Plan pl;
   int rc = make_plan(p, pl, true);
   if (rc) return rc;
+  if (pl.anchor) return KVSEL_EUNSUPPORTED;   // anchors: kvsel_run_anchors
   if (!q || !aligned16(q) || !s_attn || !idx || !counts || !offsets || !k_out || !v_out) return KVSEL_EINVAL;
   if (!aligned16(k_out) || !aligned16(v_out)) return KVSEL_EINVAL;
   if (p->value_aware && (!w_o || !aligned16(w_o) || !s_val)) return KVSEL_EINVAL;

@@ -250,6 +250,14 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   return d;
 }
 
+// First 1024-byte aligned byte of a dynamic shared-memory array (the 128-byte swizzle atoms
+// of TMA / UMMA tiles sit on 1024-byte boundaries).  The offset is added to the array
+// pointer itself rather than through an integer round trip, so the compiler still knows
+// the result points to shared memory and emits shared loads and stores through it.
+__device__ __forceinline__ uint8_t* smem_align1024(uint8_t* base) {
+  return base + ((1024u - (smem_u32(base) & 1023u)) & 1023u);
+}
+
 __device__ __forceinline__ int warp_id() { return threadIdx.x >> 5; }
 __device__ __forceinline__ int lane_id() { return threadIdx.x & 31; }
 

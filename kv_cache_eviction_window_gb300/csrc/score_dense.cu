@@ -38,10 +38,6 @@ constexpr int kTile = kNT * 256;              // bytes of one streamed tile
 
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
-__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
-  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~static_cast<uintptr_t>(1023));
-}
-
 __device__ __forceinline__ uint32_t f2key(float f) {
   const uint32_t u = __float_as_uint(f);
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
@@ -57,7 +53,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     qa_rowlse_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                      const QaArgs a) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = align1024(smem_raw);
+  uint8_t* smem = smem_align1024(smem_raw);
   uint8_t* sQ = smem;                      // [2 halves][512 rows][128 B]
   uint8_t* sK = smem + 2 * kBlockHalf;     // [stages][2 halves][64 keys][128 B]
 
@@ -229,7 +225,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     qa_keymax_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                      const QaArgs a) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = align1024(smem_raw);
+  uint8_t* smem = smem_align1024(smem_raw);
   uint8_t* sK = smem;                      // [4 M tiles][2 halves][128 keys][128 B]
   uint8_t* sQ = smem + 2 * kBlockHalf;     // [stages][2 halves][64 rows][128 B]
 

@@ -81,10 +81,6 @@ __host__ __device__ constexpr uint32_t pow2_cols(uint32_t c) {
   return c <= 32 ? 32 : c <= 64 ? 64 : c <= 128 ? 128 : c <= 256 ? 256 : 512;
 }
 
-__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
-  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~static_cast<uintptr_t>(1023));
-}
-
 __device__ __forceinline__ void chunk_coords(const ChunkTable& ck, int B, int id, int& b, int& h, int& c) {
   b = 0;
   while (b + 1 < B && ck.base[b + 1] <= id) ++b;
@@ -120,7 +116,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   static_assert(kAcc * kAccCols <= 512, "TMEM");
 
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = align1024(smem_raw);
+  uint8_t* smem = smem_align1024(smem_raw);
   uint8_t* sQ = smem;
   uint8_t* sK = smem + 2 * kQHalf;
 
@@ -298,7 +294,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     win_keysum_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                       const WinScoreArgs a, int stages, int nacc, uint32_t tmem_cols) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = align1024(smem_raw);
+  uint8_t* smem = smem_align1024(smem_raw);
   const int RP = a.R_pad;             // multiple of 64
   const int qhalf = RP * 128;
   uint8_t* sQ = smem;
@@ -563,7 +559,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
   constexpr int kCg = 32;                            // pass-1 keys per warp and tile
 
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = align1024(smem_raw);
+  uint8_t* smem = smem_align1024(smem_raw);
   uint8_t* sQ = smem;
   uint8_t* sK = smem + 2 * kQHalf;
 

@@ -325,7 +325,9 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelectArgs a,
     __syncthreads();   // the staged raw scores are no longer read
   }
   const float* s1 = pool_mode ? a.out_attn : a.s1;
-  const float* s2 = pool_mode ? a.out_val : a.s2;
+  // stage-2 scores: the value-aware score this kernel just wrote, or the caller's array
+  // (value-aware scores computed earlier, or the anchors' random keys)
+  const float* s2 = (pool_mode && a.out_val) ? a.out_val : a.s2;
 
   // stage-1 keys (forced entries at the top); in pooling mode each thread reads back the
   // values it wrote itself (same strided assignment), so plain loads suffice
@@ -477,9 +479,12 @@ int select_cluster_size_uncached(int max_len, int segments, int* chunk_cap) {
     const int cap16 = ((cap + 15) & ~15) > 16 ? ((cap + 15) & ~15) : 16;
     const size_t smem = select_smem(cap16);
     if (smem > limit) continue;
-    if (cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
-        cudaSuccess)
+    // raise (never lower) the kernel's shared-memory limit through the shared cache: a
+    // lower limit set here would fail later launches that the cache thinks are covered
+    if (ensure_smem(reinterpret_cast<const void*>(select_kernel), smem) != cudaSuccess) {
+      cudaGetLastError();
       continue;
+    }
     if (cs > 8 && cudaFuncSetAttribute(select_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
       continue;
     cudaLaunchConfig_t cfg = {};

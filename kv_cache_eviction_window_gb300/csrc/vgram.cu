@@ -25,10 +25,6 @@ constexpr int kGramSliceMax = 512;          // Dw elements per gram_kernel CTA
 constexpr int kGramChunk = 64;              // K elements per 128-byte swizzle atom column
 constexpr int kGramChunkBytes = 128 * 128;  // 128 rows x 128 B
 
-__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
-  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~static_cast<uintptr_t>(1023));
-}
-
 // ------------------------------------------------------------------------------------
 // W_h^T from W_O
 // ------------------------------------------------------------------------------------
@@ -84,7 +80,7 @@ __global__ void __launch_bounds__(256) wbar_t_kernel(const uint16_t* __restrict_
 __global__ void __launch_bounds__(160, 1) gram_kernel(const __grid_constant__ CUtensorMap twt, float* part,
                                                       int D, int slice, WaitCtl wc) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = align1024(smem_raw);
+  uint8_t* smem = smem_align1024(smem_raw);
   __shared__ __align__(8) uint64_t full_bar, done_bar;
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
@@ -186,7 +182,7 @@ __device__ __forceinline__ void vg_unit(const VgramArgs& a, int u, int& b, int& 
 __global__ void __launch_bounds__(kVgThreads, 1)
     vgram_kernel(const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tg, const VgramArgs a) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = align1024(smem_raw);
+  uint8_t* smem = smem_align1024(smem_raw);
   uint8_t* sG = smem;                   // [hi, lo][2 K halves][128 rows][128 B]
   uint8_t* sV = smem + 2 * kVgGamma;    // [stages][2 K halves][128 tokens][128 B]
 

@@ -44,10 +44,6 @@ constexpr int kVTile = kMsub * kVSub;
 constexpr int kWTile = kNT * 256;
 constexpr int kEpiCols = kNT / 2;                 // accumulator columns per epilogue warp
 
-__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
-  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~static_cast<uintptr_t>(1023));
-}
-
 __device__ __forceinline__ void unit_coords(const VnormArgs& a, int u, int& b, int& h, int& blk) {
   b = 0;
   while (b + 1 < a.rq.B && a.unit_base[b + 1] <= u) ++b;
@@ -131,7 +127,7 @@ __device__ __forceinline__ bool epi_vote_any(bool pred) {
 __global__ void __launch_bounds__(kThreads, 1)
     vnorm_kernel(const __grid_constant__ CUtensorMap tw, const VnormArgs a) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = align1024(smem_raw);
+  uint8_t* smem = smem_align1024(smem_raw);
   uint8_t* sV = smem;                // [kMsub][2 K halves][128 rows][128 B]
   uint8_t* sW = smem + kVTile;       // [kWStages][2 K halves][kNT rows][128 B]
 

@@ -252,6 +252,14 @@ def make_paged(ks: List[np.ndarray], vs: List[np.ndarray], block: int,
     return dict(k_pool=kp, v_pool=vp, block_table=table, block_size=block)
 
 
+def anchor_positions(n: int, k: int, n_recent: int, seed: int) -> np.ndarray:
+    """A given anchor list for projection-only tests: the recent window plus
+    k - |window| distinct positions drawn uniformly from the rest, ascending (int32)."""
+    nr = min(n_recent, n, k)
+    rest = _rng(seed, _TAG_RAND).choice(n - nr, size=k - nr, replace=False) if k > nr else np.zeros(0, np.int64)
+    return np.sort(np.concatenate([rest, np.arange(n - nr, n)])).astype(np.int32)
+
+
 def random_scores(n_rows: int, n: int, seed: int, tie_frac: float = 0.1) -> np.ndarray:
     """Non-negative float32 score rows with planted exact ties (for selection-only tests).
 

@@ -371,3 +371,26 @@ def test_c5_full_layer_sampled_rows():
     flat = np.concatenate([gpu["s_attn"][h] for h in range(H)])
     kept = np.concatenate([np.asarray(gpu["idx"][h]) + h * n for h in range(H)])
     GH.check_topk_property(flat, np.sort(kept), np.tile(fm, H), BL, "C5 layer top-B")
+
+
+def test_select_after_a_smaller_cluster_query():
+    """A long selection, then a short one (a new cluster-size query at a smaller shared-
+    memory size), then the long one again: the second long launch must still get its
+    shared-memory limit (the query may not lower a limit the launch path relies on)."""
+    import torch
+    from kv_cache_eviction_window_gb300 import binding as B
+
+    def run(n, seed):
+        s = datagen.random_scores(1, n, seed)[0]
+        p = B.make_params(h_kv=1, group=4, n_ctx=n, window=32, budget_ratio=0.4, n_sink=4, n_recent=32)
+        buf = B.LayerBuffers(p)
+        buf.s_attn.copy_(torch.from_numpy(s))
+        B.kvsel_select(p, buf.s_attn, None, buf.idx, buf.counts, buf.offsets, buf.ws)
+        torch.cuda.synchronize()
+        fm = O.forced_mask(n, 4, 32)
+        want = O.top_b(s.astype(np.float64), O.head_budget(n, 0.4), fm)
+        np.testing.assert_array_equal(buf.idx[:len(want)].cpu().numpy(), want)
+
+    run(131072, 1)
+    run(1000 + 17, 2)
+    run(131072, 3)
