@@ -12,8 +12,11 @@
 //                        tile arrives by TMA, the anchors of (request, head, side) sit in
 //                        shared memory in chunks of up to 256 rows, and one tcgen05 MMA
 //                        chain per chunk writes the 128 x 256 dot products to TMEM.  Two
-//                        groups of four epilogue warps take alternate tiles (one TMEM
-//                        accumulator each) and keep the running arg-max per token.
+//                        sets of eight epilogue warps take alternate tiles (one TMEM
+//                        accumulator each, four warps per column half) and keep the
+//                        running arg-max per token.
+#include <type_traits>
+
 #include "internal.cuh"
 
 namespace kvsel {
@@ -21,16 +24,16 @@ namespace {
 
 constexpr int kAnchorMax = 1024;       // anchors per (request, head) held in shared memory
 constexpr int kAnChunk = 256;          // anchors per MMA chain (UMMA N)
-constexpr int kApProducer = 8;         // warps 0-7: epilogue (two groups of four)
-constexpr int kApMma = 9;
-constexpr int kApThreads = 320;
+constexpr int kApProducer = 16;        // warps 0-15: epilogue (eight per TMEM accumulator)
+constexpr int kApMma = 17;
+constexpr int kApThreads = 576;
 constexpr int kApStages = 4;
 constexpr int kApTile = 128 * 256;     // 128 tokens x 128 bf16: two K halves of 128 rows x 128 B
 constexpr int kApB = kAnChunk * 256;   // 256 anchors x 128 bf16: two K halves of 256 rows x 128 B
 constexpr size_t kApSmem = 1024 + static_cast<size_t>(kApStages) * kApTile + kApB + 2 * 2 * kAnchorMax * 4;
 
-// the four epilogue warps of accumulator p
-__device__ __forceinline__ void group_bar(int p) { asm volatile("bar.sync %0, 128;" ::"r"(1 + p) : "memory"); }
+// the eight epilogue warps of accumulator p
+__device__ __forceinline__ void eight_bar(int p) { asm volatile("bar.sync %0, 256;" ::"r"(1 + p) : "memory"); }
 
 // One warp per anchor row: rows [0, rows) of K, then [0, rows) of V.
 __global__ void __launch_bounds__(256) anchor_norm_kernel(const uint16_t* __restrict__ ak, const uint16_t* __restrict__ av,
@@ -84,6 +87,8 @@ __global__ void __launch_bounds__(kApThreads, 1)
   __shared__ __align__(8) uint64_t bfull, bempty, done_bar;
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
+  __shared__ float s_mb[2][2][128];   // half merge: [accumulator][tile parity][token]
+  __shared__ int s_mj[2][2][128];
 
   const int warp = warp_id(), lane = lane_id();
   int* status = a.wc.status;
@@ -97,7 +102,7 @@ __global__ void __launch_bounds__(kApThreads, 1)
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&accf[s], 1);
-      mbar_init(&acce[s], 4);
+      mbar_init(&acce[s], 8);
     }
     mbar_init(&bfull, 1);
     mbar_init(&bempty, 1);
@@ -200,13 +205,15 @@ __global__ void __launch_bounds__(kApThreads, 1)
       mbar_drain(&done_bar, 0, status);
     }
   } else {
-    // epilogue: warps 4p .. 4p+3 take the CTA's tiles of parity p (TMEM accumulator p);
-    // warp q4 owns TMEM lanes (tokens) [32 q4, 32 q4 + 32)
-    const int p = warp >> 2, q4 = warp & 3;
+    // epilogue: warps 8p .. 8p+7 take the CTA's tiles of parity p (TMEM accumulator p);
+    // `half` selects the columns [128 half, 128 half + 128) of each 256-anchor chunk and
+    // q4 the TMEM lanes (tokens) [32 q4, 32 q4 + 32)
+    const int p = warp >> 3, half = (warp >> 2) & 1, q4 = warp & 3;
     const int r = q4 * 32 + lane;
+    const int pt = (warp & 7) * 32 + lane;   // thread index within the eight warps
     float* inv_p = s_inv + p * kAnchorMax;
     int* pos_p = s_pos + p * kAnchorMax;
-    int ua = 0;
+    int ua = 0, par = 0;
     long long cur = -1;
     bool ok = true;
     for (int u = lo + p; u < hi; u += 2) {
@@ -215,72 +222,62 @@ __global__ void __launch_bounds__(kApThreads, 1)
       if (key != cur) {
         // anchors of (request, head, side): inverse norms and positions
         const long long base = __ldg(a.offsets + x.seg);
-        group_bar(p);
-        for (int j = r; j < x.k; j += 128) {
+        eight_bar(p);
+        for (int j = pt; j < x.k; j += 256) {
           const long long e = base + j;
           const bool in = e >= 0 && e < a.n_rows;
           inv_p[j] = in ? __ldg(a.inv + x.side * a.n_rows + e) : 0.f;
           pos_p[j] = in ? __ldg(a.idx + e) : -1;
         }
-        group_bar(p);
+        eight_bar(p);
         cur = key;
       }
-      // anchor positions represent themselves: binary search of the ascending list (done
-      // while the tensor cores work on this tile)
       const int tok = x.tile * 128 + r;
-      int self = -1;
-      {
-        int l = 0, h2 = x.k;
-        while (l < h2) {
-          const int m = (l + h2) >> 1;
-          if (pos_p[m] < tok) l = m + 1; else h2 = m;
-        }
-        if (l < x.k && pos_p[l] == tok) self = l;
-      }
-      // eight independent running maxima (columns j = 8m + e) keep the compare chains
-      // short; each keeps its first (lowest) column on ties
-      float bst[8];
-      int bjs[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        bst[e] = -INFINITY;
-        bjs[e] = 0;
-      }
-      auto scan = [&](const float* y, int j0, int lim) {
+      // Arg-max by keyed maxima: within a 32-column round the score's five lowest mantissa
+      // bits are replaced by 31 - (column in the round), so one float max per column
+      // (three-input, over four independent partial maxima) finds the best score and,
+      // among scores equal to 2^-18 relative, the lowest column.  Rounds are compared by
+      // key (the earlier round on equal keys).  The decision and gamma carry that 2^-18
+      // relative truncation of the score.
+      float best = -INFINITY;
+      int bround = 0;
+      auto scan = [&](const float* y, int j0, int lim, auto full) {
+        constexpr bool kFull = decltype(full)::value;
+        float m[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
         for (int q = 0; q < 32; q += 8) {
           const float4 i0 = *reinterpret_cast<const float4*>(inv_p + j0 + q);
           const float4 i1 = *reinterpret_cast<const float4*>(inv_p + j0 + q + 4);
           const float iv[8] = {i0.x, i0.y, i0.z, i0.w, i1.x, i1.y, i1.z, i1.w};
+          float kk[8];
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
             const float sc = y[q + e] * iv[e];
-            // branch-free: compare, select the index, max (columns past lim never win)
-            const bool gt = sc > bst[e] && (lim >= 32 || q + e < lim);
-            bjs[e] = gt ? j0 + q + e : bjs[e];
-            bst[e] = gt ? sc : bst[e];
+            kk[e] = __int_as_float((__float_as_int(sc) & ~31) | (31 - (q + e)));
+            if (!kFull && q + e >= lim) kk[e] = -INFINITY;
           }
+          m[(q >> 3) & 3] = fmax3(m[(q >> 3) & 3], fmax3(kk[0], kk[1], kk[2]), fmax3(kk[3], kk[4], kk[5]));
+          m[((q >> 3) + 2) & 3] = fmax3(m[((q >> 3) + 2) & 3], kk[6], kk[7]);
         }
+        const float mr = fmax3(m[0], m[1], fmaxf(m[2], m[3]));
+        const bool gt = mr > best;
+        bround = gt ? j0 : bround;
+        best = gt ? mr : best;
       };
       for (int c = 0; c < x.nch; ++c) {
         ok = __all_sync(0xffffffffu, ok && mbar_wait(&accf[p], ua & 1, &s_abort, a.wc));
-        if (ok) {
+        const int nv = min(kAnChunk, x.k - c * kAnChunk) - half * 128;   // valid columns of this half
+        if (ok && nv > 0) {
           tc_fence_after();
-          const int nv = min(kAnChunk, x.k - c * kAnChunk);
-          const uint32_t taddr = tbase + (static_cast<uint32_t>(q4 * 32) << 16) + p * 256;
-          const int j0 = c * kAnChunk;
-          // 32-column rounds, the TMEM load of round i+1 in flight while round i is scanned
-          float ya[32], yb[32];
-          tmem_ld32(taddr, ya);
-          for (int c0 = 0; c0 < nv; c0 += 64) {
+          const uint32_t taddr = tbase + (static_cast<uint32_t>(q4 * 32) << 16) + p * 256 + half * 128;
+          const int j0 = c * kAnChunk + half * 128;
+          // 32-column rounds: TMEM load, wait, scan
+          for (int c0 = 0; c0 < nv && c0 < 128; c0 += 32) {
+            float y[32];
+            tmem_ld32(taddr + c0, y);
             tmem_ld_wait();
-            if (c0 + 32 < nv) tmem_ld32(taddr + c0 + 32, yb);
-            scan(ya, j0 + c0, nv - c0);
-            if (c0 + 32 < nv) {
-              tmem_ld_wait();
-              if (c0 + 64 < nv) tmem_ld32(taddr + c0 + 64, ya);
-              scan(yb, j0 + c0 + 32, nv - c0 - 32);
-            }
+            if (nv - c0 >= 32) scan(y, j0 + c0, 32, std::true_type{});
+            else scan(y, j0 + c0, nv - c0, std::false_type{});
           }
         }
         tc_fence_before();
@@ -288,24 +285,44 @@ __global__ void __launch_bounds__(kApThreads, 1)
         if (lane == 0) mbar_arrive(&acce[p]);
         ++ua;
       }
-      // merge the eight: larger score, then lower column
-      float best = bst[0];
-      int bj = bjs[0];
-#pragma unroll
-      for (int e = 1; e < 8; ++e) {
-        if (bst[e] > best || (bst[e] == best && bjs[e] < bj)) {
-          best = bst[e];
-          bj = bjs[e];
+      // this half's best column, then the merge of the two halves (double-buffered by the
+      // parity of the tile within the eight warps): larger truncated score, then lower column
+      const int bj = best == -INFINITY ? 0 : bround + 31 - (__float_as_int(best) & 31);
+      const float bq = __int_as_float(__float_as_int(best) & ~31);
+      if (half == 1) {
+        s_mb[p][par][r] = bq;
+        s_mj[p][par][r] = bj;
+      }
+      // anchor positions represent themselves: binary search of the ascending list
+      int self = -1;
+      if (half == 0) {
+        int l = 0, h2 = x.k;
+        while (l < h2) {
+          const int m = (l + h2) >> 1;
+          if (pos_p[m] < tok) l = m + 1; else h2 = m;
+        }
+        if (l < x.k && pos_p[l] == tok) self = l;
+      }
+      eight_bar(p);
+      if (half == 0) {
+        float fb = bq;
+        int fj = bj;
+        const float ob = s_mb[p][par][r];
+        const int oj = s_mj[p][par][r];
+        if (ob > fb || (ob == fb && oj < fj)) {
+          fb = ob;
+          fj = oj;
+        }
+        const int n = a.rq.n[x.b];
+        if (ok && tok < n) {
+          const int slot = self >= 0 ? self : fj;
+          const float gamma = self >= 0 ? 1.f : (x.k > 0 ? fb * inv_p[fj] : 0.f);
+          const size_t o = a.rq.soff[x.b] + static_cast<size_t>(x.h) * n + tok;
+          (x.side ? a.slot[1] : a.slot[0])[o] = slot;
+          (x.side ? a.gamma[1] : a.gamma[0])[o] = gamma;
         }
       }
-      const int n = a.rq.n[x.b];
-      if (ok && tok < n) {
-        const int slot = self >= 0 ? self : bj;
-        const float gamma = self >= 0 ? 1.f : (x.k > 0 ? best * inv_p[bj] : 0.f);
-        const size_t o = a.rq.soff[x.b] + static_cast<size_t>(x.h) * n + tok;
-        (x.side ? a.slot[1] : a.slot[0])[o] = slot;
-        (x.side ? a.gamma[1] : a.gamma[0])[o] = gamma;
-      }
+      par ^= 1;
     }
   }
   __syncwarp();
