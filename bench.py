@@ -257,6 +257,80 @@ def traffic_for(kernel_name):
     return d.get("dram_bytes_per_launch")
 
 
+def time_anchor_path(B, datagen, wl_stack, q_d, kvs, ws, stream, K, W, L, world, pk, dev):
+    """ms per layer of kvsel_run_anchors over the stack's layers (graph replay), plus the
+    live time of the projection stage (anchor norms + projection) and its rooflines."""
+    import numpy as np
+    import torch
+
+    wl = datagen.WORKLOADS[6].replace(layers=L)
+    H, n, d = wl.h_kv, wl.n_ctx, wl.head_dim
+    assert (H, n, d) == (wl_stack.h_kv, wl_stack.n_ctx, wl_stack.head_dim)
+    p = B.params_from_workload(wl)
+    bufs = [B.LayerBuffers(p, device=dev) for _ in range(L)]
+    rand = [torch.from_numpy(datagen.anchor_keys(H, n, 7000 + i).reshape(-1)).to(dev) for i in range(L)]
+    assert B.kvsel_workspace_size(p) <= ws.numel() * 4
+
+    def call(i, s):
+        b = bufs[i]
+        B.kvsel_run_anchors(p, q_d[i], kvs[i], rand[i], b.s_attn, b.idx, b.counts, b.offsets, b.k_out, b.v_out,
+                            b.slot_k, b.gamma_k, b.slot_v, b.gamma_v, ws, s)
+
+    for _ in range(W):
+        for i in range(L):
+            call(i, stream)
+    torch.cuda.synchronize()
+    # live projection-stage time (eager, stage events on the launch stream)
+    nst = len(B.STAGES)
+    pi = B.STAGES.index("project")
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(2 * nst)]
+    for e in evs:
+        e.record(stream)
+    arr = (ctypes.c_void_p * (2 * nst))(*[e.cuda_event for e in evs])
+    proj = []
+    for i in range(L):
+        B.kvsel_set_stage_events(arr)
+        call(i, stream)
+        B.kvsel_set_stage_events(None)
+        torch.cuda.synchronize()
+        proj.append(evs[2 * pi].elapsed_time(evs[2 * pi + 1]))
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g, stream=side):
+            for i in range(L):
+                call(i, side)
+    stream.wait_stream(side)
+    g.replay()
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(K):
+        g.replay()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(t0.elapsed_time(t1), world) / (K * L)
+    status = B.kvsel_get_device_status(ws)
+    k_anc = max(int(wl.budget_ratio * n), wl.n_recent)
+    pms = float(np.median(proj))
+    # projection: K and V read once, slot + gamma written per position and side; the
+    # contraction is 2 * n * k * d flop per (head, side)
+    pbytes = 2 * H * n * d * 2 + 2 * H * n * 8 + 2 * H * k_anc * d * 2
+    pflops = 2 * 2.0 * H * n * k_anc * d
+    hbm = pk.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+    tc = pk.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+    return {"what": "same Q/K/V, AnchorKV anchors: score (maxpool 7) + select (k = n/128, rho = 0.7) + "
+                    "anchor gather + nearest-anchor projection of K and V",
+            "workload": wl.name, "ms_per_layer": ms, "entries_per_s": H * n / (ms * 1e-3) * world,
+            "anchors_per_head": k_anc, "device_status": status,
+            "projection": {"kernels": "anchor_norm_kernel + anchor_proj_kernel", "ms_per_layer": pms,
+                           "algorithmic_bytes": pbytes, "achieved_gbs": pbytes / (pms * 1e-3) / 1e9,
+                           "hbm_frac": pbytes / (pms * 1e-3) / 1e9 / hbm, "flops": pflops,
+                           "achieved_tflops": pflops / (pms * 1e-3) / 1e12,
+                           "tensor_frac": pflops / (pms * 1e-3) / 1e12 / tc}}
+
+
 def main():
     args = parse()
     if args.impl == "reference":
@@ -474,6 +548,12 @@ def main():
                                "ms_per_layer": lms, "entries_per_s": H * n / (lms * 1e-3) * world,
                                "algorithmic_bytes_per_layer": alg2, "achieved_gbs": gbs2,
                                "peak_gbs": pk.get("hbm_gbs"), "frac": gbs2 / pk.get("hbm_gbs", 6800.0)}
+
+    # ---- AnchorKV anchors on the same layers: scoring (maxpool 7), anchor selection
+    # (k = n/128, rho = 0.7, recent window forced), anchor gather and nearest-anchor
+    # projection of every key and value (kvsel_run_anchors)
+    if not args.no_plain:
+        out["anchor_path"] = time_anchor_path(B, datagen, wl, q_d, kvs, ws, stream, K, W, L, world, pk, dev)
 
     # ---- end to end through the public API: pinned host -> device each step, results back
     if not args.no_e2e:

@@ -252,6 +252,11 @@ def make_paged(ks: List[np.ndarray], vs: List[np.ndarray], block: int,
     return dict(k_pool=kp, v_pool=vp, block_table=table, block_size=block)
 
 
+def anchor_keys(h_kv: int, n: int, seed: int) -> np.ndarray:
+    """[H][n] float32 i.i.d. uniform [0, 1) keys for the random share of the anchors."""
+    return _rng(seed, _TAG_RAND).random((h_kv, n), dtype=np.float32)
+
+
 def anchor_positions(n: int, k: int, n_recent: int, seed: int) -> np.ndarray:
     """A given anchor list for projection-only tests: the recent window plus
     k - |window| distinct positions drawn uniformly from the rest, ascending (int32)."""

@@ -1,6 +1,8 @@
 """Run a few layers of one workload through kvsel_run_layer, for profilers (ncu).
 
     python -m kv_cache_eviction_window_gb300.profile_case --workload 2 --layers 2 --steps 2
+    python -m kv_cache_eviction_window_gb300.profile_case --workload 2 --value-norm l2
+    python -m kv_cache_eviction_window_gb300.profile_case --workload 6      # AnchorKV anchors
 
 The inputs are the same seeded synthetic tensors as the benchmark (each layer distinct,
 larger than L2 for the 32K stack), so per-launch counters taken here scale to the
@@ -23,6 +25,7 @@ def main():
     ap.add_argument("--layers", type=int, default=2)
     ap.add_argument("--steps", type=int, default=2)
     ap.add_argument("--plain", action="store_true", help="value_aware=0")
+    ap.add_argument("--value-norm", default=None, choices=["l1", "l2"], help="value-aware norm override")
     args = ap.parse_args()
     import numpy as np
     import torch
@@ -36,6 +39,9 @@ def main():
     wl = datagen.WORKLOADS[args.workload]
     if args.plain:
         wl = wl.replace(value_aware=False)
+    if args.value_norm:
+        wl = wl.replace(value_norm=args.value_norm)
+    anchors = wl.budget_mode == "anchor"
     dev = torch.device("cuda", 0)
 
     def to_dev(u16):
@@ -58,6 +64,8 @@ def main():
             keep = (kt, vt)
         q = to_dev(x["q"])
         w = to_dev(x["w_o"]) if wl.value_aware else None
+        if anchors:   # the random keys of the anchor draw ride in the weight slot
+            w = torch.from_numpy(np.concatenate([r.reshape(-1) for r in x["rand"]])).to(dev)
         layers.append((p, q, kv, w, B.LayerBuffers(p, device=dev), keep))
     nst = len(B.STAGES)
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * nst)]
@@ -70,7 +78,12 @@ def main():
     for _ in range(args.steps):
         for (p, q, kv, w, b, _k) in layers:
             B.kvsel_set_stage_events(arr)
-            B.kvsel_run_layer(p, q, kv, w, b.s_attn, b.s_val, b.idx, b.counts, b.offsets, b.k_out, b.v_out, b.ws)
+            if anchors:
+                B.kvsel_run_anchors(p, q, kv, w, b.s_attn, b.idx, b.counts, b.offsets, b.k_out, b.v_out, b.slot_k,
+                                    b.gamma_k, b.slot_v, b.gamma_v, b.ws)
+            else:
+                B.kvsel_run_layer(p, q, kv, w, b.s_attn, b.s_val, b.idx, b.counts, b.offsets, b.k_out, b.v_out,
+                                  b.ws)
             B.kvsel_set_stage_events(None)
             torch.cuda.synchronize()
             for i in range(nst):
