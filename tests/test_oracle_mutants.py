@@ -12,9 +12,11 @@ from oracle import kvsel_oracle as O
 import tests.test_oracle_pins as P
 
 from oracle import anchor_oracle as AO
+from oracle import perturb_oracle as PO
 
 ORIG = {name: getattr(O, name) for name in dir(O) if callable(getattr(O, name))}
 A_ORIG = {name: getattr(AO, name) for name in dir(AO) if callable(getattr(AO, name))}
+P_ORIG = {name: getattr(PO, name) for name in dir(PO) if callable(getattr(PO, name))}
 
 
 def _logits_no_scale(q, k, scale=None, causal=True):
@@ -169,6 +171,45 @@ def _anchor_count_ignores_forced(n, n_forced, div=128):
     return min(n, n // div)
 
 
+def _pt_no_renormalise(A, keep):
+    return A * keep[None, :]
+
+
+def _pt_theta_2_minus_a(A, vproj, keep):
+    actual, theta, relaxed = P_ORIG["perturbation_rows"](A, vproj, keep)
+    nu = np.abs(vproj).sum(axis=1)
+    a = (A * keep[None, :]).sum(axis=1)
+    C = A @ nu
+    P = (A * keep[None, :]) @ nu
+    return actual, C - (2.0 - a) * P, relaxed
+
+
+def _pt_relaxed_all_keys(A, vproj, keep):
+    actual, theta, relaxed = P_ORIG["perturbation_rows"](A, vproj, keep)
+    a = (A * keep[None, :]).sum(axis=1)
+    return actual, theta, 2.0 * (1.0 - a) * np.abs(vproj).sum(axis=1).max()
+
+
+def _pt_slice_transposed(q, k, v, w_o, h, group, keep, scale=None, causal=True):
+    G, W, d = q.shape
+    H = w_o.shape[1] // (group * d)
+    A = PO.attention_rows(q, k, scale, causal)
+    out = np.zeros((3, G, W))
+    for g in range(group):
+        qh = g * H + h                                    # query heads numbered g-major
+        vproj = v @ w_o[:, qh * d:(qh + 1) * d].T
+        out[:, g, :] = PO.perturbation_rows(A[g], vproj, keep)
+    return out
+
+
+P_MUTANTS = {
+    "perturbation_no_renormalise": ("masked_weights", _pt_no_renormalise),
+    "perturbation_theta_2_minus_a": ("perturbation_rows", _pt_theta_2_minus_a),
+    "perturbation_relaxed_all_keys": ("perturbation_rows", _pt_relaxed_all_keys),
+    "perturbation_slice_g_major": ("perturbation_head", _pt_slice_transposed),
+}
+
+
 A_MUTANTS = {
     "anchor_abs_cosine": ("anchor_project", _anchor_abs_cosine),
     "anchor_gamma_unnormalised": ("anchor_project", _anchor_gamma_unnormalised),
@@ -219,9 +260,12 @@ def _pin_calls():
     return calls
 
 
-@pytest.mark.parametrize("mutant", sorted(MUTANTS) + sorted(A_MUTANTS))
+@pytest.mark.parametrize("mutant", sorted(MUTANTS) + sorted(A_MUTANTS) + sorted(P_MUTANTS))
 def test_pins_catch_mutant(mutant, monkeypatch):
-    if mutant in A_MUTANTS:
+    if mutant in P_MUTANTS:
+        attr, fake = P_MUTANTS[mutant]
+        monkeypatch.setattr(PO, attr, fake)
+    elif mutant in A_MUTANTS:
         attr, fake = A_MUTANTS[mutant]
         monkeypatch.setattr(AO, attr, fake)
     else:

@@ -631,3 +631,87 @@ def test_run_anchor_layer_invariants():
     top26 = O.top_b(s, 58, O.forced_mask(9000, 0, 32))
     assert set(top26.tolist()) <= set(anc.tolist())
     assert len(free) == 38
+
+
+# --------------------------------------------------------------------- output perturbation
+from oracle import perturb_oracle as PO  # noqa: E402
+
+
+def test_perturbation_two_keys_hand_example():
+    # A = (3/4, 1/4), keep {0}: ô = v'_0, o - ô = 1/4 (v'_1 - v'_0) = (0.5, 0.75);
+    # θ = A_1 (||v'_0|| + ||v'_1||) = 1/4 * 7; θ' = 2 * 1/4 * max(3, 4)
+    A = np.array([[0.75, 0.25]])
+    vp = np.array([[1.0, -2.0], [3.0, 1.0]])
+    actual, theta, relaxed = PO.perturbation_rows(A, vp, np.array([True, False]))
+    assert actual[0] == 1.25 and abs(theta[0] - 1.75) < 1e-15 and relaxed[0] == 2.0
+
+
+def test_perturbation_keep_all_is_zero_and_mask_renormalises():
+    g = np.random.default_rng(2)
+    A = g.random((5, 9))
+    A /= A.sum(1, keepdims=True)
+    vp = g.standard_normal((9, 6))
+    actual, theta, relaxed = PO.perturbation_rows(A, vp, np.ones(9, bool))
+    assert np.abs(actual).max() < 1e-12 and np.abs(theta).max() < 1e-12 and np.abs(relaxed).max() < 1e-12
+    keep = np.array([1, 0, 1, 1, 0, 0, 1, 0, 1], bool)
+    Ah = PO.masked_weights(A, keep)
+    assert np.allclose(Ah.sum(1), 1.0) and (Ah[:, ~keep] == 0).all()
+    # kept weights scale by 1 / kept mass (CriticalKV Theorem 3.2)
+    assert np.allclose(Ah[:, keep], A[:, keep] / (A[:, keep].sum(1, keepdims=True)))
+
+
+def test_perturbation_bound_chain():
+    # triangle inequality: actual <= θ <= θ' for any kept set
+    g = np.random.default_rng(8)
+    for _ in range(20):
+        n = 12
+        A = g.random((4, n)) ** 3
+        A /= A.sum(1, keepdims=True)
+        vp = g.standard_normal((n, 5)) * g.random((n, 1)) * 3
+        keep = g.random(n) < 0.5
+        keep[0] = True
+        actual, theta, relaxed = PO.perturbation_rows(A, vp, keep)
+        assert (actual <= theta + 1e-12).all() and (theta <= relaxed + 1e-12).all()
+
+
+def test_relaxed_bound_minimised_by_attention_only_selection():
+    # CriticalKV Theorem C.1: over all kept sets of size B, the top-B by A minimises θ'
+    g = np.random.default_rng(4)
+    n, B = 7, 3
+    A = g.random((1, n))
+    A /= A.sum()
+    vp = g.standard_normal((n, 4))
+    best = min(PO.perturbation_rows(A, vp, np.isin(np.arange(n), s))[2][0]
+               for s in itertools.combinations(range(n), B))
+    top = np.argsort(-A[0])[:B]
+    got = PO.perturbation_rows(A, vp, np.isin(np.arange(n), top))[2][0]
+    assert abs(got - best) < 1e-12
+
+
+def test_perturbation_head_uses_its_own_w_o_slice():
+    # only query head (h, g) = (1, 1) of H = 3, G = 2 has a non-zero slice [I_d; 0]: its
+    # projected values are the raw values, every other query head sees zeros
+    g = np.random.default_rng(6)
+    H, G, d, D, n, W = 3, 2, 4, 6, 10, 3
+    q = g.standard_normal((G, W, d))
+    k = g.standard_normal((n, d))
+    v = g.standard_normal((n, d))
+    w_o = np.zeros((D, H * G * d))
+    qh = 1 * G + 1
+    w_o[:d, qh * d:(qh + 1) * d] = np.eye(d)
+    keep = np.zeros(n, bool)
+    keep[[0, 3, 7, 8, 9]] = True
+    out = PO.perturbation_head(q, k, v, w_o, 1, G, keep)
+    A = PO.attention_rows(q, k)
+    want = np.abs((A[1] - PO.masked_weights(A[1], keep)) @ v).sum(1)
+    assert np.allclose(out[0, 1], want, rtol=1e-12, atol=1e-14)
+    assert np.abs(out[:, 0]).max() == 0.0
+
+
+def test_relaxed_bound_runs_over_the_keys_a_row_sees():
+    # the third key carries zero weight (a causal row does not see it): its large norm
+    # must not enter θ' = 2 (1 - a) max ||v'_i||_1
+    A = np.array([[0.5, 0.5, 0.0]])
+    vp = np.array([[1.0, 0.0], [0.0, -2.0], [100.0, 0.0]])
+    _, _, relaxed = PO.perturbation_rows(A, vp, np.array([True, False, False]))
+    assert relaxed[0] == 2.0 * 0.5 * 2.0
