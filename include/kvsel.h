@@ -233,7 +233,8 @@ enum {
   KVSEL_STAGE_SELECT = 5,    /* top-B selection                                      */
   KVSEL_STAGE_COMPACT = 6,   /* gather of the kept K/V rows                          */
   KVSEL_STAGE_PROJECT = 7,   /* anchors: anchor norms and nearest-anchor projection  */
-  KVSEL_STAGE_COUNT = 8
+  KVSEL_STAGE_PERTURB = 8,   /* output perturbation of a kept set (all its kernels)  */
+  KVSEL_STAGE_COUNT = 9
 };
 
 /* Diagnostics: while `events` is non-NULL, each kernel launched by this thread's
@@ -284,6 +285,37 @@ int kvsel_run_anchors(const kvsel_params* p, const void* q, const kvsel_kv* kv, 
                       float* s_attn, int32_t* idx, int32_t* counts, int64_t* offsets, void* anchor_k, void* anchor_v,
                       int32_t* slot_k, float* gamma_k, int32_t* slot_v, float* gamma_v, void* ws, size_t ws_bytes,
                       void* stream);
+
+/* ---- output perturbation of a kept set --------------------------------------------- */
+
+/* Workspace bytes of kvsel_perturbation for these parameters (host-only). */
+int kvsel_perturbation_workspace_size(const kvsel_params* p, size_t* bytes);
+
+/* How much a kept set perturbs the attention output of the observation-window queries
+ * ("CriticalKV: 출력 섭동 관점에서 KV 캐시 축출을 최적화하기", Definition 3.1, §3.3 Theorems 3.2 and
+ * 3.3, App. C.4 Theorem C.1, App. C.5 Table 9).  For window row w of query head (h, g),
+ * softmax weights A_i over the keys it sees (causal, scale as in kvsel_score), kept set S
+ * of KV head h, kept mass a = sum_{i in S} A_i and projected values v'_i = W_O^(h,g) v_i:
+ *   out[b][h][0][g][w] = ||o - ô||_1 with o = sum_i A_i v'_i and ô = sum_{i in S} A_i v'_i / a
+ *                        (eviction as a renormalised 0/1 mask on A, Theorem 3.2)
+ *   out[b][h][1][g][w] = C - (2 - 1/a) P, C = sum_i A_i ||v'_i||_1, P = sum_{i in S} A_i ||v'_i||_1
+ *                        (Theorem 3.3's bound; C when a = 0)
+ *   out[b][h][2][g][w] = 2 (1 - a) max_i ||v'_i||_1 over the keys the row sees
+ *                        (the relaxed bound that attention-only selection minimises, C.1)
+ *   p        window scoring parameters (window > 0, group * window <= 128, group <= 16,
+ *            d_model a multiple of 128); value_aware and the budget fields are not read
+ *   q, kv    as kvsel_score (V rows past a request's length in the contiguous layout must
+ *            hold finite values: they are multiplied by zero)
+ *   w_o      device bf16 [d_model][h_kv*group*head_dim]
+ *   idx/counts/offsets  device: the kept set per (request, head), as kvsel_select writes it
+ *   out      device fp32 [batch][h_kv][3][group][window]
+ *   ws       workspace of kvsel_perturbation_workspace_size bytes, 256-byte aligned
+ * The logits and the weighted value sums run on tcgen05 (bf16 inputs, fp32 accumulation;
+ * the weights enter as bf16 high and low parts); ||v'||_1 uses the value-norm GEMM once
+ * per group member; the output projection is fp32 on CUDA cores. */
+int kvsel_perturbation(const kvsel_params* p, const void* q, const kvsel_kv* kv, const void* w_o, const int32_t* idx,
+                       const int32_t* counts, const int64_t* offsets, float* out, void* ws, size_t ws_bytes,
+                       void* stream);
 
 /* Static description of an error code. */
 const char* kvsel_strerror(int code);

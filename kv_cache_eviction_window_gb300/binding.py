@@ -35,9 +35,9 @@ EXPORTS = ("kvsel_workspace_size", "kvsel_output_size", "kvsel_workspace_init", 
            "kvsel_select", "kvsel_compact", "kvsel_run_layer", "kvsel_get_device_status",
            "kvsel_set_wait_limit", "kvsel_set_stage_events", "kvsel_strerror", "kvsel_version",
            "kvsel_score_noalloc", "kvsel_launch_count", "kvsel_head_scores", "kvsel_anchor_project",
-           "kvsel_run_anchors")
+           "kvsel_run_anchors", "kvsel_perturbation_workspace_size", "kvsel_perturbation")
 NOALLOC_SCRATCH_BYTES = 16 << 20
-STAGES = ("rowstats", "keysum", "wbar", "vnorm", "finalize", "select", "compact", "project")
+STAGES = ("rowstats", "keysum", "wbar", "vnorm", "finalize", "select", "compact", "project", "perturb")
 
 
 class KvselUnavailable(RuntimeError):
@@ -108,6 +108,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
         "kvsel_head_scores": ([P, vp, vp, vp], ctypes.c_int),
         "kvsel_anchor_project": ([P, K] + [vp] * 10 + [sz, vp], ctypes.c_int),
         "kvsel_run_anchors": ([P, vp, K] + [vp] * 12 + [sz, vp], ctypes.c_int),
+        "kvsel_perturbation_workspace_size": ([P, ctypes.POINTER(sz)], ctypes.c_int),
+        "kvsel_perturbation": ([P, vp, K, vp, vp, vp, vp, vp, vp, sz, vp], ctypes.c_int),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -304,6 +306,19 @@ def kvsel_run_anchors(params, q, kv: kvsel_kv, rand_keys, s_attn, idx, counts, o
                                     _ptr(anchor_v), _ptr(slot_k), _ptr(gamma_k), _ptr(slot_v), _ptr(gamma_v),
                                     _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)),
            "kvsel_run_anchors")
+
+
+def kvsel_perturbation_workspace_size(params: kvsel_params) -> int:
+    out = ctypes.c_size_t()
+    _check(load().kvsel_perturbation_workspace_size(ctypes.byref(params), ctypes.byref(out)),
+           "kvsel_perturbation_workspace_size")
+    return out.value
+
+
+def kvsel_perturbation(params, q, kv: kvsel_kv, w_o, idx, counts, offsets, out, ws, stream=None) -> None:
+    _check(load().kvsel_perturbation(ctypes.byref(params), _ptr(q), ctypes.byref(kv), _ptr(w_o), _ptr(idx),
+                                     _ptr(counts), _ptr(offsets), _ptr(out), _ptr(ws), ws.numel() * ws.element_size(),
+                                     _stream(stream)), "kvsel_perturbation")
 
 
 def kvsel_get_device_status(ws, stream=None) -> int:

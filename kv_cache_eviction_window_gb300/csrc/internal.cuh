@@ -165,6 +165,35 @@ cudaError_t launch_anchor_norms(const uint16_t* ak, const uint16_t* av, long lon
 cudaError_t launch_anchor_project(const AnchorArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
                                   const CUtensorMap& tak, const CUtensorMap& tav, cudaStream_t st);
 
+// Output perturbation of a kept set (CriticalKV Theorems 3.2, 3.3, C.1) for the window rows
+// of every KV head.  Key chunks as in ChunkTable; rows r = g * W + w (R = G * W <= 128).
+struct PerturbArgs {
+  ReqTable rq;
+  ChunkTable ck;
+  KvSource src;
+  int G, W, R;
+  int causal;
+  float s2;                       // logit scale * log2(e)
+  int D;                          // rows of W_O
+  const uint8_t* keep;            // packed [sum_b H*n_b]: 1 = kept
+  const float* nu;                // [G][n_scores]: ||W_O^(h,g) v_i||_1 per query head of the group
+  long long n_scores;
+  float* stat_part;               // [chunks][128][7]: m (log2), Z, Z_S, Z_N, C_N, P_S, max partials
+  float* stat;                    // [B*H][128][7] merged
+  float* e_part;                  // [chunks][128][128]: sum_i c_ri v_i partials
+  float* e;                       // [B*H][128][128] merged
+  float* y_part;                  // [B*H*G][D/256][W]: partial ||W_O^(h,g) e_r||_1
+  float* out;                     // [B][H][3][G][W]: actual, bound, relaxed bound
+  WaitCtl wc;
+};
+cudaError_t launch_perturb_mask(const ReqTable& rq, const int32_t* idx, const int32_t* counts, const int64_t* offsets,
+                                int max_count, uint8_t* keep, int* status, cudaStream_t st);
+cudaError_t launch_perturb_stats(const PerturbArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, cudaStream_t st);
+cudaError_t launch_perturb_accum(const PerturbArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
+                                 const CUtensorMap& tv, cudaStream_t st);
+cudaError_t launch_perturb_finish(const PerturbArgs& a, const uint16_t* w_o, cudaStream_t st);
+int perturb_slices(int D);   // 256-feature slices of W_O rows in the projection
+
 // Raise a kernel's dynamic shared-memory limit once per device (cached).
 cudaError_t ensure_smem(const void* func, size_t bytes);
 

@@ -622,6 +622,33 @@ int do_compact(const Plan& pl, const kvsel_kv* kv, const int32_t* idx, const int
   return launch_rc(launch_compact(c, pl.max_count, sms, st));
 }
 
+// Workspace of kvsel_perturbation, after the status word and counters.
+struct PerturbLayout {
+  size_t keep = 0, nu = 0, stat_part = 0, stat = 0, e_part = 0, e = 0, y_part = 0, total = 0;
+};
+
+int perturb_plan(const kvsel_params* p, const Plan& pl, PerturbLayout& L) {
+  if (pl.qa || pl.R > 128 || pl.R < 1 || pl.G > 16) return KVSEL_EUNSUPPORTED;
+  if (p->d_model < 128 || p->d_model % 128 != 0) return KVSEL_EUNSUPPORTED;
+  size_t off = kStatusBytes + kCounterBytes;
+  L.keep = off;
+  off = align256(off + static_cast<size_t>(pl.n_scores));
+  L.nu = off;
+  off = align256(off + static_cast<size_t>(pl.G) * pl.n_scores * sizeof(float));
+  L.stat_part = off;
+  off = align256(off + static_cast<size_t>(pl.ck.total) * 128 * 7 * sizeof(float));
+  L.stat = off;
+  off = align256(off + static_cast<size_t>(pl.B) * pl.H * 128 * 7 * sizeof(float));
+  L.e_part = off;
+  off = align256(off + static_cast<size_t>(pl.ck.total) * 128 * 128 * sizeof(float));
+  L.e = off;
+  off = align256(off + static_cast<size_t>(pl.B) * pl.H * 128 * 128 * sizeof(float));
+  L.y_part = off;
+  off = align256(off + static_cast<size_t>(pl.B) * pl.H * pl.G * perturb_slices(pl.D) * pl.W * sizeof(float));
+  L.total = off;
+  return KVSEL_OK;
+}
+
 int do_anchor_project(const Plan& pl, const kvsel_kv* kv, const void* anchor_k, const void* anchor_v,
                       const int32_t* idx, const int32_t* counts, const int64_t* offsets, int32_t* slot_k,
                       float* gamma_k, int32_t* slot_v, float* gamma_v, void* ws, cudaStream_t st) {
@@ -688,6 +715,100 @@ int kvsel_anchor_project(const kvsel_params* p, const kvsel_kv* kv, const void* 
     return rc;
   return do_anchor_project(pl, kv, anchor_k, anchor_v, idx, counts, offsets, slot_k, gamma_k, slot_v, gamma_v, ws,
                            static_cast<cudaStream_t>(stream));
+}
+
+int kvsel_perturbation_workspace_size(const kvsel_params* p, size_t* bytes) {
+  if (!bytes) return KVSEL_EINVAL;
+  Plan pl;
+  int rc = make_plan(p, pl, true);
+  if (rc) return rc;
+  PerturbLayout L;
+  if ((rc = perturb_plan(p, pl, L))) return rc;
+  *bytes = L.total;
+  return KVSEL_OK;
+}
+
+int kvsel_perturbation(const kvsel_params* p, const void* q, const kvsel_kv* kv, const void* w_o, const int32_t* idx,
+                       const int32_t* counts, const int64_t* offsets, float* out, void* ws, size_t ws_bytes,
+                       void* stream) {
+  Plan pl;
+  int rc = make_plan(p, pl, true);
+  if (rc) return rc;
+  PerturbLayout L;
+  if ((rc = perturb_plan(p, pl, L))) return rc;
+  if (!q || !aligned16(q) || !w_o || !aligned16(w_o) || !idx || !counts || !offsets || !out) return KVSEL_EINVAL;
+  if ((rc = check_kv(kv, pl, true))) return rc;
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) || ws_bytes < L.total) return KVSEL_EWORKSPACE;
+  if (pl.n_scores == 0) return KVSEL_OK;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint8_t* wsb = static_cast<uint8_t*>(ws);
+  const float scale = p->scale > 0.f ? p->scale : 1.f / std::sqrt(static_cast<float>(kHeadDim));
+  PerturbArgs a{};
+  a.rq = pl.rq;
+  a.ck = pl.ck;
+  a.src = kv_source(kv);
+  a.G = pl.G;
+  a.W = pl.W;
+  a.R = pl.R;
+  a.causal = p->causal ? 1 : 0;
+  a.s2 = scale * 1.4426950408889634f;
+  a.D = pl.D;
+  a.keep = wsb + L.keep;
+  a.nu = reinterpret_cast<const float*>(wsb + L.nu);
+  a.n_scores = pl.n_scores;
+  a.stat_part = reinterpret_cast<float*>(wsb + L.stat_part);
+  a.stat = reinterpret_cast<float*>(wsb + L.stat);
+  a.e_part = reinterpret_cast<float*>(wsb + L.e_part);
+  a.e = reinterpret_cast<float*>(wsb + L.e);
+  a.y_part = reinterpret_cast<float*>(wsb + L.y_part);
+  a.out = out;
+  a.wc = wait_ctl(ws);
+  CUtensorMap tq, tk, tv;
+  {
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(pl.B) * pl.H * pl.R};
+    const cuuint64_t strides[1] = {kHeadDim * 2};
+    const cuuint32_t box[2] = {64, 128};
+    if (!encode(&tq, q, 2, dims, strides, box)) return KVSEL_EINVAL;
+  }
+  const int rows = kv->layout == KVSEL_LAYOUT_PAGED ? 0 : 128;
+  if (!kv_map(&tk, kv->k, kv, pl, rows) || !kv_map(&tv, kv->v, kv, pl, rows)) return KVSEL_EINVAL;
+  StageScope sc(KVSEL_STAGE_PERTURB, st);
+  // kept positions -> byte mask
+  if ((rc = launch_rc(cudaMemsetAsync(wsb + L.keep, 0, static_cast<size_t>(pl.n_scores), st)))) return rc;
+  if ((rc = launch_rc(launch_perturb_mask(pl.rq, idx, counts, offsets, pl.n_max, wsb + L.keep, static_cast<int*>(ws),
+                                          st))))
+    return rc;
+  // ||W_O^(h,g) v_i||_1 for every group member g: the value-norm GEMM over W_O's own slice
+  VnormArgs v{};
+  v.rq = pl.rq;
+  v.src = kv_source(kv);
+  v.v = static_cast<const uint16_t*>(kv->v);
+  v.stride_req = kv->stride_req;
+  v.stride_head = kv->stride_head;
+  v.stride_tok = kv->stride_tok;
+  v.D = pl.D;
+  v.Dw = pl.D;
+  v.units_total = pl.unit_base[pl.B];
+  for (int b = 0; b <= pl.B; ++b) v.unit_base[b] = pl.unit_base[b];
+  for (int b = 0; b < pl.B; ++b) v.blocks_per_head[b] = pl.blocks_per_head[b];
+  v.wc = wait_ctl(ws);
+  for (int g = 0; g < pl.G; ++g) {
+    float* nu_g = reinterpret_cast<float*>(wsb + L.nu) + static_cast<size_t>(g) * pl.n_scores;
+    if ((rc = launch_rc(cudaMemsetAsync(nu_g, 0, static_cast<size_t>(pl.n_scores) * sizeof(float), st)))) return rc;
+    CUtensorMap tw;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(pl.D),
+                                static_cast<cuuint64_t>(pl.H)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(pl.H) * pl.G * kHeadDim * 2,
+                                   static_cast<cuuint64_t>(pl.G) * kHeadDim * 2};
+    const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(vnorm_w_tile_rows()), 1};
+    if (!encode(&tw, static_cast<const uint16_t*>(w_o) + static_cast<size_t>(g) * kHeadDim, 3, dims, strides, box))
+      return KVSEL_EINVAL;
+    v.nu = nu_g;
+    if ((rc = launch_rc(launch_vnorm(v, tw, st)))) return rc;
+  }
+  if ((rc = launch_rc(launch_perturb_stats(a, tq, tk, st)))) return rc;
+  if ((rc = launch_rc(launch_perturb_accum(a, tq, tk, tv, st)))) return rc;
+  return launch_rc(launch_perturb_finish(a, static_cast<const uint16_t*>(w_o), st));
 }
 
 int kvsel_run_anchors(const kvsel_params* p, const void* q, const kvsel_kv* kv, const float* rand_keys,
