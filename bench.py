@@ -331,6 +331,54 @@ def time_anchor_path(B, datagen, wl_stack, q_d, kvs, ws, stream, K, W, L, world,
                            "tensor_frac": pflops / (pms * 1e-3) / 1e12 / tc}}
 
 
+def perturbation_table(B, wl, q_d, kvs, w_d, bufs, stream, dev, pk, layers=4):
+    """CriticalKV Table 9 on synthetic layers: the actual output perturbation of the window
+    queries and both bounds, averaged over rows, heads and the first `layers` layers, for the
+    value-aware (two-stage) and the attention-only kept sets at the stack's budget; plus the
+    time of kvsel_perturbation per layer."""
+    import numpy as np
+    import torch
+
+    H, G, W, n, d, D = wl.h_kv, wl.group, wl.window, wl.n_ctx, wl.head_dim, wl.d_model
+    pw = B.params_from_workload(wl)
+    wsz = max(B.kvsel_perturbation_workspace_size(pw), B.kvsel_workspace_size(pw))
+    pws = torch.zeros(wsz // 4 + 64, dtype=torch.int32, device=dev)
+    B.kvsel_workspace_init(pws)
+    out = torch.empty((1, H, 3, G, W), dtype=torch.float32, device=dev)
+    res, times = {}, []
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for name, va in (("value_aware", True), ("attention_only", False)):
+        p = B.params_from_workload(wl, value_aware=va)
+        acc = []
+        for i in range(min(layers, len(q_d))):
+            b = bufs[i]
+            B.kvsel_run_layer(p, q_d[i], kvs[i], w_d[i] if va else None, b.s_attn, b.s_val, b.idx, b.counts,
+                              b.offsets, b.k_out, b.v_out, pws, stream)
+            t0.record(stream)
+            B.kvsel_perturbation(pw, q_d[i], kvs[i], w_d[i], b.idx, b.counts, b.offsets, out, pws, stream)
+            t1.record(stream)
+            torch.cuda.synchronize()
+            times.append(t0.elapsed_time(t1))
+            acc.append(out.cpu().numpy()[0])
+        a = np.stack(acc)                                  # [layers][H][3][G][W]
+        res[name] = {"actual": float(a[:, :, 0].mean()), "bound": float(a[:, :, 1].mean()),
+                     "relaxed_bound": float(a[:, :, 2].mean())}
+    res["bound_ratio_value_aware_vs_attention_only_relaxed"] = (res["value_aware"]["bound"] /
+                                                               res["attention_only"]["relaxed_bound"])
+    ms = float(np.median(times[1:])) if len(times) > 1 else times[0]
+    # tensor work per layer: the value-norm GEMM once per group member (2 n D d per member
+    # and head), two logit passes and the weighted value sums (high and low weight parts)
+    flops = H * (G * 2.0 * n * D * d + 2 * 2.0 * G * W * n * d + 2 * 2.0 * G * W * n * d)
+    tc = pk.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+    res.update({"what": "CriticalKV Table 9 on the stack's synthetic layers (budget 40% per KV head): mean "
+                        "||o - ô||_1 of the window queries through each query head's W_O slice, the bound "
+                        "C - (2 - 1/a) P and the relaxed bound 2 (1 - a) max ||v'||_1",
+                "layers": min(layers, len(q_d)), "ms_per_layer": ms, "tensor_flops_per_layer": flops,
+                "achieved_tflops": flops / (ms * 1e-3) / 1e12,
+                "tensor_frac": flops / (ms * 1e-3) / 1e12 / tc})
+    return res
+
+
 def main():
     args = parse()
     if args.impl == "reference":
@@ -554,6 +602,8 @@ def main():
     # projection of every key and value (kvsel_run_anchors)
     if not args.no_plain:
         out["anchor_path"] = time_anchor_path(B, datagen, wl, q_d, kvs, ws, stream, K, W, L, world, pk, dev)
+        # ---- output perturbation of the kept sets (CriticalKV Table 9 on synthetic data)
+        out["perturbation"] = perturbation_table(B, wl, q_d, kvs, w_d, bufs, stream, dev, pk)
 
     # ---- end to end through the public API: pinned host -> device each step, results back
     if not args.no_e2e:
