@@ -3,6 +3,7 @@
     python -m kv_cache_eviction_window_gb300.profile_case --workload 2 --layers 2 --steps 2
     python -m kv_cache_eviction_window_gb300.profile_case --workload 2 --value-norm l2
     python -m kv_cache_eviction_window_gb300.profile_case --workload 6      # AnchorKV anchors
+    python -m kv_cache_eviction_window_gb300.profile_case --workload 2 --perturb   # + output perturbation
 
 The inputs are the same seeded synthetic tensors as the benchmark (each layer distinct,
 larger than L2 for the 32K stack), so per-launch counters taken here scale to the
@@ -26,6 +27,7 @@ def main():
     ap.add_argument("--steps", type=int, default=2)
     ap.add_argument("--plain", action="store_true", help="value_aware=0")
     ap.add_argument("--value-norm", default=None, choices=["l1", "l2"], help="value-aware norm override")
+    ap.add_argument("--perturb", action="store_true", help="also run kvsel_perturbation on each layer's kept set")
     args = ap.parse_args()
     import numpy as np
     import torch
@@ -48,6 +50,7 @@ def main():
         return torch.from_numpy(np.ascontiguousarray(u16).view(np.int16)).view(torch.bfloat16).to(dev)
 
     layers = []
+    x_w = {}   # W_O per layer for the perturbation (also when the scoring is not value-aware)
     for layer in range(args.layers):
         x = datagen.make_layer(wl, layer)
         lens = x["n_ctx"]
@@ -66,7 +69,9 @@ def main():
         w = to_dev(x["w_o"]) if wl.value_aware else None
         if anchors:   # the random keys of the anchor draw ride in the weight slot
             w = torch.from_numpy(np.concatenate([r.reshape(-1) for r in x["rand"]])).to(dev)
-        layers.append((p, q, kv, w, B.LayerBuffers(p, device=dev), keep))
+        buf = B.LayerBuffers(p, device=dev)
+        x_w[id(buf)] = to_dev(x["w_o"]) if x["w_o"] is not None else None
+        layers.append((p, q, kv, w, buf, keep))
     nst = len(B.STAGES)
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * nst)]
     for e in ev:
@@ -84,6 +89,13 @@ def main():
             else:
                 B.kvsel_run_layer(p, q, kv, w, b.s_attn, b.s_val, b.idx, b.counts, b.offsets, b.k_out, b.v_out,
                                   b.ws)
+            if args.perturb:
+                if not hasattr(b, "pt_out"):
+                    b.pt_out = torch.empty((1, wl.h_kv, 3, wl.group, wl.window), dtype=torch.float32, device=dev)
+                    b.pt_ws = torch.zeros(B.kvsel_perturbation_workspace_size(p) // 4 + 64, dtype=torch.int32,
+                                          device=dev)
+                    B.kvsel_workspace_init(b.pt_ws)
+                B.kvsel_perturbation(p, q, kv, x_w[id(b)], b.idx, b.counts, b.offsets, b.pt_out, b.pt_ws)
             B.kvsel_set_stage_events(None)
             torch.cuda.synchronize()
             for i in range(nst):
