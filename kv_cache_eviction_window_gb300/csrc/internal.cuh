@@ -134,12 +134,12 @@ struct VgramArgs {
   float* nu;                      // packed [sum_b H*n_b]
   WaitCtl wc;
 };
-// Dw-slices of the Gram partials (workspace: H * slices * 128 * 128 fp32).
+// Row slices of the Gram partials (workspace: H * slices * 128 * 128 fp32).
 int gram_slices(int Dw);
-// W_h^T (wt: [H][d][D] bf16), Gamma partials (part), Gamma hi/lo (gam: [H][2][d][d] bf16).
-// twt: 2-D map over wt (D, H*d rows), box 64 x 128.
-cudaError_t launch_value_gram(const uint16_t* w_o, uint16_t* wt, float* part, uint16_t* gam, int H, int G, int D,
-                              const CUtensorMap& twt, WaitCtl wc, cudaStream_t st);
+// Gamma partials (part) straight from W_O, then Gamma hi/lo (gam: [H][2][d][d] bf16).
+// two: 2-D map over W_O (H*G*d columns, D rows), box 64 x 64, 128-byte swizzle.  G <= 8.
+cudaError_t launch_value_gram(const CUtensorMap& two, float* part, uint16_t* gam, int H, int G, int D, WaitCtl wc,
+                              cudaStream_t st);
 // tv: V tiles of 128 tokens (kv_map); tg: 2-D map over gam (d, H*2*d rows), box 64 x 128.
 cudaError_t launch_vgram(const VgramArgs& a, const CUtensorMap& tv, const CUtensorMap& tg, cudaStream_t st);
 

@@ -123,6 +123,7 @@ int make_plan(const kvsel_params* p, Plan& pl, bool need_device) {
     if (p->value_norm != KVSEL_NORM_L1 && p->value_norm != KVSEL_NORM_L2) return KVSEL_EINVAL;
     // the Gram identity holds for one projection per token: the group-sum reading only
     if (p->value_norm == KVSEL_NORM_L2 && p->wo_mode != KVSEL_WO_GROUP_SUM) return KVSEL_EUNSUPPORTED;
+    if (p->value_norm == KVSEL_NORM_L2 && p->group > 8) return KVSEL_EUNSUPPORTED;   // Gram staging fits G <= 8
     pl.l2 = p->value_norm == KVSEL_NORM_L2;
   }
   pl.B = p->batch;
@@ -285,8 +286,10 @@ int make_plan(const kvsel_params* p, Plan& pl, bool need_device) {
   if (p->value_aware) {
     pl.ws_nu = off;
     off = align256(off + static_cast<size_t>(pl.n_scores) * sizeof(float));
-    pl.ws_wbar = off;   // W_h (L1) or W_h^T (L2), same size
-    off = align256(off + static_cast<size_t>(pl.H) * pl.Dw * kHeadDim * 2);
+    if (!pl.l2) {
+      pl.ws_wbar = off;   // W_h (the L1 path; the L2 path never materialises it)
+      off = align256(off + static_cast<size_t>(pl.H) * pl.Dw * kHeadDim * 2);
+    }
     if (pl.l2) {
       pl.ws_gpart = off;
       off = align256(off + static_cast<size_t>(pl.H) * gram_slices(pl.Dw) * kHeadDim * kHeadDim * sizeof(float));
@@ -484,15 +487,14 @@ int do_score(const kvsel_params* p, const Plan& pl, const void* q, const kvsel_k
   if (p->value_aware && pl.l2) {
     // nu = ||W_h v||_2 = sqrt(v^T Gamma_h v) with Gamma_h = W_h^T W_h (d x d)
     nu = reinterpret_cast<float*>(wsb + pl.ws_nu);
-    uint16_t* wt = reinterpret_cast<uint16_t*>(wsb + pl.ws_wbar);
     float* gpart = reinterpret_cast<float*>(wsb + pl.ws_gpart);
     uint16_t* gam = reinterpret_cast<uint16_t*>(wsb + pl.ws_gam);
-    CUtensorMap twt, tg, tv;
+    CUtensorMap two, tg, tv;
     {
-      const cuuint64_t dims[2] = {static_cast<cuuint64_t>(pl.Dw), static_cast<cuuint64_t>(pl.H) * kHeadDim};
-      const cuuint64_t strides[1] = {static_cast<cuuint64_t>(pl.Dw) * 2};
-      const cuuint32_t box[2] = {64, 128};
-      if (!encode(&twt, wt, 2, dims, strides, box)) return KVSEL_EINVAL;
+      const cuuint64_t dims[2] = {static_cast<cuuint64_t>(pl.H) * pl.G * kHeadDim, static_cast<cuuint64_t>(pl.D)};
+      const cuuint64_t strides[1] = {static_cast<cuuint64_t>(pl.H) * pl.G * kHeadDim * 2};
+      const cuuint32_t box[2] = {64, 64};
+      if (!encode(&two, w_o, 2, dims, strides, box)) return KVSEL_EINVAL;
     }
     {
       const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(pl.H) * 2 * kHeadDim};
@@ -503,8 +505,7 @@ int do_score(const kvsel_params* p, const Plan& pl, const void* q, const kvsel_k
     if (!kv_map(&tv, kv->v, kv, pl, kv->layout == KVSEL_LAYOUT_PAGED ? 0 : 128)) return KVSEL_EINVAL;
     {
       StageScope sc(KVSEL_STAGE_WBAR, st);
-      rc = launch_rc(launch_value_gram(static_cast<const uint16_t*>(w_o), wt, gpart, gam, pl.H, pl.G, pl.D, twt,
-                                       wait_ctl(ws), st));
+      rc = launch_rc(launch_value_gram(two, gpart, gam, pl.H, pl.G, pl.D, wait_ctl(ws), st));
     }
     if (rc) return rc;
     VgramArgs v{};

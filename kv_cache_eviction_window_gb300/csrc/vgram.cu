@@ -5,11 +5,11 @@
 // ||W_h v||_2^2 = v^T (W_h^T W_h) v, so with the d x d Gram matrix Gamma_h = W_h^T W_h the
 // per-token cost drops from 2*D*d to 2*d*d flop (D / d = 32x for a 4096-wide model):
 //
-//   wbar_t_kernel:     W_h^T [H][d][Dw] bf16: the group sum of the W_O slices in fp32,
-//                      rounded once (the same values wbar_kernel writes), transposed
-//                      through shared memory.
-//   gram_kernel:       Gamma_h partials over K slices of Dw on tcgen05 (A = B = a W_h^T
-//                      tile, M = N = 128), fp32 to the workspace.
+//   gram_fused_kernel: Gamma_h partials straight from W_O: per 256-row slice, the group
+//                      sum of the W_O columns of head h in fp32 (the same values wbar_kernel
+//                      rounds), rounded once to bf16 and transposed in shared memory into
+//                      a K-major operand, then A = B = that operand on tcgen05 (M = N =
+//                      128, K = 64 per batch); W_h^T is never written to memory.
 //   gram_finish_kernel: Gamma_h = sum of the partials (fixed order), split into a bf16 high
 //                      part and a bf16 remainder so the tensor cores see it to ~2^-16.
 //   vgram_kernel:      persistent: per 128-token tile, Y = V (Gamma_hi + Gamma_lo) on tcgen05
@@ -21,80 +21,52 @@
 namespace kvsel {
 namespace {
 
-constexpr int kGramSliceMax = 512;          // Dw elements per gram_kernel CTA
-constexpr int kGramChunk = 64;              // K elements per 128-byte swizzle atom column
-constexpr int kGramChunkBytes = 128 * 128;  // 128 rows x 128 B
 
 // ------------------------------------------------------------------------------------
-// W_h^T from W_O
+// Gamma partials straight from W_O (group sum, transpose and W^T W in one kernel)
 // ------------------------------------------------------------------------------------
-// Block (64-row block of W_h, head h): the G slices of 64 rows x 128 columns are summed in
-// fp32 into shared memory, then written column-major as 128 rows of 64 bf16.
-__global__ void __launch_bounds__(256) wbar_t_kernel(const uint16_t* __restrict__ w_o, uint16_t* __restrict__ wt,
-                                                      int H, int G, int D) {
-  __shared__ float tile[64][129];
-  const int h = blockIdx.y, j0 = blockIdx.x * 64;
-  const long long row_len = static_cast<long long>(H) * G * kHeadDim;
-  for (int item = threadIdx.x; item < 64 * 16; item += 256) {
-    const int r = item / 16, c8 = item % 16, j = j0 + r;
-    float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-    if (j < D) {
-      const uint16_t* src = w_o + j * row_len + static_cast<long long>(h) * G * kHeadDim + c8 * 8;
-      for (int g = 0; g < G; ++g) {
-        const uint4 p = __ldg(reinterpret_cast<const uint4*>(src + g * kHeadDim));
-        const uint32_t w[4] = {p.x, p.y, p.z, p.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          acc[2 * e] += __uint_as_float(w[e] << 16);
-          acc[2 * e + 1] += __uint_as_float(w[e] & 0xFFFF0000u);
-        }
-      }
-    }
-#pragma unroll
-    for (int e = 0; e < 8; ++e) tile[r][c8 * 8 + e] = acc[e];
-  }
-  __syncthreads();
-  // thread t writes column c = t / 2, rows [32 * (t % 2), +32): four 16-byte stores
-  const int c = threadIdx.x / 2, half = threadIdx.x % 2;
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const int r0 = half * 32 + q * 8;
-    if (j0 + r0 >= D) break;
-    uint32_t o[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const __nv_bfloat162 v2 = __floats2bfloat162_rn(tile[r0 + 2 * e][c], tile[r0 + 2 * e + 1][c]);
-      o[e] = *reinterpret_cast<const uint32_t*>(&v2);
-    }
-    *reinterpret_cast<uint4*>(wt + (static_cast<long long>(h) * kHeadDim + c) * D + j0 + r0) =
-        make_uint4(o[0], o[1], o[2], o[3]);
-  }
-}
+// Block (slice s, head h): rows [s * 256, s * 256 + 256) of W_O in batches of 64.  Per
+// batch the G column slices of head h arrive by TMA (128-byte swizzle); eight worker warps
+// sum them in fp32 into a padded tile [64 rows j][129], then write it transposed and
+// rounded to bf16 as a K-major operand [128 columns c][64 j]; one thread issues
+// D[c][c'] += sum_j A[c][j] A[c'][j] (four K = 16 UMMAs).  W_h^T never reaches memory.
+constexpr int kGfRows = 256;                 // W_O rows per CTA
+constexpr int kGfBatch = 64;                 // rows per batch (UMMA K per batch)
+constexpr int kGfWorkers = 256;
+constexpr int kGfThreads = kGfWorkers + 32;
+constexpr int kGfBox = kGfBatch * 128;       // one TMA box: 64 rows x 64 columns bf16
+constexpr int kGfA = 128 * 128;              // operand: 128 rows c x 64 j bf16 (128 B rows)
+constexpr int kGfTileStride = 129;           // fp32 tile row stride (conflict-free transposes)
 
-// ------------------------------------------------------------------------------------
-// Gamma partials
-// ------------------------------------------------------------------------------------
-// Block (slice s, head h): W_h^T[:, s*slice : (s+1)*slice] arrives as 64-element chunks
-// (TMA, 128-byte swizzle); D[m][n] = sum_k Wt[m][k] Wt[n][k] accumulates in TMEM; four
-// epilogue warps write the 128 x 128 fp32 partial.  Warp 4 allocates TMEM and issues.
-__global__ void __launch_bounds__(160, 1) gram_kernel(const __grid_constant__ CUtensorMap twt, float* part,
-                                                      int D, int slice, WaitCtl wc) {
+__device__ __forceinline__ void gf_bar() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+
+__global__ void __launch_bounds__(kGfThreads, 1)
+    gram_fused_kernel(const __grid_constant__ CUtensorMap two, float* part, int G, int D, int raw_stages, WaitCtl wc) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_align1024(smem_raw);
-  __shared__ __align__(8) uint64_t full_bar, done_bar;
+  const int raw_bytes = G * 2 * kGfBox;                  // one batch: G slices x 2 column halves
+  uint8_t* sRaw = smem;                                  // [raw_stages][G][2][64 rows][128 B]
+  uint8_t* sA = smem + raw_stages * raw_bytes;           // [2][128 c][128 B]
+  float* ft = reinterpret_cast<float*>(sA + 2 * kGfA);   // [64][129] fp32
+  __shared__ __align__(8) uint64_t rfull[2], rempty[2], afull[2], aempty[2], done_bar;
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
   const int warp = warp_id(), lane = lane_id();
   const int s = blockIdx.x, h = blockIdx.y;
-  const int k0 = s * slice;
-  const int nchunks = (min(slice, D - k0) + kGramChunk - 1) / kGramChunk;
+  const int row0 = s * kGfRows;
+  const int nb = min(kGfRows, D - row0) > 0 ? (min(kGfRows, D - row0) + kGfBatch - 1) / kGfBatch : 0;
   if (threadIdx.x == 0) {
-    mbar_init(&full_bar, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&rfull[i], 1);
+      mbar_init(&rempty[i], kGfWorkers / 32);
+      mbar_init(&afull[i], kGfWorkers / 32);
+      mbar_init(&aempty[i], 1);
+    }
     mbar_init(&done_bar, 1);
     s_abort = 0;
     fence_mbar_init();
   }
-  if (warp == 4) {
+  if (warp == 8) {
     tmem_alloc(&s_tmem, 128);
     tmem_relinquish();
   }
@@ -102,43 +74,119 @@ __global__ void __launch_bounds__(160, 1) gram_kernel(const __grid_constant__ CU
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = s_tmem;
-  if (warp == 4) {
-    if (lane == 0) {
-      tma_prefetch_desc(&twt);
-      mbar_arrive_expect_tx(&full_bar, nchunks * kGramChunkBytes);
-      for (int c = 0; c < nchunks; ++c) tma_load_2d(smem + c * kGramChunkBytes, &twt, &full_bar, k0 + c * kGramChunk, h * 128);
-      if (mbar_wait(&full_bar, 0, &s_abort, wc)) {
-        tc_fence_after();
-        constexpr uint32_t idesc = idesc_bf16_f32(128, 128);
-        for (int c = 0; c < nchunks; ++c) {
-          const uint64_t desc = sdesc_kmajor_sw128(smem_u32(smem + c * kGramChunkBytes));
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            umma_bf16(tbase, desc + ((k * 32) >> 4), desc + ((k * 32) >> 4), idesc, (c | k) ? 1u : 0u);
+
+  if (warp == 8) {
+    if (lane == 0 && nb > 0) {
+      tma_prefetch_desc(&two);
+      constexpr uint32_t idesc = idesc_bf16_f32(128, 128);
+      // the producer runs ahead by raw_stages batches; the MMA of batch t follows the
+      // workers' transpose of batch t
+      int issued = 0;
+      auto load = [&](int t) -> bool {
+        const int rs = t % raw_stages;
+        if (t >= raw_stages && !mbar_wait(&rempty[rs], ((t / raw_stages) & 1) ^ 1, &s_abort, wc)) return false;
+        mbar_arrive_expect_tx(&rfull[rs], raw_bytes);
+        uint8_t* dst = sRaw + rs * raw_bytes;
+        for (int g = 0; g < G; ++g)
+          for (int x = 0; x < 2; ++x)
+            tma_load_2d(dst + (g * 2 + x) * kGfBox, &two, &rfull[rs], (h * G + g) * 128 + x * 64, row0 + t * kGfBatch);
+        return true;
+      };
+      bool ok = true;
+      for (; ok && issued < min(nb, raw_stages); ++issued) ok = load(issued);
+      for (int t = 0; ok && t < nb; ++t) {
+        const int as = t & 1;
+        if (!mbar_wait(&afull[as], (t >> 1) & 1, &s_abort, wc)) {
+          ok = false;
+          break;
         }
-      } else {
-        mbar_drain(&full_bar, 0, wc.status);
-      }
-      umma_commit(&done_bar);
-    }
-    __syncwarp();
-  } else {
-    const bool ok = __all_sync(0xffffffffu, mbar_wait(&done_bar, 0, &s_abort, wc));
-    tc_fence_after();
-    if (ok) {
-      float* dst = part + ((static_cast<size_t>(h) * gridDim.x + s) * 128 + warp * 32 + lane) * 128;
-      for (int c0 = 0; c0 < 128; c0 += 32) {
-        float v[32];
-        tmem_ld32(tbase + (static_cast<uint32_t>(warp * 32) << 16) + c0, v);
-        tmem_ld_wait();
+        tc_fence_after();
+        const uint64_t adesc = sdesc_kmajor_sw128(smem_u32(sA + as * kGfA));
 #pragma unroll
-        for (int j = 0; j < 32; j += 4) *reinterpret_cast<float4*>(dst + c0 + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+        for (int k = 0; k < 4; ++k) umma_bf16(tbase, adesc + ((k * 32) >> 4), adesc + ((k * 32) >> 4), idesc, (t | k) ? 1u : 0u);
+        umma_commit(&aempty[as]);
+        if (issued < nb) ok = load(issued++);
+      }
+      // drain copies still in flight
+      for (int t = max(0, issued - raw_stages); t < issued; ++t) mbar_drain(&rfull[t % raw_stages], (t / raw_stages) & 1, wc.status);
+      umma_commit(&done_bar);
+      mbar_drain(&done_bar, 0, wc.status);
+    }
+  } else {
+    const int tid = threadIdx.x;
+    bool ok = true;
+    for (int t = 0; t < nb; ++t) {
+      const int rs = t % raw_stages, as = t & 1;
+      ok = __all_sync(0xffffffffu, ok && mbar_wait(&rfull[rs], (t / raw_stages) & 1, &s_abort, wc));
+      const uint8_t* raw = sRaw + rs * raw_bytes;
+      if (ok) {
+        // step 1: thread (row j = lane + 32 * (warp & 1), 16-byte chunk q) sums the G slices
+        for (int it = 0; it < 4; ++it) {
+          const int j = lane + 32 * (warp & 1);
+          const int q = (warp >> 1) + 4 * it;   // 0..15: column chunk of 8
+          float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+          for (int g = 0; g < G; ++g) {
+            const uint8_t* box = raw + (g * 2 + (q >> 3)) * kGfBox;
+            const uint4 p = *reinterpret_cast<const uint4*>(box + j * 128 + (((q & 7) ^ (j & 7)) << 4));
+            const uint32_t w4[4] = {p.x, p.y, p.z, p.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              acc[2 * e] += __uint_as_float(w4[e] << 16);
+              acc[2 * e + 1] += __uint_as_float(w4[e] & 0xFFFF0000u);
+            }
+          }
+#pragma unroll
+          for (int e = 0; e < 8; ++e) ft[j * kGfTileStride + q * 8 + e] = acc[e];
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&rempty[rs]);   // the raw stage may be refilled
+      gf_bar();                                   // the fp32 tile is complete
+      // the operand buffer was last read by the UMMAs of batch t - 2
+      if (t >= 2) ok = __all_sync(0xffffffffu, ok && mbar_wait(&aempty[as], ((t >> 1) & 1) ^ 1, &s_abort, wc));
+      if (ok) {
+        // step 2: thread (column c = tid & 127, 8-row chunk jc) writes 8 rounded values of
+        // row c of the K-major operand
+        for (int it = 0; it < 4; ++it) {
+          const int c = tid & 127;
+          const int jc = (tid >> 7) + 2 * it;   // 0..7
+          uint32_t o[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const __nv_bfloat162 v2 = __floats2bfloat162_rn(ft[(jc * 8 + 2 * e) * kGfTileStride + c],
+                                                            ft[(jc * 8 + 2 * e + 1) * kGfTileStride + c]);
+            o[e] = *reinterpret_cast<const uint32_t*>(&v2);
+          }
+          *reinterpret_cast<uint4*>(sA + as * kGfA + c * 128 + ((jc ^ (c & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&afull[as]);
+      gf_bar();                                   // the fp32 tile may be overwritten
+    }
+    // epilogue: warps 0-3 own the accumulator's lanes
+    if (warp < 4) {
+      ok = __all_sync(0xffffffffu, ok && nb > 0 && mbar_wait(&done_bar, 0, &s_abort, wc));
+      tc_fence_after();
+      if (ok) {
+        float* dst = part + ((static_cast<size_t>(h) * gridDim.x + s) * 128 + warp * 32 + lane) * 128;
+        for (int c0 = 0; c0 < 128; c0 += 32) {
+          float v[32];
+          tmem_ld32(tbase + (static_cast<uint32_t>(warp * 32) << 16) + c0, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 32; j += 4) *reinterpret_cast<float4*>(dst + c0 + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+        }
+      } else if (nb == 0) {
+        float* dst = part + ((static_cast<size_t>(h) * gridDim.x + s) * 128 + warp * 32 + lane) * 128;
+        for (int c0 = 0; c0 < 128; ++c0) dst[c0] = 0.f;
       }
     }
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 4) {
+  if (warp == 8) {
     tc_fence_after();
     tmem_dealloc(tbase, 128);
   }
@@ -150,8 +198,18 @@ __global__ void __launch_bounds__(256) gram_finish_kernel(const float* __restric
                                                           int S) {
   const int h = blockIdx.y;
   for (int e = blockIdx.x * 256 + threadIdx.x; e < 128 * 128; e += gridDim.x * 256) {
+    // eight partials loaded before they are added (in order), so the loads overlap
+    const float* src = part + static_cast<size_t>(h) * S * 128 * 128 + e;
     float g = 0.f;
-    for (int s = 0; s < S; ++s) g += part[(static_cast<size_t>(h) * S + s) * 128 * 128 + e];
+    int s = 0;
+    for (; s + 8 <= S; s += 8) {
+      float v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) v[u] = __ldg(src + static_cast<size_t>(s + u) * 128 * 128);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) g += v[u];
+    }
+    for (; s < S; ++s) g += __ldg(src + static_cast<size_t>(s) * 128 * 128);
     const __nv_bfloat16 hi = __float2bfloat16_rn(g);
     const __nv_bfloat16 lo = __float2bfloat16_rn(g - __bfloat162float(hi));
     gam[(static_cast<size_t>(h) * 2 + 0) * 128 * 128 + e] = *reinterpret_cast<const uint16_t*>(&hi);
@@ -347,25 +405,20 @@ __global__ void __launch_bounds__(kVgThreads, 1)
 
 }  // namespace
 
-// Slices of Dw per head: kGramSliceMax elements each (a multiple of the 64-element chunk,
-// so the slices tile Dw without overlap; the last one reads zeros past Dw).
-int gram_slices(int Dw) { return (Dw + kGramSliceMax - 1) / kGramSliceMax; }
+// Slices of W_O rows per head in the Gamma partials: one per 256 rows.
+int gram_slices(int Dw) { return (Dw + kGfRows - 1) / kGfRows; }
 
-cudaError_t launch_value_gram(const uint16_t* w_o, uint16_t* wt, float* part, uint16_t* gam, int H, int G, int D,
-                              const CUtensorMap& twt, WaitCtl wc, cudaStream_t st) {
-  wbar_t_kernel<<<dim3((D + 63) / 64, H), 256, 0, st>>>(w_o, wt, H, G, D);
-  note_launch();
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+cudaError_t launch_value_gram(const CUtensorMap& two, float* part, uint16_t* gam, int H, int G, int D, WaitCtl wc,
+                              cudaStream_t st) {
   const int S = gram_slices(D);
-  const int slice = kGramSliceMax;
-  const size_t smem = 1024 + static_cast<size_t>((slice + kGramChunk - 1) / kGramChunk) * kGramChunkBytes;
-  e = ensure_smem(reinterpret_cast<const void*>(gram_kernel), smem);
+  const int raw_stages = G <= 4 ? 2 : 1;
+  const size_t smem = 1024 + static_cast<size_t>(raw_stages) * G * 2 * kGfBox + 2 * kGfA +
+                      static_cast<size_t>(kGfBatch) * kGfTileStride * sizeof(float);
+  cudaError_t e = ensure_smem(reinterpret_cast<const void*>(gram_fused_kernel), smem);
   if (e != cudaSuccess) return e;
-  gram_kernel<<<dim3(S, H), 160, smem, st>>>(twt, part, D, slice, wc);
+  gram_fused_kernel<<<dim3(S, H), kGfThreads, smem, st>>>(two, part, G, D, raw_stages, wc);
   note_launch();
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
   gram_finish_kernel<<<dim3(64, H), 256, 0, st>>>(part, gam, S);
   note_launch();
   return cudaGetLastError();
