@@ -336,6 +336,57 @@ def time_anchor_path(B, datagen, wl_stack, q_d, kvs, ws, stream, K, W, L, world,
                            "tensor_frac": pflops / (pms * 1e-3) / 1e12 / tc}}
 
 
+def time_query_agnostic(B, datagen, stream, dev, pk, K, W):
+    """KVzip's query-agnostic scoring on the Llama-3.1-70B 32K layer shape (all G*n = 262144
+    positions of a KV head as queries, non-causal): the softmax score (row log-sum-exp
+    pass, then the per-key max pass) and the softmax-free KVzip-logit score (one pass),
+    each through kvsel_score, then the whole call with the per-layer budget."""
+    import numpy as np
+    import torch
+
+    wl = datagen.WORKLOADS[5]
+    H, G, n, d = wl.h_kv, wl.group, wl.n_ctx, wl.head_dim
+    inp = datagen.make_layer(wl, 0)
+
+    def to_dev(u16):
+        return torch.from_numpy(np.ascontiguousarray(u16).view(np.int16)).view(torch.bfloat16).to(dev)
+
+    q = to_dev(inp["q"])
+    kt, vt = to_dev(np.stack(inp["k"])), to_dev(np.stack(inp["v"]))
+    kv = B.make_kv_contiguous(kt, vt)
+    tc = pk.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+    res = {"workload": wl.name, "what": "KVzip query-agnostic scores of one layer (H 8, G 8, n 32768), "
+                                        "kvsel_score alone (tensor roofline) and kvsel_run_layer "
+                                        "(score + per-layer top-30% + compact)"}
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for name, red, passes in (("softmax", "max", 2), ("logit", "max_logit", 1)):
+        p = B.params_from_workload(wl, reduce=red)
+        b = B.LayerBuffers(p, device=dev)
+
+        def timed(fn):
+            for _ in range(W):
+                fn()
+            torch.cuda.synchronize()
+            t0.record(stream)
+            for _ in range(K):
+                fn()
+            t1.record(stream)
+            torch.cuda.synchronize()
+            return t0.elapsed_time(t1) / K
+
+        ms_score = timed(lambda: B.kvsel_score(p, q, kv, None, b.s_attn, None, b.ws, stream))
+        ms_layer = timed(lambda: B.kvsel_run_layer(p, q, kv, None, b.s_attn, None, b.idx, b.counts, b.offsets,
+                                                    b.k_out, b.v_out, b.ws, stream))
+        flops = passes * 2.0 * G * n * n * d * H
+        res[name] = {"score_ms": ms_score, "layer_ms": ms_layer, "score_tflops": flops / (ms_score * 1e-3) / 1e12,
+                     "tensor_frac": flops / (ms_score * 1e-3) / 1e12 / tc, "flops": flops,
+                     "entries_per_s": H * n / (ms_layer * 1e-3), "device_status": B.kvsel_get_device_status(b.ws)}
+        del b
+    del q, kt, vt
+    torch.cuda.empty_cache()
+    return res
+
+
 def perturbation_table(B, wl, q_d, kvs, w_d, bufs, stream, dev, pk, layers=4):
     """CriticalKV Table 9 on synthetic layers: the actual output perturbation of the window
     queries and both bounds, averaged over rows, heads and the first `layers` layers, for the
@@ -609,6 +660,8 @@ def main():
         out["anchor_path"] = time_anchor_path(B, datagen, wl, q_d, kvs, ws, stream, K, W, L, world, pk, dev)
         # ---- output perturbation of the kept sets (CriticalKV Table 9 on synthetic data)
         out["perturbation"] = perturbation_table(B, wl, q_d, kvs, w_d, bufs, stream, dev, pk)
+        # ---- KVzip query-agnostic scoring (softmax and softmax-free) on its own layer shape
+        out["query_agnostic_path"] = time_query_agnostic(B, datagen, stream, dev, pk, max(K // 2, 2), W)
 
     # ---- end to end through the public API: pinned host -> device each step, results back
     if not args.no_e2e:
