@@ -124,15 +124,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(&full_bar[s], u & 1, &s_abort, a.wc)) break;
         if (!mbar_wait(&acce_bar[acc], (ua & 1) ^ 1, &s_abort, a.wc)) break;
         tc_fence_after();
-        const uint32_t kb = smem_u32(sK + s * kTile);
-        const uint32_t qb = smem_u32(sQ);
+        // descriptors: the tile bases once, then byte offsets added to the address field
+        const uint64_t kd0 = sdesc_kmajor_sw128(smem_u32(sK + s * kTile));
+        const uint64_t qd0 = sdesc_kmajor_sw128(smem_u32(sQ));
 #pragma unroll
         for (int mt = 0; mt < kMT; ++mt) {
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
             const uint32_t koff = (k & 3) * 32;
-            const uint64_t da = sdesc_kmajor_sw128(qb + (k >> 2) * kBlockHalf + mt * 16384 + koff);
-            const uint64_t db = sdesc_kmajor_sw128(kb + (k >> 2) * (kNT * 128) + koff);
+            const uint64_t da = qd0 + (((k >> 2) * kBlockHalf + mt * 16384 + koff) >> 4);
+            const uint64_t db = kd0 + (((k >> 2) * (kNT * 128) + koff) >> 4);
             umma_bf16(tbase + acc * kAccCols + mt * kNT, da, db, idesc, k > 0 ? 1u : 0u);
           }
         }
@@ -301,15 +302,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(&full_bar[s], u & 1, &s_abort, a.wc)) break;
         if (!mbar_wait(&acce_bar[acc], (ua & 1) ^ 1, &s_abort, a.wc)) break;
         tc_fence_after();
-        const uint32_t kbase = smem_u32(sK);
-        const uint32_t qbase = smem_u32(sQ + s * kTile);
+        const uint64_t kd0 = sdesc_kmajor_sw128(smem_u32(sK));
+        const uint64_t qd0 = sdesc_kmajor_sw128(smem_u32(sQ + s * kTile));
 #pragma unroll
         for (int mt = 0; mt < kMT; ++mt) {
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
             const uint32_t koff = (k & 3) * 32;
-            const uint64_t da = sdesc_kmajor_sw128(kbase + mt * 32768 + (k >> 2) * 16384 + koff);
-            const uint64_t db = sdesc_kmajor_sw128(qbase + (k >> 2) * (kNT * 128) + koff);
+            const uint64_t da = kd0 + ((mt * 32768 + (k >> 2) * 16384 + koff) >> 4);
+            const uint64_t db = qd0 + (((k >> 2) * (kNT * 128) + koff) >> 4);
             umma_bf16(tbase + acc * kAccCols + mt * kNT, da, db, idesc, k > 0 ? 1u : 0u);
           }
         }

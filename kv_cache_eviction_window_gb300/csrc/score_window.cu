@@ -185,15 +185,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(&full_bar[s], u & 1, &s_abort, a.wc)) break;
         if (!mbar_wait(&acce_bar[acc], (ua & 1) ^ 1, &s_abort, a.wc)) break;
         tc_fence_after();
-        const uint32_t kbase = smem_u32(sK + s * kKStage);
-        const uint32_t qbase = smem_u32(sQ);
+        // descriptors: the tile bases once, then byte offsets added to the address field
+        const uint64_t kd0 = sdesc_kmajor_sw128(smem_u32(sK + s * kKStage));
+        const uint64_t qd0 = sdesc_kmajor_sw128(smem_u32(sQ));
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
             const uint32_t koff = (k & 3) * 32;
-            const uint64_t da = sdesc_kmajor_sw128(qbase + (k >> 2) * kQHalf + mt * 16384 + koff);
-            const uint64_t db = sdesc_kmajor_sw128(kbase + (k >> 2) * (NT * 128) + koff);
+            const uint64_t da = qd0 + (((k >> 2) * kQHalf + mt * 16384 + koff) >> 4);
+            const uint64_t db = kd0 + (((k >> 2) * (NT * 128) + koff) >> 4);
             umma_bf16(tbase + acc * kAccCols + mt * NT, da, db, idesc, k > 0 ? 1u : 0u);
           }
         }
@@ -366,16 +367,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(&full_bar[s], u & 1, &s_abort, a.wc)) break;
         if (!mbar_wait(&acce_bar[acc], (ua & 1) ^ 1, &s_abort, a.wc)) break;
         tc_fence_after();
-        const uint32_t kbase = smem_u32(sK + s * kKTileBytes);
-        const uint32_t qbase = smem_u32(sQ);
+        const uint64_t kd0 = sdesc_kmajor_sw128(smem_u32(sK + s * kKTileBytes));
+        const uint64_t qd0 = sdesc_kmajor_sw128(smem_u32(sQ));
         for (int n0 = 0; n0 < R; n0 += 256) {
           const int nc = min(256, R - n0);
           const uint32_t idesc = idesc_bf16_f32(128, nc);
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
             const uint32_t koff = (k & 3) * 32;
-            const uint64_t da = sdesc_kmajor_sw128(kbase + (k >> 2) * (kTileKeys * 128) + koff);
-            const uint64_t db = sdesc_kmajor_sw128(qbase + (k >> 2) * qhalf + n0 * 128 + koff);
+            const uint64_t da = kd0 + (((k >> 2) * (kTileKeys * 128) + koff) >> 4);
+            const uint64_t db = qd0 + (static_cast<uint32_t>((k >> 2) * qhalf + n0 * 128 + koff) >> 4);
             umma_bf16(tbase + acc * RP + n0, da, db, idesc, k > 0 ? 1u : 0u);
           }
         }
@@ -629,7 +630,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
   } else if (warp == kFMmaWarp) {
     if (lane == 0 && ntiles > 0) {
       bool ok = mbar_wait(&q_bar, 0, &s_abort, a.wc);
-      const uint32_t qbase = smem_u32(sQ);
+      const uint64_t qd0 = sdesc_kmajor_sw128(smem_u32(sQ));
       // pass 1: A = window rows, B = keys
       constexpr uint32_t idesc1 = idesc_bf16_f32(128, NT);
       for (int t = 0; ok && t < ntiles; ++t) {
@@ -641,15 +642,14 @@ __global__ void __launch_bounds__(kFThreads, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t kbase = smem_u32(sK + s * kKStage);
+        const uint64_t kd0 = sdesc_kmajor_sw128(smem_u32(sK + s * kKStage));
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
             const uint32_t koff = (k & 3) * 32;
-            umma_bf16(tbase + acc * kAccCols + mt * NT,
-                      sdesc_kmajor_sw128(qbase + (k >> 2) * kQHalf + mt * 16384 + koff),
-                      sdesc_kmajor_sw128(kbase + (k >> 2) * (NT * 128) + koff), idesc1, k > 0 ? 1u : 0u);
+            umma_bf16(tbase + acc * kAccCols + mt * NT, qd0 + (((k >> 2) * kQHalf + mt * 16384 + koff) >> 4),
+                      kd0 + (((k >> 2) * (NT * 128) + koff) >> 4), idesc1, k > 0 ? 1u : 0u);
           }
         }
         umma_commit(&empty_bar[s]);
@@ -678,15 +678,15 @@ __global__ void __launch_bounds__(kFThreads, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t kbase = smem_u32(sK + s * kKStage);
+        const uint64_t kd0 = sdesc_kmajor_sw128(smem_u32(sK + s * kKStage));
         for (int n0 = 0; n0 < R; n0 += 256) {
           const int nc = min(256, R - n0);
           const uint32_t idesc = idesc_bf16_f32(128, nc);
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
             const uint32_t koff = (k & 3) * 32;
-            umma_bf16(tbase + acc * kAccCols + n0, sdesc_kmajor_sw128(kbase + (k >> 2) * (NT * 128) + koff),
-                      sdesc_kmajor_sw128(qbase + (k >> 2) * kQHalf + n0 * 128 + koff), idesc, k > 0 ? 1u : 0u);
+            umma_bf16(tbase + acc * kAccCols + n0, kd0 + (((k >> 2) * (NT * 128) + koff) >> 4),
+                      qd0 + (static_cast<uint32_t>((k >> 2) * kQHalf + n0 * 128 + koff) >> 4), idesc, k > 0 ? 1u : 0u);
           }
         }
         umma_commit(&empty_bar[s]);
