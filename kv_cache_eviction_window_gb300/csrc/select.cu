@@ -60,6 +60,15 @@ __device__ __forceinline__ void red_add_cluster(uint32_t addr, uint32_t v) {
 __device__ __forceinline__ void st_cluster(uint32_t addr, uint32_t v) {
   asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
+// 4-byte global -> shared copy that does not hold a register while in flight
+__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)),
+               "l"(static_cast<unsigned long long>(__cvta_generic_to_global(src)))
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+constexpr int kBatch = 8;   // entries per thread whose global loads are issued together
 
 // Block-wide exclusive scan of two counters (one pair per thread).
 __device__ __forceinline__ void block_excl_scan2(SelShared& S, uint32_t a, uint32_t b, uint32_t& ea, uint32_t& eb,
@@ -120,23 +129,20 @@ __device__ void radix_select(cgx::cluster_group& cl, SelShared& S, SelState& st,
     return;
   }
   uint32_t* my_hist = S.whist[w];
+  // S.whist is all zero on entry and on exit: the thread that sums a bin clears it
   for (int pass = 0; pass < 4; ++pass, ++st.pass) {
     const int buf = st.pass % 3, nxt = (st.pass + 1) % 3;
     const int sh = 24 - 8 * pass;
-    // the next pass's buffer was last read two barriers ago
-    for (int i = threadIdx.x; i < kWarps * kBins; i += kThreads) (&S.whist[0][0])[i] = 0;
-    if (threadIdx.x < kBins) S.merged[nxt][threadIdx.x] = 0;
-    __syncthreads();
-    // four keys loaded before their four atomics, so the loads overlap
-    for (int e0 = 0; e0 < cnt_local; e0 += 4 * kThreads) {
-      uint32_t k[4];
+    // kBatch keys loaded before their atomics, so the loads overlap
+    for (int e0 = 0; e0 < cnt_local; e0 += kBatch * kThreads) {
+      uint32_t k[kBatch];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
+      for (int u = 0; u < kBatch; ++u) {
         const int e = e0 + u * kThreads + threadIdx.x;
         k[u] = e < cnt_local ? keys[e] : 0u;   // out-of-range slots are skipped below
       }
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
+      for (int u = 0; u < kBatch; ++u) {
         const int e = e0 + u * kThreads + threadIdx.x;
         if (e < cnt_local && (k[u] & mask) == prefix) atomicAdd(&my_hist[(k[u] >> sh) & 0xFFu], 1u);
       }
@@ -145,38 +151,41 @@ __device__ void radix_select(cgx::cluster_group& cl, SelShared& S, SelState& st,
     if (threadIdx.x < kBins) {
       uint32_t c = 0;
 #pragma unroll
-      for (int ww = 0; ww < kWarps; ++ww) c += S.whist[ww][threadIdx.x];
+      for (int ww = 0; ww < kWarps; ++ww) {
+        c += S.whist[ww][threadIdx.x];
+        S.whist[ww][threadIdx.x] = 0;
+      }
+      // the next pass's cluster buffer was last read two cluster barriers ago; remote
+      // CTAs add into it only after the barrier below
+      S.merged[nxt][threadIdx.x] = 0;
       if (c)
         for (unsigned r = 0; r < CS; ++r) red_add_cluster(cluster_addr(&S.merged[buf][threadIdx.x], r), c);
     }
     cl.sync();
-    if (threadIdx.x < kBins) {
-      // bin t = thread t; suffix sums from the top find the bin holding the krem-th largest
-      const uint32_t v = S.merged[buf][threadIdx.x];
-      uint32_t incl = v;   // sum over bins [t, warp end)
+    if (w == 0) {
+      // one warp finds the digit: lane l holds bins [8l, 8l + 8); bins of higher lanes and
+      // higher slots hold larger keys
+      const uint4 b0 = *reinterpret_cast<const uint4*>(&S.merged[buf][8 * lane]);
+      const uint4 b1 = *reinterpret_cast<const uint4*>(&S.merged[buf][8 * lane + 4]);
+      const uint32_t v[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+      uint32_t tot = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) tot += v[j];
+      uint32_t incl = tot;   // keys in the bins of lanes [lane, 32)
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const uint32_t x = __shfl_down_sync(0xffffffffu, incl, o);
         if (lane + o < 32) incl += x;
       }
-      if (lane == 0) S.wsum_gt[w] = incl;   // warp total
-    }
-    __syncthreads();
-    if (threadIdx.x < kBins) {
-      const uint32_t v = S.merged[buf][threadIdx.x];
-      uint32_t incl = v;
+      uint32_t above = incl - tot;   // keys in bins above this lane's
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t x = __shfl_down_sync(0xffffffffu, incl, o);
-        if (lane + o < 32) incl += x;
-      }
-      uint32_t above_w = 0;
-      for (int i = w + 1; i < kBins / 32; ++i) above_w += S.wsum_gt[i];
-      const uint32_t above = above_w + incl - v;   // keys in bins above this one
-      if (above < krem && krem <= above + v) {
-        S.res_prefix = prefix | (static_cast<uint32_t>(threadIdx.x) << sh);
-        S.res_krem = krem - above;
-        S.res_bin = v;
+      for (int j = 7; j >= 0; --j) {
+        if (above < krem && krem <= above + v[j]) {   // exactly one (lane, j) holds the krem-th largest
+          S.res_prefix = prefix | (static_cast<uint32_t>(8 * lane + j) << sh);
+          S.res_krem = krem - above;
+          S.res_bin = v[j];
+        }
+        above += v[j];
       }
     }
     __syncthreads();
@@ -214,11 +223,19 @@ __device__ void apply_selection(cgx::cluster_group& cl, SelShared& S, SelState& 
   const int wa = lo_local + min(cnt, w * per_w);
   const int wb = lo_local + min(cnt, (w + 1) * per_w);
   uint32_t ngt = 0, neq = 0;
-  for (int e0 = wa; e0 < wb; e0 += 32) {
-    const int e = e0 + lane;
-    const uint32_t k = e < wb ? keys[e] : 0u;
-    ngt += __popc(__ballot_sync(0xffffffffu, e < wb && k > T));
-    neq += __popc(__ballot_sync(0xffffffffu, e < wb && k == T));
+  for (int e0 = wa; e0 < wb; e0 += 32 * kBatch) {
+    uint32_t k[kBatch];
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int e = e0 + 32 * u + lane;
+      k[u] = e < wb ? keys[e] : 0u;
+    }
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int e = e0 + 32 * u + lane;
+      ngt += __popc(__ballot_sync(0xffffffffu, e < wb && k[u] > T));
+      neq += __popc(__ballot_sync(0xffffffffu, e < wb && k[u] == T));
+    }
   }
   // per-warp totals -> exclusive prefix over warps (lane 0 of each warp contributes)
   uint32_t egt, eeq, tgt, teq;
@@ -256,17 +273,25 @@ __device__ void apply_selection(cgx::cluster_group& cl, SelShared& S, SelState& 
   uint32_t eq_rank = qs + eeq;
   const uint32_t avail_w = krem > qs ? krem - qs : 0u;
   uint32_t slot = sel + egt + (eeq < avail_w ? eeq : avail_w);
-  for (int e0 = wa; e0 < wb; e0 += 32) {
-    const int e = e0 + lane;
-    const uint32_t k = e < wb ? keys[e] : 0u;
-    const bool gt = e < wb && k > T;
-    const bool eq = e < wb && k == T;
-    const unsigned meq = __ballot_sync(0xffffffffu, eq);
-    const bool take = gt || (eq && eq_rank + __popc(meq & lt) < krem);
-    const unsigned mtake = __ballot_sync(0xffffffffu, take);
-    if (take) visit(e, slot + __popc(mtake & lt));
-    slot += __popc(mtake);
-    eq_rank += __popc(meq);
+  for (int e0 = wa; e0 < wb; e0 += 32 * kBatch) {
+    uint32_t k[kBatch];
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int e = e0 + 32 * u + lane;
+      k[u] = e < wb ? keys[e] : 0u;
+    }
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int e = e0 + 32 * u + lane;
+      const bool gt = e < wb && k[u] > T;
+      const bool eq = e < wb && k[u] == T;
+      const unsigned meq = __ballot_sync(0xffffffffu, eq);
+      const bool take = gt || (eq && eq_rank + __popc(meq & lt) < krem);
+      const unsigned mtake = __ballot_sync(0xffffffffu, take);
+      if (take) visit(e, slot + __popc(mtake & lt));
+      slot += __popc(mtake);
+      eq_rank += __popc(meq);
+    }
   }
   __syncthreads();   // visits (flags, counters) are complete before the caller reads them
 }
@@ -296,62 +321,122 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelectArgs a,
   const int nforced = min(n, ns + nr);
 
   const bool pool_mode = a.raw != nullptr;
+  // stage-2 scores: the value-aware score this kernel writes, or the caller's array
+  // (value-aware scores computed earlier, or the anchors' random keys)
+  const float* s2 = (pool_mode && a.out_val) ? a.out_val : a.s2;
+  // when a thread owns at most kBatch entries, its stage-2 keys stay in registers
+  const bool k2_reg = a.two_stage && cnt <= kBatch * kThreads;
+  uint32_t k2[kBatch];
+#pragma unroll
+  for (int u = 0; u < kBatch; ++u) k2[u] = 0u;
   if (pool_mode) {
-    // stage the raw scores of [c_lo - half, c_hi + half) in the key array, pool each of
-    // this CTA's entries inside its own head, combine with nu, write the API outputs
+    // stage the raw scores of positions [c_lo - half, c_hi + half) at index
+    // (position - c_lo + half), every copy in flight at once.  Then each thread pools its
+    // kBatch entries of a round (entry e = r0 + u*kThreads + tid) in registers, all window
+    // taps interleaved; a round reads staged indices [r0, r0 + R + 2*half) and, after a
+    // barrier, writes the keys [r0, r0 + R), which no later round reads.
     const int half = a.pool != 0 ? a.pool_kernel / 2 : 0;
     const int lo = max(0, c_lo - half), hi = min(L, c_hi + half);
     float* stage = reinterpret_cast<float*>(keys);
-    for (int e = threadIdx.x; e < hi - lo; e += kThreads) stage[e] = __ldg(a.raw + sbase + lo + e);
+    for (int x = lo + static_cast<int>(threadIdx.x); x < hi; x += kThreads)
+      cp_async4(stage + (x - c_lo + half), a.raw + sbase + x);
+    cp_async_wait_all();
     __syncthreads();
-    for (int e = threadIdx.x; e < cnt; e += kThreads) {
-      const int g = c_lo + e;
-      const int i = per_layer ? g % n : g;
-      const int wlo = max(0, i - half) - i, whi = min(n - 1, i + half) - i;   // window offsets
-      float p;
-      if (a.pool == 1) {
-        p = stage[g - lo];
-        for (int d = wlo; d <= whi; ++d) p = fmaxf(p, stage[g + d - lo]);
-      } else if (a.pool == 2) {
-        float acc = 0.f;
-        for (int d = wlo; d <= whi; ++d) acc += stage[g + d - lo];
-        p = acc / static_cast<float>(a.pool_kernel);
-      } else {
-        p = stage[g - lo];
-      }
-      a.out_attn[sbase + g] = p;
-      if (a.out_val) a.out_val[sbase + g] = (p + a.eps) * __ldg(a.nu + sbase + g);
-    }
-    __syncthreads();   // the staged raw scores are no longer read
-  }
-  const float* s1 = pool_mode ? a.out_attn : a.s1;
-  // stage-2 scores: the value-aware score this kernel just wrote, or the caller's array
-  // (value-aware scores computed earlier, or the anchors' random keys)
-  const float* s2 = (pool_mode && a.out_val) ? a.out_val : a.s2;
-
-  // stage-1 keys (forced entries at the top); in pooling mode each thread reads back the
-  // values it wrote itself (same strided assignment), so plain loads suffice
-  for (int e0 = 0; e0 < cnt; e0 += 4 * kThreads) {
-    float v[4];
+    for (int r0 = 0; r0 < cnt; r0 += kBatch * kThreads) {
+      float nuv[kBatch], p[kBatch];
+      int wlo[kBatch], whi[kBatch], pos[kBatch];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int e = e0 + u * kThreads + threadIdx.x;
-      v[u] = e < cnt ? (pool_mode ? s1[sbase + c_lo + e] : __ldg(s1 + sbase + c_lo + e)) : 0.f;
-    }
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int e = e0 + u * kThreads + threadIdx.x;
-      if (e < cnt) {
+      for (int u = 0; u < kBatch; ++u) {
+        const int e = r0 + u * kThreads + static_cast<int>(threadIdx.x);
         const int g = c_lo + e;
-        const int i = per_layer ? g % n : g;
-        const bool forced = (i < ns) || (i >= n - nr);
-        keys[e] = forced ? kKeyMax : f2key(v[u]);
-        flag[e] = 0;
+        int i = g;
+        if (per_layer) i = g % n;
+        pos[u] = i;
+        // window offsets inside the entry's own head; an empty window past the chunk
+        wlo[u] = e < cnt ? max(0, i - half) - i : 1;
+        whi[u] = e < cnt ? min(n - 1, i + half) - i : 0;
+        // nu for the value-aware score, else the caller's stage-2 score
+        nuv[u] = (e < cnt && (a.out_val || k2_reg)) ? __ldg((a.out_val ? a.nu : a.s2) + sbase + g) : 0.f;
+        p[u] = (a.pool == 1) ? -INFINITY : 0.f;
+      }
+      if (a.pool == 0) {
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+          const int e = r0 + u * kThreads + static_cast<int>(threadIdx.x);
+          if (e < cnt) p[u] = stage[e + half];
+        }
+      } else {
+        for (int d = -half; d <= half; ++d) {
+#pragma unroll
+          for (int u = 0; u < kBatch; ++u) {
+            const int e = r0 + u * kThreads + static_cast<int>(threadIdx.x);
+            if (d >= wlo[u] && d <= whi[u]) {
+              const float x = stage[e + half + d];
+              p[u] = (a.pool == 1) ? fmaxf(p[u], x) : p[u] + x;
+            }
+          }
+        }
+        if (a.pool == 2) {
+#pragma unroll
+          for (int u = 0; u < kBatch; ++u) p[u] = p[u] / static_cast<float>(a.pool_kernel);
+        }
+      }
+      uint32_t key[kBatch];
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const int e = r0 + u * kThreads + static_cast<int>(threadIdx.x);
+        key[u] = 0u;
+        if (e < cnt) {
+          const int g = c_lo + e;
+          a.out_attn[sbase + g] = p[u];
+          if (a.out_val) {
+            const float sv = (p[u] + a.eps) * nuv[u];
+            a.out_val[sbase + g] = sv;
+            k2[u] = f2key(sv);
+          } else if (k2_reg) {
+            k2[u] = f2key(nuv[u]);
+          }
+          const bool forced = (pos[u] < ns) || (pos[u] >= n - nr);
+          key[u] = forced ? kKeyMax : f2key(p[u]);
+        }
+      }
+      __syncthreads();   // this round's staged values are read
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const int e = r0 + u * kThreads + static_cast<int>(threadIdx.x);
+        if (e < cnt) {
+          keys[e] = key[u];
+          flag[e] = 0;
+        }
+      }
+    }
+  } else {
+    for (int e0 = 0; e0 < cnt; e0 += kBatch * kThreads) {
+      float v[kBatch];
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const int e = e0 + u * kThreads + static_cast<int>(threadIdx.x);
+        v[u] = e < cnt ? __ldg(a.s1 + sbase + c_lo + e) : 0.f;
+        if (k2_reg) k2[u] = e < cnt ? f2key(__ldg(s2 + sbase + c_lo + e)) : 0u;
+      }
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const int e = e0 + u * kThreads + static_cast<int>(threadIdx.x);
+        if (e < cnt) {
+          const int g = c_lo + e;
+          int i = g;
+          if (per_layer) i = g % n;
+          const bool forced = (i < ns) || (i >= n - nr);
+          keys[e] = forced ? kKeyMax : f2key(v[u]);
+          flag[e] = 0;
+        }
       }
     }
   }
+
   if (threadIdx.x < kMaxHeads) S.head_cnt[threadIdx.x] = 0;
   for (int i = threadIdx.x; i < 3 * kBins; i += kThreads) (&S.merged[0][0])[i] = 0;
+  for (int i = threadIdx.x; i < kWarps * kBins; i += kThreads) (&S.whist[0][0])[i] = 0;
   SelState sst;
   cl.sync();   // every CTA's buffers are zero before any remote reduction lands
 
@@ -363,17 +448,26 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelectArgs a,
       radix_select(cl, S, sst, keys, cnt, static_cast<uint32_t>(a.budget1[b]), T, krem);
       apply_selection(cl, S, sst, keys, 0, cnt, T, krem, [&](int e, uint32_t) { flag[e] = 1; });
       // stage 2: the remaining B - b' by the value-aware score, stage-1 picks forced in
-      for (int e0 = 0; e0 < cnt; e0 += 4 * kThreads) {
-        float v[4];
+      if (k2_reg) {
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int e = e0 + u * kThreads + threadIdx.x;
-          v[u] = e < cnt ? (pool_mode ? s2[sbase + c_lo + e] : __ldg(s2 + sbase + c_lo + e)) : 0.f;
+        for (int u = 0; u < kBatch; ++u) {
+          const int e = u * kThreads + static_cast<int>(threadIdx.x);
+          if (e < cnt) keys[e] = flag[e] ? kKeyMax : k2[u];
         }
+      } else {
+        // each thread reads back only values it wrote itself, so plain loads see them
+        for (int e0 = 0; e0 < cnt; e0 += kBatch * kThreads) {
+          float v[kBatch];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int e = e0 + u * kThreads + threadIdx.x;
-          if (e < cnt) keys[e] = flag[e] ? kKeyMax : f2key(v[u]);
+          for (int u = 0; u < kBatch; ++u) {
+            const int e = e0 + u * kThreads + threadIdx.x;
+            v[u] = e < cnt ? (pool_mode ? s2[sbase + c_lo + e] : __ldg(s2 + sbase + c_lo + e)) : 0.f;
+          }
+#pragma unroll
+          for (int u = 0; u < kBatch; ++u) {
+            const int e = e0 + u * kThreads + threadIdx.x;
+            if (e < cnt) keys[e] = flag[e] ? kKeyMax : f2key(v[u]);
+          }
         }
       }
       __syncthreads();

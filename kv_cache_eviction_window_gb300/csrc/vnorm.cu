@@ -336,13 +336,21 @@ __global__ void wbar_kernel(const uint16_t* __restrict__ w_o, uint16_t* __restri
     const uint16_t* src = w_o + j * row_len + static_cast<long long>(h) * G * kHeadDim + c8 * 8;
     if (wo_mode == 0) {
       float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-      for (int g = 0; g < G; ++g) {
-        const uint4 p = __ldg(reinterpret_cast<const uint4*>(src + g * kHeadDim));
-        const uint32_t w[4] = {p.x, p.y, p.z, p.w};
+      // the loads of four slices are issued together, then summed in slice order
+      for (int g0 = 0; g0 < G; g0 += 4) {
+        uint4 p[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          acc[2 * i] += __uint_as_float(w[i] << 16);
-          acc[2 * i + 1] += __uint_as_float(w[i] & 0xFFFF0000u);
+        for (int u = 0; u < 4; ++u)
+          p[u] = g0 + u < G ? __ldg(reinterpret_cast<const uint4*>(src + (g0 + u) * kHeadDim)) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          if (g0 + u >= G) break;
+          const uint32_t w[4] = {p[u].x, p[u].y, p[u].z, p[u].w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            acc[2 * i] += __uint_as_float(w[i] << 16);
+            acc[2 * i + 1] += __uint_as_float(w[i] & 0xFFFF0000u);
+          }
         }
       }
       uint32_t o[4];
