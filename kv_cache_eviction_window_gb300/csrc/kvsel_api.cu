@@ -263,9 +263,24 @@ int make_plan(const kvsel_params* p, Plan& pl, bool need_device) {
     const int br = qa_block_rows();
     pl.qa_row_blocks = static_cast<int>((GN + br - 1) / br);
     pl.qa_key_blocks = (n + br - 1) / br;
+    // query-row slices per key block: at least eight CTAs per SM in all, and a whole
+    // number of waves (one CTA per SM) to within 3% where a slice count up to 64 gives one
     const long long want = 8ll * pl.num_sms;
     const long long base = static_cast<long long>(pl.H) * std::max(pl.qa_key_blocks, 1);
-    pl.qa_row_splits = static_cast<int>(std::min<long long>(64, std::max<long long>(1, (want + base - 1) / base)));
+    const int s0 = static_cast<int>(std::min<long long>(64, std::max<long long>(1, (want + base - 1) / base)));
+    int best_s = s0;
+    double best_eff = 0.0;
+    for (int sp = s0; sp <= 64; ++sp) {
+      const long long ctas = base * sp;
+      const long long waves = (ctas + pl.num_sms - 1) / pl.num_sms;
+      const double eff = static_cast<double>(ctas) / static_cast<double>(waves * pl.num_sms);
+      if (eff > best_eff + 1e-9) {
+        best_eff = eff;
+        best_s = sp;
+      }
+      if (eff >= 0.97) break;
+    }
+    pl.qa_row_splits = best_s;
     pl.ws_c2 = off;
     off = align256(off + static_cast<size_t>(pl.H) * GN * sizeof(float));
     pl.ws_tmax = off;

@@ -10,7 +10,7 @@
 //   qa_rowlse_kernel: A = a block of 512 query rows (4 M tiles), B = 64-key tiles
 //     streamed over all n keys; every epilogue thread keeps an online (max, sum) for its
 //     rows; writes c2_r = (m_r + log2 Z_r) in log2 units.
-//   qa_keymax_kernel: A = a block of 512 keys (4 M tiles, resident), B = 64-row query
+//   qa_keymax_kernel: A = a block of 512 keys (4 M tiles, resident), B = 128-row query
 //     tiles streamed over a slice of the rows; every thread keeps max_r (l_ri*s2 - c2_r)
 //     for its keys; slices merge with an order-preserving atomicMax in global memory.
 //   qa_finish_kernel: s_raw_i = exp2(max).
@@ -222,19 +222,28 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ------------------------------------------------------------------------------------
 // pass 2: per key, max over a slice of query rows of (l * s2 - c2_row)
 // ------------------------------------------------------------------------------------
+// The 512 resident keys are four M tiles; query rows stream as 128-row tiles, so every UMMA
+// is 128 x 128 x 16 (N = 64 leaves the tensor pipe idle between short instructions).  Each
+// M tile owns one 128-column TMEM accumulator; the epilogue releases it as soon as its
+// columns are in registers, so the next tile's UMMAs for that M tile can start while the
+// other three are still being drained.
+constexpr int kNT2 = 128;                     // query rows per streamed tile
+constexpr int kStages2 = 3;
+constexpr int kTile2 = kNT2 * 256;            // bytes of one streamed tile (two 64-column halves)
+constexpr uint32_t kSlotCols = kNT2;          // one accumulator slot per M tile
+
 __global__ void __launch_bounds__(kThreads, 1)
     qa_keymax_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                      const QaArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_align1024(smem_raw);
   uint8_t* sK = smem;                      // [4 M tiles][2 halves][128 keys][128 B]
-  uint8_t* sQ = smem + 2 * kBlockHalf;     // [stages][2 halves][64 rows][128 B]
+  uint8_t* sQ = smem + 2 * kBlockHalf;     // [stages][2 halves][128 rows][128 B]
 
-  __shared__ __align__(8) uint64_t full_bar[kStages], empty_bar[kStages], accf_bar[kAcc], acce_bar[kAcc];
+  __shared__ __align__(8) uint64_t full_bar[kStages2], empty_bar[kStages2], accf_bar[kMT], acce_bar[kMT];
   __shared__ __align__(8) uint64_t k_bar, done_bar;
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
-  __shared__ float s_x[kMT][4][32];
 
   const int warp = warp_id(), lane = lane_id();
   const int per_head = a.key_blocks * a.row_splits;
@@ -245,15 +254,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n = a.n, GN = a.GN;
   const int rows_per = (GN + a.row_splits - 1) / a.row_splits;
   const int r_begin = rs * rows_per, r_end = min(GN, r_begin + rows_per);
-  const int ntiles = r_end > r_begin ? (r_end - r_begin + kNT - 1) / kNT : 0;
+  const int ntiles = r_end > r_begin ? (r_end - r_begin + kNT2 - 1) / kNT2 : 0;
   int* status = a.wc.status;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < kStages2; ++s) {
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], 1);
     }
-    for (int s = 0; s < kAcc; ++s) {
+    for (int s = 0; s < kMT; ++s) {
       mbar_init(&accf_bar[s], 1);
       mbar_init(&acce_bar[s], kEpiWarps);
     }
@@ -282,89 +291,111 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       int t = 0;
       for (; t < ntiles; ++t) {
-        const int s = t % kStages, u = t / kStages;
+        const int s = t % kStages2, u = t / kStages2;
         if (!mbar_wait(&empty_bar[s], (u & 1) ^ 1, &s_abort, a.wc)) break;
-        mbar_arrive_expect_tx(&full_bar[s], kTile);
-        const int qrow = h * GN + r_begin + t * kNT;
-        tma_load_2d(sQ + s * kTile, &tq, &full_bar[s], 0, qrow);
-        tma_load_2d(sQ + s * kTile + kNT * 128, &tq, &full_bar[s], 64, qrow);
+        mbar_arrive_expect_tx(&full_bar[s], kTile2);
+        const int qrow = h * GN + r_begin + t * kNT2;
+        uint8_t* dst = sQ + s * kTile2;
+        // the tensor map's box is 64 rows x 64 columns: two row halves per column half
+        tma_load_2d(dst, &tq, &full_bar[s], 0, qrow);
+        tma_load_2d(dst + 64 * 128, &tq, &full_bar[s], 0, qrow + 64);
+        tma_load_2d(dst + kNT2 * 128, &tq, &full_bar[s], 64, qrow);
+        tma_load_2d(dst + kNT2 * 128 + 64 * 128, &tq, &full_bar[s], 64, qrow + 64);
       }
-      for (int tt = max(0, t - kStages); tt < t; ++tt) mbar_drain(&full_bar[tt % kStages], (tt / kStages) & 1, status);
+      for (int tt = max(0, t - kStages2); tt < t; ++tt) mbar_drain(&full_bar[tt % kStages2], (tt / kStages2) & 1, status);
       mbar_drain(&k_bar, 0, status);
     }
   } else if (warp == kMmaWarp) {
     if (lane == 0 && ntiles > 0) {
       bool ok = mbar_wait(&k_bar, 0, &s_abort, a.wc);
-      constexpr uint32_t idesc = idesc_bf16_f32(128, kNT);
+      constexpr uint32_t idesc = idesc_bf16_f32(128, kNT2);
+      const uint64_t kd0 = sdesc_kmajor_sw128(smem_u32(sK));
       for (int t = 0; ok && t < ntiles; ++t) {
-        const int s = t % kStages, u = t / kStages;
-        const int acc = t % kAcc, ua = t / kAcc;
+        const int s = t % kStages2, u = t / kStages2;
         if (!mbar_wait(&full_bar[s], u & 1, &s_abort, a.wc)) break;
-        if (!mbar_wait(&acce_bar[acc], (ua & 1) ^ 1, &s_abort, a.wc)) break;
         tc_fence_after();
-        const uint64_t kd0 = sdesc_kmajor_sw128(smem_u32(sK));
-        const uint64_t qd0 = sdesc_kmajor_sw128(smem_u32(sQ + s * kTile));
-#pragma unroll
+        const uint64_t qd0 = sdesc_kmajor_sw128(smem_u32(sQ + s * kTile2));
+#pragma unroll 1
         for (int mt = 0; mt < kMT; ++mt) {
+          if (!mbar_wait(&acce_bar[mt], (t & 1) ^ 1, &s_abort, a.wc)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
             const uint32_t koff = (k & 3) * 32;
             const uint64_t da = kd0 + ((mt * 32768 + (k >> 2) * 16384 + koff) >> 4);
-            const uint64_t db = qd0 + (((k >> 2) * (kNT * 128) + koff) >> 4);
-            umma_bf16(tbase + acc * kAccCols + mt * kNT, da, db, idesc, k > 0 ? 1u : 0u);
+            const uint64_t db = qd0 + (((k >> 2) * (kNT2 * 128) + koff) >> 4);
+            umma_bf16(tbase + mt * kSlotCols, da, db, idesc, k > 0 ? 1u : 0u);
           }
+          umma_commit(&accf_bar[mt]);
         }
+        if (!ok) break;
         umma_commit(&empty_bar[s]);
-        umma_commit(&accf_bar[acc]);
       }
       umma_commit(&done_bar);
       mbar_drain(&done_bar, 0, status);
     }
   } else {
+    // thread = key q4*32 + lane of every M tile; warp half cg takes query rows [64cg, 64cg + 64)
     const int q4 = warp & 3, cg = warp >> 2;
     const float s2 = a.s2;
     float best[kMT];
 #pragma unroll
     for (int mt = 0; mt < kMT; ++mt) best[mt] = -INFINITY;
-    for (int t = 0; t < ntiles; ++t) {
-      const int acc = t % kAcc, ua = t / kAcc;
-      bool ok = mbar_wait(&accf_bar[acc], ua & 1, &s_abort, a.wc);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) break;
-      tc_fence_after();
-      // c2 of this thread's 32 query rows: one coalesced load, broadcast by shuffles
-      const int rrow = r_begin + t * kNT + cg * 32 + lane;
-      const float myc2 = rrow < r_end ? (a.logit ? 0.f : __ldg(a.c2 + static_cast<size_t>(h) * GN + rrow)) : INFINITY;
-      float nc[32];
+    bool alive = true;
+    for (int t = 0; alive && t < ntiles; ++t) {
+      // -c2 of this warp half's 64 query rows: two coalesced loads, broadcast by shuffles
+      const int rr = r_begin + t * kNT2 + cg * 64 + lane;
+      const float c0 = rr < r_end ? (a.logit ? 0.f : __ldg(a.c2 + static_cast<size_t>(h) * GN + rr)) : INFINITY;
+      const float c1 = rr + 32 < r_end ? (a.logit ? 0.f : __ldg(a.c2 + static_cast<size_t>(h) * GN + rr + 32)) : INFINITY;
+      float nc[64];
 #pragma unroll
-      for (int j = 0; j < 32; ++j) nc[j] = -__shfl_sync(0xffffffffu, myc2, j);
+      for (int j = 0; j < 32; ++j) {
+        nc[j] = -__shfl_sync(0xffffffffu, c0, j);
+        nc[32 + j] = -__shfl_sync(0xffffffffu, c1, j);
+      }
 #pragma unroll
       for (int mt = 0; mt < kMT; ++mt) {
-        float v[32];
-        tmem_ld32(tbase + (static_cast<uint32_t>(q4 * 32) << 16) + acc * kAccCols + mt * kNT + cg * 32, v);
+        bool ok = mbar_wait(&accf_bar[mt], t & 1, &s_abort, a.wc);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) {
+          alive = false;
+          break;
+        }
+        tc_fence_after();
+        float v[64];
+        const uint32_t taddr = tbase + (static_cast<uint32_t>(q4 * 32) << 16) + mt * kSlotCols + cg * 64;
+        tmem_ld32(taddr, v);
+        tmem_ld32(taddr + 32, v + 32);
         tmem_ld_wait();
+        // the columns are in registers: hand the slot back to the UMMA warp
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acce_bar[mt]);
         float b0 = best[mt], b1 = -INFINITY;
 #pragma unroll
-        for (int j = 0; j < 32; j += 2) {
-          b0 = fmaxf(b0, fmaf(v[j], s2, nc[j]));
-          b1 = fmaxf(b1, fmaf(v[j + 1], s2, nc[j + 1]));
+        for (int j = 0; j < 64; j += 4) {
+          b0 = fmax3(b0, fmaf(v[j], s2, nc[j]), fmaf(v[j + 1], s2, nc[j + 1]));
+          b1 = fmax3(b1, fmaf(v[j + 2], s2, nc[j + 2]), fmaf(v[j + 3], s2, nc[j + 3]));
         }
         best[mt] = fmaxf(b0, b1);
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&acce_bar[acc]);
     }
+    // every UMMA has completed (the last accumulator of each slot was waited for), so the
+    // streamed-tile buffers are free to hold the two halves' partial maxima
+    float* s_x = reinterpret_cast<float*>(sQ);   // [kMT][4][32]
     if (cg == 1) {
 #pragma unroll
-      for (int mt = 0; mt < kMT; ++mt) s_x[mt][q4][lane] = best[mt];
+      for (int mt = 0; mt < kMT; ++mt) s_x[(mt * 4 + q4) * 32 + lane] = best[mt];
     }
     epi_bar();
-    if (cg == 0) {
+    if (cg == 0 && alive) {
 #pragma unroll
       for (int mt = 0; mt < kMT; ++mt) {
         const int key = key0 + mt * 128 + q4 * 32 + lane;
-        const float bm = fmaxf(best[mt], s_x[mt][q4][lane]);
+        const float bm = fmaxf(best[mt], s_x[(mt * 4 + q4) * 32 + lane]);
         if (key < n && ntiles > 0) atomicMax(a.tmax + static_cast<size_t>(h) * n + key, f2key(bm));
       }
     }
@@ -420,7 +451,7 @@ cudaError_t launch_qa_rowlse(const QaArgs& a, const CUtensorMap& tq, const CUten
 }
 
 cudaError_t launch_qa_keymax(const QaArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, cudaStream_t st) {
-  const size_t smem = 1024 + 2 * kBlockHalf + kStages * kTile;
+  const size_t smem = 1024 + 2 * kBlockHalf + kStages2 * kTile2;
   cudaError_t e = ensure_smem(reinterpret_cast<const void*>(qa_keymax_kernel), smem);
   if (e != cudaSuccess) return e;
   e = cudaMemsetAsync(a.tmax, 0, static_cast<size_t>(a.H) * a.n * sizeof(uint32_t), st);
