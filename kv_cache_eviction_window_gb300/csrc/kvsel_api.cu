@@ -416,12 +416,12 @@ int do_score(const kvsel_params* p, const Plan& pl, const void* q, const kvsel_k
   const float scale = p->scale > 0.f ? p->scale : 1.f / std::sqrt(static_cast<float>(kHeadDim));
   if (pl.qa) {
     const int n = pl.rq.n[0];
-    CUtensorMap tq, tk64, tk128;
+    CUtensorMap tq, tk128;
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(pl.H) * pl.G * n};
     const cuuint64_t strides[1] = {kHeadDim * 2};
     const cuuint32_t box[2] = {64, 64};
     if (!encode(&tq, q, 2, dims, strides, box)) return KVSEL_EINVAL;
-    if (!kv_map(&tk64, kv->k, kv, pl, 64) || !kv_map(&tk128, kv->k, kv, pl, 128)) return KVSEL_EINVAL;
+    if (!kv_map(&tk128, kv->k, kv, pl, 128)) return KVSEL_EINVAL;
     QaArgs a{};
     a.H = pl.H;
     a.n = n;
@@ -438,7 +438,7 @@ int do_score(const kvsel_params* p, const Plan& pl, const void* q, const kvsel_k
     int rc;
     if (!a.logit) {
       StageScope sc(KVSEL_STAGE_ROWSTATS, st);
-      rc = launch_rc(launch_qa_rowlse(a, tq, tk64, st));
+      rc = launch_rc(launch_qa_rowlse(a, tq, tk128, st));
       if (rc) return rc;
     }
     {

@@ -7,7 +7,7 @@
 // Per KV head the queries are the G*n rows of Q[h] (all positions of all group heads),
 // non-causal over all n keys:  S_i = max_r exp(l_ri - c_r),  c_r = log sum_j exp(l_rj).
 //
-//   qa_rowlse_kernel: A = a block of 512 query rows (4 M tiles), B = 64-key tiles
+//   qa_rowlse_kernel: A = a block of 512 query rows (4 M tiles), B = 128-key tiles
 //     streamed over all n keys; every epilogue thread keeps an online (max, sum) for its
 //     rows; writes c2_r = (m_r + log2 Z_r) in log2 units.
 //   qa_keymax_kernel: A = a block of 512 keys (4 M tiles, resident), B = 128-row query
@@ -22,21 +22,22 @@
 namespace kvsel {
 namespace {
 
-constexpr int kEpiWarps = 8;
-constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
-constexpr int kThreads = 320;
 constexpr float kNegBig = -1.0e30f;
-constexpr int kMT = 4;                 // 128-row M tiles per CTA (512 rows or keys)
-constexpr int kNT = 64;                // streamed tile rows (keys in pass 1, queries in pass 2)
-constexpr int kStages = 4;
-constexpr int kAcc = 2;
-constexpr uint32_t kAccCols = kMT * kNT;      // 256
-constexpr uint32_t kTmemCols = kAcc * kAccCols;
+constexpr int kMT = 4;                        // 128-row M tiles per CTA (512 rows or keys), resident
 constexpr int kBlockHalf = kMT * 128 * 128;   // bytes of one column half of the resident block
-constexpr int kTile = kNT * 256;              // bytes of one streamed tile
+constexpr int kNT = 128;                      // rows per streamed tile (keys in pass 1, queries in pass 2)
+constexpr int kStages = 3;
+constexpr int kTile = kNT * 256;              // bytes of one streamed tile (two 64-column halves)
+constexpr uint32_t kSlotCols = kNT;           // one 128-column accumulator slot per M tile
+constexpr uint32_t kTmemCols = kMT * kSlotCols;
+// 16 epilogue warps (four per TMEM lane quadrant, 32 accumulator columns each), so that
+// the latency of one warp's TMEM loads hides behind the others' arithmetic
+constexpr int kEpiWarps = 16;
+constexpr int kProducerWarp = 16;
+constexpr int kMmaWarp = 17;
+constexpr int kThreads = 576;
 
-__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 512;" ::: "memory"); }
 
 __device__ __forceinline__ uint32_t f2key(float f) {
   const uint32_t u = __float_as_uint(f);
@@ -46,6 +47,12 @@ __device__ __forceinline__ float key2f(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }
 
+// Both passes stream 128-row tiles, so every UMMA is 128 x 128 x 16 (N = 64 leaves the
+// tensor pipe idle between short instructions).  The resident block is four M tiles and
+// each M tile owns one 128-column TMEM accumulator; the epilogue releases it as soon as its
+// columns are in registers, so the next tile's UMMAs for that M tile start while the other
+// three are still being drained.
+
 // ------------------------------------------------------------------------------------
 // pass 1: log-sum-exp of every query row over all keys
 // ------------------------------------------------------------------------------------
@@ -54,14 +61,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                      const QaArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_align1024(smem_raw);
-  uint8_t* sQ = smem;                      // [2 halves][512 rows][128 B]
-  uint8_t* sK = smem + 2 * kBlockHalf;     // [stages][2 halves][64 keys][128 B]
+  uint8_t* sQ = smem;                      // [4 M tiles][2 halves][128 rows][128 B]
+  uint8_t* sK = smem + 2 * kBlockHalf;     // [stages][2 halves][128 keys][128 B]
 
-  __shared__ __align__(8) uint64_t full_bar[kStages], empty_bar[kStages], accf_bar[kAcc], acce_bar[kAcc];
+  __shared__ __align__(8) uint64_t full_bar[kStages], empty_bar[kStages], accf_bar[kMT], acce_bar[kMT];
   __shared__ __align__(8) uint64_t q_bar, done_bar;
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
-  __shared__ float s_xm[kMT][4][32], s_xz[kMT][4][32];
 
   const int warp = warp_id(), lane = lane_id();
   const int h = blockIdx.x / a.row_blocks;
@@ -75,7 +81,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], 1);
     }
-    for (int s = 0; s < kAcc; ++s) {
+    for (int s = 0; s < kMT; ++s) {
       mbar_init(&accf_bar[s], 1);
       mbar_init(&acce_bar[s], kEpiWarps);
     }
@@ -99,10 +105,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tk);
       mbar_arrive_expect_tx(&q_bar, 2 * kBlockHalf);
       const int qrow0 = h * GN + row0;
-      for (int rb = 0; rb < kMT * 128; rb += 64) {
-        tma_load_2d(sQ + rb * 128, &tq, &q_bar, 0, qrow0 + rb);
-        tma_load_2d(sQ + kBlockHalf + rb * 128, &tq, &q_bar, 64, qrow0 + rb);
-      }
+      for (int mt = 0; mt < kMT; ++mt)
+        for (int rb = 0; rb < 128; rb += 64) {
+          tma_load_2d(sQ + mt * 32768 + rb * 128, &tq, &q_bar, 0, qrow0 + mt * 128 + rb);
+          tma_load_2d(sQ + mt * 32768 + 16384 + rb * 128, &tq, &q_bar, 64, qrow0 + mt * 128 + rb);
+        }
       int t = 0;
       for (; t < ntiles; ++t) {
         const int s = t % kStages, u = t / kStages;
@@ -118,32 +125,36 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       bool ok = mbar_wait(&q_bar, 0, &s_abort, a.wc);
       constexpr uint32_t idesc = idesc_bf16_f32(128, kNT);
+      const uint64_t qd0 = sdesc_kmajor_sw128(smem_u32(sQ));
       for (int t = 0; ok && t < ntiles; ++t) {
         const int s = t % kStages, u = t / kStages;
-        const int acc = t % kAcc, ua = t / kAcc;
         if (!mbar_wait(&full_bar[s], u & 1, &s_abort, a.wc)) break;
-        if (!mbar_wait(&acce_bar[acc], (ua & 1) ^ 1, &s_abort, a.wc)) break;
         tc_fence_after();
-        // descriptors: the tile bases once, then byte offsets added to the address field
         const uint64_t kd0 = sdesc_kmajor_sw128(smem_u32(sK + s * kTile));
-        const uint64_t qd0 = sdesc_kmajor_sw128(smem_u32(sQ));
-#pragma unroll
+#pragma unroll 1
         for (int mt = 0; mt < kMT; ++mt) {
+          if (!mbar_wait(&acce_bar[mt], (t & 1) ^ 1, &s_abort, a.wc)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
             const uint32_t koff = (k & 3) * 32;
-            const uint64_t da = qd0 + (((k >> 2) * kBlockHalf + mt * 16384 + koff) >> 4);
+            const uint64_t da = qd0 + ((mt * 32768 + (k >> 2) * 16384 + koff) >> 4);
             const uint64_t db = kd0 + (((k >> 2) * (kNT * 128) + koff) >> 4);
-            umma_bf16(tbase + acc * kAccCols + mt * kNT, da, db, idesc, k > 0 ? 1u : 0u);
+            umma_bf16(tbase + mt * kSlotCols, da, db, idesc, k > 0 ? 1u : 0u);
           }
+          umma_commit(&accf_bar[mt]);
         }
+        if (!ok) break;
         umma_commit(&empty_bar[s]);
-        umma_commit(&accf_bar[acc]);
       }
       umma_commit(&done_bar);
       mbar_drain(&done_bar, 0, status);
     }
   } else {
+    // thread = query row q4*32 + lane of every M tile; warp group cg takes keys [32cg, 32cg + 32)
     const int q4 = warp & 3, cg = warp >> 2;
     const float s2 = a.s2;
     float m[kMT], z[kMT];
@@ -152,61 +163,77 @@ __global__ void __launch_bounds__(kThreads, 1)
       m[mt] = kNegBig;
       z[mt] = 0.f;
     }
-    for (int t = 0; t < ntiles; ++t) {
-      const int acc = t % kAcc, ua = t / kAcc;
-      bool ok = mbar_wait(&accf_bar[acc], ua & 1, &s_abort, a.wc);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) break;
-      tc_fence_after();
-      const int key0 = t * kNT + cg * 32;
-      const bool tail = key0 + 32 > n;
+    bool alive = true;
+    for (int t = 0; alive && t < ntiles; ++t) {
+      const int kc0 = t * kNT + cg * 32;
+      const bool tail = kc0 + 32 > n;
 #pragma unroll
       for (int mt = 0; mt < kMT; ++mt) {
+        bool ok = mbar_wait(&accf_bar[mt], t & 1, &s_abort, a.wc);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) {
+          alive = false;
+          break;
+        }
+        tc_fence_after();
         float v[32];
-        tmem_ld32(tbase + (static_cast<uint32_t>(q4 * 32) << 16) + acc * kAccCols + mt * kNT + cg * 32, v);
+        tmem_ld32(tbase + (static_cast<uint32_t>(q4 * 32) << 16) + mt * kSlotCols + cg * 32, v);
         tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acce_bar[mt]);
         if (tail) {
 #pragma unroll
           for (int j = 0; j < 32; ++j)
-            if (key0 + j >= n) v[j] = -INFINITY;
+            if (kc0 + j >= n) v[j] = -INFINITY;
         }
-        float cmax = v[0];
+        float cmax = fmax3(v[0], v[1], v[2]);
 #pragma unroll
-        for (int j = 1; j < 32; ++j) cmax = fmaxf(cmax, v[j]);
+        for (int j = 3; j < 31; j += 2) cmax = fmax3(cmax, v[j], v[j + 1]);
+        cmax = fmaxf(cmax, v[31]);
         const float mn = fmaxf(m[mt], cmax * s2);
-        float p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
+        // exp2(l * s2 - mn): packed FMA, four partial sums
+        const uint64_t s2p = pack2(s2, s2), nmn = pack2(-mn, -mn);
+        uint64_t p2[2] = {0ull, 0ull};
 #pragma unroll
         for (int j = 0; j < 32; j += 4) {
-          p0 += ex2_approx(fmaf(v[j + 0], s2, -mn));
-          p1 += ex2_approx(fmaf(v[j + 1], s2, -mn));
-          p2 += ex2_approx(fmaf(v[j + 2], s2, -mn));
-          p3 += ex2_approx(fmaf(v[j + 3], s2, -mn));
+          float x0, x1, x2, x3;
+          unpack2(ffma2(pack2(v[j + 0], v[j + 1]), s2p, nmn), x0, x1);
+          unpack2(ffma2(pack2(v[j + 2], v[j + 3]), s2p, nmn), x2, x3);
+          p2[0] = fadd2(p2[0], pack2(ex2_approx(x0), ex2_approx(x1)));
+          p2[1] = fadd2(p2[1], pack2(ex2_approx(x2), ex2_approx(x3)));
         }
-        z[mt] = z[mt] * ex2_approx(m[mt] - mn) + ((p0 + p1) + (p2 + p3));
+        float q0, q1;
+        unpack2(fadd2(p2[0], p2[1]), q0, q1);
+        z[mt] = z[mt] * ex2_approx(m[mt] - mn) + (q0 + q1);
         m[mt] = mn;
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&acce_bar[acc]);
     }
-    if (cg == 1) {
+    // every UMMA has completed, so the streamed-tile buffers hold the key groups' partials
+    float* s_xm = reinterpret_cast<float*>(sK);   // [3 key groups][kMT][4][32]
+    float* s_xz = s_xm + 3 * kMT * 128;
+    if (cg > 0) {
 #pragma unroll
       for (int mt = 0; mt < kMT; ++mt) {
-        s_xm[mt][q4][lane] = m[mt];
-        s_xz[mt][q4][lane] = z[mt];
+        s_xm[(((cg - 1) * kMT + mt) * 4 + q4) * 32 + lane] = m[mt];
+        s_xz[(((cg - 1) * kMT + mt) * 4 + q4) * 32 + lane] = z[mt];
       }
     }
     epi_bar();
-    if (cg == 0) {
+    if (cg == 0 && alive) {
 #pragma unroll
       for (int mt = 0; mt < kMT; ++mt) {
         const int r = row0 + mt * 128 + q4 * 32 + lane;
-        if (r < GN) {
-          const float m1 = s_xm[mt][q4][lane], z1 = s_xz[mt][q4][lane];
-          const float mm = fmaxf(m[mt], m1);
-          const float zz = z[mt] * ex2_approx(m[mt] - mm) + z1 * ex2_approx(m1 - mm);
-          a.c2[static_cast<size_t>(h) * GN + r] = mm + lg2_approx(zz);
+        float mm = m[mt];
+#pragma unroll
+        for (int g = 0; g < 3; ++g) mm = fmaxf(mm, s_xm[((g * kMT + mt) * 4 + q4) * 32 + lane]);
+        float zz = z[mt] * ex2_approx(m[mt] - mm);
+#pragma unroll
+        for (int g = 0; g < 3; ++g) {
+          const int i = ((g * kMT + mt) * 4 + q4) * 32 + lane;
+          zz += s_xz[i] * ex2_approx(s_xm[i] - mm);
         }
+        if (r < GN) a.c2[static_cast<size_t>(h) * GN + r] = mm + lg2_approx(zz);
       }
     }
   }
@@ -227,11 +254,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 // M tile owns one 128-column TMEM accumulator; the epilogue releases it as soon as its
 // columns are in registers, so the next tile's UMMAs for that M tile can start while the
 // other three are still being drained.
-constexpr int kNT2 = 128;                     // query rows per streamed tile
-constexpr int kStages2 = 3;
-constexpr int kTile2 = kNT2 * 256;            // bytes of one streamed tile (two 64-column halves)
-constexpr uint32_t kSlotCols = kNT2;          // one accumulator slot per M tile
-
 __global__ void __launch_bounds__(kThreads, 1)
     qa_keymax_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                      const QaArgs a) {
@@ -240,7 +262,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sK = smem;                      // [4 M tiles][2 halves][128 keys][128 B]
   uint8_t* sQ = smem + 2 * kBlockHalf;     // [stages][2 halves][128 rows][128 B]
 
-  __shared__ __align__(8) uint64_t full_bar[kStages2], empty_bar[kStages2], accf_bar[kMT], acce_bar[kMT];
+  __shared__ __align__(8) uint64_t full_bar[kStages], empty_bar[kStages], accf_bar[kMT], acce_bar[kMT];
   __shared__ __align__(8) uint64_t k_bar, done_bar;
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
@@ -254,11 +276,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n = a.n, GN = a.GN;
   const int rows_per = (GN + a.row_splits - 1) / a.row_splits;
   const int r_begin = rs * rows_per, r_end = min(GN, r_begin + rows_per);
-  const int ntiles = r_end > r_begin ? (r_end - r_begin + kNT2 - 1) / kNT2 : 0;
+  const int ntiles = r_end > r_begin ? (r_end - r_begin + kNT - 1) / kNT : 0;
   int* status = a.wc.status;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages2; ++s) {
+    for (int s = 0; s < kStages; ++s) {
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], 1);
     }
@@ -291,30 +313,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       int t = 0;
       for (; t < ntiles; ++t) {
-        const int s = t % kStages2, u = t / kStages2;
+        const int s = t % kStages, u = t / kStages;
         if (!mbar_wait(&empty_bar[s], (u & 1) ^ 1, &s_abort, a.wc)) break;
-        mbar_arrive_expect_tx(&full_bar[s], kTile2);
-        const int qrow = h * GN + r_begin + t * kNT2;
-        uint8_t* dst = sQ + s * kTile2;
+        mbar_arrive_expect_tx(&full_bar[s], kTile);
+        const int qrow = h * GN + r_begin + t * kNT;
+        uint8_t* dst = sQ + s * kTile;
         // the tensor map's box is 64 rows x 64 columns: two row halves per column half
         tma_load_2d(dst, &tq, &full_bar[s], 0, qrow);
         tma_load_2d(dst + 64 * 128, &tq, &full_bar[s], 0, qrow + 64);
-        tma_load_2d(dst + kNT2 * 128, &tq, &full_bar[s], 64, qrow);
-        tma_load_2d(dst + kNT2 * 128 + 64 * 128, &tq, &full_bar[s], 64, qrow + 64);
+        tma_load_2d(dst + kNT * 128, &tq, &full_bar[s], 64, qrow);
+        tma_load_2d(dst + kNT * 128 + 64 * 128, &tq, &full_bar[s], 64, qrow + 64);
       }
-      for (int tt = max(0, t - kStages2); tt < t; ++tt) mbar_drain(&full_bar[tt % kStages2], (tt / kStages2) & 1, status);
+      for (int tt = max(0, t - kStages); tt < t; ++tt) mbar_drain(&full_bar[tt % kStages], (tt / kStages) & 1, status);
       mbar_drain(&k_bar, 0, status);
     }
   } else if (warp == kMmaWarp) {
     if (lane == 0 && ntiles > 0) {
       bool ok = mbar_wait(&k_bar, 0, &s_abort, a.wc);
-      constexpr uint32_t idesc = idesc_bf16_f32(128, kNT2);
+      constexpr uint32_t idesc = idesc_bf16_f32(128, kNT);
       const uint64_t kd0 = sdesc_kmajor_sw128(smem_u32(sK));
       for (int t = 0; ok && t < ntiles; ++t) {
-        const int s = t % kStages2, u = t / kStages2;
+        const int s = t % kStages, u = t / kStages;
         if (!mbar_wait(&full_bar[s], u & 1, &s_abort, a.wc)) break;
         tc_fence_after();
-        const uint64_t qd0 = sdesc_kmajor_sw128(smem_u32(sQ + s * kTile2));
+        const uint64_t qd0 = sdesc_kmajor_sw128(smem_u32(sQ + s * kTile));
 #pragma unroll 1
         for (int mt = 0; mt < kMT; ++mt) {
           if (!mbar_wait(&acce_bar[mt], (t & 1) ^ 1, &s_abort, a.wc)) {
@@ -326,7 +348,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int k = 0; k < 8; ++k) {
             const uint32_t koff = (k & 3) * 32;
             const uint64_t da = kd0 + ((mt * 32768 + (k >> 2) * 16384 + koff) >> 4);
-            const uint64_t db = qd0 + (((k >> 2) * (kNT2 * 128) + koff) >> 4);
+            const uint64_t db = qd0 + (((k >> 2) * (kNT * 128) + koff) >> 4);
             umma_bf16(tbase + mt * kSlotCols, da, db, idesc, k > 0 ? 1u : 0u);
           }
           umma_commit(&accf_bar[mt]);
@@ -338,24 +360,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_drain(&done_bar, 0, status);
     }
   } else {
-    // thread = key q4*32 + lane of every M tile; warp half cg takes query rows [64cg, 64cg + 64)
+    // thread = key q4*32 + lane of every M tile; warp group cg takes query rows [32cg, 32cg + 32)
     const int q4 = warp & 3, cg = warp >> 2;
     const float s2 = a.s2;
+    const float* c2h = a.c2 + static_cast<size_t>(h) * GN;
     float best[kMT];
 #pragma unroll
     for (int mt = 0; mt < kMT; ++mt) best[mt] = -INFINITY;
     bool alive = true;
+    // -c2 of this warp's 32 query rows, loaded one tile ahead
+    auto load_c = [&](int t) {
+      const int rr = r_begin + t * kNT + cg * 32 + lane;
+      return (t < ntiles && rr < r_end) ? (a.logit ? 0.f : __ldg(c2h + rr)) : INFINITY;
+    };
+    float c_next = load_c(0);
     for (int t = 0; alive && t < ntiles; ++t) {
-      // -c2 of this warp half's 64 query rows: two coalesced loads, broadcast by shuffles
-      const int rr = r_begin + t * kNT2 + cg * 64 + lane;
-      const float c0 = rr < r_end ? (a.logit ? 0.f : __ldg(a.c2 + static_cast<size_t>(h) * GN + rr)) : INFINITY;
-      const float c1 = rr + 32 < r_end ? (a.logit ? 0.f : __ldg(a.c2 + static_cast<size_t>(h) * GN + rr + 32)) : INFINITY;
-      float nc[64];
+      const float c_cur = c_next;
+      c_next = load_c(t + 1);
+      float nc[32];
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        nc[j] = -__shfl_sync(0xffffffffu, c0, j);
-        nc[32 + j] = -__shfl_sync(0xffffffffu, c1, j);
-      }
+      for (int j = 0; j < 32; ++j) nc[j] = -__shfl_sync(0xffffffffu, c_cur, j);
 #pragma unroll
       for (int mt = 0; mt < kMT; ++mt) {
         bool ok = mbar_wait(&accf_bar[mt], t & 1, &s_abort, a.wc);
@@ -365,10 +389,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
-        float v[64];
-        const uint32_t taddr = tbase + (static_cast<uint32_t>(q4 * 32) << 16) + mt * kSlotCols + cg * 64;
-        tmem_ld32(taddr, v);
-        tmem_ld32(taddr + 32, v + 32);
+        float v[32];
+        tmem_ld32(tbase + (static_cast<uint32_t>(q4 * 32) << 16) + mt * kSlotCols + cg * 32, v);
         tmem_ld_wait();
         // the columns are in registers: hand the slot back to the UMMA warp
         tc_fence_before();
@@ -376,26 +398,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(&acce_bar[mt]);
         float b0 = best[mt], b1 = -INFINITY;
 #pragma unroll
-        for (int j = 0; j < 64; j += 4) {
+        for (int j = 0; j < 32; j += 4) {
           b0 = fmax3(b0, fmaf(v[j], s2, nc[j]), fmaf(v[j + 1], s2, nc[j + 1]));
           b1 = fmax3(b1, fmaf(v[j + 2], s2, nc[j + 2]), fmaf(v[j + 3], s2, nc[j + 3]));
         }
         best[mt] = fmaxf(b0, b1);
       }
     }
-    // every UMMA has completed (the last accumulator of each slot was waited for), so the
-    // streamed-tile buffers are free to hold the two halves' partial maxima
-    float* s_x = reinterpret_cast<float*>(sQ);   // [kMT][4][32]
-    if (cg == 1) {
+    // every UMMA has completed (each slot's last accumulator was waited for), so the
+    // streamed-tile buffers are free to hold the row groups' partial maxima
+    float* s_x = reinterpret_cast<float*>(sQ);   // [3 row groups][kMT][4][32]
+    if (cg > 0) {
 #pragma unroll
-      for (int mt = 0; mt < kMT; ++mt) s_x[(mt * 4 + q4) * 32 + lane] = best[mt];
+      for (int mt = 0; mt < kMT; ++mt) s_x[(((cg - 1) * kMT + mt) * 4 + q4) * 32 + lane] = best[mt];
     }
     epi_bar();
     if (cg == 0 && alive) {
 #pragma unroll
       for (int mt = 0; mt < kMT; ++mt) {
         const int key = key0 + mt * 128 + q4 * 32 + lane;
-        const float bm = fmaxf(best[mt], s_x[(mt * 4 + q4) * 32 + lane]);
+        float bm = best[mt];
+#pragma unroll
+        for (int g = 0; g < 3; ++g) bm = fmaxf(bm, s_x[((g * kMT + mt) * 4 + q4) * 32 + lane]);
         if (key < n && ntiles > 0) atomicMax(a.tmax + static_cast<size_t>(h) * n + key, f2key(bm));
       }
     }
@@ -451,7 +475,7 @@ cudaError_t launch_qa_rowlse(const QaArgs& a, const CUtensorMap& tq, const CUten
 }
 
 cudaError_t launch_qa_keymax(const QaArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, cudaStream_t st) {
-  const size_t smem = 1024 + 2 * kBlockHalf + kStages2 * kTile2;
+  const size_t smem = 1024 + 2 * kBlockHalf + kStages * kTile;
   cudaError_t e = ensure_smem(reinterpret_cast<const void*>(qa_keymax_kernel), smem);
   if (e != cudaSuccess) return e;
   e = cudaMemsetAsync(a.tmax, 0, static_cast<size_t>(a.H) * a.n * sizeof(uint32_t), st);

@@ -4,6 +4,7 @@
     python -m kv_cache_eviction_window_gb300.profile_case --workload 2 --value-norm l2
     python -m kv_cache_eviction_window_gb300.profile_case --workload 6      # AnchorKV anchors
     python -m kv_cache_eviction_window_gb300.profile_case --workload 2 --perturb   # + output perturbation
+    python -m kv_cache_eviction_window_gb300.profile_case --workload 5 --n-ctx 8192  # query-agnostic, smaller n
 
 The inputs are the same seeded synthetic tensors as the benchmark (each layer distinct,
 larger than L2 for the 32K stack), so per-launch counters taken here scale to the
@@ -28,6 +29,7 @@ def main():
     ap.add_argument("--plain", action="store_true", help="value_aware=0")
     ap.add_argument("--value-norm", default=None, choices=["l1", "l2"], help="value-aware norm override")
     ap.add_argument("--perturb", action="store_true", help="also run kvsel_perturbation on each layer's kept set")
+    ap.add_argument("--n-ctx", type=int, default=None, help="context length override (a smaller case of the shape)")
     args = ap.parse_args()
     import numpy as np
     import torch
@@ -43,6 +45,8 @@ def main():
         wl = wl.replace(value_aware=False)
     if args.value_norm:
         wl = wl.replace(value_norm=args.value_norm)
+    if args.n_ctx:
+        wl = wl.replace(n_ctx=args.n_ctx)
     anchors = wl.budget_mode == "anchor"
     dev = torch.device("cuda", 0)
 
