@@ -96,7 +96,7 @@ struct QaArgs {
   int n;                          // keys (context length)
   int GN;                         // query rows per head (G * n)
   int row_blocks;                 // pass 1: blocks of 512 query rows per head
-  int key_blocks;                 // pass 2: blocks of 512 keys per head
+  int key_blocks;                 // pass 2: blocks of 256 keys per head
   int row_splits;                 // pass 2: query-row slices per key block
   float s2;                       // logit scale * log2(e)
   float* c2;                      // [H][GN] row log-sum-exp, log2 units
@@ -107,7 +107,9 @@ struct QaArgs {
 };
 cudaError_t launch_qa_rowlse(const QaArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, cudaStream_t st);
 cudaError_t launch_qa_keymax(const QaArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, cudaStream_t st);
-int qa_block_rows();
+int qa_block_rows();    // pass 1: query rows per CTA
+int qa_key_block();     // pass 2: keys per CTA
+int qa_query_tile();    // pass 2: query rows per streamed tile
 
 struct VnormArgs {
   ReqTable rq;

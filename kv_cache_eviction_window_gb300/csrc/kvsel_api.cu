@@ -262,7 +262,7 @@ int make_plan(const kvsel_params* p, Plan& pl, bool need_device) {
     const long long GN = static_cast<long long>(pl.G) * n;
     const int br = qa_block_rows();
     pl.qa_row_blocks = static_cast<int>((GN + br - 1) / br);
-    pl.qa_key_blocks = (n + br - 1) / br;
+    pl.qa_key_blocks = (n + qa_key_block() - 1) / qa_key_block();
     // query-row slices per key block: at least eight CTAs per SM in all, and a whole
     // number of waves (one CTA per SM) to within 3% where a slice count up to 64 gives one
     const long long want = 8ll * pl.num_sms;
@@ -416,11 +416,12 @@ int do_score(const kvsel_params* p, const Plan& pl, const void* q, const kvsel_k
   const float scale = p->scale > 0.f ? p->scale : 1.f / std::sqrt(static_cast<float>(kHeadDim));
   if (pl.qa) {
     const int n = pl.rq.n[0];
-    CUtensorMap tq, tk128;
+    CUtensorMap tq, tq2, tk128;
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(pl.H) * pl.G * n};
     const cuuint64_t strides[1] = {kHeadDim * 2};
     const cuuint32_t box[2] = {64, 64};
-    if (!encode(&tq, q, 2, dims, strides, box)) return KVSEL_EINVAL;
+    const cuuint32_t box2[2] = {64, static_cast<cuuint32_t>(qa_query_tile())};   // pass 2: one tile per column half
+    if (!encode(&tq, q, 2, dims, strides, box) || !encode(&tq2, q, 2, dims, strides, box2)) return KVSEL_EINVAL;
     if (!kv_map(&tk128, kv->k, kv, pl, 128)) return KVSEL_EINVAL;
     QaArgs a{};
     a.H = pl.H;
@@ -443,7 +444,7 @@ int do_score(const kvsel_params* p, const Plan& pl, const void* q, const kvsel_k
     }
     {
       StageScope sc(KVSEL_STAGE_KEYSUM, st);
-      rc = launch_rc(launch_qa_keymax(a, tq, tk128, st));
+      rc = launch_rc(launch_qa_keymax(a, tq2, tk128, st));
     }
     if (rc) return rc;
     StageScope sc(KVSEL_STAGE_FINALIZE, st);

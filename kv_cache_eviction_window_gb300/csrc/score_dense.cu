@@ -10,7 +10,7 @@
 //   qa_rowlse_kernel: A = a block of 512 query rows (4 M tiles), B = 128-key tiles
 //     streamed over all n keys; every epilogue thread keeps an online (max, sum) for its
 //     rows; writes c2_r = (m_r + log2 Z_r) in log2 units.
-//   qa_keymax_kernel: A = a block of 512 keys (4 M tiles, resident), B = 128-row query
+//   qa_keymax_kernel: A = a block of 256 keys (2 M tiles, resident), B = 256-row query
 //     tiles streamed over a slice of the rows; every thread keeps max_r (l_ri*s2 - c2_r)
 //     for its keys; slices merge with an order-preserving atomicMax in global memory.
 //   qa_finish_kernel: s_raw_i = exp2(max).
@@ -47,11 +47,11 @@ __device__ __forceinline__ float key2f(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }
 
-// Both passes stream 128-row tiles, so every UMMA is 128 x 128 x 16 (N = 64 leaves the
-// tensor pipe idle between short instructions).  The resident block is four M tiles and
-// each M tile owns one 128-column TMEM accumulator; the epilogue releases it as soon as its
-// columns are in registers, so the next tile's UMMAs for that M tile start while the other
-// three are still being drained.
+// Pass 1 streams 128-key tiles against 512 resident query rows: every UMMA is 128 x 128 x 16
+// (N = 64 leaves the tensor pipe idle between short instructions) and the pass is paced by
+// its exponentials.  Each M tile owns one 128-column TMEM accumulator; the epilogue
+// releases it as soon as its columns are in registers, so the next tile's UMMAs for that M
+// tile start while the other three are still being drained.
 
 // ------------------------------------------------------------------------------------
 // pass 1: log-sum-exp of every query row over all keys
@@ -249,42 +249,50 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ------------------------------------------------------------------------------------
 // pass 2: per key, max over a slice of query rows of (l * s2 - c2_row)
 // ------------------------------------------------------------------------------------
-// The 512 resident keys are four M tiles; query rows stream as 128-row tiles, so every UMMA
-// is 128 x 128 x 16 (N = 64 leaves the tensor pipe idle between short instructions).  Each
-// M tile owns one 128-column TMEM accumulator; the epilogue releases it as soon as its
-// columns are in registers, so the next tile's UMMAs for that M tile can start while the
-// other three are still being drained.
+// This pass has no exponentials, so it runs at the tensor pipe's pace, and 128 x 256 x 16
+// UMMAs keep that pipe busier than N = 128: the resident block is 256 keys (two M tiles,
+// one 256-column accumulator slot each) and query rows stream as 256-row tiles.
+constexpr int kMT2 = 2;                       // resident 128-key M tiles
+constexpr int kNT2 = 256;                     // query rows per streamed tile (UMMA N)
+constexpr int kStages2 = 2;
+constexpr int kKBlock2 = kMT2 * 32768;        // bytes of the resident keys
+constexpr int kTile2 = kNT2 * 256;            // bytes of one streamed tile (two 64-column halves)
+constexpr uint32_t kSlotCols2 = kNT2;         // one 256-column accumulator slot per M tile
+constexpr int kRowsPerWarp2 = kNT2 / 4;       // query rows (accumulator columns) per epilogue warp
+
 __global__ void __launch_bounds__(kThreads, 1)
     qa_keymax_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                      const QaArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_align1024(smem_raw);
-  uint8_t* sK = smem;                      // [4 M tiles][2 halves][128 keys][128 B]
-  uint8_t* sQ = smem + 2 * kBlockHalf;     // [stages][2 halves][128 rows][128 B]
+  uint8_t* sK = smem;                      // [2 M tiles][2 halves][128 keys][128 B]
+  uint8_t* sQ = smem + kKBlock2;           // [stages][2 halves][256 rows][128 B]
 
-  __shared__ __align__(8) uint64_t full_bar[kStages], empty_bar[kStages], accf_bar[kMT], acce_bar[kMT];
+  __shared__ __align__(8) uint64_t full_bar[kStages2], empty_bar[kStages2], accf_bar[kMT2], acce_bar[kMT2];
   __shared__ __align__(8) uint64_t k_bar, done_bar;
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
+  __shared__ __align__(16) float s_nc[kEpiWarps][kRowsPerWarp2];   // -c2 of each warp's rows
 
   const int warp = warp_id(), lane = lane_id();
   const int per_head = a.key_blocks * a.row_splits;
   const int h = blockIdx.x / per_head;
   const int rem = blockIdx.x % per_head;
   const int kb = rem / a.row_splits, rs = rem % a.row_splits;
-  const int key0 = kb * kMT * 128;
+  const int key0 = kb * kMT2 * 128;
   const int n = a.n, GN = a.GN;
-  const int rows_per = (GN + a.row_splits - 1) / a.row_splits;
-  const int r_begin = rs * rows_per, r_end = min(GN, r_begin + rows_per);
-  const int ntiles = r_end > r_begin ? (r_end - r_begin + kNT - 1) / kNT : 0;
+  // slices are whole tiles, so a tile never straddles two slices
+  const int rows_per = ((GN + a.row_splits - 1) / a.row_splits + kNT2 - 1) / kNT2 * kNT2;
+  const int r_begin = min(GN, rs * rows_per), r_end = min(GN, r_begin + rows_per);
+  const int ntiles = r_end > r_begin ? (r_end - r_begin + kNT2 - 1) / kNT2 : 0;
   int* status = a.wc.status;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < kStages2; ++s) {
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], 1);
     }
-    for (int s = 0; s < kMT; ++s) {
+    for (int s = 0; s < kMT2; ++s) {
       mbar_init(&accf_bar[s], 1);
       mbar_init(&acce_bar[s], kEpiWarps);
     }
@@ -306,39 +314,36 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0 && ntiles > 0) {
       tma_prefetch_desc(&tq);
       tma_prefetch_desc(&tk);
-      mbar_arrive_expect_tx(&k_bar, 2 * kBlockHalf);
-      for (int mt = 0; mt < kMT; ++mt) {
+      mbar_arrive_expect_tx(&k_bar, kKBlock2);
+      for (int mt = 0; mt < kMT2; ++mt) {
         tma_load_4d(sK + mt * 32768, &tk, &k_bar, 0, key0 + mt * 128, h, 0);
         tma_load_4d(sK + mt * 32768 + 16384, &tk, &k_bar, 64, key0 + mt * 128, h, 0);
       }
       int t = 0;
       for (; t < ntiles; ++t) {
-        const int s = t % kStages, u = t / kStages;
+        const int s = t % kStages2, u = t / kStages2;
         if (!mbar_wait(&empty_bar[s], (u & 1) ^ 1, &s_abort, a.wc)) break;
-        mbar_arrive_expect_tx(&full_bar[s], kTile);
-        const int qrow = h * GN + r_begin + t * kNT;
-        uint8_t* dst = sQ + s * kTile;
-        // the tensor map's box is 64 rows x 64 columns: two row halves per column half
-        tma_load_2d(dst, &tq, &full_bar[s], 0, qrow);
-        tma_load_2d(dst + 64 * 128, &tq, &full_bar[s], 0, qrow + 64);
-        tma_load_2d(dst + kNT * 128, &tq, &full_bar[s], 64, qrow);
-        tma_load_2d(dst + kNT * 128 + 64 * 128, &tq, &full_bar[s], 64, qrow + 64);
+        mbar_arrive_expect_tx(&full_bar[s], kTile2);
+        const int qrow = h * GN + r_begin + t * kNT2;
+        // the tensor map's box is 256 rows x 64 columns: one load per column half
+        tma_load_2d(sQ + s * kTile2, &tq, &full_bar[s], 0, qrow);
+        tma_load_2d(sQ + s * kTile2 + kNT2 * 128, &tq, &full_bar[s], 64, qrow);
       }
-      for (int tt = max(0, t - kStages); tt < t; ++tt) mbar_drain(&full_bar[tt % kStages], (tt / kStages) & 1, status);
+      for (int tt = max(0, t - kStages2); tt < t; ++tt) mbar_drain(&full_bar[tt % kStages2], (tt / kStages2) & 1, status);
       mbar_drain(&k_bar, 0, status);
     }
   } else if (warp == kMmaWarp) {
     if (lane == 0 && ntiles > 0) {
       bool ok = mbar_wait(&k_bar, 0, &s_abort, a.wc);
-      constexpr uint32_t idesc = idesc_bf16_f32(128, kNT);
+      constexpr uint32_t idesc = idesc_bf16_f32(128, kNT2);
       const uint64_t kd0 = sdesc_kmajor_sw128(smem_u32(sK));
       for (int t = 0; ok && t < ntiles; ++t) {
-        const int s = t % kStages, u = t / kStages;
+        const int s = t % kStages2, u = t / kStages2;
         if (!mbar_wait(&full_bar[s], u & 1, &s_abort, a.wc)) break;
         tc_fence_after();
-        const uint64_t qd0 = sdesc_kmajor_sw128(smem_u32(sQ + s * kTile));
+        const uint64_t qd0 = sdesc_kmajor_sw128(smem_u32(sQ + s * kTile2));
 #pragma unroll 1
-        for (int mt = 0; mt < kMT; ++mt) {
+        for (int mt = 0; mt < kMT2; ++mt) {
           if (!mbar_wait(&acce_bar[mt], (t & 1) ^ 1, &s_abort, a.wc)) {
             ok = false;
             break;
@@ -348,8 +353,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int k = 0; k < 8; ++k) {
             const uint32_t koff = (k & 3) * 32;
             const uint64_t da = kd0 + ((mt * 32768 + (k >> 2) * 16384 + koff) >> 4);
-            const uint64_t db = qd0 + (((k >> 2) * (kNT * 128) + koff) >> 4);
-            umma_bf16(tbase + mt * kSlotCols, da, db, idesc, k > 0 ? 1u : 0u);
+            const uint64_t db = qd0 + (((k >> 2) * (kNT2 * 128) + koff) >> 4);
+            umma_bf16(tbase + mt * kSlotCols2, da, db, idesc, k > 0 ? 1u : 0u);
           }
           umma_commit(&accf_bar[mt]);
         }
@@ -360,28 +365,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_drain(&done_bar, 0, status);
     }
   } else {
-    // thread = key q4*32 + lane of every M tile; warp group cg takes query rows [32cg, 32cg + 32)
+    // thread = key q4*32 + lane of both M tiles; warp group cg takes query rows [64cg, 64cg + 64)
     const int q4 = warp & 3, cg = warp >> 2;
     const float s2 = a.s2;
     const float* c2h = a.c2 + static_cast<size_t>(h) * GN;
-    float best[kMT];
+    float best[kMT2];
 #pragma unroll
-    for (int mt = 0; mt < kMT; ++mt) best[mt] = -INFINITY;
+    for (int mt = 0; mt < kMT2; ++mt) best[mt] = -INFINITY;
     bool alive = true;
-    // -c2 of this warp's 32 query rows, loaded one tile ahead
-    auto load_c = [&](int t) {
-      const int rr = r_begin + t * kNT + cg * 32 + lane;
+    // c2 of this warp's 64 rows, loaded a tile ahead (two rows per lane)
+    auto load_c = [&](int t, int half) {
+      const int rr = r_begin + t * kNT2 + cg * kRowsPerWarp2 + half * 32 + lane;
       return (t < ntiles && rr < r_end) ? (a.logit ? 0.f : __ldg(c2h + rr)) : INFINITY;
     };
-    float c_next = load_c(0);
+    float cn0 = load_c(0, 0), cn1 = load_c(0, 1);
+    const float4* nc4 = reinterpret_cast<const float4*>(&s_nc[warp][0]);
     for (int t = 0; alive && t < ntiles; ++t) {
-      const float c_cur = c_next;
-      c_next = load_c(t + 1);
-      float nc[32];
+      __syncwarp();   // the previous tile's reads of s_nc are done
+      s_nc[warp][lane] = -cn0;
+      s_nc[warp][32 + lane] = -cn1;
+      __syncwarp();
+      cn0 = load_c(t + 1, 0);
+      cn1 = load_c(t + 1, 1);
 #pragma unroll
-      for (int j = 0; j < 32; ++j) nc[j] = -__shfl_sync(0xffffffffu, c_cur, j);
-#pragma unroll
-      for (int mt = 0; mt < kMT; ++mt) {
+      for (int mt = 0; mt < kMT2; ++mt) {
         bool ok = mbar_wait(&accf_bar[mt], t & 1, &s_abort, a.wc);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) {
@@ -389,8 +396,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
-        float v[32];
-        tmem_ld32(tbase + (static_cast<uint32_t>(q4 * 32) << 16) + mt * kSlotCols + cg * 32, v);
+        float v[kRowsPerWarp2];
+        const uint32_t taddr = tbase + (static_cast<uint32_t>(q4 * 32) << 16) + mt * kSlotCols2 + cg * kRowsPerWarp2;
+        tmem_ld32(taddr, v);
+        tmem_ld32(taddr + 32, v + 32);
         tmem_ld_wait();
         // the columns are in registers: hand the slot back to the UMMA warp
         tc_fence_before();
@@ -398,28 +407,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(&acce_bar[mt]);
         float b0 = best[mt], b1 = -INFINITY;
 #pragma unroll
-        for (int j = 0; j < 32; j += 4) {
-          b0 = fmax3(b0, fmaf(v[j], s2, nc[j]), fmaf(v[j + 1], s2, nc[j + 1]));
-          b1 = fmax3(b1, fmaf(v[j + 2], s2, nc[j + 2]), fmaf(v[j + 3], s2, nc[j + 3]));
+        for (int j = 0; j < kRowsPerWarp2; j += 4) {
+          const float4 c = nc4[j >> 2];   // the same address in every lane: a broadcast
+          b0 = fmax3(b0, fmaf(v[j], s2, c.x), fmaf(v[j + 1], s2, c.y));
+          b1 = fmax3(b1, fmaf(v[j + 2], s2, c.z), fmaf(v[j + 3], s2, c.w));
         }
         best[mt] = fmaxf(b0, b1);
       }
     }
     // every UMMA has completed (each slot's last accumulator was waited for), so the
     // streamed-tile buffers are free to hold the row groups' partial maxima
-    float* s_x = reinterpret_cast<float*>(sQ);   // [3 row groups][kMT][4][32]
+    float* s_x = reinterpret_cast<float*>(sQ);   // [3 row groups][kMT2][4][32]
     if (cg > 0) {
 #pragma unroll
-      for (int mt = 0; mt < kMT; ++mt) s_x[(((cg - 1) * kMT + mt) * 4 + q4) * 32 + lane] = best[mt];
+      for (int mt = 0; mt < kMT2; ++mt) s_x[(((cg - 1) * kMT2 + mt) * 4 + q4) * 32 + lane] = best[mt];
     }
     epi_bar();
     if (cg == 0 && alive) {
 #pragma unroll
-      for (int mt = 0; mt < kMT; ++mt) {
+      for (int mt = 0; mt < kMT2; ++mt) {
         const int key = key0 + mt * 128 + q4 * 32 + lane;
         float bm = best[mt];
 #pragma unroll
-        for (int g = 0; g < 3; ++g) bm = fmaxf(bm, s_x[((g * kMT + mt) * 4 + q4) * 32 + lane]);
+        for (int g = 0; g < 3; ++g) bm = fmaxf(bm, s_x[((g * kMT2 + mt) * 4 + q4) * 32 + lane]);
         if (key < n && ntiles > 0) atomicMax(a.tmax + static_cast<size_t>(h) * n + key, f2key(bm));
       }
     }
@@ -475,7 +485,7 @@ cudaError_t launch_qa_rowlse(const QaArgs& a, const CUtensorMap& tq, const CUten
 }
 
 cudaError_t launch_qa_keymax(const QaArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, cudaStream_t st) {
-  const size_t smem = 1024 + 2 * kBlockHalf + kStages * kTile;
+  const size_t smem = 1024 + kKBlock2 + kStages2 * kTile2;
   cudaError_t e = ensure_smem(reinterpret_cast<const void*>(qa_keymax_kernel), smem);
   if (e != cudaSuccess) return e;
   e = cudaMemsetAsync(a.tmax, 0, static_cast<size_t>(a.H) * a.n * sizeof(uint32_t), st);
@@ -492,6 +502,8 @@ cudaError_t launch_qa_keymax(const QaArgs& a, const CUtensorMap& tq, const CUten
 }
 
 int qa_block_rows() { return kMT * 128; }
+int qa_key_block() { return kMT2 * 128; }
+int qa_query_tile() { return kNT2; }
 
 cudaError_t launch_head_max(const ReqTable& rq, const float* s, float* out, cudaStream_t st) {
   if (rq.B * rq.H <= 0) return cudaSuccess;
