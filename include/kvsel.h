@@ -177,7 +177,8 @@ int kvsel_select(const kvsel_params* p, const float* s_attn, const float* s_val,
 /* Gather the kept K/V rows into dense per-segment buffers (bit-exact copies).
  *   idx/counts/offsets as produced by kvsel_select (device)
  *   k_out, v_out  device bf16 [n_kept][head_dim]
- * Indices outside [0, n_b) are skipped and flagged in the status word when ws != NULL. */
+ * Indices outside [0, n_b) are flagged in the status word when ws != NULL; their output
+ * rows are written as zeros.  k_out and v_out must be 16-byte aligned. */
 int kvsel_compact(const kvsel_params* p, const kvsel_kv* kv, const int32_t* idx, const int32_t* counts,
                   const int64_t* offsets, void* k_out, void* v_out, void* ws, size_t ws_bytes, void* stream);
 
