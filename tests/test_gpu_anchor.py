@@ -267,3 +267,16 @@ def test_anchor_degenerate_no_anchors_and_all_forced():
     gpu2 = run_gpu_anchors(wl2, inp2)
     ora2 = AO.run_anchor_workload_layer(wl2, inp2, project=False)
     _compare_anchor_run(wl2, inp2, gpu2, ora2)
+
+
+def test_anchor_selection_more_entries_per_cta_than_registers_hold():
+    """One KV head of 70000 keys: each CTA of the 16-CTA selection cluster holds 4375
+    entries, so the random keys of the second stage are read back from memory rather than
+    kept in registers."""
+    from oracle import anchor_oracle as AO
+
+    wl = datagen.WORKLOADS[6].replace(h_kv=1)
+    inp = datagen.make_layer(wl, 0, n_ctx=70000)
+    gpu = run_gpu_anchors(wl, inp)
+    ora = AO.run_anchor_workload_layer(wl, inp, project=False)
+    _compare_anchor_run(wl, inp, gpu, ora, sample=1500)

@@ -394,3 +394,54 @@ def test_select_after_a_smaller_cluster_query():
     run(131072, 1)
     run(1000 + 17, 2)
     run(131072, 3)
+
+
+def test_two_stage_select_more_entries_per_cta_than_registers_hold():
+    """One KV head of 70000 keys: its selection cluster of 16 CTAs gives each CTA 4375
+    entries, more than its threads keep in registers (8 x 512), so the value-aware keys of
+    the second stage are read back from the scores the selection kernel wrote."""
+    wl = datagen.WORKLOADS[2].replace(layers=1, h_kv=1, d_model=512)
+    inp = datagen.make_layer(wl, 0, n_ctx=70000)
+    ora = O.run_workload_layer(wl, inp)
+    gpu = GH.run_gpu_layer(wl, inp)
+    _check_layer(wl, inp, gpu, ora)
+
+
+def test_compact_out_of_range_index_is_zeroed_and_flagged():
+    """kvsel_compact with two out-of-range indices among valid ones: the valid rows are
+    bit-exact copies, the bad rows come out as zeros, and the status word reports it."""
+    import torch
+    from kv_cache_eviction_window_gb300 import binding as B
+
+    wl = datagen.WORKLOADS[2].replace(layers=1, h_kv=2)
+    n = 700
+    inp = datagen.make_layer(wl, 0, n_ctx=n)
+    p = B.params_from_workload(wl, n_ctx=n)
+    kc, vc = np.stack(inp["k"]), np.stack(inp["v"])   # [1][H][n][d]
+    kt, vt = GH.torch_bf16(kc), GH.torch_bf16(vc)
+    kv = B.make_kv_contiguous(kt, vt)
+    rng = np.random.default_rng(3)
+    per_head = [np.sort(rng.choice(n, size=150, replace=False)).astype(np.int32) for _ in range(wl.h_kv)]
+    per_head[0][10] = n + 5      # past the context
+    per_head[1][77] = -3         # negative
+    flat = np.concatenate(per_head)
+    counts = np.array([len(x) for x in per_head], np.int32)
+    offsets = np.array([0, len(per_head[0])], np.int64)
+    ws = torch.zeros(B.kvsel_workspace_size(p) // 4 + 64, dtype=torch.int32, device="cuda")
+    B.kvsel_workspace_init(ws)
+    k_out = torch.full((len(flat), wl.head_dim), 7.0, dtype=torch.bfloat16, device="cuda")
+    v_out = torch.full((len(flat), wl.head_dim), 7.0, dtype=torch.bfloat16, device="cuda")
+    B.kvsel_compact(p, kv, torch.from_numpy(flat).cuda(), torch.from_numpy(counts).cuda(),
+                    torch.from_numpy(offsets).cuda(), k_out, v_out, ws)
+    torch.cuda.synchronize()
+    assert B.kvsel_get_device_status(ws) == B.KVSEL_EDEVICE
+    ko = k_out.cpu().view(torch.int16).numpy().view(np.uint16)
+    vo = v_out.cpu().view(torch.int16).numpy().view(np.uint16)
+    for h in range(wl.h_kv):
+        o = int(offsets[h])
+        for r, i in enumerate(per_head[h]):
+            if 0 <= i < n:
+                np.testing.assert_array_equal(ko[o + r], kc[0, h, i])
+                np.testing.assert_array_equal(vo[o + r], vc[0, h, i])
+            else:
+                assert not ko[o + r].any() and not vo[o + r].any(), f"head {h} row {r}"
