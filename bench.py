@@ -336,7 +336,20 @@ def time_anchor_path(B, datagen, wl_stack, q_d, kvs, ws, stream, K, W, L, world,
                            "tensor_frac": pflops / (pms * 1e-3) / 1e12 / tc}}
 
 
-def time_query_agnostic(B, datagen, stream, dev, pk, K, W):
+def binding_roofline(seconds, nbytes, flops, exps, pk, ex2_per_s):
+    """The time each resource alone would need (bytes at the measured HBM copy rate, flops
+    at the measured bf16 burst rate, exponentials at the measured ex2 rate), the largest of
+    them (the binding one) and its share of the measured time."""
+    terms = {"hbm_us": nbytes / (pk.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]) * 1e9) * 1e6,
+             "tensor_us": flops / (pk.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]) * 1e12) * 1e6}
+    if ex2_per_s:
+        terms["ex2_us"] = exps / ex2_per_s * 1e6
+    binding = max(terms, key=terms.get)
+    return {"terms": terms, "binding": binding[:-3], "time_lb_us": terms[binding],
+            "fraction": terms[binding] / (seconds * 1e6)}
+
+
+def time_query_agnostic(B, datagen, stream, dev, pk, K, W, ex2_per_s=None):
     """KVzip's query-agnostic scoring on the Llama-3.1-70B 32K layer shape (all G*n = 262144
     positions of a KV head as queries, non-causal): the softmax score (row log-sum-exp
     pass, then the per-key max pass) and the softmax-free KVzip-logit score (one pass),
@@ -378,9 +391,12 @@ def time_query_agnostic(B, datagen, stream, dev, pk, K, W):
         ms_layer = timed(lambda: B.kvsel_run_layer(p, q, kv, None, b.s_attn, None, b.idx, b.counts, b.offsets,
                                                     b.k_out, b.v_out, b.ws, stream))
         flops = passes * 2.0 * G * n * n * d * H
+        exps = (G * n * n * H) if passes == 2 else 0   # the row log-sum-exp pass
+        qbytes = H * G * n * d * 2 + H * n * d * 2
         res[name] = {"score_ms": ms_score, "layer_ms": ms_layer, "score_tflops": flops / (ms_score * 1e-3) / 1e12,
                      "tensor_frac": flops / (ms_score * 1e-3) / 1e12 / tc, "flops": flops,
-                     "entries_per_s": H * n / (ms_layer * 1e-3), "device_status": B.kvsel_get_device_status(b.ws)}
+                     "entries_per_s": H * n / (ms_layer * 1e-3), "device_status": B.kvsel_get_device_status(b.ws),
+                     "roofline_bound": binding_roofline(ms_score * 1e-3, qbytes, flops, exps, pk, ex2_per_s)}
         del b
     del q, kt, vt
     torch.cuda.empty_cache()
@@ -606,6 +622,17 @@ def main():
            "gpu_launches": K * launches_per_step, "device_status": status, "roofline": roof, "launch": launch_mode,
            "stage_ms_per_layer": {k: (round(v, 5) if v else v) for k, v in stage_ms.items()}}
 
+    # the exponential unit's measured rate: the co-bound of the softmax passes
+    ex2_rate = None
+    try:
+        torch.cuda.synchronize()
+        scratch = torch.empty(1 << 16, dtype=torch.uint8, device=dev)   # >= 16 bytes per SM
+        ex2_rate = B.kvsel_probe_ex2_rate(scratch)
+        out["sfu"] = {"what": "MUFU ex2.approx.ftz.f32 throughput (kvsel_probe_ex2_rate: one CTA per SM, "
+                              "independent chains)", "ex2_per_clk_per_sm": ex2_rate[0], "ex2_per_s": ex2_rate[1]}
+    except Exception as e:  # pragma: no cover - reported, not fatal
+        out["sfu"] = {"unavailable": str(e)[:200]}
+
     def time_variant(p):
         """ms per layer of the same layers under parameters p (graph replay when possible)."""
         for _ in range(W):
@@ -640,10 +667,14 @@ def main():
         pms = time_variant(B.params_from_workload(wl, value_aware=False))
         alg = H * n * d * 2 + kept_rw + small
         gbs = alg / (pms * 1e-3) / 1e9
+        R = wl.group * wl.window
         out["hbm_path"] = {"what": "same layers, value_aware=0 (score+select+compact, no W_O pass)",
                            "ms_per_layer": pms, "entries_per_s": H * n / (pms * 1e-3) * world,
                            "algorithmic_bytes_per_layer": alg, "achieved_gbs": gbs,
-                           "peak_gbs": pk.get("hbm_gbs"), "frac": gbs / pk.get("hbm_gbs", 6800.0)}
+                           "peak_gbs": pk.get("hbm_gbs"), "frac": gbs / pk.get("hbm_gbs", 6800.0),
+                           # two scoring passes: 2*R*d flop and R exponentials per key and pass
+                           "roofline_bound": binding_roofline(pms * 1e-3, alg, 2 * 2.0 * R * d * n * H, 2 * R * n * H,
+                                                              pk, ex2_rate[1] if ex2_rate else None)}
         # ---- the L2 value norm through the d x d Gram matrix (CriticalKV App. C.3 distance)
         lms = time_variant(B.params_from_workload(wl, value_norm="l2"))
         alg2 = 2 * H * n * d * 2 + wl.d_model * wl.h_kv * wl.group * d * 2 + 2 * H * Bh * d * 2 + small
@@ -661,7 +692,8 @@ def main():
         # ---- output perturbation of the kept sets (CriticalKV Table 9 on synthetic data)
         out["perturbation"] = perturbation_table(B, wl, q_d, kvs, w_d, bufs, stream, dev, pk)
         # ---- KVzip query-agnostic scoring (softmax and softmax-free) on its own layer shape
-        out["query_agnostic_path"] = time_query_agnostic(B, datagen, stream, dev, pk, max(K // 2, 2), W)
+        out["query_agnostic_path"] = time_query_agnostic(B, datagen, stream, dev, pk, max(K // 2, 2), W,
+                                                         ex2_per_s=ex2_rate[1] if ex2_rate else None)
 
     # ---- end to end through the public API: pinned host -> device each step, results back
     if not args.no_e2e:

@@ -250,6 +250,16 @@ void kvsel_set_stage_events(void* const* events);
  * capture).  The difference across a call is that call's kernel count.  Never fails. */
 uint64_t kvsel_launch_count(void);
 
+/* Measured throughput of the GPU's exponential unit (ex2.approx.ftz.f32, the instruction
+ * every softmax exponential of the path uses): one CTA per SM runs independent ex2 chains
+ * for about a millisecond on the current device's legacy default stream.
+ *   scratch         device, 16-byte aligned, at least 16 * (number of SMs) bytes
+ *   per_clk_per_sm  host out: ex2 results per SM clock per SM (the CTAs' cycle counts)
+ *   per_second      host out: ex2 results per second over the device (CUDA events)
+ * Synchronises the device.  KVSEL_EINVAL for null or short arguments, KVSEL_EWORKSPACE for
+ * too small a scratch, KVSEL_ECUDA on a CUDA error. */
+int kvsel_probe_ex2_rate(void* scratch, size_t scratch_bytes, double* per_clk_per_sm, double* per_second);
+
 /* Head-level scores (KVzip §3.4, §3.6): head_out[b*h_kv + h] = the maximum over the
  * sequence of request b, head h of `scores` (packed as kvsel_score writes them, device fp32
  * [n_scores]); -inf for an empty request.  head_out: device fp32 [batch*h_kv].  Asynchronous

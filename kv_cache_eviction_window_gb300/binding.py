@@ -35,7 +35,7 @@ EXPORTS = ("kvsel_workspace_size", "kvsel_output_size", "kvsel_workspace_init", 
            "kvsel_select", "kvsel_compact", "kvsel_run_layer", "kvsel_get_device_status",
            "kvsel_set_wait_limit", "kvsel_set_stage_events", "kvsel_strerror", "kvsel_version",
            "kvsel_score_noalloc", "kvsel_launch_count", "kvsel_head_scores", "kvsel_anchor_project",
-           "kvsel_run_anchors", "kvsel_perturbation_workspace_size", "kvsel_perturbation")
+           "kvsel_run_anchors", "kvsel_perturbation_workspace_size", "kvsel_perturbation", "kvsel_probe_ex2_rate")
 NOALLOC_SCRATCH_BYTES = 16 << 20
 STAGES = ("rowstats", "keysum", "wbar", "vnorm", "finalize", "select", "compact", "project", "perturb")
 
@@ -110,6 +110,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
         "kvsel_run_anchors": ([P, vp, K] + [vp] * 12 + [sz, vp], ctypes.c_int),
         "kvsel_perturbation_workspace_size": ([P, ctypes.POINTER(sz)], ctypes.c_int),
         "kvsel_perturbation": ([P, vp, K, vp, vp, vp, vp, vp, vp, sz, vp], ctypes.c_int),
+        "kvsel_probe_ex2_rate": ([vp, sz, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double)],
+                                 ctypes.c_int),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -222,6 +224,15 @@ def kvsel_strerror(code: int) -> str:
 
 def kvsel_launch_count() -> int:
     return int(load().kvsel_launch_count())
+
+
+def kvsel_probe_ex2_rate(scratch) -> tuple:
+    """(ex2 per clock per SM, ex2 per second on the device) from the exponential-unit probe;
+    `scratch` is a device tensor of at least 16 bytes per SM."""
+    per_clk, per_s = ctypes.c_double(), ctypes.c_double()
+    _check(load().kvsel_probe_ex2_rate(_ptr(scratch), scratch.numel() * scratch.element_size(), ctypes.byref(per_clk),
+                                       ctypes.byref(per_s)), "kvsel_probe_ex2_rate")
+    return per_clk.value, per_s.value
 
 
 def kvsel_head_scores(params, scores, head_out, stream=None) -> None:

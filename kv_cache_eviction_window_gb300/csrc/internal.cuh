@@ -264,4 +264,8 @@ struct CompactArgs {
 };
 cudaError_t launch_compact(const CompactArgs& a, int max_count, int num_sms, cudaStream_t st);
 
+// Exponential-unit throughput probe (one CTA per SM): ex2 count per CTA for `iters`.
+cudaError_t probe_ex2(int sms, int iters, float* sink, unsigned long long* cycles, cudaStream_t st);
+double probe_ex2_per_cta(int iters);
+
 }  // namespace kvsel

@@ -9,6 +9,7 @@
 #include <cstring>
 #include <map>
 #include <mutex>
+#include <vector>
 
 #include "../../include/kvsel.h"
 #include "internal.cuh"
@@ -872,6 +873,41 @@ int kvsel_head_scores(const kvsel_params* p, const float* scores, float* head_ou
 }
 
 const char* kvsel_version(void) { return "kvsel 0.1 (sm_103a)"; }
+
+int kvsel_probe_ex2_rate(void* scratch, size_t scratch_bytes, double* per_clk_per_sm, double* per_second) {
+  if (!scratch || !per_clk_per_sm || !per_second || (reinterpret_cast<uintptr_t>(scratch) & 15u)) return KVSEL_EINVAL;
+  int sms = 0;
+  if (device_sms(&sms) || sms < 1) return KVSEL_ECUDA;
+  if (scratch_bytes < 16u * static_cast<size_t>(sms)) return KVSEL_EWORKSPACE;
+  constexpr int kIters = 4096;
+  auto* cycles = static_cast<unsigned long long*>(scratch);
+  auto* sink = reinterpret_cast<float*>(cycles + sms);
+  cudaEvent_t e0 = nullptr, e1 = nullptr;
+  int rc = KVSEL_ECUDA;
+  std::vector<unsigned long long> host(static_cast<size_t>(sms));
+  float ms = 0.f;
+  if (cudaEventCreate(&e0) != cudaSuccess || cudaEventCreate(&e1) != cudaSuccess) goto done;
+  if (kvsel::probe_ex2(sms, kIters / 8, sink, cycles, nullptr) != cudaSuccess) goto done;   // warm-up
+  if (cudaEventRecord(e0, nullptr) != cudaSuccess) goto done;
+  if (kvsel::probe_ex2(sms, kIters, sink, cycles, nullptr) != cudaSuccess) goto done;
+  if (cudaEventRecord(e1, nullptr) != cudaSuccess || cudaEventSynchronize(e1) != cudaSuccess) goto done;
+  if (cudaEventElapsedTime(&ms, e0, e1) != cudaSuccess || ms <= 0.f) goto done;
+  if (cudaMemcpy(host.data(), cycles, sizeof(unsigned long long) * sms, cudaMemcpyDeviceToHost) != cudaSuccess)
+    goto done;
+  {
+    unsigned long long cmax = 1;
+    for (unsigned long long c : host) cmax = c > cmax ? c : cmax;
+    const double per_cta = kvsel::probe_ex2_per_cta(kIters);
+    *per_clk_per_sm = per_cta / static_cast<double>(cmax);
+    *per_second = per_cta * sms / (static_cast<double>(ms) * 1e-3);
+    rc = KVSEL_OK;
+  }
+done:
+  if (rc != KVSEL_OK) cudaGetLastError();
+  if (e0) cudaEventDestroy(e0);
+  if (e1) cudaEventDestroy(e1);
+  return rc;
+}
 
 const char* kvsel_strerror(int code) {
   switch (code) {

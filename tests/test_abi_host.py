@@ -125,3 +125,11 @@ def test_query_agnostic_sizes(B):
            budget_mode="layer", budget_ratio=0.3, n_ctx=32768)
     n_scores, n_kept, n_seg = B.kvsel_output_size(p)
     assert (n_scores, n_kept, n_seg) == (8 * 32768, math.floor(0.3 * 32768 * 8), 8)
+
+
+def test_ex2_probe_rejects_null_and_misaligned_arguments(B):
+    lib = B.load()
+    a, b = ctypes.c_double(), ctypes.c_double()
+    assert lib.kvsel_probe_ex2_rate(None, 4096, ctypes.byref(a), ctypes.byref(b)) == B.KVSEL_EINVAL
+    assert lib.kvsel_probe_ex2_rate(ctypes.c_void_p(16), 4096, None, ctypes.byref(b)) == B.KVSEL_EINVAL
+    assert lib.kvsel_probe_ex2_rate(ctypes.c_void_p(24), 4096, ctypes.byref(a), ctypes.byref(b)) == B.KVSEL_EINVAL

@@ -445,3 +445,19 @@ def test_compact_out_of_range_index_is_zeroed_and_flagged():
                 np.testing.assert_array_equal(vo[o + r], vc[0, h, i])
             else:
                 assert not ko[o + r].any() and not vo[o + r].any(), f"head {h} row {r}"
+
+
+def test_ex2_probe_rate_is_plausible():
+    """The exponential-unit probe: a positive rate per SM clock within what an SM can issue,
+    and a device rate consistent with it at a clock between 0.5 and 3 GHz."""
+    import torch
+    from kv_cache_eviction_window_gb300 import binding as B
+
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    per_clk, per_s = B.kvsel_probe_ex2_rate(torch.empty(16 * sms, dtype=torch.uint8, device="cuda"))
+    assert 4.0 <= per_clk <= 128.0, per_clk
+    ghz = per_s / (per_clk * sms) / 1e9
+    assert 0.5 <= ghz <= 3.0, ghz
+    with pytest.raises(B.KvselError) as e:
+        B.kvsel_probe_ex2_rate(torch.empty(16 * sms - 16, dtype=torch.uint8, device="cuda"))
+    assert e.value.code == B.KVSEL_EWORKSPACE
