@@ -41,6 +41,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-plain", action="store_true")
+    # internal: one oracle unit in this process (spawned with one BLAS / OpenMP thread)
+    ap.add_argument("--oracle-unit", action="store_true", help=argparse.SUPPRESS)
     return ap.parse_args()
 
 
@@ -202,6 +204,34 @@ def run_cpu_baseline(wl, layers, budget_s=12.0):
     return {"value": done / dt, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
             "sample": f"{units} (layer, KV head) units of {wl.n_ctx} entries each from layers 0.., "
                       f"all score+select+compact steps (fp64 numpy, BLAS threads = host cores); {dt:.1f} s"}
+
+
+def run_oracle_unit():
+    """One (layer 0, KV head 0) unit of the oracle; prints its entries/s as JSON."""
+    from kv_cache_eviction_window_gb300 import datagen
+
+    wl = datagen.WORKLOADS[WORKLOAD_ID]
+    inputs = datagen.make_layer(wl, 0)
+    t0 = time.perf_counter()
+    done = oracle_sample(wl, inputs, [0])
+    print(json.dumps({"entries_per_s": done / (time.perf_counter() - t0)}), flush=True)
+    return 0
+
+
+def run_cpu_baseline_single_thread():
+    """The same oracle unit in a fresh interpreter limited to one BLAS / OpenMP thread."""
+    env = dict(os.environ)
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "NUMEXPR_NUM_THREADS"):
+        env[k] = "1"
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    try:
+        r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-unit"], env=env,
+                           capture_output=True, text=True, timeout=180)
+        line = [ln for ln in r.stdout.splitlines() if ln.startswith("{")][-1]
+        return {"value": json.loads(line)["entries_per_s"], "unit": UNIT, "cores": 1,
+                "sample": "one (layer, KV head) unit; BLAS and OpenMP limited to one thread"}
+    except Exception as e:  # pragma: no cover - reported, not fatal
+        return {"unavailable": str(e)[:200]}
 
 
 def run_reference(args):
@@ -453,6 +483,8 @@ def perturbation_table(B, wl, q_d, kvs, w_d, bufs, stream, dev, pk, layers=4):
 
 def main():
     args = parse()
+    if args.oracle_unit:
+        return run_oracle_unit()
     if args.impl == "reference":
         return run_reference(args)
     import numpy as np
@@ -749,6 +781,7 @@ def main():
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = run_cpu_baseline(wl, host)
+        out["cpu_baseline"]["single_thread"] = run_cpu_baseline_single_thread()
     out["input_generation_s"] = round(t_gen, 2)
     if rank == 0:
         print(json.dumps(out), flush=True)
