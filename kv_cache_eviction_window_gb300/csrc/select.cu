@@ -192,9 +192,10 @@ __device__ void radix_select(cgx::cluster_group& cl, SelShared& S, SelState& st,
     prefix = S.res_prefix;
     krem = S.res_krem;
     mask |= 0xFFu << sh;
-    if (krem == S.res_bin && prefix != 0u && pass < 3) {
-      // every key of the threshold bin is taken: the selection is all keys >= prefix,
-      // i.e. keys > prefix - 1 with no ties to resolve (the same decision in every CTA)
+    if (krem == S.res_bin && prefix != 0u) {
+      // every key of the threshold bin is taken (after the last pass: every key equal to
+      // the threshold): the selection is all keys >= prefix, i.e. keys > prefix - 1 with
+      // no ties to resolve (the same decision in every CTA)
       ++st.pass;
       T = prefix - 1u;
       krem_out = 0;
@@ -444,15 +445,19 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelectArgs a,
   if (!per_layer) {
     const uint32_t B = static_cast<uint32_t>(a.budget[b]);
     if (a.two_stage) {
-      // stage 1: b' = max(floor(alpha*B), |F|) entries by the attention score
+      // stage 1: b' = max(floor(alpha*B), |F|) entries by the attention score.  Without
+      // ties to resolve (krem == 0, the usual case) the picks are exactly the keys above T
+      // and need no ordered pass; otherwise they are flagged in index order.
       radix_select(cl, S, sst, keys, cnt, static_cast<uint32_t>(a.budget1[b]), T, krem);
-      apply_selection(cl, S, sst, keys, 0, cnt, T, krem, [&](int e, uint32_t) { flag[e] = 1; });
+      const bool by_threshold = (krem == 0u);
+      if (!by_threshold)
+        apply_selection(cl, S, sst, keys, 0, cnt, T, krem, [&](int e, uint32_t) { flag[e] = 1; });
       // stage 2: the remaining B - b' by the value-aware score, stage-1 picks forced in
       if (k2_reg) {
 #pragma unroll
         for (int u = 0; u < kBatch; ++u) {
           const int e = u * kThreads + static_cast<int>(threadIdx.x);
-          if (e < cnt) keys[e] = flag[e] ? kKeyMax : k2[u];
+          if (e < cnt) keys[e] = (by_threshold ? keys[e] > T : flag[e] != 0) ? kKeyMax : k2[u];
         }
       } else {
         // each thread reads back only values it wrote itself, so plain loads see them
@@ -466,7 +471,7 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelectArgs a,
 #pragma unroll
           for (int u = 0; u < kBatch; ++u) {
             const int e = e0 + u * kThreads + threadIdx.x;
-            if (e < cnt) keys[e] = flag[e] ? kKeyMax : f2key(v[u]);
+            if (e < cnt) keys[e] = (by_threshold ? keys[e] > T : flag[e] != 0) ? kKeyMax : f2key(v[u]);
           }
         }
       }
