@@ -531,7 +531,10 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelectArgs a,
       }
     }
   }
-  cl.sync();   // no CTA leaves while others may still read its shared memory
+  // per-layer mode: rank 0 has just read the other CTAs' head counts, so no CTA leaves
+  // before it is done.  Per-head mode makes no remote access after the apply step's own
+  // cluster barrier, so its CTAs may leave at once.
+  if (per_layer) cl.sync();
 }
 
 size_t select_smem(int chunk_cap) {
