@@ -57,6 +57,11 @@ __device__ __forceinline__ uint32_t cluster_addr(const void* p, uint32_t rank) {
 __device__ __forceinline__ void red_add_cluster(uint32_t addr, uint32_t v) {
   asm volatile("red.relaxed.cluster.shared::cluster.add.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
+// The two halves of a cluster barrier, so that independent work can run between them.
+__device__ __forceinline__ void cluster_arrive_release() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait_acquire() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
 __device__ __forceinline__ void st_cluster(uint32_t addr, uint32_t v) {
   asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
@@ -321,6 +326,13 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelectArgs a,
   const int ns = a.n_sink, nr = a.n_recent;
   const int nforced = min(n, ns + nr);
 
+  // the buffers other CTAs add into are zeroed first; the matching wait comes after the
+  // pooling below, so the cluster barrier's latency hides behind it
+  if (threadIdx.x < kMaxHeads) S.head_cnt[threadIdx.x] = 0;
+  for (int i = threadIdx.x; i < 3 * kBins; i += kThreads) (&S.merged[0][0])[i] = 0;
+  for (int i = threadIdx.x; i < kWarps * kBins; i += kThreads) (&S.whist[0][0])[i] = 0;
+  cluster_arrive_release();
+
   const bool pool_mode = a.raw != nullptr;
   // stage-2 scores: the value-aware score this kernel writes, or the caller's array
   // (value-aware scores computed earlier, or the anchors' random keys)
@@ -435,11 +447,9 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelectArgs a,
     }
   }
 
-  if (threadIdx.x < kMaxHeads) S.head_cnt[threadIdx.x] = 0;
-  for (int i = threadIdx.x; i < 3 * kBins; i += kThreads) (&S.merged[0][0])[i] = 0;
-  for (int i = threadIdx.x; i < kWarps * kBins; i += kThreads) (&S.whist[0][0])[i] = 0;
   SelState sst;
-  cl.sync();   // every CTA's buffers are zero before any remote reduction lands
+  cluster_wait_acquire();   // every CTA's buffers are zero before any remote reduction lands
+  __syncthreads();          // the keys built above are visible to every thread
 
   uint32_t T, krem;
   if (!per_layer) {
