@@ -461,3 +461,36 @@ def test_ex2_probe_rate_is_plausible():
     with pytest.raises(B.KvselError) as e:
         B.kvsel_probe_ex2_rate(torch.empty(16 * sms - 16, dtype=torch.uint8, device="cuda"))
     assert e.value.code == B.KVSEL_EWORKSPACE
+
+
+def test_c4_full_batch_sampled():
+    """The ragged serving batch at full size: 16 requests of 2048-65536 tokens in a paged
+    cache (block 16, shuffled block table), value-aware.  Per request, one head's pooled
+    scores are checked against the oracle in full and its value-aware scores on sampled
+    tokens; every head's kept set is checked as the two-stage top-B of the GPU's own scores,
+    and every compacted row against the cache, bit for bit."""
+    wl = datagen.WORKLOADS[4]
+    inp = datagen.make_layer(wl, 0)
+    gpu = GH.run_gpu_layer(wl, inp)
+    plain = wl.replace(value_aware=False)
+    rng = np.random.default_rng(11)
+    w_o = O.bf16_to_f64(inp["w_o"])
+    for b, g in enumerate(gpu):
+        n = g["n"]
+        assert g["status"] == 0
+        h = b % wl.h_kv
+        one = {"q": inp["q"][b:b + 1], "k": [inp["k"][b]], "v": [inp["v"][b]], "w_o": inp["w_o"], "n_ctx": [n]}
+        o = O.run_workload_layer(plain, one, heads=[h], compact_out=False)[0]
+        GH.assert_scores_close(g["s_attn"][h], o["s_pool"][h], f"s_attn req {b} head {h}")
+        sample = np.concatenate([rng.choice(n, 128, replace=False), np.arange(4), n - np.arange(1, 5)])
+        v = O.bf16_to_f64(inp["v"][b][h][sample])
+        want = O.combine(o["s_pool"][h][sample], O.value_norm(v, w_o, h, wl.group), wl.eps)
+        GH.assert_scores_close(g["s_val"][h][sample], want, f"s_val sample req {b} head {h}")
+        fm = O.forced_mask(n, wl.n_sink, wl.n_recent)
+        B = O.head_budget(n, wl.budget_ratio)
+        b1 = max(int(math.floor(wl.alpha * B)), int(fm.sum()))
+        for hh in range(wl.h_kv):
+            k1 = GH.topk_mask(g["s_attn"][hh], fm, b1)
+            GH.check_topk_property(g["s_val"][hh], g["idx"][hh], k1, B, f"two-stage req {b} head {hh}")
+            np.testing.assert_array_equal(g["k_out"][hh], inp["k"][b][hh][g["idx"][hh]])
+            np.testing.assert_array_equal(g["v_out"][hh], inp["v"][b][hh][g["idx"][hh]])
