@@ -494,3 +494,31 @@ def test_c4_full_batch_sampled():
             GH.check_topk_property(g["s_val"][hh], g["idx"][hh], k1, B, f"two-stage req {b} head {hh}")
             np.testing.assert_array_equal(g["k_out"][hh], inp["k"][b][hh][g["idx"][hh]])
             np.testing.assert_array_equal(g["v_out"][hh], inp["v"][b][hh][g["idx"][hh]])
+
+
+def test_c2_full_layer_l2_norm_sampled():
+    """The L2 value norm (the d x d Gram path) on the 32K Llama-3.1-8B layer: value-aware
+    scores on 264 sampled tokens per head against the oracle's ||W_h v||_2, the kept set as
+    the two-stage top-B of the GPU's own scores, and the compacted rows bit for bit."""
+    wl = datagen.WORKLOADS[2].replace(value_norm="l2")
+    inp = datagen.make_layer(wl, 0)
+    g = GH.run_gpu_layer(wl, inp)[0]
+    assert g["status"] == 0
+    n = wl.n_ctx
+    o = O.run_workload_layer(wl.replace(value_aware=False), inp, compact_out=False, heads=list(range(wl.h_kv)))[0]
+    rng = np.random.default_rng(4)
+    w_o = O.bf16_to_f64(inp["w_o"])
+    fm = O.forced_mask(n, wl.n_sink, wl.n_recent)
+    B = O.head_budget(n, wl.budget_ratio)
+    b1 = max(int(math.floor(wl.alpha * B)), int(fm.sum()))
+    for h in range(wl.h_kv):
+        GH.assert_scores_close(g["s_attn"][h], o["s_pool"][h], f"s_attn h{h}")
+        sample = np.concatenate([rng.choice(n, 256, replace=False), np.arange(4), n - np.arange(1, 5)])
+        v = O.bf16_to_f64(inp["v"][0][h][sample])
+        nu = O.value_norm(v, w_o, h, wl.group, norm="l2")
+        GH.assert_scores_close(g["s_val"][h][sample], O.combine(o["s_pool"][h][sample], nu, wl.eps),
+                               f"s_val (L2) sample h{h}")
+        k1 = GH.topk_mask(g["s_attn"][h], fm, b1)
+        GH.check_topk_property(g["s_val"][h], g["idx"][h], k1, B, f"two-stage (L2) h{h}")
+        np.testing.assert_array_equal(g["k_out"][h], inp["k"][0][h][g["idx"][h]])
+        np.testing.assert_array_equal(g["v_out"][h], inp["v"][0][h][g["idx"][h]])
