@@ -19,7 +19,8 @@ Sources (cited by page title and section):
          un-replicated cache), §6.5 (softmax-free variant, KVzip-logit), §7.1
          (variable-length decode).
   [VKV]  "VestigeKV: The NoPE-MLA KV Cache Carries Its Own Eviction Signal in a Vestigial
-         Branch": §4.1 (4 sinks + recent window are always kept).
+         Branch": §4.1 (4 sinks + recent window are always kept; evicted rows are
+         archived, not deleted: kept and archived sides partition the positions).
   [AKV]  "AnchorKV: Anchor-Residual KV Cache Compression": §3.2 (recent window always
          kept; SnapKV pooled scoring).
 
@@ -292,6 +293,21 @@ def compact(x: np.ndarray, idx: np.ndarray) -> np.ndarray:
     """Kept rows of one KV head's cache in index order ([KVZ] §4.2: eviction acts on the
     un-replicated KV head; §7.1: per-head variable-length result)."""
     return x[np.asarray(idx, dtype=np.int64)]
+
+
+def partition(n: int, idx: np.ndarray):
+    """Kept positions and their complement, the evicted ones, both ascending ([VKV] §4.1:
+    eviction moves rows from the hot cache to an archive and deletes nothing, so every
+    position of [0, n) is in exactly one of the two sets)."""
+    kept = np.zeros(n, dtype=bool)
+    kept[np.asarray(idx, dtype=np.int64)] = True
+    return np.flatnonzero(kept), np.flatnonzero(~kept)
+
+
+def archive(x: np.ndarray, idx: np.ndarray) -> np.ndarray:
+    """Evicted rows of one KV head's cache in index order ([VKV] §4.1: the archive side of
+    the partition, bit-exact)."""
+    return x[partition(x.shape[0], idx)[1]]
 
 
 def unpage(pool: np.ndarray, table: np.ndarray, n: int) -> np.ndarray:

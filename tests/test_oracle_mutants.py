@@ -202,6 +202,22 @@ def _pt_slice_transposed(q, k, v, w_o, h, group, keep, scale=None, causal=True):
     return out
 
 
+def _partition_drops_last(n, idx):
+    kept = np.zeros(n, dtype=bool)
+    kept[np.asarray(idx, dtype=np.int64)] = True
+    return np.flatnonzero(kept), np.flatnonzero(~kept[:-1])
+
+
+def _partition_one_based(n, idx):
+    kept = np.zeros(n + 1, dtype=bool)
+    kept[np.asarray(idx, dtype=np.int64) + 1] = True
+    return np.flatnonzero(kept[:n]), np.flatnonzero(~kept[:n])
+
+
+def _archive_descending(x, idx):
+    return x[O.partition(x.shape[0], idx)[1][::-1]]
+
+
 P_MUTANTS = {
     "perturbation_no_renormalise": ("masked_weights", _pt_no_renormalise),
     "perturbation_theta_2_minus_a": ("perturbation_rows", _pt_theta_2_minus_a),
@@ -238,6 +254,9 @@ MUTANTS = {
     "logit_first_group_head": ("query_agnostic_logit_scores", _logit_first_group_head_only),
     "head_scores_mean": ("head_scores", _head_scores_mean),
     "value_norm_l2_no_sqrt": ("value_norm", _value_norm_l2_no_sqrt),
+    "partition_drops_last": ("partition", _partition_drops_last),
+    "partition_one_based": ("partition", _partition_one_based),
+    "archive_descending": ("archive", _archive_descending),
 }
 
 

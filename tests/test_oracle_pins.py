@@ -498,6 +498,46 @@ def test_compact_and_paging():
     np.testing.assert_array_equal(O.compact(k, np.arange(k.shape[0])), k)
 
 
+# --------------------------------------------------------------------- partition / archive
+def test_partition_hand_example():
+    """VestigeKV §4.1: eviction archives rows instead of deleting them.  By hand: of the
+    positions 0..5, keeping 0, 2 and 5 leaves 1, 3 and 4 for the archive; the archived
+    rows are those rows in position order."""
+    kept, ev = O.partition(6, np.array([5, 0, 2]))
+    assert kept.tolist() == [0, 2, 5]
+    assert ev.tolist() == [1, 3, 4]
+    x = np.arange(12, dtype=np.uint16).reshape(6, 2)
+    np.testing.assert_array_equal(O.archive(x, np.array([0, 2, 5])), np.array([[2, 3], [6, 7], [8, 9]]))
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_partition_invariants_and_reassembly(seed):
+    """Both sides ascending, disjoint, together exactly [0, n); kept rows and archived rows
+    put back at their positions give the cache again, bit for bit."""
+    rng = np.random.default_rng(seed)
+    n = int(rng.integers(1, 300))
+    b = int(rng.integers(0, n + 1))
+    idx = np.sort(rng.choice(n, size=b, replace=False))
+    kept, ev = O.partition(n, idx)
+    assert np.all(np.diff(kept) > 0) and np.all(np.diff(ev) > 0)
+    assert len(kept) + len(ev) == n
+    assert not set(kept.tolist()) & set(ev.tolist())
+    assert sorted(kept.tolist() + ev.tolist()) == list(range(n))
+    x = rng.integers(0, 1 << 16, size=(n, 4), dtype=np.uint16)
+    back = np.zeros_like(x)
+    back[kept] = O.compact(x, idx)
+    back[ev] = O.archive(x, idx)
+    np.testing.assert_array_equal(back, x)
+
+
+def test_partition_extremes():
+    kept, ev = O.partition(5, np.arange(5))
+    assert kept.tolist() == list(range(5)) and ev.size == 0
+    kept, ev = O.partition(5, np.array([], dtype=np.int64))
+    assert kept.size == 0 and ev.tolist() == list(range(5))
+    assert O.archive(np.zeros((0, 3)), np.array([], dtype=np.int64)).shape == (0, 3)
+
+
 # --------------------------------------------------------------------- end to end
 def test_run_layer_small_invariants():
     wl = datagen.WORKLOADS[2].replace(layers=1, n_ctx=700, d_model=256)
