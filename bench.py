@@ -46,6 +46,29 @@ def parse():
     return ap.parse_args()
 
 
+EX2_PROBE_LIB = os.path.join(ROOT, "libkvsel_ex2probe.so")
+
+
+def load_ex2_probe():
+    """The exponential-unit probe (bench_ex2_probe.cu, built beside libkvsel by build())."""
+    lib = ctypes.CDLL(EX2_PROBE_LIB)
+    f = lib.kvsel_probe_ex2_rate
+    f.argtypes = [ctypes.c_void_p, ctypes.c_size_t, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double)]
+    f.restype = ctypes.c_int
+    return f
+
+
+def ex2_probe_rate(scratch):
+    """(ex2 per clock per SM, ex2 per second on the device); `scratch` is a device tensor of
+    at least 16 bytes per SM.  Raises RuntimeError with the probe's return code."""
+    per_clk, per_s = ctypes.c_double(), ctypes.c_double()
+    rc = load_ex2_probe()(scratch.data_ptr(), scratch.numel() * scratch.element_size(), ctypes.byref(per_clk),
+                          ctypes.byref(per_s))
+    if rc != 0:
+        raise RuntimeError(f"kvsel_probe_ex2_rate returned {rc}")
+    return per_clk.value, per_s.value
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -659,8 +682,8 @@ def main():
     try:
         torch.cuda.synchronize()
         scratch = torch.empty(1 << 16, dtype=torch.uint8, device=dev)   # >= 16 bytes per SM
-        ex2_rate = B.kvsel_probe_ex2_rate(scratch)
-        out["sfu"] = {"what": "MUFU ex2.approx.ftz.f32 throughput (kvsel_probe_ex2_rate: one CTA per SM, "
+        ex2_rate = ex2_probe_rate(scratch)
+        out["sfu"] = {"what": "MUFU ex2.approx.ftz.f32 throughput (bench_ex2_probe.cu: one CTA per SM, "
                               "independent chains)", "ex2_per_clk_per_sm": ex2_rate[0], "ex2_per_s": ex2_rate[1]}
     except Exception as e:  # pragma: no cover - reported, not fatal
         out["sfu"] = {"unavailable": str(e)[:200]}

@@ -119,6 +119,10 @@ typedef struct kvsel_params {
   int32_t batch;        /* requests in the call (<= KVSEL_MAX_BATCH)                      */
   const int32_t* n_ctx_per_req; /* host [batch] context lengths, or NULL                  */
   int32_t value_norm;   /* KVSEL_NORM_*: ||W_h v||_1 (default) or ||W_h v||_2            */
+  uint64_t wait_cycles; /* bound of one device-side wait, in SM clock cycles; 0 = default
+                           (2e9, about 1 s at the boost clock).  A wait that runs out ends
+                           its kernel with KVSEL_ETIMEOUT in the device status word; 1
+                           makes every wait that is not already satisfied give up at once */
 } kvsel_params;
 
 /* K/V cache view, contiguous or paged (block_size tokens per block). */
@@ -182,6 +186,30 @@ int kvsel_select(const kvsel_params* p, const float* s_attn, const float* s_val,
 int kvsel_compact(const kvsel_params* p, const kvsel_kv* kv, const int32_t* idx, const int32_t* counts,
                   const int64_t* offsets, void* k_out, void* v_out, void* ws, size_t ws_bytes, void* stream);
 
+/* Partition every (request, KV head) segment into the kept positions and their complement,
+ * the evicted ones, and write the rows of both sides ("VestigeKV: The NoPE-MLA KV Cache
+ * Carries Its Own Eviction Signal in a Vestigial Branch", §4.1: eviction deletes nothing;
+ * the evicted rows go to an archive, bit-exact, and every position lands in exactly one
+ * of the two sides).  One pass reads every K/V row once and writes it once.
+ *   idx/counts/offsets  device, the kept set as kvsel_select writes it (ascending per
+ *            segment; offsets the exclusive prefix sum of counts from 0)
+ *   ev_idx   device int32 [n_scores - n_kept]: evicted positions, ascending per segment
+ *   ev_counts / ev_offsets  device int32 / int64 [batch*h_kv]: n_b - counts, and the
+ *            exclusive prefix sum of ev_counts (segments in the same order as counts)
+ *   k_ev, v_ev          device bf16 [n_scores - n_kept][head_dim]: the evicted rows, packed
+ *            like ev_idx
+ *   k_kept, v_kept      device bf16 [n_kept][head_dim] or both NULL: the kept rows, packed
+ *            like idx (what kvsel_compact writes)
+ *   ws       NULL, or a workspace of at least 256 bytes whose status word records entries
+ *            found out of range (KVSEL_EDEVICE through kvsel_get_device_status)
+ * A segment whose count or offset does not fit the buffers, or a kept list that is not
+ * strictly ascending, is skipped (its rows are not written) and flagged in the status
+ * word; nothing outside the buffers is touched.  Sizes: kvsel_output_size
+ * (n_scores - n_kept evicted rows in all). */
+int kvsel_partition(const kvsel_params* p, const kvsel_kv* kv, const int32_t* idx, const int32_t* counts,
+                    const int64_t* offsets, int32_t* ev_idx, int32_t* ev_counts, int64_t* ev_offsets, void* k_ev,
+                    void* v_ev, void* k_kept, void* v_kept, void* ws, size_t ws_bytes, void* stream);
+
 /* score -> select -> compact for one layer, enqueued back to back on `stream`.
  * s_attn / s_val are written as in kvsel_score (s_val may be NULL when !value_aware). */
 int kvsel_run_layer(const kvsel_params* p, const void* q, const kvsel_kv* kv, const void* w_o, float* s_attn,
@@ -203,24 +231,24 @@ int kvsel_run_layer(const kvsel_params* p, const void* q, const kvsel_kv* kv, co
  * loads the library until the process exits.  No allocation of any kind is made.
  *   Returns KVSEL_EWORKSPACE when the request needs more scratch than that buffer
  *   (kvsel_workspace_size > KVSEL_NOALLOC_SCRATCH_BYTES), before any launch.
- *   All calls share the buffer, which keeps the last call's contents (each call clears
- *   the status word it needs at zero): calls whose GPU work overlaps race; serialise
- *   them.  The first call on a device resolves the buffer's device address with that
- *   device current; make it before any stream capture.  The device status word of these
- *   calls is internal (not readable through kvsel_get_device_status). */
+ *   All calls share the buffer, which keeps the last call's contents (each call zeroes the
+ *   status word at its start, so read the status after a call and before the next one): calls whose GPU work overlaps race; serialise
+ *   them.  The buffer's device address is looked up (cudaGetSymbolAddress) by every call
+ *   made outside stream capture, in the calling thread's current context, and recorded
+ *   for that context; a call under stream capture uses the recorded address, so make at
+ *   least one call per context (device) before capturing any.  Errors found on the device
+ *   (a bounded wait that ran out, a block-table entry out of range) are read and cleared
+ *   with kvsel_get_device_status(NULL, stream, &status) on the same device. */
 int kvsel_score_noalloc(const kvsel_params* p, const void* q, const kvsel_kv* kv, const void* w_o, float* s_attn,
                         float* s_val, void* stream);
 
 /* ---- diagnostics --------------------------------------------------------------------- */
 
 /* Synchronise `stream`, read and clear the workspace's device status word.  *status is
- * KVSEL_OK, KVSEL_ETIMEOUT (a bounded device wait ran out) or KVSEL_EDEVICE. */
+ * KVSEL_OK, KVSEL_ETIMEOUT (a bounded device wait ran out) or KVSEL_EDEVICE (an index or
+ * block-table entry out of range was skipped).  ws == NULL reads and clears the status
+ * word of the built-in buffer that kvsel_score_noalloc uses on the current device. */
 int kvsel_get_device_status(void* ws, void* stream, int* status);
-
-/* Cycle budget of one device-side wait (default ~1 s at the boost clock).  Lowering it to
- * 0 makes every wait that is not already satisfied give up at once; the tests use this
- * to exercise the timeout path.  Host-side setting for subsequent launches. */
-void kvsel_set_wait_limit(uint64_t cycles);
 
 /* Stages of the path, in launch order within one layer. */
 enum {
@@ -249,16 +277,6 @@ void kvsel_set_stage_events(void* const* events);
  * threads; a launch recorded into a CUDA graph under stream capture counts once, at
  * capture).  The difference across a call is that call's kernel count.  Never fails. */
 uint64_t kvsel_launch_count(void);
-
-/* Measured throughput of the GPU's exponential unit (ex2.approx.ftz.f32, the instruction
- * every softmax exponential of the path uses): one CTA per SM runs independent ex2 chains
- * for about a millisecond on the current device's legacy default stream.
- *   scratch         device, 16-byte aligned, at least 16 * (number of SMs) bytes
- *   per_clk_per_sm  host out: ex2 results per SM clock per SM (the CTAs' cycle counts)
- *   per_second      host out: ex2 results per second over the device (CUDA events)
- * Synchronises the device.  KVSEL_EINVAL for null or short arguments, KVSEL_EWORKSPACE for
- * too small a scratch, KVSEL_ECUDA on a CUDA error. */
-int kvsel_probe_ex2_rate(void* scratch, size_t scratch_bytes, double* per_clk_per_sm, double* per_second);
 
 /* Head-level scores (KVzip §3.4, §3.6): head_out[b*h_kv + h] = the maximum over the
  * sequence of request b, head h of `scores` (packed as kvsel_score writes them, device fp32

@@ -2,8 +2,10 @@
 
 Each CUDA translation unit compiles in parallel to an object under ``_build/``; the
 objects link into ``kv_cache_eviction_window_gb300/libkvsel.so`` with the static CUDA
-runtime (the TMA tensor-map encoder is looked up through the runtime at first use).  ``build()`` is idempotent: it rebuilds when a source or
-header is newer than the library.
+runtime (the TMA tensor-map encoder is looked up through the runtime at first use).
+The benchmark's exponential-unit probe (``bench_ex2_probe.cu`` beside ``bench.py``, not
+part of the library) builds into its own ``libkvsel_ex2probe.so`` in the same step.
+``build()`` is idempotent: it rebuilds when a source or header is newer than its library.
 """
 from __future__ import annotations
 
@@ -18,6 +20,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libkvsel.so")
+PROBE_SRC = os.path.join(ROOT, "bench_ex2_probe.cu")
+PROBE_LIB = os.path.join(ROOT, "libkvsel_ex2probe.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          "--expt-relaxed-constexpr", "-I", os.path.join(ROOT, "include")]
@@ -35,11 +39,11 @@ def sources():
 
 
 def _stale() -> bool:
-    if not os.path.exists(LIB):
+    if not os.path.exists(LIB) or not os.path.exists(PROBE_LIB):
         return True
-    t = os.path.getmtime(LIB)
+    t = min(os.path.getmtime(LIB), os.path.getmtime(PROBE_LIB))
     deps = sources() + glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(ROOT, "include", "*.h"))
-    return any(os.path.getmtime(p) > t for p in deps)
+    return any(os.path.getmtime(p) > t for p in deps + [PROBE_SRC])
 
 
 def build(force: bool = False, verbose: bool = False) -> str:
@@ -59,8 +63,18 @@ def build(force: bool = False, verbose: bool = False) -> str:
             sys.stderr.write(r.stdout + r.stderr)
         return obj
 
+    def build_probe() -> None:
+        tmp = PROBE_LIB + ".tmp"
+        cmd = [nvcc, *ARCH, *FLAGS, "-shared", PROBE_SRC, "-o", tmp]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"nvcc failed for {PROBE_SRC}:\n{r.stdout}\n{r.stderr}")
+        os.replace(tmp, PROBE_LIB)
+
     with ThreadPoolExecutor(max(1, min(8, os.cpu_count() or 1))) as ex:
+        probe = ex.submit(build_probe)
         objs = list(ex.map(compile_one, sources()))
+        probe.result()
     tmp = LIB + ".tmp"
     cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)

@@ -32,10 +32,10 @@ LAYOUT_CONTIGUOUS, LAYOUT_PAGED = 0, 1
 MAX_BATCH = 128
 
 EXPORTS = ("kvsel_workspace_size", "kvsel_output_size", "kvsel_workspace_init", "kvsel_score",
-           "kvsel_select", "kvsel_compact", "kvsel_run_layer", "kvsel_get_device_status",
-           "kvsel_set_wait_limit", "kvsel_set_stage_events", "kvsel_strerror", "kvsel_version",
+           "kvsel_select", "kvsel_compact", "kvsel_partition", "kvsel_run_layer", "kvsel_get_device_status",
+           "kvsel_set_stage_events", "kvsel_strerror", "kvsel_version",
            "kvsel_score_noalloc", "kvsel_launch_count", "kvsel_head_scores", "kvsel_anchor_project",
-           "kvsel_run_anchors", "kvsel_perturbation_workspace_size", "kvsel_perturbation", "kvsel_probe_ex2_rate")
+           "kvsel_run_anchors", "kvsel_perturbation_workspace_size", "kvsel_perturbation")
 NOALLOC_SCRATCH_BYTES = 16 << 20
 STAGES = ("rowstats", "keysum", "wbar", "vnorm", "finalize", "select", "compact", "project", "perturb")
 
@@ -61,6 +61,7 @@ class kvsel_params(ctypes.Structure):
         ("budget_mode", ctypes.c_int32), ("budget_ratio", ctypes.c_double),
         ("floor_ratio", ctypes.c_double), ("batch", ctypes.c_int32),
         ("n_ctx_per_req", ctypes.POINTER(ctypes.c_int32)), ("value_norm", ctypes.c_int32),
+        ("wait_cycles", ctypes.c_uint64),
     ]
 
 
@@ -97,9 +98,9 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
         "kvsel_score": ([P, vp, K, vp, vp, vp, vp, sz, vp], ctypes.c_int),
         "kvsel_select": ([P, vp, vp, vp, vp, vp, vp, sz, vp], ctypes.c_int),
         "kvsel_compact": ([P, K, vp, vp, vp, vp, vp, vp, sz, vp], ctypes.c_int),
+        "kvsel_partition": ([P, K] + [vp] * 11 + [sz, vp], ctypes.c_int),
         "kvsel_run_layer": ([P, vp, K, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp], ctypes.c_int),
         "kvsel_get_device_status": ([vp, vp, ctypes.POINTER(ctypes.c_int)], ctypes.c_int),
-        "kvsel_set_wait_limit": ([ctypes.c_uint64], None),
         "kvsel_set_stage_events": ([ctypes.c_void_p], None),
         "kvsel_score_noalloc": ([P, vp, K, vp, vp, vp, vp], ctypes.c_int),
         "kvsel_strerror": ([ctypes.c_int], ctypes.c_char_p),
@@ -110,8 +111,6 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
         "kvsel_run_anchors": ([P, vp, K] + [vp] * 12 + [sz, vp], ctypes.c_int),
         "kvsel_perturbation_workspace_size": ([P, ctypes.POINTER(sz)], ctypes.c_int),
         "kvsel_perturbation": ([P, vp, K, vp, vp, vp, vp, vp, vp, sz, vp], ctypes.c_int),
-        "kvsel_probe_ex2_rate": ([vp, sz, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double)],
-                                 ctypes.c_int),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -129,7 +128,8 @@ def make_params(*, h_kv: int, group: int, n_ctx: int, window: int, head_dim: int
                 value_aware: bool = False, wo_mode: str = "group_sum", eps: float = 1e-4,
                 alpha: float = 0.5, n_sink: int = 4, n_recent: int = 32,
                 budget_mode: str = "head", budget_ratio: float = 0.2, floor_ratio: float = 0.0,
-                n_ctx_per_req: Optional[Sequence[int]] = None, value_norm: str = "l1") -> kvsel_params:
+                n_ctx_per_req: Optional[Sequence[int]] = None, value_norm: str = "l1",
+                wait_cycles: int = 0) -> kvsel_params:
     p = kvsel_params()
     p.h_kv, p.group, p.head_dim, p.d_model = h_kv, group, head_dim, d_model
     p.n_ctx, p.window, p.q_chunk, p.causal = n_ctx, window, q_chunk, int(bool(causal))
@@ -139,6 +139,7 @@ def make_params(*, h_kv: int, group: int, n_ctx: int, window: int, head_dim: int
     p.n_sink, p.n_recent = n_sink, n_recent
     p.budget_mode, p.budget_ratio, p.floor_ratio = BUDGET[budget_mode], budget_ratio, floor_ratio
     p.value_norm = VALUE_NORM[value_norm]
+    p.wait_cycles = int(wait_cycles)
     if n_ctx_per_req is not None:
         arr = (ctypes.c_int32 * len(n_ctx_per_req))(*[int(x) for x in n_ctx_per_req])
         p._n_arr = arr  # keep alive
@@ -226,23 +227,10 @@ def kvsel_launch_count() -> int:
     return int(load().kvsel_launch_count())
 
 
-def kvsel_probe_ex2_rate(scratch) -> tuple:
-    """(ex2 per clock per SM, ex2 per second on the device) from the exponential-unit probe;
-    `scratch` is a device tensor of at least 16 bytes per SM."""
-    per_clk, per_s = ctypes.c_double(), ctypes.c_double()
-    _check(load().kvsel_probe_ex2_rate(_ptr(scratch), scratch.numel() * scratch.element_size(), ctypes.byref(per_clk),
-                                       ctypes.byref(per_s)), "kvsel_probe_ex2_rate")
-    return per_clk.value, per_s.value
-
-
 def kvsel_head_scores(params, scores, head_out, stream=None) -> None:
     """head_out[b*h_kv + h] = max over the sequence of request b, head h of `scores`."""
     _check(load().kvsel_head_scores(ctypes.byref(params), _ptr(scores), _ptr(head_out), _stream(stream)),
            "kvsel_head_scores")
-
-
-def kvsel_set_wait_limit(cycles: int) -> None:
-    load().kvsel_set_wait_limit(int(cycles))
 
 
 def kvsel_set_stage_events(events) -> None:
@@ -294,6 +282,16 @@ def kvsel_compact(params, kv: kvsel_kv, idx, counts, offsets, k_out, v_out, ws=N
                                 _ptr(k_out), _ptr(v_out), _ptr(ws), nbytes, _stream(stream)), "kvsel_compact")
 
 
+def kvsel_partition(params, kv: kvsel_kv, idx, counts, offsets, ev_idx, ev_counts, ev_offsets, k_ev, v_ev,
+                    k_kept=None, v_kept=None, ws=None, stream=None) -> None:
+    """Kept set and its complement: evicted positions and the evicted (and optionally the
+    kept) K/V rows, bit-exact."""
+    nbytes = 0 if ws is None else ws.numel() * ws.element_size()
+    _check(load().kvsel_partition(ctypes.byref(params), ctypes.byref(kv), _ptr(idx), _ptr(counts), _ptr(offsets),
+                                  _ptr(ev_idx), _ptr(ev_counts), _ptr(ev_offsets), _ptr(k_ev), _ptr(v_ev),
+                                  _ptr(k_kept), _ptr(v_kept), _ptr(ws), nbytes, _stream(stream)), "kvsel_partition")
+
+
 def kvsel_run_layer(params, q, kv: kvsel_kv, w_o, s_attn, s_val, idx, counts, offsets, k_out, v_out, ws,
                     stream=None) -> None:
     _check(load().kvsel_run_layer(ctypes.byref(params), _ptr(q), ctypes.byref(kv), _ptr(w_o), _ptr(s_attn),
@@ -333,6 +331,8 @@ def kvsel_perturbation(params, q, kv: kvsel_kv, w_o, idx, counts, offsets, out, 
 
 
 def kvsel_get_device_status(ws, stream=None) -> int:
+    """Read and clear the status word of workspace `ws`, or with ws=None the one of the
+    built-in buffer that kvsel_score_noalloc uses on the current device."""
     st = ctypes.c_int()
     _check(load().kvsel_get_device_status(_ptr(ws), _stream(stream), ctypes.byref(st)), "kvsel_get_device_status")
     return st.value

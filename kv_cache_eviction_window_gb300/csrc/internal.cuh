@@ -196,6 +196,10 @@ cudaError_t launch_perturb_accum(const PerturbArgs& a, const CUtensorMap& tq, co
 cudaError_t launch_perturb_finish(const PerturbArgs& a, const uint16_t* w_o, cudaStream_t st);
 int perturb_slices(int D);   // 256-feature slices of W_O rows in the projection
 
+// Device address of kvsel_score_noalloc's built-in scratch buffer in the current context
+// (KVSEL_OK, or KVSEL_ECUDA when it cannot be looked up).
+int noalloc_scratch_address(cudaStream_t st, void** out);
+
 // Raise a kernel's dynamic shared-memory limit once per device (cached).
 cudaError_t ensure_smem(const void* func, size_t bytes);
 
@@ -264,8 +268,29 @@ struct CompactArgs {
 };
 cudaError_t launch_compact(const CompactArgs& a, int max_count, int num_sms, cudaStream_t st);
 
-// Exponential-unit throughput probe (one CTA per SM): ex2 count per CTA for `iters`.
-cudaError_t probe_ex2(int sms, int iters, float* sink, unsigned long long* cycles, cudaStream_t st);
-double probe_ex2_per_cta(int iters);
+// Partition of every segment into kept and evicted positions with both sides' rows
+// (kvsel_partition).  Grid: (64-position tiles of the longest request, segments).
+struct PartitionArgs {
+  ReqTable rq;
+  KvSource src;
+  const uint16_t* k;
+  const uint16_t* v;
+  long long stride_req, stride_head, stride_tok;
+  const int32_t* idx;             // kept positions, ascending per segment
+  const int32_t* counts;
+  const int64_t* offsets;
+  long long n_kept;               // rows of idx / k_kept / v_kept
+  long long n_evicted;            // rows of ev_idx / k_ev / v_ev
+  int32_t* ev_idx;                // evicted positions, ascending per segment
+  int32_t* ev_counts;
+  int64_t* ev_offsets;
+  uint16_t* k_ev;
+  uint16_t* v_ev;
+  uint16_t* k_kept;               // may be null (then v_kept is null too)
+  uint16_t* v_kept;
+  int* status;                    // may be null
+};
+cudaError_t launch_partition(const PartitionArgs& a, int n_max, cudaStream_t st);
+
 
 }  // namespace kvsel

@@ -42,7 +42,7 @@ void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
 namespace {
 
-std::atomic<unsigned long long> g_wait_limit{2000000000ull};   // ~1 s at the boost clock
+constexpr unsigned long long kDefaultWaitCycles = 2000000000ull;   // ~1 s at the boost clock
 
 thread_local void* const* t_stage_events = nullptr;
 
@@ -87,6 +87,7 @@ struct Plan {
   size_t ws_c2 = 0, ws_tmax = 0;   // query-agnostic scoring
   size_t ws_gpart = 0, ws_gam = 0;  // L2 value norm: Gram partials and Gamma hi/lo
   int qa_row_blocks = 0, qa_key_blocks = 0, qa_row_splits = 0;
+  unsigned long long wait_limit = kDefaultWaitCycles;   // cycles one device-side wait may spin
 };
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -111,6 +112,7 @@ int make_plan(const kvsel_params* p, Plan& pl, bool need_device) {
       p->budget_mode != KVSEL_BUDGET_ANCHOR)
     return KVSEL_EINVAL;
   pl.anchor = p->budget_mode == KVSEL_BUDGET_ANCHOR;
+  pl.wait_limit = p->wait_cycles ? p->wait_cycles : kDefaultWaitCycles;
   if (pl.anchor && !(p->alpha >= 0.f && p->alpha <= 1.f)) return KVSEL_EINVAL;
   if (!(p->budget_ratio >= 0.0 && p->budget_ratio <= 1.0) || !(p->floor_ratio >= 0.0 && p->floor_ratio <= 1.0))
     return KVSEL_EINVAL;
@@ -406,7 +408,7 @@ int check_ws(const Plan& pl, void* ws, size_t ws_bytes) {
   return KVSEL_OK;
 }
 
-WaitCtl wait_ctl(void* ws) { return WaitCtl{g_wait_limit.load(), static_cast<int*>(ws)}; }
+WaitCtl wait_ctl(const Plan& pl, void* ws) { return WaitCtl{pl.wait_limit, static_cast<int*>(ws)}; }
 
 int do_score(const kvsel_params* p, const Plan& pl, const void* q, const kvsel_kv* kv, const void* w_o, float* s_attn,
              float* s_val, void* ws, cudaStream_t st, bool finalize = true) {
@@ -436,7 +438,7 @@ int do_score(const kvsel_params* p, const Plan& pl, const void* q, const kvsel_k
     a.c2 = reinterpret_cast<float*>(wsb + pl.ws_c2);
     a.tmax = reinterpret_cast<uint32_t*>(wsb + pl.ws_tmax);
     a.s_raw = s_raw;
-    a.wc = wait_ctl(ws);
+    a.wc = wait_ctl(pl, ws);
     int rc;
     if (!a.logit) {
       StageScope sc(KVSEL_STAGE_ROWSTATS, st);
@@ -477,7 +479,7 @@ int do_score(const kvsel_params* p, const Plan& pl, const void* q, const kvsel_k
   a.s2 = scale * 1.4426950408889634f;
   a.part = part;
   a.s_raw = s_raw;
-  a.wc = wait_ctl(ws);
+  a.wc = wait_ctl(pl, ws);
   int rc;
   cudaError_t fe = cudaErrorNotSupported;
   if (pl.mt <= 2) {
@@ -522,7 +524,7 @@ int do_score(const kvsel_params* p, const Plan& pl, const void* q, const kvsel_k
     if (!kv_map(&tv, kv->v, kv, pl, kv->layout == KVSEL_LAYOUT_PAGED ? 0 : 128)) return KVSEL_EINVAL;
     {
       StageScope sc(KVSEL_STAGE_WBAR, st);
-      rc = launch_rc(launch_value_gram(two, gpart, gam, pl.H, pl.G, pl.D, wait_ctl(ws), st));
+      rc = launch_rc(launch_value_gram(two, gpart, gam, pl.H, pl.G, pl.D, wait_ctl(pl, ws), st));
     }
     if (rc) return rc;
     VgramArgs v{};
@@ -532,7 +534,7 @@ int do_score(const kvsel_params* p, const Plan& pl, const void* q, const kvsel_k
     for (int b = 0; b <= pl.B; ++b) v.unit_base[b] = pl.g_unit_base[b];
     for (int b = 0; b < pl.B; ++b) v.blocks_per_head[b] = pl.g_blocks_per_head[b];
     v.nu = nu;
-    v.wc = wait_ctl(ws);
+    v.wc = wait_ctl(pl, ws);
     {
       StageScope sc(KVSEL_STAGE_VNORM, st);
       rc = launch_rc(launch_vgram(v, tv, tg, st));
@@ -566,7 +568,7 @@ int do_score(const kvsel_params* p, const Plan& pl, const void* q, const kvsel_k
     for (int b = 0; b <= pl.B; ++b) v.unit_base[b] = pl.unit_base[b];
     for (int b = 0; b < pl.B; ++b) v.blocks_per_head[b] = pl.blocks_per_head[b];
     v.nu = nu;
-    v.wc = wait_ctl(ws);
+    v.wc = wait_ctl(pl, ws);
     {
       StageScope sc(KVSEL_STAGE_VNORM, st);
       rc = launch_rc(launch_vnorm(v, tw, st));
@@ -701,7 +703,7 @@ int do_anchor_project(const Plan& pl, const kvsel_kv* kv, const void* anchor_k, 
   a.slot[1] = slot_v;
   a.gamma[0] = gamma_k;
   a.gamma[1] = gamma_v;
-  a.wc = wait_ctl(ws);
+  a.wc = wait_ctl(pl, ws);
   return launch_rc(launch_anchor_project(a, tk, tv, tak, tav, st));
 }
 
@@ -780,7 +782,7 @@ int kvsel_perturbation(const kvsel_params* p, const void* q, const kvsel_kv* kv,
   a.e = reinterpret_cast<float*>(wsb + L.e);
   a.y_part = reinterpret_cast<float*>(wsb + L.y_part);
   a.out = out;
-  a.wc = wait_ctl(ws);
+  a.wc = wait_ctl(pl, ws);
   CUtensorMap tq, tk, tv;
   {
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(pl.B) * pl.H * pl.R};
@@ -809,7 +811,7 @@ int kvsel_perturbation(const kvsel_params* p, const void* q, const kvsel_kv* kv,
   v.units_total = pl.unit_base[pl.B];
   for (int b = 0; b <= pl.B; ++b) v.unit_base[b] = pl.unit_base[b];
   for (int b = 0; b < pl.B; ++b) v.blocks_per_head[b] = pl.blocks_per_head[b];
-  v.wc = wait_ctl(ws);
+  v.wc = wait_ctl(pl, ws);
   for (int g = 0; g < pl.G; ++g) {
     float* nu_g = reinterpret_cast<float*>(wsb + L.nu) + static_cast<size_t>(g) * pl.n_scores;
     if ((rc = launch_rc(cudaMemsetAsync(nu_g, 0, static_cast<size_t>(pl.n_scores) * sizeof(float), st)))) return rc;
@@ -874,41 +876,6 @@ int kvsel_head_scores(const kvsel_params* p, const float* scores, float* head_ou
 
 const char* kvsel_version(void) { return "kvsel 0.1 (sm_103a)"; }
 
-int kvsel_probe_ex2_rate(void* scratch, size_t scratch_bytes, double* per_clk_per_sm, double* per_second) {
-  if (!scratch || !per_clk_per_sm || !per_second || (reinterpret_cast<uintptr_t>(scratch) & 15u)) return KVSEL_EINVAL;
-  int sms = 0;
-  if (device_sms(&sms) || sms < 1) return KVSEL_ECUDA;
-  if (scratch_bytes < 16u * static_cast<size_t>(sms)) return KVSEL_EWORKSPACE;
-  constexpr int kIters = 4096;
-  auto* cycles = static_cast<unsigned long long*>(scratch);
-  auto* sink = reinterpret_cast<float*>(cycles + sms);
-  cudaEvent_t e0 = nullptr, e1 = nullptr;
-  int rc = KVSEL_ECUDA;
-  std::vector<unsigned long long> host(static_cast<size_t>(sms));
-  float ms = 0.f;
-  if (cudaEventCreate(&e0) != cudaSuccess || cudaEventCreate(&e1) != cudaSuccess) goto done;
-  if (kvsel::probe_ex2(sms, kIters / 8, sink, cycles, nullptr) != cudaSuccess) goto done;   // warm-up
-  if (cudaEventRecord(e0, nullptr) != cudaSuccess) goto done;
-  if (kvsel::probe_ex2(sms, kIters, sink, cycles, nullptr) != cudaSuccess) goto done;
-  if (cudaEventRecord(e1, nullptr) != cudaSuccess || cudaEventSynchronize(e1) != cudaSuccess) goto done;
-  if (cudaEventElapsedTime(&ms, e0, e1) != cudaSuccess || ms <= 0.f) goto done;
-  if (cudaMemcpy(host.data(), cycles, sizeof(unsigned long long) * sms, cudaMemcpyDeviceToHost) != cudaSuccess)
-    goto done;
-  {
-    unsigned long long cmax = 1;
-    for (unsigned long long c : host) cmax = c > cmax ? c : cmax;
-    const double per_cta = kvsel::probe_ex2_per_cta(kIters);
-    *per_clk_per_sm = per_cta / static_cast<double>(cmax);
-    *per_second = per_cta * sms / (static_cast<double>(ms) * 1e-3);
-    rc = KVSEL_OK;
-  }
-done:
-  if (rc != KVSEL_OK) cudaGetLastError();
-  if (e0) cudaEventDestroy(e0);
-  if (e1) cudaEventDestroy(e1);
-  return rc;
-}
-
 const char* kvsel_strerror(int code) {
   switch (code) {
     case KVSEL_OK: return "ok";
@@ -922,8 +889,6 @@ const char* kvsel_strerror(int code) {
     default: return "unknown error";
   }
 }
-
-void kvsel_set_wait_limit(uint64_t cycles) { g_wait_limit.store(cycles); }
 
 void kvsel_set_stage_events(void* const* events) { t_stage_events = events; }
 
@@ -991,6 +956,46 @@ int kvsel_compact(const kvsel_params* p, const kvsel_kv* kv, const int32_t* idx,
   return do_compact(pl, kv, idx, counts, offsets, k_out, v_out, ws, static_cast<cudaStream_t>(stream));
 }
 
+int kvsel_partition(const kvsel_params* p, const kvsel_kv* kv, const int32_t* idx, const int32_t* counts,
+                    const int64_t* offsets, int32_t* ev_idx, int32_t* ev_counts, int64_t* ev_offsets, void* k_ev,
+                    void* v_ev, void* k_kept, void* v_kept, void* ws, size_t ws_bytes, void* stream) {
+  Plan pl;
+  int rc = make_plan(p, pl, false);
+  if (rc) return rc;
+  if (pl.anchor) return KVSEL_EUNSUPPORTED;
+  const long long n_ev = pl.n_scores - pl.n_kept;
+  if (!idx || !counts || !offsets || !ev_counts || !ev_offsets) return KVSEL_EINVAL;
+  if (n_ev > 0 && (!ev_idx || !k_ev || !v_ev || !aligned16(k_ev) || !aligned16(v_ev))) return KVSEL_EINVAL;
+  if ((k_kept == nullptr) != (v_kept == nullptr)) return KVSEL_EINVAL;
+  if (k_kept && (!aligned16(k_kept) || !aligned16(v_kept))) return KVSEL_EINVAL;
+  if ((rc = check_kv(kv, pl, true))) return rc;
+  if (ws && ws_bytes < kStatusBytes) return KVSEL_EWORKSPACE;
+  PartitionArgs a{};
+  a.rq = pl.rq;
+  a.src = kv_source(kv);
+  a.k = static_cast<const uint16_t*>(kv->k);
+  a.v = static_cast<const uint16_t*>(kv->v);
+  a.stride_req = kv->stride_req;
+  a.stride_head = kv->stride_head;
+  a.stride_tok = kv->stride_tok;
+  a.idx = idx;
+  a.counts = counts;
+  a.offsets = offsets;
+  a.n_kept = pl.n_kept;
+  a.n_evicted = n_ev;
+  a.ev_idx = ev_idx;
+  a.ev_counts = ev_counts;
+  a.ev_offsets = ev_offsets;
+  a.k_ev = static_cast<uint16_t*>(k_ev);
+  a.v_ev = static_cast<uint16_t*>(v_ev);
+  a.k_kept = static_cast<uint16_t*>(k_kept);
+  a.v_kept = static_cast<uint16_t*>(v_kept);
+  a.status = static_cast<int*>(ws);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  StageScope sc(KVSEL_STAGE_COMPACT, st);
+  return launch_rc(launch_partition(a, pl.n_max, st));
+}
+
 int kvsel_run_layer(const kvsel_params* p, const void* q, const kvsel_kv* kv, const void* w_o, float* s_attn,
                     float* s_val, int32_t* idx, int32_t* counts, int64_t* offsets, void* k_out, void* v_out, void* ws,
                     size_t ws_bytes, void* stream) {
@@ -1024,8 +1029,10 @@ int kvsel_run_layer(const kvsel_params* p, const void* q, const kvsel_kv* kv, co
 }
 
 int kvsel_get_device_status(void* ws, void* stream, int* status) {
-  if (!ws || !status) return KVSEL_EINVAL;
+  if (!status) return KVSEL_EINVAL;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // no workspace: the built-in buffer of kvsel_score_noalloc on the current device
+  if (!ws && noalloc_scratch_address(st, &ws) != KVSEL_OK) return KVSEL_ECUDA;
   int word = 0;
   if (cudaMemcpyAsync(&word, ws, sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess) return KVSEL_ECUDA;
   if (cudaStreamSynchronize(st) != cudaSuccess) return KVSEL_ECUDA;

@@ -12,10 +12,20 @@
 // Costs and rules: every GPU that loads the library holds KVSEL_NOALLOC_SCRATCH_BYTES of
 // device memory for this buffer until the process exits.  All calls share the one buffer
 // and it keeps the previous call's contents; each call clears the part that must start at
-// zero (the device status word) and fully rewrites the rest before reading it.  Calls whose
-// GPU work overlaps (different streams, or different host threads, on one device) race on
-// the buffer: serialise them.  The first call on each device looks up the buffer's device
-// address with that device current; make that first call before any stream capture.
+// zero (the device status word and the grid-barrier counters) and fully rewrites the rest
+// before reading it.  Calls whose GPU work overlaps (different streams, or different host
+// threads, on one device) race on the buffer: serialise them.
+//
+// The host-side name of the array is only a stand-in, never a device address.  Every call
+// made outside stream capture looks the address up with cudaGetSymbolAddress in the
+// calling thread's current context and records it for that context; a call under stream
+// capture uses the recorded address (one call per context must come before any capture).
+// Looking it up again on every uncaptured call keeps the address right after the context
+// is destroyed and re-created (cudaDeviceReset), which may give the new context the same
+// handle as the old one.
+#include <cudaTypedefs.h>
+
+#include <map>
 #include <mutex>
 
 #include "../../include/kvsel.h"
@@ -25,26 +35,53 @@ namespace {
 
 __device__ __align__(256) unsigned char g_noalloc_scratch[KVSEL_NOALLOC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
 std::mutex g_addr_mutex;
-void* g_addr[kMaxDevices] = {};
+std::map<CUcontext, void*> g_addr;   // device address of the buffer, per context
 
-// Device address of the scratch buffer on the current device (the host-side symbol is
-// only a stand-in and must never be handed to a kernel).
-int scratch_address(void** out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return KVSEL_ECUDA;
-  std::lock_guard<std::mutex> lock(g_addr_mutex);
-  if (!g_addr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return KVSEL_ECUDA;
-    g_addr[dev] = p;
-  }
-  *out = g_addr[dev];
-  return KVSEL_OK;
+// The calling thread's current context, through the runtime's driver entry point (the
+// library links no libcuda).  nullptr when it cannot be queried.
+CUcontext current_context() {
+  static PFN_cuCtxGetCurrent_v4000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(f);
+  });
+  CUcontext ctx = nullptr;
+  if (fn && fn(&ctx) != CUDA_SUCCESS) ctx = nullptr;
+  return ctx;
 }
 
 }  // namespace
+
+namespace kvsel {
+
+// Device address of the built-in buffer in the current context (see the file comment).
+int noalloc_scratch_address(cudaStream_t st, void** out) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(st, &cs) != cudaSuccess) return KVSEL_ECUDA;
+  if (cs != cudaStreamCaptureStatusNone) {
+    const CUcontext ctx = current_context();
+    std::lock_guard<std::mutex> lock(g_addr_mutex);
+    auto it = g_addr.find(ctx);
+    if (it == g_addr.end()) return KVSEL_ECUDA;   // no uncaptured call in this context yet
+    *out = it->second;
+    return KVSEL_OK;
+  }
+  // the lookup also initialises the runtime's context on this thread's device
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return KVSEL_ECUDA;
+  const CUcontext ctx = current_context();
+  std::lock_guard<std::mutex> lock(g_addr_mutex);
+  g_addr[ctx] = p;
+  *out = p;
+  return KVSEL_OK;
+}
+
+}  // namespace kvsel
 
 extern "C" int kvsel_score_noalloc(const kvsel_params* p, const void* q, const kvsel_kv* kv, const void* w_o,
                                    float* s_attn, float* s_val, void* stream) {
@@ -52,12 +89,11 @@ extern "C" int kvsel_score_noalloc(const kvsel_params* p, const void* q, const k
   int rc = kvsel_workspace_size(p, &need);
   if (rc) return rc;
   if (need > KVSEL_NOALLOC_SCRATCH_BYTES) return KVSEL_EWORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
   void* scratch = nullptr;
-  if ((rc = scratch_address(&scratch))) return rc;
+  if ((rc = kvsel::noalloc_scratch_address(st, &scratch))) return rc;
   // the status word and the barrier counters start at zero for this call; everything else
   // is rewritten
-  if (cudaMemsetAsync(scratch, 0, kvsel::kStatusBytes + kvsel::kCounterBytes, static_cast<cudaStream_t>(stream)) !=
-      cudaSuccess)
-    return KVSEL_ECUDA;
+  if (cudaMemsetAsync(scratch, 0, kvsel::kStatusBytes + kvsel::kCounterBytes, st) != cudaSuccess) return KVSEL_ECUDA;
   return kvsel_score(p, q, kv, w_o, s_attn, s_val, scratch, KVSEL_NOALLOC_SCRATCH_BYTES, stream);
 }

@@ -1,10 +1,10 @@
 """Run a few layers of one workload through kvsel_run_layer, for profilers (ncu).
 
-    python -m kv_cache_eviction_window_gb300.profile_case --workload 2 --layers 2 --steps 2
-    python -m kv_cache_eviction_window_gb300.profile_case --workload 2 --value-norm l2
-    python -m kv_cache_eviction_window_gb300.profile_case --workload 6      # AnchorKV anchors
-    python -m kv_cache_eviction_window_gb300.profile_case --workload 2 --perturb   # + output perturbation
-    python -m kv_cache_eviction_window_gb300.profile_case --workload 5 --n-ctx 8192  # query-agnostic, smaller n
+    python profile_case.py --workload 2 --layers 2 --steps 2
+    python profile_case.py --workload 2 --value-norm l2
+    python profile_case.py --workload 6      # AnchorKV anchors
+    python profile_case.py --workload 2 --perturb   # + output perturbation
+    python profile_case.py --workload 5 --n-ctx 8192  # query-agnostic, smaller n
 
 The inputs are the same seeded synthetic tensors as the benchmark (each layer distinct,
 larger than L2 for the 32K stack), so per-launch counters taken here scale to the
@@ -17,7 +17,7 @@ import ctypes
 import os
 import sys
 
-ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 

@@ -48,9 +48,9 @@ def test_struct_layout_matches_header(B):
     import subprocess
     import tempfile
 
-    src = '#include <stdio.h>\n#include <stddef.h>\n#include "kvsel.h"\nint main(){printf("%zu %zu %zu %zu\\n",' \
+    src = '#include <stdio.h>\n#include <stddef.h>\n#include "kvsel.h"\nint main(){printf("%zu %zu %zu %zu %zu\\n",' \
           'sizeof(kvsel_params), sizeof(kvsel_kv), offsetof(kvsel_params, budget_ratio),' \
-          'offsetof(kvsel_kv, block_table));return 0;}\n'
+          'offsetof(kvsel_kv, block_table), offsetof(kvsel_params, wait_cycles));return 0;}\n'
     with tempfile.TemporaryDirectory() as d:
         c = os.path.join(d, "s.c")
         open(c, "w").write(src)
@@ -58,7 +58,7 @@ def test_struct_layout_matches_header(B):
         subprocess.check_call(["gcc", "-I", os.path.join(ROOT, "include"), c, "-o", exe])
         out = subprocess.check_output([exe]).decode().split()
     want = [ctypes.sizeof(B.kvsel_params), ctypes.sizeof(B.kvsel_kv), B.kvsel_params.budget_ratio.offset,
-            B.kvsel_kv.block_table.offset]
+            B.kvsel_kv.block_table.offset, B.kvsel_params.wait_cycles.offset]
     assert [int(x) for x in out] == want
 
 
@@ -128,8 +128,16 @@ def test_query_agnostic_sizes(B):
 
 
 def test_ex2_probe_rejects_null_and_misaligned_arguments(B):
-    lib = B.load()
+    import bench
+
+    f = bench.load_ex2_probe()
     a, b = ctypes.c_double(), ctypes.c_double()
-    assert lib.kvsel_probe_ex2_rate(None, 4096, ctypes.byref(a), ctypes.byref(b)) == B.KVSEL_EINVAL
-    assert lib.kvsel_probe_ex2_rate(ctypes.c_void_p(16), 4096, None, ctypes.byref(b)) == B.KVSEL_EINVAL
-    assert lib.kvsel_probe_ex2_rate(ctypes.c_void_p(24), 4096, ctypes.byref(a), ctypes.byref(b)) == B.KVSEL_EINVAL
+    assert f(None, 4096, ctypes.byref(a), ctypes.byref(b)) == -1
+    assert f(16, 4096, None, ctypes.byref(b)) == -1
+    assert f(24, 4096, ctypes.byref(a), ctypes.byref(b)) == -1
+
+
+def test_probe_is_not_part_of_the_library(B):
+    lib = ctypes.CDLL(B.LIB_PATH)
+    assert not hasattr(lib, "kvsel_probe_ex2_rate")
+    assert not hasattr(lib, "kvsel_set_wait_limit")   # the wait budget is a per-call parameter

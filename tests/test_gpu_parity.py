@@ -305,18 +305,16 @@ def test_c3_full_layer():
 
 # ---------------------------------------------------------------------- device status
 def test_bounded_wait_timeout_reports_status():
-    """A wait budget of 0 cycles makes the pipeline waits give up: the kernels end with
-    KVSEL_ETIMEOUT in the status word and the context stays usable."""
+    """A wait budget of 1 cycle (kvsel_params.wait_cycles) makes the pipeline waits give
+    up: the kernels end with KVSEL_ETIMEOUT in the status word and the context stays
+    usable.  The budget is a per-call parameter, so the next call with the default runs
+    normally."""
     from kv_cache_eviction_window_gb300 import binding as B
 
     wl = datagen.WORKLOADS[1].replace(h_kv=2)
     inp = datagen.make_layer(wl, 0, n_ctx=2048)
-    try:
-        B.kvsel_set_wait_limit(0)
-        out = GH.run_gpu_layer(wl, inp)
-        assert out[0]["status"] == B.KVSEL_ETIMEOUT
-    finally:
-        B.kvsel_set_wait_limit(2_000_000_000)
+    out = GH.run_gpu_layer(wl, inp, wait_cycles=1)
+    assert out[0]["status"] == B.KVSEL_ETIMEOUT
     ora = O.run_workload_layer(wl, inp)
     gpu = GH.run_gpu_layer(wl, inp)
     _check_layer(wl, inp, gpu, ora)
@@ -448,19 +446,19 @@ def test_compact_out_of_range_index_is_zeroed_and_flagged():
 
 
 def test_ex2_probe_rate_is_plausible():
-    """The exponential-unit probe: a positive rate per SM clock within what an SM can issue,
-    and a device rate consistent with it at a clock between 0.5 and 3 GHz."""
+    """The benchmark's exponential-unit probe: a positive rate per SM clock within what an
+    SM can issue, and a device rate consistent with it at a clock between 0.5 and 3 GHz."""
     import torch
-    from kv_cache_eviction_window_gb300 import binding as B
+
+    import bench
 
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    per_clk, per_s = B.kvsel_probe_ex2_rate(torch.empty(16 * sms, dtype=torch.uint8, device="cuda"))
+    per_clk, per_s = bench.ex2_probe_rate(torch.empty(16 * sms, dtype=torch.uint8, device="cuda"))
     assert 4.0 <= per_clk <= 128.0, per_clk
     ghz = per_s / (per_clk * sms) / 1e9
     assert 0.5 <= ghz <= 3.0, ghz
-    with pytest.raises(B.KvselError) as e:
-        B.kvsel_probe_ex2_rate(torch.empty(16 * sms - 16, dtype=torch.uint8, device="cuda"))
-    assert e.value.code == B.KVSEL_EWORKSPACE
+    with pytest.raises(RuntimeError, match="returned -4"):
+        bench.ex2_probe_rate(torch.empty(16 * sms - 16, dtype=torch.uint8, device="cuda"))
 
 
 def test_c4_full_batch_sampled():
