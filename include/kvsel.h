@@ -278,6 +278,12 @@ void kvsel_set_stage_events(void* const* events);
  * capture).  The difference across a call is that call's kernel count.  Never fails. */
 uint64_t kvsel_launch_count(void);
 
+/* Diagnostics: how query-agnostic scoring (window == 0) splits its work on the current
+ * device: *key_blocks = blocks of 256 keys per head, *row_splits = slices of the G*n query
+ * rows per key block (the per-key maximum of each slice is merged with an atomic max).
+ * Host-only; errors as kvsel_workspace_size, KVSEL_EINVAL when window != 0. */
+int kvsel_query_agnostic_split(const kvsel_params* p, int32_t* key_blocks, int32_t* row_splits);
+
 /* Head-level scores (KVzip §3.4, §3.6): head_out[b*h_kv + h] = the maximum over the
  * sequence of request b, head h of `scores` (packed as kvsel_score writes them, device fp32
  * [n_scores]); -inf for an empty request.  head_out: device fp32 [batch*h_kv].  Asynchronous

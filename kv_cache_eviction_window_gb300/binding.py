@@ -35,7 +35,8 @@ EXPORTS = ("kvsel_workspace_size", "kvsel_output_size", "kvsel_workspace_init", 
            "kvsel_select", "kvsel_compact", "kvsel_partition", "kvsel_run_layer", "kvsel_get_device_status",
            "kvsel_set_stage_events", "kvsel_strerror", "kvsel_version",
            "kvsel_score_noalloc", "kvsel_launch_count", "kvsel_head_scores", "kvsel_anchor_project",
-           "kvsel_run_anchors", "kvsel_perturbation_workspace_size", "kvsel_perturbation")
+           "kvsel_run_anchors", "kvsel_perturbation_workspace_size", "kvsel_perturbation",
+           "kvsel_query_agnostic_split")
 NOALLOC_SCRATCH_BYTES = 16 << 20
 STAGES = ("rowstats", "keysum", "wbar", "vnorm", "finalize", "select", "compact", "project", "perturb")
 
@@ -107,6 +108,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
         "kvsel_version": ([], ctypes.c_char_p),
         "kvsel_launch_count": ([], ctypes.c_uint64),
         "kvsel_head_scores": ([P, vp, vp, vp], ctypes.c_int),
+        "kvsel_query_agnostic_split": ([P, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32)],
+                                       ctypes.c_int),
         "kvsel_anchor_project": ([P, K] + [vp] * 10 + [sz, vp], ctypes.c_int),
         "kvsel_run_anchors": ([P, vp, K] + [vp] * 12 + [sz, vp], ctypes.c_int),
         "kvsel_perturbation_workspace_size": ([P, ctypes.POINTER(sz)], ctypes.c_int),
@@ -225,6 +228,14 @@ def kvsel_strerror(code: int) -> str:
 
 def kvsel_launch_count() -> int:
     return int(load().kvsel_launch_count())
+
+
+def kvsel_query_agnostic_split(params) -> tuple:
+    """(key blocks per head, query-row slices per key block) of query-agnostic scoring."""
+    kb, rs = ctypes.c_int32(), ctypes.c_int32()
+    _check(load().kvsel_query_agnostic_split(ctypes.byref(params), ctypes.byref(kb), ctypes.byref(rs)),
+           "kvsel_query_agnostic_split")
+    return kb.value, rs.value
 
 
 def kvsel_head_scores(params, scores, head_out, stream=None) -> None:

@@ -901,6 +901,17 @@ int kvsel_workspace_size(const kvsel_params* p, size_t* bytes) {
   return KVSEL_OK;
 }
 
+int kvsel_query_agnostic_split(const kvsel_params* p, int32_t* key_blocks, int32_t* row_splits) {
+  if (!key_blocks || !row_splits) return KVSEL_EINVAL;
+  Plan pl;
+  const int rc = make_plan(p, pl, true);
+  if (rc) return rc;
+  if (!pl.qa) return KVSEL_EINVAL;
+  *key_blocks = pl.qa_key_blocks;
+  *row_splits = pl.qa_row_splits;
+  return KVSEL_OK;
+}
+
 int kvsel_output_size(const kvsel_params* p, int64_t* n_scores, int64_t* n_kept, int64_t* n_segments) {
   Plan pl;
   const int rc = make_plan(p, pl, false);

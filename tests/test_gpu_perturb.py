@@ -3,9 +3,12 @@
 
 The kept sets come from the oracle's own selection, or from a seeded random draw; the
 GPU computes the actual perturbation and both bounds per window row of every query head.
-Tolerance: relative 2e-3 with an absolute floor of 1e-5 of the largest value of each
-quantity per head.  The weights reach the tensor cores as bf16 high and low parts (2^-16
-relative) and everything accumulates in fp32.
+Tolerance: relative 1e-3 (the score tolerance of the other parity tests) with an absolute
+floor of 1e-5 of the largest value of each quantity per head.  The error of the actual
+perturbation is bounded by u * theta, theta the Theorem 3.3 bound of the same row (the sum
+of |c_i| ||v'_i||_1 over the keys), u about 2^-17 for the bf16 high and low parts of the
+weights plus the fp32 accumulation over the keys; theta is at most about 6x the actual
+value on these layers, far inside 1e-3.
 """
 import numpy as np
 import pytest
@@ -15,7 +18,7 @@ from tests import gpu_harness as GH
 
 pytestmark = pytest.mark.gpu
 
-RTOL = 2e-3
+RTOL = 1e-3
 AFLOOR = 1e-5
 
 
