@@ -537,19 +537,44 @@ def main():
     k_d = [to_dev(x["k"][0]) for x in host]
     v_d = [to_dev(x["v"][0]) for x in host]
     w_d = [to_dev(x["w_o"]) for x in host]
-    params = B.params_from_workload(wl)
+    # W_h depends on the model's weights alone: built once per layer at load time
+    # (kvsel_prepare_w_o), outside the timed step, like any weight preprocessing
+    params = B.params_from_workload(wl, w_o_prepared=True)
+    params_raw = B.params_from_workload(wl)
     bufs = [B.LayerBuffers(params, device=dev) for _ in range(L)]
     # one workspace for every variant timed below (the L2 path needs Gram scratch too)
     ws_bytes = max(B.kvsel_workspace_size(x) for x in
                    (params, B.params_from_workload(wl, value_aware=False), B.params_from_workload(wl, value_norm="l2")))
+    ws_bytes = max(ws_bytes, B.kvsel_workspace_size(params_raw))
     ws = torch.empty(ws_bytes // 4 + 64, dtype=torch.int32, device=dev)
     B.kvsel_workspace_init(ws)
     kvs = [B.make_kv_contiguous(k_d[i], v_d[i]) for i in range(L)]
     stream = torch.cuda.current_stream()
+    # the prepared value-norm weights of every layer (L1: W_h; L2: its Gram matrix)
+    p_l2 = B.params_from_workload(wl, value_norm="l2", w_o_prepared=True)
+    wp_d = [torch.empty(B.kvsel_prepared_w_o_size(params) // 2 + 128, dtype=torch.int16, device=dev) for _ in range(L)]
+    wp2_d = [torch.empty(B.kvsel_prepared_w_o_size(p_l2) // 2 + 128, dtype=torch.int16, device=dev) for _ in range(L)]
+    pe0, pe1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    pe0.record(stream)
+    for i in range(L):
+        B.kvsel_prepare_w_o(params, w_d[i], wp_d[i], ws, stream)
+    pe1.record(stream)
+    for i in range(L):
+        B.kvsel_prepare_w_o(p_l2, w_d[i], wp2_d[i], ws, stream)
+    torch.cuda.synchronize()
+    prep_ms_per_layer = pe0.elapsed_time(pe1) / L
+
+    def w_for(p, i):
+        """The w_o argument of layer i under parameters p."""
+        if not p.value_aware:
+            return None
+        if not p.w_o_prepared:
+            return w_d[i]
+        return wp2_d[i] if p.value_norm == B.VALUE_NORM["l2"] else wp_d[i]
 
     def layer_call(i, p=params, w=None):
         b = bufs[i]
-        B.kvsel_run_layer(p, q_d[i], kvs[i], w_d[i] if p.value_aware else None, b.s_attn, b.s_val, b.idx,
+        B.kvsel_run_layer(p, q_d[i], kvs[i], w_for(p, i), b.s_attn, b.s_val, b.idx,
                           b.counts, b.offsets, b.k_out, b.v_out, ws, stream)
 
     # ---- stage events for the live per-kernel timing
@@ -582,7 +607,7 @@ def main():
                 for i in range(L):
                     if events is not None:
                         B.kvsel_set_stage_events(events[i])
-                    B.kvsel_run_layer(p, q_d[i], kvs[i], w_d[i] if p.value_aware else None, bufs[i].s_attn,
+                    B.kvsel_run_layer(p, q_d[i], kvs[i], w_for(p, i), bufs[i].s_attn,
                                       bufs[i].s_val, bufs[i].idx, bufs[i].counts, bufs[i].offsets, bufs[i].k_out,
                                       bufs[i].v_out, ws, side)
                 B.kvsel_set_stage_events(None)
@@ -743,13 +768,23 @@ def main():
                            "roofline_bound": binding_roofline(pms * 1e-3, alg, 2 * 2.0 * R * d * n * H, 2 * R * n * H,
                                                               pk, ex2_rate[1] if ex2_rate else None)}
         # ---- the L2 value norm through the d x d Gram matrix (CriticalKV App. C.3 distance)
-        lms = time_variant(B.params_from_workload(wl, value_norm="l2"))
+        lms = time_variant(p_l2)
         alg2 = 2 * H * n * d * 2 + wl.d_model * wl.h_kv * wl.group * d * 2 + 2 * H * Bh * d * 2 + small
         gbs2 = alg2 / (lms * 1e-3) / 1e9
         out["l2_gram_path"] = {"what": "same layers, value-aware with ||W_h v||_2 via Gamma = W_h^T W_h",
                                "ms_per_layer": lms, "entries_per_s": H * n / (lms * 1e-3) * world,
                                "algorithmic_bytes_per_layer": alg2, "achieved_gbs": gbs2,
                                "peak_gbs": pk.get("hbm_gbs"), "frac": gbs2 / pk.get("hbm_gbs", 6800.0)}
+
+    # ---- the headline step with W_O passed to every call (W_h rebuilt inside each layer)
+    if not args.no_plain:
+        ums = time_variant(params_raw)
+        out["w_o_per_call"] = {"what": "the headline step with W_O given to every kvsel_run_layer call (W_h built "
+                                       "inside each call) instead of prepared once per model",
+                               "ms_per_layer": ums, "ms_per_step": ums * L,
+                               "entries_per_s": H * n / (ums * 1e-3) * world}
+    out["w_o_prepare"] = {"what": "kvsel_prepare_w_o: W_h of one layer from W_O, once per model (not in the step)",
+                          "ms_per_layer": prep_ms_per_layer}
 
     # ---- AnchorKV anchors on the same layers: scoring (maxpool 7), anchor selection
     # (k = n/128, rho = 0.7, recent window forced), anchor gather and nearest-anchor
@@ -767,14 +802,14 @@ def main():
         pin = []
         for x in host:
             t = {}
-            for key, arr in (("q", x["q"]), ("k", x["k"][0]), ("v", x["v"][0]), ("w", x["w_o"])):
+            for key, arr in (("q", x["q"]), ("k", x["k"][0]), ("v", x["v"][0])):
                 h = torch.empty(arr.shape, dtype=torch.bfloat16, pin_memory=True)
                 h.view(torch.int16).numpy()[...] = arr.view(np.int16)
                 t[key] = h
             t["idx"] = torch.empty(bufs[0].idx.shape, dtype=torch.int32, pin_memory=True)
             t["counts"] = torch.empty(bufs[0].counts.shape, dtype=torch.int32, pin_memory=True)
             pin.append(t)
-        h2d = sum(t[k].numel() * 2 for t in pin for k in ("q", "k", "v", "w"))
+        h2d = sum(t[k].numel() * 2 for t in pin for k in ("q", "k", "v"))
         d2h = sum(t["idx"].numel() * 4 + t["counts"].numel() * 4 for t in pin)
         copy = torch.cuda.Stream()
         c_done = [torch.cuda.Event() for _ in range(L)]
@@ -787,7 +822,6 @@ def main():
                     q_d[i].copy_(pin[i]["q"], non_blocking=True)
                     k_d[i].copy_(pin[i]["k"], non_blocking=True)
                     v_d[i].copy_(pin[i]["v"], non_blocking=True)
-                    w_d[i].copy_(pin[i]["w"], non_blocking=True)
                     x_done[i].record(copy)
                 stream.wait_event(x_done[i])
                 layer_call(i)
@@ -811,8 +845,10 @@ def main():
         ems = max_over_ranks(max(t0.elapsed_time(t1), wall * 1e3), world)
         out["e2e"] = {"value": job_value(K * L * H * n, ems, world), "unit": UNIT, "h2d_bytes_per_step": h2d,
                       "d2h_bytes_per_step": d2h, "ms_per_step": ems / K,
-                      "how": "kvsel_run_layer per layer; per-layer H2D of Q/K/V/W_O from pinned host on a copy "
-                             "stream overlapped with the previous layer's compute; idx/counts D2H per layer"}
+                      "how": "kvsel_run_layer per layer; per-layer H2D of the request's Q/K/V from pinned host on a "
+                             "copy stream overlapped with the previous layer's compute (the model's prepared W_h "
+                             "stays resident); idx/counts D2H per layer; the compacted K/V and the scores stay on "
+                             "the device for the decode step that reads them"}
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = run_cpu_baseline(wl, host)

@@ -119,6 +119,8 @@ typedef struct kvsel_params {
   int32_t batch;        /* requests in the call (<= KVSEL_MAX_BATCH)                      */
   const int32_t* n_ctx_per_req; /* host [batch] context lengths, or NULL                  */
   int32_t value_norm;   /* KVSEL_NORM_*: ||W_h v||_1 (default) or ||W_h v||_2            */
+  int32_t w_o_prepared; /* 1: the w_o argument of the scoring calls is the output of
+                           kvsel_prepare_w_o for these parameters, not W_O itself        */
   uint64_t wait_cycles; /* bound of one device-side wait, in SM clock cycles; 0 = default
                            (2e9, about 1 s at the boost clock).  A wait that runs out ends
                            its kernel with KVSEL_ETIMEOUT in the device status word; 1
@@ -152,6 +154,28 @@ int kvsel_output_size(const kvsel_params* p, int64_t* n_scores, int64_t* n_kept,
 
 /* Zero the workspace's device status word (do once after allocating a workspace). */
 int kvsel_workspace_init(void* ws, size_t ws_bytes, void* stream);
+
+/* ---- weights prepared once per model ------------------------------------------------------ */
+
+/* Bytes of the prepared value-norm weights of kvsel_prepare_w_o (value_aware only):
+ * L1 norm: W_h for every KV head, [h_kv][d_model][head_dim] bf16 (the per-head W_O reading:
+ * [h_kv][group*d_model][head_dim]); L2 norm: Gamma_h = W_h^T W_h as a bf16 high part and
+ * remainder, [h_kv][2][head_dim][head_dim].  Host-only. */
+int kvsel_prepared_w_o_size(const kvsel_params* p, size_t* bytes);
+
+/* The value-aware criterion projects each value through W_h, the sum of the group's W_O
+ * column slices ("CriticalKV: 출력 섭동 관점에서 KV 캐시 축출을 최적화하기", §3.4 Algorithm 1, App.
+ * D.4).  W_h depends on the model's weights alone, so it can be built once per model (per
+ * layer) instead of inside every scoring call: this call writes it (or, for the L2 norm,
+ * its Gram matrix) into w_prep; scoring calls whose params set w_o_prepared = 1 then take
+ * w_prep as their w_o argument.  Results are bit-identical to passing W_O itself.
+ *   w_o     device bf16 [d_model][h_kv*group*head_dim]
+ *   w_prep  device, 256-byte aligned, kvsel_prepared_w_o_size bytes
+ *   ws      L2 norm: device workspace of kvsel_workspace_size bytes (for params with
+ *           w_o_prepared = 0; it holds the Gram partials); L1 norm: not used, may be NULL
+ * Asynchronous on `stream`. */
+int kvsel_prepare_w_o(const kvsel_params* p, const void* w_o, void* w_prep, size_t w_prep_bytes, void* ws,
+                      size_t ws_bytes, void* stream);
 
 /* ---- the path ------------------------------------------------------------------------ */
 
@@ -211,7 +235,10 @@ int kvsel_partition(const kvsel_params* p, const kvsel_kv* kv, const int32_t* id
                     void* v_ev, void* k_kept, void* v_kept, void* ws, size_t ws_bytes, void* stream);
 
 /* score -> select -> compact for one layer, enqueued back to back on `stream`.
- * s_attn / s_val are written as in kvsel_score (s_val may be NULL when !value_aware). */
+ * s_attn / s_val are written as in kvsel_score (s_val may be NULL when !value_aware).
+ * k_out and v_out may both be NULL: the call then ends after the selection, for a
+ * caller that gathers the kept rows itself later (kvsel_compact or kvsel_partition, for
+ * example on another stream while the next layer is scored). */
 int kvsel_run_layer(const kvsel_params* p, const void* q, const kvsel_kv* kv, const void* w_o, float* s_attn,
                     float* s_val, int32_t* idx, int32_t* counts, int64_t* offsets, void* k_out, void* v_out,
                     void* ws, size_t ws_bytes, void* stream);

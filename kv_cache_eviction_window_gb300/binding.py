@@ -36,7 +36,7 @@ EXPORTS = ("kvsel_workspace_size", "kvsel_output_size", "kvsel_workspace_init", 
            "kvsel_set_stage_events", "kvsel_strerror", "kvsel_version",
            "kvsel_score_noalloc", "kvsel_launch_count", "kvsel_head_scores", "kvsel_anchor_project",
            "kvsel_run_anchors", "kvsel_perturbation_workspace_size", "kvsel_perturbation",
-           "kvsel_query_agnostic_split")
+           "kvsel_query_agnostic_split", "kvsel_prepared_w_o_size", "kvsel_prepare_w_o")
 NOALLOC_SCRATCH_BYTES = 16 << 20
 STAGES = ("rowstats", "keysum", "wbar", "vnorm", "finalize", "select", "compact", "project", "perturb")
 
@@ -62,7 +62,7 @@ class kvsel_params(ctypes.Structure):
         ("budget_mode", ctypes.c_int32), ("budget_ratio", ctypes.c_double),
         ("floor_ratio", ctypes.c_double), ("batch", ctypes.c_int32),
         ("n_ctx_per_req", ctypes.POINTER(ctypes.c_int32)), ("value_norm", ctypes.c_int32),
-        ("wait_cycles", ctypes.c_uint64),
+        ("w_o_prepared", ctypes.c_int32), ("wait_cycles", ctypes.c_uint64),
     ]
 
 
@@ -108,6 +108,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
         "kvsel_version": ([], ctypes.c_char_p),
         "kvsel_launch_count": ([], ctypes.c_uint64),
         "kvsel_head_scores": ([P, vp, vp, vp], ctypes.c_int),
+        "kvsel_prepared_w_o_size": ([P, ctypes.POINTER(sz)], ctypes.c_int),
+        "kvsel_prepare_w_o": ([P, vp, vp, sz, vp, sz, vp], ctypes.c_int),
         "kvsel_query_agnostic_split": ([P, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32)],
                                        ctypes.c_int),
         "kvsel_anchor_project": ([P, K] + [vp] * 10 + [sz, vp], ctypes.c_int),
@@ -132,7 +134,7 @@ def make_params(*, h_kv: int, group: int, n_ctx: int, window: int, head_dim: int
                 alpha: float = 0.5, n_sink: int = 4, n_recent: int = 32,
                 budget_mode: str = "head", budget_ratio: float = 0.2, floor_ratio: float = 0.0,
                 n_ctx_per_req: Optional[Sequence[int]] = None, value_norm: str = "l1",
-                wait_cycles: int = 0) -> kvsel_params:
+                wait_cycles: int = 0, w_o_prepared: bool = False) -> kvsel_params:
     p = kvsel_params()
     p.h_kv, p.group, p.head_dim, p.d_model = h_kv, group, head_dim, d_model
     p.n_ctx, p.window, p.q_chunk, p.causal = n_ctx, window, q_chunk, int(bool(causal))
@@ -143,6 +145,7 @@ def make_params(*, h_kv: int, group: int, n_ctx: int, window: int, head_dim: int
     p.budget_mode, p.budget_ratio, p.floor_ratio = BUDGET[budget_mode], budget_ratio, floor_ratio
     p.value_norm = VALUE_NORM[value_norm]
     p.wait_cycles = int(wait_cycles)
+    p.w_o_prepared = int(bool(w_o_prepared))
     if n_ctx_per_req is not None:
         arr = (ctypes.c_int32 * len(n_ctx_per_req))(*[int(x) for x in n_ctx_per_req])
         p._n_arr = arr  # keep alive
@@ -228,6 +231,21 @@ def kvsel_strerror(code: int) -> str:
 
 def kvsel_launch_count() -> int:
     return int(load().kvsel_launch_count())
+
+
+def kvsel_prepared_w_o_size(params) -> int:
+    out = ctypes.c_size_t()
+    _check(load().kvsel_prepared_w_o_size(ctypes.byref(params), ctypes.byref(out)), "kvsel_prepared_w_o_size")
+    return out.value
+
+
+def kvsel_prepare_w_o(params, w_o, w_prep, ws=None, stream=None) -> None:
+    """The value-norm weights of W_O (W_h, or its Gram matrix for the L2 norm) into w_prep,
+    once per model; scoring calls with w_o_prepared=True then take w_prep as their w_o."""
+    nbytes = 0 if ws is None else ws.numel() * ws.element_size()
+    _check(load().kvsel_prepare_w_o(ctypes.byref(params), _ptr(w_o), _ptr(w_prep),
+                                    w_prep.numel() * w_prep.element_size(), _ptr(ws), nbytes, _stream(stream)),
+           "kvsel_prepare_w_o")
 
 
 def kvsel_query_agnostic_split(params) -> tuple:

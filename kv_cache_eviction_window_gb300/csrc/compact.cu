@@ -10,7 +10,8 @@
 // of K (and of V) are contiguous, so one bulk copy per side writes them from shared
 // memory.  Sources are the contiguous cache or the block pool through the block table.
 // Copies are bit-exact; a row whose index is out of range (or whose block-table entry is)
-// is written as zeros and flagged in the status word.
+// is written as zeros and flagged in the status word, and a segment whose count and offset
+// would place rows outside the outputs is skipped and flagged.
 #include "internal.cuh"
 
 namespace kvsel {
@@ -53,8 +54,13 @@ __global__ void __launch_bounds__(kThreads) compact_kernel(const CompactArgs a) 
   const int seg = blockIdx.y;
   const int b = seg / a.rq.H, h = seg - (seg / a.rq.H) * a.rq.H;
   const int n = a.rq.n[b];
-  const int count = __ldg(a.counts + seg);
+  int count = __ldg(a.counts + seg);
   const long long off = __ldg(a.offsets + seg);
+  // the segment's output rows must lie inside the outputs (counts / offsets from the caller)
+  if (count > 0 && (off < 0 || off + count > a.n_kept)) {
+    if (blockIdx.x == 0 && threadIdx.x == 0 && a.status) atomicOr(a.status, DEV_BAD_INDEX);
+    count = 0;
+  }
   for (int r0 = blockIdx.x * kRows; r0 < count; r0 += gridDim.x * kRows) {
     const int rows = min(kRows, count - r0);
     if (threadIdx.x < kRows) {

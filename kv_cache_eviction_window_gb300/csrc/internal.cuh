@@ -210,6 +210,7 @@ cudaError_t launch_win_keysum(const WinScoreArgs& a, const CUtensorMap& tq, cons
 cudaError_t launch_win_fused(const WinScoreArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
                              unsigned int* grid_count, cudaStream_t st);
 
+
 // Also zeroes nu[0, nu_count), which launch_vnorm (next on the stream) accumulates into.
 cudaError_t launch_wbar(const uint16_t* w_o, uint16_t* wbar, int H, int G, int D, int wo_mode, float* nu,
                         long long nu_count, cudaStream_t st);
@@ -264,6 +265,7 @@ struct CompactArgs {
   const int64_t* offsets;
   uint16_t* k_out;
   uint16_t* v_out;
+  long long n_kept;               // rows of k_out / v_out
   int* status;                    // may be null
 };
 cudaError_t launch_compact(const CompactArgs& a, int max_count, int num_sms, cudaStream_t st);

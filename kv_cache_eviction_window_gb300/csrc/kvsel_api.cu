@@ -88,6 +88,8 @@ struct Plan {
   size_t ws_gpart = 0, ws_gam = 0;  // L2 value norm: Gram partials and Gamma hi/lo
   int qa_row_blocks = 0, qa_key_blocks = 0, qa_row_splits = 0;
   unsigned long long wait_limit = kDefaultWaitCycles;   // cycles one device-side wait may spin
+  bool prepared = false;   // w_o is kvsel_prepare_w_o's output
+  size_t prep_bytes = 0;   // its size
 };
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -128,6 +130,8 @@ int make_plan(const kvsel_params* p, Plan& pl, bool need_device) {
     if (p->value_norm == KVSEL_NORM_L2 && p->wo_mode != KVSEL_WO_GROUP_SUM) return KVSEL_EUNSUPPORTED;
     if (p->value_norm == KVSEL_NORM_L2 && p->group > 8) return KVSEL_EUNSUPPORTED;   // Gram staging fits G <= 8
     pl.l2 = p->value_norm == KVSEL_NORM_L2;
+    if (p->w_o_prepared != 0 && p->w_o_prepared != 1) return KVSEL_EINVAL;
+    pl.prepared = p->w_o_prepared == 1;
   }
   pl.B = p->batch;
   pl.H = p->h_kv;
@@ -304,15 +308,20 @@ int make_plan(const kvsel_params* p, Plan& pl, bool need_device) {
   if (p->value_aware) {
     pl.ws_nu = off;
     off = align256(off + static_cast<size_t>(pl.n_scores) * sizeof(float));
-    if (!pl.l2) {
+    pl.prep_bytes = pl.l2 ? static_cast<size_t>(pl.H) * 2 * kHeadDim * kHeadDim * 2
+                          : static_cast<size_t>(pl.H) * pl.Dw * kHeadDim * 2;
+    if (!pl.l2 && !pl.prepared) {
       pl.ws_wbar = off;   // W_h (the L1 path; the L2 path never materialises it)
-      off = align256(off + static_cast<size_t>(pl.H) * pl.Dw * kHeadDim * 2);
+      off = align256(off + pl.prep_bytes);
     }
     if (pl.l2) {
+      // the Gram partials (also what kvsel_prepare_w_o needs), and Gamma unless prepared
       pl.ws_gpart = off;
       off = align256(off + static_cast<size_t>(pl.H) * gram_slices(pl.Dw) * kHeadDim * kHeadDim * sizeof(float));
-      pl.ws_gam = off;
-      off = align256(off + static_cast<size_t>(pl.H) * 2 * kHeadDim * kHeadDim * 2);
+      if (!pl.prepared) {
+        pl.ws_gam = off;
+        off = align256(off + pl.prep_bytes);
+      }
     }
   }
   if (pl.anchor) {
@@ -507,9 +516,10 @@ int do_score(const kvsel_params* p, const Plan& pl, const void* q, const kvsel_k
     // nu = ||W_h v||_2 = sqrt(v^T Gamma_h v) with Gamma_h = W_h^T W_h (d x d)
     nu = reinterpret_cast<float*>(wsb + pl.ws_nu);
     float* gpart = reinterpret_cast<float*>(wsb + pl.ws_gpart);
-    uint16_t* gam = reinterpret_cast<uint16_t*>(wsb + pl.ws_gam);
+    uint16_t* gam = pl.prepared ? static_cast<uint16_t*>(const_cast<void*>(w_o))
+                                : reinterpret_cast<uint16_t*>(wsb + pl.ws_gam);
     CUtensorMap two, tg, tv;
-    {
+    if (!pl.prepared) {
       const cuuint64_t dims[2] = {static_cast<cuuint64_t>(pl.H) * pl.G * kHeadDim, static_cast<cuuint64_t>(pl.D)};
       const cuuint64_t strides[1] = {static_cast<cuuint64_t>(pl.H) * pl.G * kHeadDim * 2};
       const cuuint32_t box[2] = {64, 64};
@@ -522,7 +532,7 @@ int do_score(const kvsel_params* p, const Plan& pl, const void* q, const kvsel_k
       if (!encode(&tg, gam, 2, dims, strides, box)) return KVSEL_EINVAL;
     }
     if (!kv_map(&tv, kv->v, kv, pl, kv->layout == KVSEL_LAYOUT_PAGED ? 0 : 128)) return KVSEL_EINVAL;
-    {
+    if (!pl.prepared) {
       StageScope sc(KVSEL_STAGE_WBAR, st);
       rc = launch_rc(launch_value_gram(two, gpart, gam, pl.H, pl.G, pl.D, wait_ctl(pl, ws), st));
     }
@@ -542,11 +552,14 @@ int do_score(const kvsel_params* p, const Plan& pl, const void* q, const kvsel_k
     if (rc) return rc;
   } else if (p->value_aware) {
     nu = reinterpret_cast<float*>(wsb + pl.ws_nu);
-    uint16_t* wbar = reinterpret_cast<uint16_t*>(wsb + pl.ws_wbar);
+    uint16_t* wbar = pl.prepared ? static_cast<uint16_t*>(const_cast<void*>(w_o))
+                                 : reinterpret_cast<uint16_t*>(wsb + pl.ws_wbar);
     {
       StageScope sc(KVSEL_STAGE_WBAR, st);
-      rc = launch_rc(launch_wbar(static_cast<const uint16_t*>(w_o), wbar, pl.H, pl.G, pl.D, p->wo_mode, nu,
-                                 pl.n_scores, st));
+      // W_h (unless prepared) and the zeroed nu that the value-norm kernel accumulates into
+      rc = pl.prepared ? launch_rc(cudaMemsetAsync(nu, 0, static_cast<size_t>(pl.n_scores) * sizeof(float), st))
+                       : launch_rc(launch_wbar(static_cast<const uint16_t*>(w_o), wbar, pl.H, pl.G, pl.D, p->wo_mode,
+                                               nu, pl.n_scores, st));
     }
     if (rc) return rc;
     CUtensorMap tw;
@@ -635,6 +648,7 @@ int do_compact(const Plan& pl, const kvsel_kv* kv, const int32_t* idx, const int
   c.offsets = offsets;
   c.k_out = static_cast<uint16_t*>(k_out);
   c.v_out = static_cast<uint16_t*>(v_out);
+  c.n_kept = pl.n_kept;
   c.status = static_cast<int*>(ws);
   int sms = pl.num_sms;
   if (!sms && device_sms(&sms)) return KVSEL_ECUDA;
@@ -756,6 +770,7 @@ int kvsel_perturbation(const kvsel_params* p, const void* q, const kvsel_kv* kv,
   if (rc) return rc;
   PerturbLayout L;
   if ((rc = perturb_plan(p, pl, L))) return rc;
+  if (p->w_o_prepared) return KVSEL_EINVAL;   // the harness projects through W_O's own slices
   if (!q || !aligned16(q) || !w_o || !aligned16(w_o) || !idx || !counts || !offsets || !out) return KVSEL_EINVAL;
   if ((rc = check_kv(kv, pl, true))) return rc;
   if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) || ws_bytes < L.total) return KVSEL_EWORKSPACE;
@@ -901,6 +916,44 @@ int kvsel_workspace_size(const kvsel_params* p, size_t* bytes) {
   return KVSEL_OK;
 }
 
+int kvsel_prepared_w_o_size(const kvsel_params* p, size_t* bytes) {
+  if (!bytes) return KVSEL_EINVAL;
+  Plan pl;
+  const int rc = make_plan(p, pl, false);
+  if (rc) return rc;
+  if (!p->value_aware) return KVSEL_EINVAL;
+  *bytes = pl.l2 ? static_cast<size_t>(pl.H) * 2 * kHeadDim * kHeadDim * 2
+                 : static_cast<size_t>(pl.H) * pl.Dw * kHeadDim * 2;
+  return KVSEL_OK;
+}
+
+int kvsel_prepare_w_o(const kvsel_params* p, const void* w_o, void* w_prep, size_t w_prep_bytes, void* ws,
+                      size_t ws_bytes, void* stream) {
+  if (!p) return KVSEL_EINVAL;
+  kvsel_params q = *p;
+  q.w_o_prepared = 0;   // the plan of the unprepared call: W_O in, its derived weights out
+  Plan pl;
+  int rc = make_plan(&q, pl, true);
+  if (rc) return rc;
+  if (!q.value_aware || !w_o || !aligned16(w_o) || !w_prep || (reinterpret_cast<uintptr_t>(w_prep) & 255u))
+    return KVSEL_EINVAL;
+  if (w_prep_bytes < pl.prep_bytes) return KVSEL_EINVAL;
+  if (pl.l2 && (rc = check_ws(pl, ws, ws_bytes))) return rc;   // the L1 weights need no scratch
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (pl.l2) {
+    CUtensorMap two;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(pl.H) * pl.G * kHeadDim, static_cast<cuuint64_t>(pl.D)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(pl.H) * pl.G * kHeadDim * 2};
+    const cuuint32_t box[2] = {64, 64};
+    if (!encode(&two, w_o, 2, dims, strides, box)) return KVSEL_EINVAL;
+    float* gpart = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + pl.ws_gpart);
+    return launch_rc(launch_value_gram(two, gpart, static_cast<uint16_t*>(w_prep), pl.H, pl.G, pl.D,
+                                       wait_ctl(pl, ws), st));
+  }
+  return launch_rc(launch_wbar(static_cast<const uint16_t*>(w_o), static_cast<uint16_t*>(w_prep), pl.H, pl.G, pl.D,
+                               q.wo_mode, nullptr, 0, st));
+}
+
 int kvsel_query_agnostic_split(const kvsel_params* p, int32_t* key_blocks, int32_t* row_splits) {
   if (!key_blocks || !row_splits) return KVSEL_EINVAL;
   Plan pl;
@@ -1014,10 +1067,12 @@ int kvsel_run_layer(const kvsel_params* p, const void* q, const kvsel_kv* kv, co
   int rc = make_plan(p, pl, true);
   if (rc) return rc;
   if (pl.anchor) return KVSEL_EUNSUPPORTED;   // anchors: kvsel_run_anchors
-  if (!q || !aligned16(q) || !s_attn || !idx || !counts || !offsets || !k_out || !v_out) return KVSEL_EINVAL;
-  if (!aligned16(k_out) || !aligned16(v_out)) return KVSEL_EINVAL;
+  if (!q || !aligned16(q) || !s_attn || !idx || !counts || !offsets) return KVSEL_EINVAL;
+  // no outputs for the rows: score and select only (the caller compacts later)
+  const bool compact = k_out != nullptr || v_out != nullptr;
+  if (compact && (!k_out || !v_out || !aligned16(k_out) || !aligned16(v_out))) return KVSEL_EINVAL;
   if (p->value_aware && (!w_o || !aligned16(w_o) || !s_val)) return KVSEL_EINVAL;
-  if ((rc = check_kv(kv, pl, true))) return rc;
+  if ((rc = check_kv(kv, pl, compact || p->value_aware))) return rc;
   if (pl.qa && kv->layout != KVSEL_LAYOUT_CONTIGUOUS) return KVSEL_EUNSUPPORTED;
   if ((rc = check_ws(pl, ws, ws_bytes))) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -1035,7 +1090,7 @@ int kvsel_run_layer(const kvsel_params* p, const void* q, const kvsel_kv* kv, co
   } else if ((rc = do_select(p, pl, s_attn, s_val, idx, counts, offsets, st))) {
     return rc;
   }
-  if (pl.n_kept == 0) return KVSEL_OK;
+  if (pl.n_kept == 0 || !compact) return KVSEL_OK;
   return do_compact(pl, kv, idx, counts, offsets, k_out, v_out, ws, st);
 }
 
