@@ -286,6 +286,18 @@ def select_per_layer(scores: np.ndarray, budget: int, forced: np.ndarray,
     return [flat[(flat >= h * n) & (flat < (h + 1) * n)] - h * n for h in range(H)]
 
 
+def select_two_stage_per_layer(s_pool: np.ndarray, s_val: np.ndarray, budget: int, forced: np.ndarray,
+                               floor_per_head: int, alpha: float = ALPHA_DEFAULT) -> List[np.ndarray]:
+    """Value-aware selection under one budget per layer ([CKV] §3.4 Algorithm 2: line 1
+    allocates the layer's budget across heads, AdaKV-style; line 8 then runs Algorithm 1
+    per head).  Reading: head h's budget b_h is the number of its entries in the layer-wide
+    top-``budget`` of the pooled attention score (with the per-head floor, as in
+    select_per_layer); each head then keeps b_h entries by the two-stage criterion."""
+    alloc = select_per_layer(s_pool, budget, forced, floor_per_head)
+    return [select_two_stage(s_pool[h], s_val[h], len(alloc[h]), forced[h], alpha)
+            for h in range(s_pool.shape[0])]
+
+
 # ---------------------------------------------------------------------------------------
 # compaction
 # ---------------------------------------------------------------------------------------
@@ -366,11 +378,12 @@ def run_layer(q_bits: np.ndarray, k_bits: Sequence[np.ndarray], v_bits: Sequence
             else:
                 idx = [top_b(s_pool[h], bh, fm) for h in range(H)]
         elif budget_mode == "layer":
-            if value_aware:
-                raise NotImplementedError("value-aware selection under a per-layer budget")
             bl = int(math.floor(budget_ratio * n * H))
             fl = int(math.floor(floor_ratio * n))
-            idx = select_per_layer(s_pool, bl, np.stack([fm] * H), fl)
+            if value_aware:
+                idx = select_two_stage_per_layer(s_pool, s_val, bl, np.stack([fm] * H), fl, alpha)
+            else:
+                idx = select_per_layer(s_pool, bl, np.stack([fm] * H), fl)
         else:
             raise ValueError(budget_mode)
         r = dict(n=n, s_raw=s_raw, s_pool=s_pool, nu=nu, s_val=s_val, idx=idx)

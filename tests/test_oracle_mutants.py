@@ -202,6 +202,12 @@ def _pt_slice_transposed(q, k, v, w_o, h, group, keep, scale=None, causal=True):
     return out
 
 
+def _two_stage_per_layer_uniform_split(s_pool, s_val, budget, forced, floor_per_head, alpha=0.5):
+    H = s_pool.shape[0]
+    b = budget // H
+    return [O.select_two_stage(s_pool[h], s_val[h], b, forced[h], alpha) for h in range(H)]
+
+
 def _partition_drops_last(n, idx):
     kept = np.zeros(n, dtype=bool)
     kept[np.asarray(idx, dtype=np.int64)] = True
@@ -255,6 +261,7 @@ MUTANTS = {
     "head_scores_mean": ("head_scores", _head_scores_mean),
     "value_norm_l2_no_sqrt": ("value_norm", _value_norm_l2_no_sqrt),
     "partition_drops_last": ("partition", _partition_drops_last),
+    "two_stage_per_layer_uniform_split": ("select_two_stage_per_layer", _two_stage_per_layer_uniform_split),
     "partition_one_based": ("partition", _partition_one_based),
     "archive_descending": ("archive", _archive_descending),
 }

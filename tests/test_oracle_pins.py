@@ -498,6 +498,45 @@ def test_compact_and_paging():
     np.testing.assert_array_equal(O.compact(k, np.arange(k.shape[0])), k)
 
 
+def test_two_stage_per_layer_budget_hand_example():
+    """CriticalKV Algorithm 2 line 1 then Algorithm 1 per head, by hand: two heads of four
+    entries, layer budget 4, no forced entries, no floor, alpha = 0.5.  The pooled scores
+    put three of the layer's top four in head 0 and one in head 1, so b_0 = 3, b_1 = 1.
+    Head 0: stage 1 keeps floor(1.5) = 1 entry by score (entry 0), stage 2 the two best
+    of the others by s_val (entries 2 and 3, s_val 9 and 5; entry 2 has the lowest pooled
+    score of the head).  Head 1: stage 1 keeps floor(0.5) = 0, so
+    stage 2 takes the single best s_val (entry 2), though its pooled score is lowest."""
+    s_pool = np.array([[0.9, 0.8, 0.1, 0.7], [0.6, 0.05, 0.01, 0.02]])
+    s_val = np.array([[1.0, 2.0, 9.0, 5.0], [0.1, 0.2, 7.0, 0.3]])
+    fm = np.zeros((2, 4), dtype=bool)
+    out = O.select_two_stage_per_layer(s_pool, s_val, 4, fm, 0, 0.5)
+    assert out[0].tolist() == [0, 2, 3]
+    assert out[1].tolist() == [2]
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_two_stage_per_layer_budget_invariants(seed):
+    """Per head: the allocation of the layer budget (counts add up to B_L, each at least
+    the floor), two-stage selection within it (alpha = 1 gives back the attention-only
+    per-layer selection), forced entries always kept."""
+    rng = np.random.default_rng(seed)
+    H, n = 3, 40
+    s_pool = rng.random((H, n))
+    s_val = rng.random((H, n))
+    fm = np.stack([O.forced_mask(n, 2, 3)] * H)
+    B_L, fl = 45, 8
+    out = O.select_two_stage_per_layer(s_pool, s_val, B_L, fm, fl, 0.5)
+    alloc = O.select_per_layer(s_pool, B_L, fm, fl)
+    assert [len(x) for x in out] == [len(x) for x in alloc]
+    assert sum(len(x) for x in out) == B_L and all(len(x) >= fl for x in out)
+    for h in range(H):
+        assert set(np.flatnonzero(fm[h]).tolist()) <= set(out[h].tolist())
+        np.testing.assert_array_equal(out[h], O.select_two_stage(s_pool[h], s_val[h], len(alloc[h]), fm[h], 0.5))
+    same = O.select_two_stage_per_layer(s_pool, s_val, B_L, fm, fl, 1.0)
+    for h in range(H):
+        np.testing.assert_array_equal(same[h], alloc[h])
+
+
 # --------------------------------------------------------------------- partition / archive
 def test_partition_hand_example():
     """VestigeKV §4.1: eviction archives rows instead of deleting them.  By hand: of the
