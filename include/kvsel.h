@@ -194,6 +194,9 @@ int kvsel_score(const kvsel_params* p, const void* q, const kvsel_kv* kv, const 
 
 /* Select the kept entries from the scores (CriticalKV Algorithm 1 when value_aware;
  * per-layer budget with per-head floors, KVzip §4.2, when budget_mode is PER_LAYER).
+ * Both together follow CriticalKV Algorithm 2: the layer budget is split over the heads
+ * by the layer-wide top of s_attn (line 1, with the floors), then each head keeps its
+ * share by the two-stage criterion (line 8).
  * Forced entries (sinks, recent window) are always kept and count inside the budget.
  *   s_attn  device fp32 [n_scores]; s_val device fp32 [n_scores] or NULL
  *   idx     device int32 [n_kept]; counts device int32 [batch*h_kv];

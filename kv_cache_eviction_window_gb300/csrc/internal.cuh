@@ -250,6 +250,11 @@ struct SelectArgs {
   int32_t* counts;
   int64_t* offsets;               // written for every segment
   long long seg_out[kMaxBatch];   // output offset of request b's first segment
+  // per-head mode with budgets set on the device (value-aware selection under a per-layer
+  // budget): segment s keeps dev_counts[s] entries at dev_offsets[s]; counts and offsets
+  // are then not rewritten
+  const int32_t* dev_counts;
+  const int64_t* dev_offsets;
 };
 cudaError_t launch_select(const SelectArgs& a, int cluster, int chunk_cap, cudaStream_t st);
 int select_cluster_size(int max_len, int segments, int* chunk_cap);

@@ -124,7 +124,7 @@ int make_plan(const kvsel_params* p, Plan& pl, bool need_device) {
     if (p->wo_mode != KVSEL_WO_GROUP_SUM && p->wo_mode != KVSEL_WO_PER_HEAD) return KVSEL_EINVAL;
     if (p->d_model < 128 || p->d_model % 128 != 0) return KVSEL_EUNSUPPORTED;
     if (!(p->alpha >= 0.f && p->alpha <= 1.f) || !(p->eps >= 0.f)) return KVSEL_EINVAL;
-    if (p->budget_mode != KVSEL_BUDGET_PER_HEAD) return KVSEL_EUNSUPPORTED;
+    if (p->budget_mode == KVSEL_BUDGET_ANCHOR) return KVSEL_EUNSUPPORTED;
     if (p->value_norm != KVSEL_NORM_L1 && p->value_norm != KVSEL_NORM_L2) return KVSEL_EINVAL;
     // the Gram identity holds for one projection per token: the group-sum reading only
     if (p->value_norm == KVSEL_NORM_L2 && p->wo_mode != KVSEL_WO_GROUP_SUM) return KVSEL_EUNSUPPORTED;
@@ -630,7 +630,29 @@ int do_select(const kvsel_params* p, const Plan& pl, const float* s_attn, const 
   const int cs = select_cluster_size(std::max(max_len, 1), segs, &cap);
   if (cs < 0) return KVSEL_EUNSUPPORTED;
   StageScope sc(KVSEL_STAGE_SELECT, st);
-  return launch_rc(launch_select(a, cs, cap, st));
+  if (p->budget_mode != KVSEL_BUDGET_PER_LAYER || !p->value_aware) return launch_rc(launch_select(a, cs, cap, st));
+  // Value-aware selection under a per-layer budget (CriticalKV Algorithm 2, line 1 then
+  // line 8): the layer-wide top of the pooled attention score sets each head's budget
+  // (counts/offsets; its pooling also writes s_attn and s_val), then the two-stage
+  // selection runs per head within that budget, reading the budgets on the device.
+  a.two_stage = 0;
+  int rc = launch_rc(launch_select(a, cs, cap, st));
+  if (rc) return rc;
+  SelectArgs h = a;
+  h.mode = KVSEL_BUDGET_PER_HEAD;
+  h.two_stage = 1;
+  h.raw = nullptr;
+  h.nu = nullptr;
+  h.out_attn = nullptr;
+  h.out_val = nullptr;
+  h.s1 = out_attn ? out_attn : s_attn;
+  h.s2 = out_val ? out_val : s_val;
+  h.dev_counts = counts;
+  h.dev_offsets = offsets;
+  int cap2 = 0;
+  const int cs2 = select_cluster_size(std::max(pl.n_max, 1), pl.B * pl.H, &cap2);
+  if (cs2 < 0) return KVSEL_EUNSUPPORTED;
+  return launch_rc(launch_select(h, cs2, cap2, st));
 }
 
 int do_compact(const Plan& pl, const kvsel_kv* kv, const int32_t* idx, const int32_t* counts, const int64_t* offsets,

@@ -453,12 +453,23 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelectArgs a,
 
   uint32_t T, krem;
   if (!per_layer) {
-    const uint32_t B = static_cast<uint32_t>(a.budget[b]);
+    // the segment's budget: fixed per request, or set on the device by an earlier
+    // per-layer selection (its per-head counts and offsets)
+    uint32_t B = static_cast<uint32_t>(a.budget[b]);
+    uint32_t B1 = static_cast<uint32_t>(a.budget1[b]);
+    long long out0 = a.seg_out[b] + static_cast<long long>(h0) * B;
+    if (a.dev_counts) {
+      const int c = __ldg(a.dev_counts + seg);
+      B = static_cast<uint32_t>(min(max(c, 0), n));
+      out0 = __ldg(a.dev_offsets + seg);
+      long long b1 = static_cast<long long>(floor(static_cast<double>(a.alpha) * static_cast<double>(B)));
+      B1 = static_cast<uint32_t>(max(b1, static_cast<long long>(nforced)));
+    }
     if (a.two_stage) {
       // stage 1: b' = max(floor(alpha*B), |F|) entries by the attention score.  Without
       // ties to resolve (krem == 0, the usual case) the picks are exactly the keys above T
       // and need no ordered pass; otherwise they are flagged in index order.
-      radix_select(cl, S, sst, keys, cnt, static_cast<uint32_t>(a.budget1[b]), T, krem);
+      radix_select(cl, S, sst, keys, cnt, B1, T, krem);
       const bool by_threshold = (krem == 0u);
       if (!by_threshold)
         apply_selection(cl, S, sst, keys, 0, cnt, T, krem, [&](int e, uint32_t) { flag[e] = 1; });
@@ -488,11 +499,10 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelectArgs a,
       __syncthreads();
     }
     radix_select(cl, S, sst, keys, cnt, B, T, krem);
-    const long long out0 = a.seg_out[b] + static_cast<long long>(h0) * B;
     apply_selection(cl, S, sst, keys, 0, cnt, T, krem, [&](int e, uint32_t slot) {
       if (slot < B) a.idx[out0 + slot] = c_lo + e;
     });
-    if (rank == 0 && threadIdx.x == 0) {
+    if (rank == 0 && threadIdx.x == 0 && !a.dev_counts) {
       a.counts[seg] = static_cast<int32_t>(B);
       a.offsets[seg] = out0;
     }

@@ -96,7 +96,7 @@ def _p(B, **kw):
     (dict(window=0, causal=False, reduce="max", value_aware=True, d_model=4096), -3),
     (dict(group=3, window=10), -3),             # 30 window rows: not a multiple of 32
     (dict(window=8192), -1),                    # window longer than the context
-    (dict(value_aware=True, d_model=4096, budget_mode="layer"), -3),
+    (dict(value_aware=True, d_model=4096, budget_mode="anchor"), -3),
     (dict(value_aware=True, d_model=100), -3),
     (dict(value_aware=True, d_model=4096, value_norm="l2", wo_mode="per_head"), -3),   # Gram needs one W_h
     (dict(budget_mode="layer", budget_ratio=0.1, floor_ratio=0.2), -2),

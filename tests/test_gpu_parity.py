@@ -69,10 +69,33 @@ def _check_layer(wl, inp, gpu, ora, heads=None):
                 ths.append((o["s_pool"][h], GH.kth_key(o["s_pool"][h], fm, fh)))
                 keep[h, O.top_b(o["s_pool"][h], fh, fm)] = True
             tl = GH.kth_key(flat, keep.reshape(-1), BL)
-            for h in range(H):
-                assert len(g["idx"][h]) >= fh
-                GH.check_selection_near_ties(g["idx"][h], o["idx"][h], fm, n, len(g["idx"][h]),
-                                             ths + [(o["s_pool"][h], tl)], f"layer sel b{b} h{h}")
+            if wl.value_aware:
+                # the layer budget's split over heads (CriticalKV Algorithm 2, line 1): the
+                # oracle's allocation, up to entries near the layer threshold
+                alloc = O.select_per_layer(o["s_pool"], BL, np.stack([fm] * H), fl)
+                for h in range(H):
+                    slack = sum(GH.near(x, tl) for x in o["s_pool"][h]) + \
+                        sum(GH.near(x, ths[h][1]) for x in o["s_pool"][h])
+                    assert abs(len(g["idx"][h]) - len(alloc[h])) <= slack, (b, h, len(g["idx"][h]), len(alloc[h]))
+                # then Algorithm 1 within each head's budget (line 8), as in per-head mode
+                for h in range(H):
+                    Bh = len(g["idx"][h])
+                    assert Bh >= fh
+                    b1 = max(int(math.floor(wl.alpha * Bh)), int(fm.sum()))
+                    t1 = GH.kth_key(o["s_pool"][h], fm, b1)
+                    keep1 = np.zeros(n, bool)
+                    keep1[O.top_b(o["s_pool"][h], b1, fm)] = True
+                    t2 = GH.kth_key(o["s_val"][h], keep1, Bh)
+                    want = O.select_two_stage(o["s_pool"][h], o["s_val"][h], Bh, fm, wl.alpha)
+                    GH.check_selection_near_ties(g["idx"][h], want, fm, n, Bh,
+                                                 [(o["s_pool"][h], t1), (o["s_val"][h], t2)], f"layer va b{b} h{h}")
+                    k1 = GH.topk_mask(g["s_attn"][h], fm, b1)
+                    GH.check_topk_property(g["s_val"][h], g["idx"][h], k1, Bh, f"layer two-stage b{b} h{h}")
+            else:
+                for h in range(H):
+                    assert len(g["idx"][h]) >= fh
+                    GH.check_selection_near_ties(g["idx"][h], o["idx"][h], fm, n, len(g["idx"][h]),
+                                                 ths + [(o["s_pool"][h], tl)], f"layer sel b{b} h{h}")
         # compaction is bit-exact given the GPU's own indices
         for h in hs:
             np.testing.assert_array_equal(g["k_out"][h], inp["k"][b][h][g["idx"][h]])
@@ -130,6 +153,19 @@ def test_c3_per_layer_budget(n):
     inp = datagen.make_layer(wl, 0, n_ctx=n)
     ora = O.run_workload_layer(wl, inp)
     gpu = GH.run_gpu_layer(wl, inp)
+    _check_layer(wl, inp, gpu, ora)
+
+
+@pytest.mark.parametrize("n,split", [(1500, False), (3333, False), (3333, True)])
+def test_c3_value_aware_per_layer_budget(n, split):
+    """Value-aware selection under one budget per layer (CriticalKV Algorithm 2: the layer
+    budget split over heads by the pooled attention score, then Algorithm 1 per head) on
+    the Qwen2.5-7B layer shape (4 KV heads, group 7, 448 window rows, W_O 3584 x 3584),
+    through kvsel_run_layer and through the three split calls."""
+    wl = datagen.WORKLOADS[3].replace(value_aware=True, d_model=3584)
+    inp = datagen.make_layer(wl, 0, n_ctx=n)
+    ora = O.run_workload_layer(wl, inp, compact_out=False)
+    gpu = GH.run_gpu_layer(wl, inp, split=split)
     _check_layer(wl, inp, gpu, ora)
 
 
