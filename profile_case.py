@@ -5,6 +5,7 @@
     python profile_case.py --workload 6      # AnchorKV anchors
     python profile_case.py --workload 2 --perturb   # + output perturbation
     python profile_case.py --workload 5 --n-ctx 8192  # query-agnostic, smaller n
+    python profile_case.py --workload 2 --plain --partition   # + kept/evicted partition
 
 The inputs are the same seeded synthetic tensors as the benchmark (each layer distinct,
 larger than L2 for the 32K stack), so per-launch counters taken here scale to the
@@ -30,6 +31,7 @@ def main():
     ap.add_argument("--value-norm", default=None, choices=["l1", "l2"], help="value-aware norm override")
     ap.add_argument("--perturb", action="store_true", help="also run kvsel_perturbation on each layer's kept set")
     ap.add_argument("--n-ctx", type=int, default=None, help="context length override (a smaller case of the shape)")
+    ap.add_argument("--partition", action="store_true", help="also run kvsel_partition on each layer's kept set")
     args = ap.parse_args()
     import numpy as np
     import torch
@@ -93,6 +95,16 @@ def main():
             else:
                 B.kvsel_run_layer(p, q, kv, w, b.s_attn, b.s_val, b.idx, b.counts, b.offsets, b.k_out, b.v_out,
                                   b.ws)
+            if args.partition:
+                if not hasattr(b, "ev_idx"):
+                    n_ev = max(b.n_scores - b.n_kept, 1)
+                    b.ev_idx = torch.empty(n_ev, dtype=torch.int32, device=dev)
+                    b.ev_counts = torch.empty(b.n_seg, dtype=torch.int32, device=dev)
+                    b.ev_offsets = torch.empty(b.n_seg, dtype=torch.int64, device=dev)
+                    b.k_ev = torch.empty((n_ev, 128), dtype=torch.bfloat16, device=dev)
+                    b.v_ev = torch.empty((n_ev, 128), dtype=torch.bfloat16, device=dev)
+                B.kvsel_partition(p, kv, b.idx, b.counts, b.offsets, b.ev_idx, b.ev_counts, b.ev_offsets, b.k_ev,
+                                  b.v_ev, b.k_out, b.v_out, b.ws)
             if args.perturb:
                 if not hasattr(b, "pt_out"):
                     b.pt_out = torch.empty((1, wl.h_kv, 3, wl.group, wl.window), dtype=torch.float32, device=dev)
