@@ -87,6 +87,8 @@ struct WinScoreArgs {
   float s2;                       // logit scale * log2(e)
   float* part;                    // per (b, h): [2][R_pad][chunk_pad]: row max (log2 units) and sum
   float* s_raw;                   // packed [sum_b H*n_b] reduced scores
+  float* nu_zero;                 // optional, packed like s_raw: zeroed by the fused launch for
+                                  // the value-norm kernel that accumulates into it next
   WaitCtl wc;
 };
 

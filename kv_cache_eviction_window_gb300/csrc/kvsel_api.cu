@@ -488,6 +488,8 @@ int do_score(const kvsel_params* p, const Plan& pl, const void* q, const kvsel_k
   a.s2 = scale * 1.4426950408889634f;
   a.part = part;
   a.s_raw = s_raw;
+  // the L1 value norms are accumulated atomically: the fused launch zeroes them on the way
+  a.nu_zero = (p->value_aware && !pl.l2) ? reinterpret_cast<float*>(wsb + pl.ws_nu) : nullptr;
   a.wc = wait_ctl(pl, ws);
   int rc;
   cudaError_t fe = cudaErrorNotSupported;
@@ -554,14 +556,15 @@ int do_score(const kvsel_params* p, const Plan& pl, const void* q, const kvsel_k
     nu = reinterpret_cast<float*>(wsb + pl.ws_nu);
     uint16_t* wbar = pl.prepared ? static_cast<uint16_t*>(const_cast<void*>(w_o))
                                  : reinterpret_cast<uint16_t*>(wsb + pl.ws_wbar);
-    {
+    if (!pl.prepared || fe != cudaSuccess) {
       StageScope sc(KVSEL_STAGE_WBAR, st);
       // W_h (unless prepared) and the zeroed nu that the value-norm kernel accumulates into
+      // (already zeroed by the fused scoring launch when that ran)
       rc = pl.prepared ? launch_rc(cudaMemsetAsync(nu, 0, static_cast<size_t>(pl.n_scores) * sizeof(float), st))
                        : launch_rc(launch_wbar(static_cast<const uint16_t*>(w_o), wbar, pl.H, pl.G, pl.D, p->wo_mode,
-                                               nu, pl.n_scores, st));
+                                               nu, fe == cudaSuccess ? 0 : pl.n_scores, st));
+      if (rc) return rc;
     }
-    if (rc) return rc;
     CUtensorMap tw;
     const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(pl.Dw),
                                 static_cast<cuuint64_t>(pl.H)};

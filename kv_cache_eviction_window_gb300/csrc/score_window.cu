@@ -507,15 +507,46 @@ __global__ void __launch_bounds__(kThreads, 1)
 // K tiles are still in L2.  The TMA producer and the UMMA warp run straight on into
 // pass 2 (K and Q do not depend on the barrier); only the epilogue waits.
 //
+// Shared-memory matrix descriptor: K-major operand, 32-byte swizzle.  Rows are 32 B
+// (16 bf16: one UMMA K step), 8-row groups (256 B) follow each other.  `saddr` must be
+// 256-byte aligned.  The swizzle only exchanges the two 16-byte halves of a row, so an
+// operand whose other side is constant along K may be written without it.
+__device__ __forceinline__ uint64_t sdesc_kmajor_sw32(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);   // start address      [0,14)
+  d |= static_cast<uint64_t>(1u) << 16;                  // leading byte off.  [16,30)
+  d |= static_cast<uint64_t>(256u >> 4) << 32;           // stride byte offset [32,46)
+  d |= static_cast<uint64_t>(1u) << 46;                  // descriptor version [46,48)
+  d |= static_cast<uint64_t>(6u) << 61;                  // swizzle: 32 B      [61,64)
+  return d;
+}
+__device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
 // The epilogue has 16 warps, four per TMEM lane quadrant, so that every SM sub-partition
 // keeps four warps of exponentials in flight.  Pass 1: each warp takes a 32-key column
 // group of every tile.  Pass 2: two groups of eight warps take alternate tiles; in a
 // group the two warps of a lane quadrant split the window rows in halves and add their
 // partial sums through shared memory.
+//
+// Pass 2 needs l_rj * s2 - c2_r for every window row r, c2_r = m_r + log2 Z_r.  The row
+// constant is added by the tensor core, not the epilogue: one more K step multiplies a
+// block of ones (keys side) by the constants -c2_r / s2 split into three bf16 parts
+// (rows side), so the accumulator holds l_rj - c2_r / s2 and the epilogue only scales it.
+// Reading 64 constants from shared memory per tile would queue behind the UMMA operand
+// reads, which keep the shared-memory port busy during pass 2.
+//
+// Two warps issue the UMMAs, one the even tiles and one the odd ones (each with its own
+// accumulators and commits).  One issuing thread spends about 54 cycles per M = 128,
+// N = 128 UMMA and more per commit and wait, while the tensor core needs 64 cycles per
+// such UMMA, so a single issuer leaves the tensor core idle for part of every tile.
 constexpr int kFEpiWarps = 16;
 constexpr int kFProducerWarp = 16;
-constexpr int kFMmaWarp = 17;
-constexpr int kFThreads = 576;
+constexpr int kFMmaWarp = 17;       // UMMA issue: warps 17 and 18 take alternate tiles
+constexpr int kFThreads = 608;
 
 __device__ __forceinline__ void fused_epi_bar() { asm volatile("bar.sync 1, 512;" ::: "memory"); }
 
@@ -552,7 +583,9 @@ __global__ void __launch_bounds__(kFThreads, 1)
     win_fused_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                      const WinScoreArgs a, unsigned int* grid_count) {
   constexpr int NT = 128, STAGES = (MT == 1) ? 5 : 4, kAcc = 2;
-  constexpr int kAcc2 = (MT == 1) ? 4 : 2;           // pass-2 accumulators (R <= MT*128 columns each)
+  // pass-2 accumulators: R <= 128 uses eight half-tile accumulators (N = R/2, columns
+  // 128c and 128c + 64 for tile class c = t % 4); R > 128 uses two of N = R
+  constexpr int kAcc2 = (MT == 1) ? 8 : 2;
   constexpr uint32_t kAccCols = MT * 128;
   constexpr uint32_t kTmemCols = 512;
   constexpr int kQHalf = MT * 128 * 128;
@@ -563,14 +596,15 @@ __global__ void __launch_bounds__(kFThreads, 1)
   uint8_t* smem = smem_align1024(smem_raw);
   uint8_t* sQ = smem;
   uint8_t* sK = smem + 2 * kQHalf;
+  uint8_t* sOnes = sK + STAGES * kKStage;   // 128 rows x 16 bf16 ones (32-byte swizzle rows)
+  uint8_t* sC = sOnes + 128 * 32;           // MT*128 rows x 16 bf16: -c2_r / s2 in three parts
 
   __shared__ __align__(8) uint64_t full_bar[STAGES], empty_bar[STAGES];
   __shared__ __align__(8) uint64_t accf1[kAcc], acce1[kAcc], accf2[kAcc2], acce2[kAcc2];
-  __shared__ __align__(8) uint64_t q_bar, done_bar;
+  __shared__ __align__(8) uint64_t q_bar, done_bar[2], c_bar;
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
   __shared__ float s_xm[MT][4][128], s_xz[MT][4][128];   // pass-1 partials per column group
-  __shared__ __align__(16) float s_nc2[MT * 128];          // -(m_r + log2 Z_r) per window row
   __shared__ float s_part[2][128];                         // pass-2 half sums per group
 
   const int warp = warp_id(), lane = lane_id();
@@ -594,13 +628,18 @@ __global__ void __launch_bounds__(kFThreads, 1)
     }
     for (int s = 0; s < kAcc2; ++s) {
       mbar_init(&accf2[s], 1);
-      mbar_init(&acce2[s], kFEpiWarps / 2);
+      mbar_init(&acce2[s], MT == 1 ? 4 : kFEpiWarps / 2);   // the warps that read one pass-2 accumulator
     }
     mbar_init(&q_bar, 1);
-    mbar_init(&done_bar, 1);
+    mbar_init(&done_bar[0], 1);
+    mbar_init(&done_bar[1], 1);
+    mbar_init(&c_bar, 1);
     s_abort = 0;
     fence_mbar_init();
   }
+  for (int i = threadIdx.x; i < 128 * 32 / 16; i += kFThreads)   // bf16 1.0 = 0x3f80
+    reinterpret_cast<uint4*>(sOnes)[i] = make_uint4(0x3f803f80u, 0x3f803f80u, 0x3f803f80u, 0x3f803f80u);
+  fence_proxy_async_smem();
   if (warp == kFMmaWarp) {
     tmem_alloc(&s_tmem, kTmemCols);
     tmem_relinquish();
@@ -609,6 +648,10 @@ __global__ void __launch_bounds__(kFThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = s_tmem;
+  if (a.nu_zero != nullptr && warp < kFEpiWarps) {   // this chunk's value norms start from zero
+    float* z = a.nu_zero + static_cast<size_t>(a.rq.soff[b]) + static_cast<size_t>(h) * n;
+    for (int k = key_begin + static_cast<int>(threadIdx.x); k < key_end; k += kFEpiWarps * 32) z[k] = 0.f;
+  }
 
   if (warp == kFProducerWarp) {
     if (lane == 0 && ntiles > 0) {
@@ -627,13 +670,14 @@ __global__ void __launch_bounds__(kFThreads, 1)
       for (int tt = max(0, T - STAGES); tt < T; ++tt) mbar_drain(&full_bar[tt % STAGES], (tt / STAGES) & 1, status);
       mbar_drain(&q_bar, 0, status);
     }
-  } else if (warp == kFMmaWarp) {
-    if (lane == 0 && ntiles > 0) {
+  } else if (warp == kFMmaWarp || warp == kFMmaWarp + 1) {
+    const int iss = warp - kFMmaWarp;   // this warp issues tiles iss, iss + 2, ...
+    if (lane == 0 && ntiles > iss) {
       bool ok = mbar_wait(&q_bar, 0, &s_abort, a.wc);
       const uint64_t qd0 = sdesc_kmajor_sw128(smem_u32(sQ));
-      // pass 1: A = window rows, B = keys
+      // pass 1: A = window rows, B = keys (accumulator t % 2 = iss)
       constexpr uint32_t idesc1 = idesc_bf16_f32(128, NT);
-      for (int t = 0; ok && t < ntiles; ++t) {
+      for (int t = iss; ok && t < ntiles; t += 2) {
         const int s = t % STAGES, u = t / STAGES;
         const int acc = t % kAcc, ua = t / kAcc;
         if (!mbar_wait(&full_bar[s], u & 1, &s_abort, a.wc) ||
@@ -655,45 +699,135 @@ __global__ void __launch_bounds__(kFThreads, 1)
         umma_commit(&empty_bar[s]);
         umma_commit(&accf1[acc]);
       }
-      // pass 2: A = keys (M = 128), B = window rows (N = R in chunks of <= 256)
-      for (int t = 0; ok && t < ntiles; ++t) {
-        const int T = ntiles + t;
-        const int s = T % STAGES, u = T / STAGES;
-        const int acc = t % kAcc2, ua = t / kAcc2;
-        if (!mbar_wait(&full_bar[s], u & 1, &s_abort, a.wc)) {
-          ok = false;
-          break;
-        }
-        if (t < kAcc2) {
-          // first pass-2 use of these columns: pass 1's last use of them is released
-          if (acc < kAcc) {
-            const int last1 = ((ntiles - 1 - acc) >= 0) ? ntiles - 1 - ((ntiles - 1 - acc) % kAcc) : -1;
-            if (last1 >= 0 && !mbar_wait(&acce1[acc], (last1 / kAcc) & 1, &s_abort, a.wc)) {
-              ok = false;
-              break;
-            }
-          }
-        } else if (!mbar_wait(&acce2[acc], (ua & 1) ^ 1, &s_abort, a.wc)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint64_t kd0 = sdesc_kmajor_sw128(smem_u32(sK + s * kKStage));
+      // pass 2: A = keys (M = 128), B = window rows; a ninth K step adds -c2_r / s2
+      // (ones x C).  The logits of the first tiles (as many as there are accumulators) are
+      // issued before the row statistics exist (during the grid barrier); their constants
+      // follow.  A pass-2 tile's columns always belong to the pass-1 accumulator of the
+      // same parity, so this warp reuses only columns it used in pass 1.
+      const uint64_t onesd = sdesc_kmajor_sw32(smem_u32(sOnes));
+      auto add_row_consts = [&](int acc) {
         for (int n0 = 0; n0 < R; n0 += 256) {
           const int nc = min(256, R - n0);
-          const uint32_t idesc = idesc_bf16_f32(128, nc);
+          umma_bf16(tbase + acc * kAccCols + n0, onesd, sdesc_kmajor_sw32(smem_u32(sC + n0 * 32)),
+                    idesc_bf16_f32(128, nc), 1u);
+        }
+      };
+      if constexpr (MT == 1) {
+        // tile t (class c = t % 4) fills accumulator halves 2c (window rows [0, R/2)) and
+        // 2c + 1 (rows [R/2, R)); the epilogue releases each half when it has summed it,
+        // so the next tile of the class starts while the second half is being summed
+        const int Rh = R / 2;
+        const uint32_t idesc_h = idesc_bf16_f32(128, Rh);
+        auto logits_half = [&](uint64_t kd0, int hcol, int r0) {
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
             const uint32_t koff = (k & 3) * 32;
-            umma_bf16(tbase + acc * kAccCols + n0, kd0 + (((k >> 2) * (NT * 128) + koff) >> 4),
-                      qd0 + (static_cast<uint32_t>((k >> 2) * kQHalf + n0 * 128 + koff) >> 4), idesc, k > 0 ? 1u : 0u);
+            umma_bf16(tbase + hcol, kd0 + (((k >> 2) * (NT * 128) + koff) >> 4),
+                      qd0 + (static_cast<uint32_t>((k >> 2) * kQHalf + r0 * 128 + koff) >> 4), idesc_h,
+                      k > 0 ? 1u : 0u);
+          }
+        };
+        auto consts_half = [&](int hcol, int r0) {
+          umma_bf16(tbase + hcol, onesd, sdesc_kmajor_sw32(smem_u32(sC + r0 * 32)), idesc_h, 1u);
+        };
+        const int early = min(ntiles, 4);
+        for (int t = iss; ok && t < ntiles; t += 2) {
+          const int T = ntiles + t;
+          const int s = T % STAGES, u = T / STAGES;
+          const int c = t & 3, uc = t >> 2;
+          if (!mbar_wait(&full_bar[s], u & 1, &s_abort, a.wc)) {
+            ok = false;
+            break;
+          }
+          const uint64_t kd0 = sdesc_kmajor_sw128(smem_u32(sK + s * kKStage));
+          for (int hh = 0; ok && hh < 2; ++hh) {
+            const int ai = 2 * c + hh;
+            if (t < 4) {
+              // columns 128c .. 128c + 127 were pass-1 accumulator c: wait for its last release
+              if (hh == 0 && c < kAcc) {
+                const int last1 = ((ntiles - 1 - c) >= 0) ? ntiles - 1 - ((ntiles - 1 - c) % kAcc) : -1;
+                if (last1 >= 0 && !mbar_wait(&acce1[c], (last1 / kAcc) & 1, &s_abort, a.wc)) ok = false;
+              }
+            } else if (!mbar_wait(&acce2[ai], (uc & 1) ^ 1, &s_abort, a.wc)) {
+              ok = false;
+            }
+            if (!ok) break;
+            tc_fence_after();
+            logits_half(kd0, 128 * c + 64 * hh, hh * Rh);
+            if (t >= early) {
+              consts_half(128 * c + 64 * hh, hh * Rh);
+              umma_commit(&accf2[ai]);
+            }
+          }
+          if (!ok) break;
+          umma_commit(&empty_bar[s]);   // the K stage is free once both halves' logits are done
+          if (t < early && t + 2 >= early) {   // this warp's last tile issued before the constants
+            if (!mbar_wait(&c_bar, 0, &s_abort, a.wc)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            for (int t2 = iss; t2 <= t; t2 += 2)
+              for (int hh = 0; hh < 2; ++hh) {
+                consts_half(128 * (t2 & 3) + 64 * hh, hh * Rh);
+                umma_commit(&accf2[2 * (t2 & 3) + hh]);
+              }
           }
         }
-        umma_commit(&empty_bar[s]);
-        umma_commit(&accf2[acc]);
+      } else {
+        const int early = min(ntiles, kAcc2);
+        for (int t = iss; ok && t < ntiles; t += 2) {
+          const int T = ntiles + t;
+          const int s = T % STAGES, u = T / STAGES;
+          const int acc = t % kAcc2, ua = t / kAcc2;
+          if (!mbar_wait(&full_bar[s], u & 1, &s_abort, a.wc)) {
+            ok = false;
+            break;
+          }
+          if (t < kAcc2) {
+            // first pass-2 use of these columns: pass 1's last use of them is released
+            if (acc < kAcc) {
+              const int last1 = ((ntiles - 1 - acc) >= 0) ? ntiles - 1 - ((ntiles - 1 - acc) % kAcc) : -1;
+              if (last1 >= 0 && !mbar_wait(&acce1[acc], (last1 / kAcc) & 1, &s_abort, a.wc)) {
+                ok = false;
+                break;
+              }
+            }
+          } else if (!mbar_wait(&acce2[acc], (ua & 1) ^ 1, &s_abort, a.wc)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t kd0 = sdesc_kmajor_sw128(smem_u32(sK + s * kKStage));
+          for (int n0 = 0; n0 < R; n0 += 256) {
+            const int nc = min(256, R - n0);
+            const uint32_t idesc = idesc_bf16_f32(128, nc);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              const uint32_t koff = (k & 3) * 32;
+              umma_bf16(tbase + acc * kAccCols + n0, kd0 + (((k >> 2) * (NT * 128) + koff) >> 4),
+                        qd0 + (static_cast<uint32_t>((k >> 2) * kQHalf + n0 * 128 + koff) >> 4), idesc, k > 0 ? 1u : 0u);
+            }
+          }
+          umma_commit(&empty_bar[s]);   // the K stage is free once the logits are done
+          if (t < early && t + 2 >= early) {   // this warp's last tile issued before the constants
+            if (!mbar_wait(&c_bar, 0, &s_abort, a.wc)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            for (int t2 = iss; t2 <= t; t2 += 2) {
+              add_row_consts(t2 % kAcc2);
+              umma_commit(&accf2[t2 % kAcc2]);
+            }
+          } else if (t >= early) {
+            add_row_consts(acc);
+            umma_commit(&accf2[acc]);
+          }
+        }
       }
-      umma_commit(&done_bar);
-      mbar_drain(&done_bar, 0, status);
+      umma_commit(&done_bar[iss]);
+      mbar_drain(&done_bar[iss], 0, status);
     }
   } else {
     // ---------------- epilogue, pass 1: warp (q4, cg) takes keys [32cg, 32cg + 32) of a tile ----------------
@@ -830,75 +964,128 @@ __global__ void __launch_bounds__(kFThreads, 1)
                 z4[i].z * ex2_approx(m4[i].z - mm) + z4[i].w * ex2_approx(m4[i].w - mm);
 #pragma unroll
         for (int o = 1; o < kTpr; o <<= 1) zz += __shfl_xor_sync(0xffffffffu, zz, o);
-        if (part == 0 && r < RP) s_nc2[r] = r < R ? -(mm + lg2_approx(zz)) : 0.f;
+        if (part == 0 && r < R) {
+          // -c2_r / s2 = hi + mid + lo, each part exact in bf16 (about 24 bits in all)
+          const float x = -(mm + lg2_approx(zz)) / s2;
+          const __nv_bfloat16 hi = __float2bfloat16_rn(x);
+          const float x1 = x - __bfloat162float(hi);
+          const __nv_bfloat16 mid = __float2bfloat16_rn(x1);
+          const __nv_bfloat16 lo = __float2bfloat16_rn(x1 - __bfloat162float(mid));
+          const uint32_t w0 = static_cast<uint32_t>(__bfloat16_as_ushort(hi)) |
+                              (static_cast<uint32_t>(__bfloat16_as_ushort(mid)) << 16);
+          const uint32_t w1 = static_cast<uint32_t>(__bfloat16_as_ushort(lo));
+          uint4* row = reinterpret_cast<uint4*>(sC + r * 32);
+          row[0] = make_uint4(w0, w1, 0u, 0u);
+          row[1] = make_uint4(0u, 0u, 0u, 0u);
+          fence_proxy_async_smem();
+        }
       }
       fused_epi_bar();
-      // ---------------- epilogue, pass 2: group g takes tiles g, g+2, ...; halves split the rows ----------------
-      const int grp = cg >> 1, hf = cg & 1;
-      const int Rh = R / 2;   // a multiple of 32
+      if (threadIdx.x == 0) mbar_arrive(&c_bar);   // the MMA warp may add the row constants
+      // ---------------- epilogue, pass 2 ----------------
       const bool is_max = (a.reduce == 2);
       const float row_scale = (a.reduce == 1) ? 1.f / static_cast<float>(R) : 1.f;
       const size_t out_base = static_cast<size_t>(a.rq.soff[b]) + static_cast<size_t>(h) * n;
-      for (int t = grp; t < ntiles; t += 2) {
-        const int acc = t % kAcc2, ua = t / kAcc2;
-        const bool ok = mbar_wait(&accf2[acc], ua & 1, &s_abort, a.wc);
-        if (!group_all(grp, ok)) break;   // the eight warps of the group leave together
-        tc_fence_after();
-        const int key = key_begin + t * NT + q4 * 32 + lane;
-        const int wmin = a.causal ? key - (n - W) : -1;
-        float acc_sum = 0.f, acc_max = -INFINITY;
-        const uint32_t trow = tbase + (static_cast<uint32_t>(q4 * 32) << 16) + acc * kAccCols + hf * Rh;
-#pragma unroll 1
-        for (int c0 = 0; c0 < Rh; c0 += 64) {
-          const int ca = hf * Rh + c0;   // window row of column 0 of this chunk
-          const bool two = c0 + 32 < Rh;
-          float v[64];
-          tmem_ld32(trow + c0, v);
-          if (two) tmem_ld32(trow + c0 + 32, v + 32);
-          tmem_ld_wait();
-          if (!two) {
+      // window rows [ca, ca + 32) of this thread's key, as accumulator values l - c2_r / s2:
+      // the causal tail masked, then exp2(x * s2) summed (or x * s2 maximised)
+      auto rows32 = [&](float* v, int ca, int wmin, float& acc_sum, float& acc_max) {
+        if (wmin > 0) {
+          // causal tail: rows whose window position precedes the key do not see it
+          int w = ca % W;
 #pragma unroll
-            for (int j = 32; j < 64; ++j) v[j] = -INFINITY;
-          }
-          if (wmin > 0) {
-            // causal tail: rows whose window position precedes the key do not see it
-            int w = ca % W;
-#pragma unroll
-            for (int j = 0; j < 64; ++j) {
-              if (w < wmin) v[j] = -INFINITY;
-              w = (w + 1 == W) ? 0 : w + 1;
-            }
-          }
-          if (is_max) {
-#pragma unroll
-            for (int j = 0; j < 64; ++j) v[j] = fmaf(v[j], s2, s_nc2[min(ca + j, R - 1)]);
-            acc_max = fmaxf(acc_max, tree_max<64>(v));
-          } else {
-            // exp2(l * s2 - c2_r): packed FMA with the row constants read as pairs
-            const uint64_t s2p = pack2(s2, s2);
-            uint64_t p2[4] = {0ull, 0ull, 0ull, 0ull};
-#pragma unroll
-            for (int j = 0; j < 64; j += 4) {
-              const float4 cc = *reinterpret_cast<const float4*>(&s_nc2[min(ca + j, RP - 4)]);
-              float x0, x1, x2, x3;
-              unpack2(ffma2(pack2(v[j + 0], v[j + 1]), s2p, pack2(cc.x, cc.y)), x0, x1);
-              unpack2(ffma2(pack2(v[j + 2], v[j + 3]), s2p, pack2(cc.z, cc.w)), x2, x3);
-              p2[(j >> 2) & 3] = fadd2(p2[(j >> 2) & 3], pack2(ex2_approx(x0), ex2_approx(x1)));
-              p2[(j >> 2) & 3] = fadd2(p2[(j >> 2) & 3], pack2(ex2_approx(x2), ex2_approx(x3)));
-            }
-            float q0, q1;
-            unpack2(fadd2(fadd2(p2[0], p2[1]), fadd2(p2[2], p2[3])), q0, q1);
-            acc_sum += q0 + q1;
+          for (int j = 0; j < 32; ++j) {
+            if (w < wmin) v[j] = -INFINITY;
+            w = (w + 1 == W) ? 0 : w + 1;
           }
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&acce2[acc]);
-        if (hf == 1) s_part[grp][q4 * 32 + lane] = is_max ? acc_max : acc_sum;
-        group_bar(grp);
-        if (hf == 0 && key < n) {
-          const float o = s_part[grp][q4 * 32 + lane];
-          a.s_raw[out_base + key] = is_max ? ex2_approx(fmaxf(acc_max, o)) : (acc_sum + o) * row_scale;
+        if (is_max) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] *= s2;
+          acc_max = fmaxf(acc_max, tree_max<32>(v));
+        } else {
+          const uint64_t s2p = pack2(s2, s2);
+          uint64_t p2[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+          for (int j = 0; j < 32; j += 4) {
+            float x0, x1, x2, x3;
+            unpack2(fmul2(pack2(v[j + 0], v[j + 1]), s2p), x0, x1);
+            unpack2(fmul2(pack2(v[j + 2], v[j + 3]), s2p), x2, x3);
+            p2[(j >> 2) & 3] = fadd2(p2[(j >> 2) & 3], pack2(ex2_approx(x0), ex2_approx(x1)));
+            p2[(j >> 2) & 3] = fadd2(p2[(j >> 2) & 3], pack2(ex2_approx(x2), ex2_approx(x3)));
+          }
+          float q0, q1;
+          unpack2(fadd2(fadd2(p2[0], p2[1]), fadd2(p2[2], p2[3])), q0, q1);
+          acc_sum += q0 + q1;
+        }
+      };
+      if constexpr (MT == 1) {
+        // warp (q4, cg) takes tiles cg, cg + 4, ... and sums every window row of its 32 keys
+        // alone: rows [0, R/2) from accumulator half 2cg, then rows [R/2, R) from half
+        // 2cg + 1, releasing each half as soon as it is summed.  The four warps of a lane
+        // quadrant work on different tiles, so their TMEM loads and exponentials
+        // interleave on the SM sub-partition, and no warp waits for another.
+        for (int t = cg; t < ntiles && alive; t += 4) {
+          const int uc = t >> 2;
+          const int key = key_begin + t * NT + q4 * 32 + lane;
+          const int wmin = a.causal ? key - (n - W) : -1;
+          float acc_sum = 0.f, acc_max = -INFINITY;
+          for (int hh = 0; hh < 2; ++hh) {
+            const int ai = 2 * cg + hh;
+            const bool ok = mbar_wait(&accf2[ai], uc & 1, &s_abort, a.wc);
+            if (!__all_sync(0xffffffffu, ok)) {
+              alive = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t trow = tbase + (static_cast<uint32_t>(q4 * 32) << 16) + 128 * cg + 64 * hh;
+            const int Rh = R / 2;   // 32 or 64 rows in this half
+            float va[32], vb[32];
+            tmem_ld32(trow, va);
+            tmem_ld_wait();
+            if (Rh == 64) {
+              tmem_ld32(trow + 32, vb);   // loads while the first 32 rows are summed
+              rows32(va, hh * Rh, wmin, acc_sum, acc_max);
+              tmem_ld_wait();
+              rows32(vb, hh * Rh + 32, wmin, acc_sum, acc_max);
+            } else {
+              rows32(va, hh * Rh, wmin, acc_sum, acc_max);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acce2[ai]);
+          }
+          if (alive && key < n) a.s_raw[out_base + key] = is_max ? ex2_approx(acc_max) : acc_sum * row_scale;
+        }
+      } else {
+        // R > 128: group g (eight warps) takes tiles g, g+2, ...; the two warps of a lane
+        // quadrant split the window rows in halves and add their sums through shared memory
+        const int grp = cg >> 1, hf = cg & 1;
+        const int Rh = R / 2;   // a multiple of 32
+        for (int t = grp; t < ntiles; t += 2) {
+          const int acc = t % kAcc2, ua = t / kAcc2;
+          const bool ok = mbar_wait(&accf2[acc], ua & 1, &s_abort, a.wc);
+          if (!group_all(grp, ok)) break;   // the eight warps of the group leave together
+          tc_fence_after();
+          const int key = key_begin + t * NT + q4 * 32 + lane;
+          const int wmin = a.causal ? key - (n - W) : -1;
+          float acc_sum = 0.f, acc_max = -INFINITY;
+          const uint32_t trow = tbase + (static_cast<uint32_t>(q4 * 32) << 16) + acc * kAccCols + hf * Rh;
+#pragma unroll 1
+          for (int c0 = 0; c0 < Rh; c0 += 32) {
+            float v[32];
+            tmem_ld32(trow + c0, v);
+            tmem_ld_wait();
+            rows32(v, hf * Rh + c0, wmin, acc_sum, acc_max);
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&acce2[acc]);
+          if (hf == 1) s_part[grp][q4 * 32 + lane] = is_max ? acc_max : acc_sum;
+          group_bar(grp);
+          if (hf == 0 && key < n) {
+            const float o = s_part[grp][q4 * 32 + lane];
+            a.s_raw[out_base + key] = is_max ? ex2_approx(fmaxf(acc_max, o)) : (acc_sum + o) * row_scale;
+          }
         }
       }
     }
@@ -943,7 +1130,8 @@ cudaError_t launch_win_fused(const WinScoreArgs& a, const CUtensorMap& tq, const
   const int mt = a.R <= 128 ? 1 : 2;
   const void* fn = mt == 1 ? reinterpret_cast<const void*>(win_fused_kernel<1>)
                            : reinterpret_cast<const void*>(win_fused_kernel<2>);
-  const size_t smem = 1024 + 2 * static_cast<size_t>(mt) * 128 * 128 + (mt == 1 ? 5 : 4) * 128 * 256;
+  const size_t smem = 1024 + 2 * static_cast<size_t>(mt) * 128 * 128 + (mt == 1 ? 5 : 4) * 128 * 256 +
+                      128 * 32 + static_cast<size_t>(mt) * 128 * 32;   // ones and row constants
   cudaError_t e = ensure_smem(fn, smem);
   if (e != cudaSuccess) return e;
   int dev = 0, sms = 0, per_sm = 0;
