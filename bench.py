@@ -812,6 +812,16 @@ def main():
         h2d = sum(t[k].numel() * 2 for t in pin for k in ("q", "k", "v"))
         d2h = sum(t["idx"].numel() * 4 + t["counts"].numel() * 4 for t in pin)
         copy = torch.cuda.Stream()
+        # the host link's own rate: one layer's K copied from pinned memory, best of three
+        link_gbs = 0.0
+        with torch.cuda.stream(copy):
+            for _ in range(3):
+                a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a0.record(copy)
+                k_d[0].copy_(pin[0]["k"], non_blocking=True)
+                a1.record(copy)
+                a1.synchronize()
+                link_gbs = max(link_gbs, pin[0]["k"].numel() * 2 / (a0.elapsed_time(a1) * 1e-3) / 1e9)
         c_done = [torch.cuda.Event() for _ in range(L)]
         x_done = [torch.cuda.Event() for _ in range(L)]
 
@@ -843,8 +853,14 @@ def main():
         torch.cuda.synchronize()
         wall = time.perf_counter() - w0
         ems = max_over_ranks(max(t0.elapsed_time(t1), wall * 1e3), world)
+        link_ms = h2d / (link_gbs * 1e9) * 1e3 if link_gbs > 0 else None
         out["e2e"] = {"value": job_value(K * L * H * n, ems, world), "unit": UNIT, "h2d_bytes_per_step": h2d,
                       "d2h_bytes_per_step": d2h, "ms_per_step": ems / K,
+                      "host_link": {"h2d_gbs": round(link_gbs, 1),
+                                    "ms_per_step_at_link_rate": round(link_ms, 3) if link_ms else None,
+                                    "frac": round(link_ms / (ems / K), 3) if link_ms else None,
+                                    "what": "the step's H2D bytes at the measured pinned-host copy rate, "
+                                            "against the measured e2e step"},
                       "how": "kvsel_run_layer per layer; per-layer H2D of the request's Q/K/V from pinned host on a "
                              "copy stream overlapped with the previous layer's compute (the model's prepared W_h "
                              "stays resident); idx/counts D2H per layer; the compacted K/V and the scores stay on "
