@@ -119,6 +119,23 @@ def test_c2_value_aware_ragged(n):
     _check_layer(wl, inp, gpu, ora)
 
 
+@pytest.mark.parametrize("group,window,value_aware", [
+    (2, 32, True),    # R = 64: the single-launch scoring with 32-row accumulator halves
+    (6, 32, False),   # R = 192: the two-group pass 2 over N = 192
+    (4, 64, True),    # R = 256: the largest window the single-launch scoring takes
+    (8, 32, False),
+])
+def test_window_rows_of_the_single_launch_scoring(group, window, value_aware):
+    """Window-row counts other than the workloads' 128 that the single cooperative scoring
+    launch handles (R a multiple of 64 up to 256), with several tiles per chunk and a
+    ragged last tile (CriticalKV §3.4, Algorithm 2: the observation window's softmax)."""
+    wl = datagen.WORKLOADS[2].replace(layers=1, group=group, window=window, value_aware=value_aware)
+    inp = datagen.make_layer(wl, 11, n_ctx=2085)
+    ora = O.run_workload_layer(wl, inp)
+    gpu = GH.run_gpu_layer(wl, inp)
+    _check_layer(wl, inp, gpu, ora)
+
+
 @pytest.mark.parametrize("n", [1000, 2085])
 def test_c2_value_aware_l2_norm(n):
     """nu = ||W_h v||_2 through the d x d Gram matrix (the other distance of CriticalKV
