@@ -773,7 +773,10 @@ def main():
     small = int(wl.h_kv * wl.group * wl.window * d * 2) + 2 * H * n * 4
     # ---- the plain-score path on the same layers (spec HBM target)
     if not args.no_plain:
-        pms = time_variant(B.params_from_workload(wl, value_aware=False))
+        # with several layers in flight, the plain layers are sized for half the SMs, so
+        # that two layers' scoring launches run side by side (kvsel_params.sm_budget)
+        sm_plain = torch.cuda.get_device_properties(dev).multi_processor_count // 2 if S > 1 else 0
+        pms = time_variant(B.params_from_workload(wl, value_aware=False, sm_budget=sm_plain))
         alg = H * n * d * 2 + kept_rw + small
         gbs = alg / (pms * 1e-3) / 1e9
         R = wl.group * wl.window
@@ -781,7 +784,7 @@ def main():
                                      "peak_gbs": pk.get("hbm_gbs"), "us_per_layer": pms * 1e3,
                                      "what": "plain C2 layer (score+select+compact), algorithmic bytes / time"}
         out["hbm_path"] = {"what": "same layers, value_aware=0 (score+select+compact, no W_O pass)",
-                           "ms_per_layer": pms, "entries_per_s": H * n / (pms * 1e-3) * world,
+                           "layer_streams": S, "sm_budget": sm_plain, "ms_per_layer": pms, "entries_per_s": H * n / (pms * 1e-3) * world,
                            "algorithmic_bytes_per_layer": alg, "achieved_gbs": gbs,
                            "peak_gbs": pk.get("hbm_gbs"), "frac": gbs / pk.get("hbm_gbs", 6800.0),
                            # two scoring passes: 2*R*d flop and R exponentials per key and pass

@@ -125,6 +125,12 @@ typedef struct kvsel_params {
                            (2e9, about 1 s at the boost clock).  A wait that runs out ends
                            its kernel with KVSEL_ETIMEOUT in the device status word; 1
                            makes every wait that is not already satisfied give up at once */
+  int32_t sm_budget;    /* SMs the call sizes its one-CTA-per-SM kernels for (the
+                           cooperative scoring launch, the value-norm GEMM): 0 = every SM
+                           of the device.  A smaller budget leaves SMs to calls running
+                           at the same time on other streams (independent layers), so
+                           that, e.g., two layers' scoring kernels run side by side; the
+                           results do not depend on it beyond fp32 rounding order       */
 } kvsel_params;
 
 /* K/V cache view, contiguous or paged (block_size tokens per block). */

@@ -124,6 +124,7 @@ struct VnormArgs {
   int unit_base[kMaxBatch + 1];   // first unit of request b
   int blocks_per_head[kMaxBatch]; // token blocks per head of request b
   float* nu;                      // packed [sum_b H*n_b]
+  int grid_cap;                   // CTAs at most (the call's SM budget); 0 = every SM
   WaitCtl wc;
 };
 

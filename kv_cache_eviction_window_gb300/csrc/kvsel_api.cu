@@ -115,6 +115,7 @@ int make_plan(const kvsel_params* p, Plan& pl, bool need_device) {
     return KVSEL_EINVAL;
   pl.anchor = p->budget_mode == KVSEL_BUDGET_ANCHOR;
   pl.wait_limit = p->wait_cycles ? p->wait_cycles : kDefaultWaitCycles;
+  if (p->sm_budget < 0) return KVSEL_EINVAL;
   if (pl.anchor && !(p->alpha >= 0.f && p->alpha <= 1.f)) return KVSEL_EINVAL;
   if (!(p->budget_ratio >= 0.0 && p->budget_ratio <= 1.0) || !(p->floor_ratio >= 0.0 && p->floor_ratio <= 1.0))
     return KVSEL_EINVAL;
@@ -215,6 +216,7 @@ int make_plan(const kvsel_params* p, Plan& pl, bool need_device) {
   if (!need_device) return KVSEL_OK;
   int rc = device_sms(&pl.num_sms);
   if (rc) return rc;
+  if (p->sm_budget > 0 && p->sm_budget < pl.num_sms) pl.num_sms = p->sm_budget;
 
   // key chunks: about one chunk per SM over all (request, head) pairs
   long long t256 = 0;
@@ -584,6 +586,7 @@ int do_score(const kvsel_params* p, const Plan& pl, const void* q, const kvsel_k
     for (int b = 0; b <= pl.B; ++b) v.unit_base[b] = pl.unit_base[b];
     for (int b = 0; b < pl.B; ++b) v.blocks_per_head[b] = pl.blocks_per_head[b];
     v.nu = nu;
+    v.grid_cap = pl.num_sms;
     v.wc = wait_ctl(pl, ws);
     {
       StageScope sc(KVSEL_STAGE_VNORM, st);
@@ -851,6 +854,7 @@ int kvsel_perturbation(const kvsel_params* p, const void* q, const kvsel_kv* kv,
   v.units_total = pl.unit_base[pl.B];
   for (int b = 0; b <= pl.B; ++b) v.unit_base[b] = pl.unit_base[b];
   for (int b = 0; b < pl.B; ++b) v.blocks_per_head[b] = pl.blocks_per_head[b];
+  v.grid_cap = pl.num_sms;
   v.wc = wait_ctl(pl, ws);
   for (int g = 0; g < pl.G; ++g) {
     float* nu_g = reinterpret_cast<float*>(wsb + L.nu) + static_cast<size_t>(g) * pl.n_scores;

@@ -394,6 +394,7 @@ cudaError_t launch_vnorm(const VnormArgs& a, const CUtensorMap& tw, cudaStream_t
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (a.grid_cap > 0 && a.grid_cap < sms) sms = a.grid_cap;
   const int grid = a.units_total < sms ? a.units_total : sms;
   vnorm_kernel<<<grid, kThreads, smem, st>>>(tw, a);
   note_launch();

@@ -48,9 +48,10 @@ def test_struct_layout_matches_header(B):
     import subprocess
     import tempfile
 
-    src = '#include <stdio.h>\n#include <stddef.h>\n#include "kvsel.h"\nint main(){printf("%zu %zu %zu %zu %zu\\n",' \
+    src = '#include <stdio.h>\n#include <stddef.h>\n#include "kvsel.h"\nint main(){printf("%zu %zu %zu %zu %zu %zu\\n",' \
           'sizeof(kvsel_params), sizeof(kvsel_kv), offsetof(kvsel_params, budget_ratio),' \
-          'offsetof(kvsel_kv, block_table), offsetof(kvsel_params, wait_cycles));return 0;}\n'
+          'offsetof(kvsel_kv, block_table), offsetof(kvsel_params, wait_cycles),' \
+          'offsetof(kvsel_params, sm_budget));return 0;}\n'
     with tempfile.TemporaryDirectory() as d:
         c = os.path.join(d, "s.c")
         open(c, "w").write(src)
@@ -58,7 +59,7 @@ def test_struct_layout_matches_header(B):
         subprocess.check_call(["gcc", "-I", os.path.join(ROOT, "include"), c, "-o", exe])
         out = subprocess.check_output([exe]).decode().split()
     want = [ctypes.sizeof(B.kvsel_params), ctypes.sizeof(B.kvsel_kv), B.kvsel_params.budget_ratio.offset,
-            B.kvsel_kv.block_table.offset, B.kvsel_params.wait_cycles.offset]
+            B.kvsel_kv.block_table.offset, B.kvsel_params.wait_cycles.offset, B.kvsel_params.sm_budget.offset]
     assert [int(x) for x in out] == want
 
 
@@ -96,6 +97,7 @@ def _p(B, **kw):
     (dict(window=0, causal=False, reduce="max", value_aware=True, d_model=4096), -3),
     (dict(group=3, window=10), -3),             # 30 window rows: not a multiple of 32
     (dict(window=8192), -1),                    # window longer than the context
+    (dict(sm_budget=-1), -1),                   # a negative SM budget
     (dict(value_aware=True, d_model=4096, budget_mode="anchor"), -3),
     (dict(value_aware=True, d_model=100), -3),
     (dict(value_aware=True, d_model=4096, value_norm="l2", wo_mode="per_head"), -3),   # Gram needs one W_h

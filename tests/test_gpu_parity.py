@@ -136,6 +136,18 @@ def test_window_rows_of_the_single_launch_scoring(group, window, value_aware):
     _check_layer(wl, inp, gpu, ora)
 
 
+@pytest.mark.parametrize("budget,value_aware", [(40, True), (76, False), (200, True)])
+def test_sm_budget_sizes_the_kernels_not_the_result(budget, value_aware):
+    """kvsel_params.sm_budget only changes how many CTAs the one-per-SM kernels use (key
+    chunks of the scoring launch, value-norm CTAs): the layer still matches the oracle.
+    A budget above the device's SM count means every SM."""
+    wl = datagen.WORKLOADS[2].replace(layers=1, value_aware=value_aware)
+    inp = datagen.make_layer(wl, 5, n_ctx=5000)
+    ora = O.run_workload_layer(wl, inp)
+    gpu = GH.run_gpu_layer(wl, inp, sm_budget=budget)
+    _check_layer(wl, inp, gpu, ora)
+
+
 @pytest.mark.parametrize("n", [1000, 2085])
 def test_c2_value_aware_l2_norm(n):
     """nu = ||W_h v||_2 through the d x d Gram matrix (the other distance of CriticalKV
