@@ -541,26 +541,29 @@ def main():
     w_d = [to_dev(x["w_o"]) for x in host]
     # W_h depends on the model's weights alone: built once per layer at load time
     # (kvsel_prepare_w_o), outside the timed step, like any weight preprocessing
-    params = B.params_from_workload(wl, w_o_prepared=True)
-    params_raw = B.params_from_workload(wl)
+    # the stack's layers are independent: the timed graphs issue them round-robin over
+    # S streams, each with its own workspace, so that one layer's latency-bound selection
+    # runs beside other layers' scoring and compaction.  Overlapping calls set
+    # concurrent = 1 (no cooperative launch that could wait for SMs another call holds).
+    S = max(1, min(args.streams, L))
+    conc = S > 1
+    params = B.params_from_workload(wl, w_o_prepared=True, concurrent=conc)
+    params_raw = B.params_from_workload(wl, concurrent=conc)
     bufs = [B.LayerBuffers(params, device=dev) for _ in range(L)]
     # one workspace for every variant timed below (the L2 path needs Gram scratch too)
     ws_bytes = max(B.kvsel_workspace_size(x) for x in
-                   (params, B.params_from_workload(wl, value_aware=False), B.params_from_workload(wl, value_norm="l2")))
+                   (params, B.params_from_workload(wl, value_aware=False, concurrent=conc),
+                    B.params_from_workload(wl, value_norm="l2", concurrent=conc)))
     ws_bytes = max(ws_bytes, B.kvsel_workspace_size(params_raw))
     ws = torch.empty(ws_bytes // 4 + 64, dtype=torch.int32, device=dev)
     B.kvsel_workspace_init(ws)
-    # the stack's layers are independent: the timed graphs issue them round-robin over
-    # S streams, each with its own workspace, so that one layer's latency-bound selection
-    # runs beside other layers' scoring and compaction
-    S = max(1, min(args.streams, L))
     ws_s = [ws] + [torch.empty(ws_bytes // 4 + 64, dtype=torch.int32, device=dev) for _ in range(S - 1)]
     for x in ws_s[1:]:
         B.kvsel_workspace_init(x)
     kvs = [B.make_kv_contiguous(k_d[i], v_d[i]) for i in range(L)]
     stream = torch.cuda.current_stream()
     # the prepared value-norm weights of every layer (L1: W_h; L2: its Gram matrix)
-    p_l2 = B.params_from_workload(wl, value_norm="l2", w_o_prepared=True)
+    p_l2 = B.params_from_workload(wl, value_norm="l2", w_o_prepared=True, concurrent=conc)
     wp_d = [torch.empty(B.kvsel_prepared_w_o_size(params) // 2 + 128, dtype=torch.int16, device=dev) for _ in range(L)]
     wp2_d = [torch.empty(B.kvsel_prepared_w_o_size(p_l2) // 2 + 128, dtype=torch.int16, device=dev) for _ in range(L)]
     pe0, pe1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -776,7 +779,7 @@ def main():
         # with several layers in flight, the plain layers are sized for half the SMs, so
         # that two layers' scoring launches run side by side (kvsel_params.sm_budget)
         sm_plain = torch.cuda.get_device_properties(dev).multi_processor_count // 2 if S > 1 else 0
-        pms = time_variant(B.params_from_workload(wl, value_aware=False, sm_budget=sm_plain))
+        pms = time_variant(B.params_from_workload(wl, value_aware=False, sm_budget=sm_plain, concurrent=conc))
         alg = H * n * d * 2 + kept_rw + small
         gbs = alg / (pms * 1e-3) / 1e9
         R = wl.group * wl.window

@@ -125,12 +125,22 @@ typedef struct kvsel_params {
                            (2e9, about 1 s at the boost clock).  A wait that runs out ends
                            its kernel with KVSEL_ETIMEOUT in the device status word; 1
                            makes every wait that is not already satisfied give up at once */
-  int32_t sm_budget;    /* SMs the call sizes its one-CTA-per-SM kernels for (the
-                           cooperative scoring launch, the value-norm GEMM): 0 = every SM
-                           of the device.  A smaller budget leaves SMs to calls running
-                           at the same time on other streams (independent layers), so
-                           that, e.g., two layers' scoring kernels run side by side; the
-                           results do not depend on it beyond fp32 rounding order       */
+  int32_t sm_budget;    /* SMs the call sizes its one-CTA-per-SM kernels for (the key
+                           chunks of the scoring pass, the value-norm GEMM): 0 = every
+                           SM of the device.  A smaller budget leaves SMs to calls
+                           running at the same time on other streams (independent
+                           layers), so that, e.g., two layers' scoring kernels run side
+                           by side; the results do not depend on it beyond fp32 rounding
+                           order                                                         */
+  int32_t concurrent;   /* 1: other work may run on the device at the same time (calls
+                           on other streams).  The call then uses only kernels that make
+                           progress whatever else is resident: the two scoring passes run
+                           as two launches.  0: when R <= 256 they run as one cooperative
+                           launch whose CTAs wait for each other at a per-head barrier,
+                           which needs every key chunk's CTA resident at once; two such
+                           calls running at the same time can each hold SMs the other
+                           waits for, until their bounded waits end them with
+                           KVSEL_ETIMEOUT.  Set 1 whenever calls overlap                 */
 } kvsel_params;
 
 /* K/V cache view, contiguous or paged (block_size tokens per block). */

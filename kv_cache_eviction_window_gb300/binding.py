@@ -63,6 +63,7 @@ class kvsel_params(ctypes.Structure):
         ("floor_ratio", ctypes.c_double), ("batch", ctypes.c_int32),
         ("n_ctx_per_req", ctypes.POINTER(ctypes.c_int32)), ("value_norm", ctypes.c_int32),
         ("w_o_prepared", ctypes.c_int32), ("wait_cycles", ctypes.c_uint64), ("sm_budget", ctypes.c_int32),
+        ("concurrent", ctypes.c_int32),
     ]
 
 
@@ -134,7 +135,8 @@ def make_params(*, h_kv: int, group: int, n_ctx: int, window: int, head_dim: int
                 alpha: float = 0.5, n_sink: int = 4, n_recent: int = 32,
                 budget_mode: str = "head", budget_ratio: float = 0.2, floor_ratio: float = 0.0,
                 n_ctx_per_req: Optional[Sequence[int]] = None, value_norm: str = "l1",
-                wait_cycles: int = 0, w_o_prepared: bool = False, sm_budget: int = 0) -> kvsel_params:
+                wait_cycles: int = 0, w_o_prepared: bool = False, sm_budget: int = 0,
+                concurrent: bool = False) -> kvsel_params:
     p = kvsel_params()
     p.h_kv, p.group, p.head_dim, p.d_model = h_kv, group, head_dim, d_model
     p.n_ctx, p.window, p.q_chunk, p.causal = n_ctx, window, q_chunk, int(bool(causal))
@@ -146,6 +148,7 @@ def make_params(*, h_kv: int, group: int, n_ctx: int, window: int, head_dim: int
     p.value_norm = VALUE_NORM[value_norm]
     p.wait_cycles = int(wait_cycles)
     p.sm_budget = int(sm_budget)
+    p.concurrent = int(bool(concurrent))
     p.w_o_prepared = int(bool(w_o_prepared))
     if n_ctx_per_req is not None:
         arr = (ctypes.c_int32 * len(n_ctx_per_req))(*[int(x) for x in n_ctx_per_req])

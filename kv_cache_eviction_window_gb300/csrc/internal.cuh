@@ -137,6 +137,7 @@ struct VgramArgs {
   int unit_base[kMaxBatch + 1];
   int blocks_per_head[kMaxBatch];
   float* nu;                      // packed [sum_b H*n_b]
+  int grid_cap;                   // CTAs at most (the call's SM budget); 0 = every SM
   WaitCtl wc;
 };
 // Row slices of the Gram partials (workspace: H * slices * 128 * 128 fp32).

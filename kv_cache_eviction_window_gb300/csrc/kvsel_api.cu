@@ -115,7 +115,7 @@ int make_plan(const kvsel_params* p, Plan& pl, bool need_device) {
     return KVSEL_EINVAL;
   pl.anchor = p->budget_mode == KVSEL_BUDGET_ANCHOR;
   pl.wait_limit = p->wait_cycles ? p->wait_cycles : kDefaultWaitCycles;
-  if (p->sm_budget < 0) return KVSEL_EINVAL;
+  if (p->sm_budget < 0 || p->concurrent < 0 || p->concurrent > 1) return KVSEL_EINVAL;
   if (pl.anchor && !(p->alpha >= 0.f && p->alpha <= 1.f)) return KVSEL_EINVAL;
   if (!(p->budget_ratio >= 0.0 && p->budget_ratio <= 1.0) || !(p->floor_ratio >= 0.0 && p->floor_ratio <= 1.0))
     return KVSEL_EINVAL;
@@ -495,8 +495,9 @@ int do_score(const kvsel_params* p, const Plan& pl, const void* q, const kvsel_k
   a.wc = wait_ctl(pl, ws);
   int rc;
   cudaError_t fe = cudaErrorNotSupported;
-  if (pl.mt <= 2) {
+  if (pl.mt <= 2 && !p->concurrent) {
     // both passes in one cooperative launch when every chunk fits on the device at once
+    // (not when other work may hold SMs: the launch's CTAs wait for each other)
     StageScope sc(KVSEL_STAGE_ROWSTATS, st);
     fe = launch_win_fused(a, tq, tk2, reinterpret_cast<unsigned int*>(wsb + kStatusBytes), st);
     if (fe != cudaSuccess && fe != cudaErrorNotSupported) return KVSEL_ECUDA;
@@ -548,6 +549,7 @@ int do_score(const kvsel_params* p, const Plan& pl, const void* q, const kvsel_k
     for (int b = 0; b <= pl.B; ++b) v.unit_base[b] = pl.g_unit_base[b];
     for (int b = 0; b < pl.B; ++b) v.blocks_per_head[b] = pl.g_blocks_per_head[b];
     v.nu = nu;
+    v.grid_cap = pl.num_sms;
     v.wc = wait_ctl(pl, ws);
     {
       StageScope sc(KVSEL_STAGE_VNORM, st);

@@ -432,6 +432,7 @@ cudaError_t launch_vgram(const VgramArgs& a, const CUtensorMap& tv, const CUtens
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (a.grid_cap > 0 && a.grid_cap < sms) sms = a.grid_cap;
   const int grid = a.units_total < sms ? a.units_total : sms;
   vgram_kernel<<<grid, kVgThreads, smem, st>>>(tv, tg, a);
   note_launch();

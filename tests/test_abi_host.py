@@ -48,10 +48,10 @@ def test_struct_layout_matches_header(B):
     import subprocess
     import tempfile
 
-    src = '#include <stdio.h>\n#include <stddef.h>\n#include "kvsel.h"\nint main(){printf("%zu %zu %zu %zu %zu %zu\\n",' \
+    src = '#include <stdio.h>\n#include <stddef.h>\n#include "kvsel.h"\nint main(){printf("%zu %zu %zu %zu %zu %zu %zu\\n",' \
           'sizeof(kvsel_params), sizeof(kvsel_kv), offsetof(kvsel_params, budget_ratio),' \
           'offsetof(kvsel_kv, block_table), offsetof(kvsel_params, wait_cycles),' \
-          'offsetof(kvsel_params, sm_budget));return 0;}\n'
+          'offsetof(kvsel_params, sm_budget), offsetof(kvsel_params, concurrent));return 0;}\n'
     with tempfile.TemporaryDirectory() as d:
         c = os.path.join(d, "s.c")
         open(c, "w").write(src)
@@ -59,7 +59,8 @@ def test_struct_layout_matches_header(B):
         subprocess.check_call(["gcc", "-I", os.path.join(ROOT, "include"), c, "-o", exe])
         out = subprocess.check_output([exe]).decode().split()
     want = [ctypes.sizeof(B.kvsel_params), ctypes.sizeof(B.kvsel_kv), B.kvsel_params.budget_ratio.offset,
-            B.kvsel_kv.block_table.offset, B.kvsel_params.wait_cycles.offset, B.kvsel_params.sm_budget.offset]
+            B.kvsel_kv.block_table.offset, B.kvsel_params.wait_cycles.offset, B.kvsel_params.sm_budget.offset,
+            B.kvsel_params.concurrent.offset]
     assert [int(x) for x in out] == want
 
 
