@@ -213,9 +213,6 @@ cudaError_t launch_win_rowstats(const WinScoreArgs& a, const CUtensorMap& tq, co
 cudaError_t launch_win_keysum(const WinScoreArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, cudaStream_t st);
 cudaError_t launch_win_fused(const WinScoreArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
                              unsigned int* grid_count, cudaStream_t st);
-// The two passes as two ordinary launches (for calls that may share the device).
-cudaError_t launch_win_two_pass(const WinScoreArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
-                                cudaStream_t st);
 
 
 // Also zeroes nu[0, nu_count), which launch_vnorm (next on the stream) accumulates into.

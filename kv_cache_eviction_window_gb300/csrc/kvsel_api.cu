@@ -503,12 +503,6 @@ int do_score(const kvsel_params* p, const Plan& pl, const void* q, const kvsel_k
     if (fe != cudaSuccess && fe != cudaErrorNotSupported) return KVSEL_ECUDA;
   }
   if (fe == cudaSuccess) StageScope sc(KVSEL_STAGE_KEYSUM, st);   // pass 2 ran inside the fused launch
-  if (fe == cudaErrorNotSupported && p->concurrent && pl.mt <= 2) {
-    // the same kernels as the fused launch, one pass per launch (no grid barrier)
-    StageScope sc(KVSEL_STAGE_ROWSTATS, st);
-    fe = launch_win_two_pass(a, tq, tk2, st);
-    if (fe != cudaSuccess && fe != cudaErrorNotSupported) return KVSEL_ECUDA;
-  }
   if (fe == cudaErrorNotSupported) {
     {
       StageScope sc(KVSEL_STAGE_ROWSTATS, st);

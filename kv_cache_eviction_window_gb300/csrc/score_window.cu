@@ -578,14 +578,10 @@ __device__ __forceinline__ bool group_all(int grp, bool pred) {
 }
 __device__ __forceinline__ void group_bar(int grp) { asm volatile("bar.sync %0, 256;" ::"r"(4 + grp) : "memory"); }
 
-// PH selects the passes: 0 both (cooperative launch, per-head grid barrier between
-// them), 1 pass 1 only (writes the chunk partials), 2 pass 2 only (reads them).  The
-// one-pass variants wait for no other CTA, so they may share the device with other work.
-template <int MT, int PH>
+template <int MT>
 __global__ void __launch_bounds__(kFThreads, 1)
     win_fused_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                      const WinScoreArgs a, unsigned int* grid_count) {
-  constexpr bool kP1 = (PH != 2), kP2 = (PH != 1);
   constexpr int NT = 128, STAGES = (MT == 1) ? 5 : 4, kAcc = 2;
   // pass-2 accumulators: R <= 128 uses eight half-tile accumulators (N = R/2, columns
   // 128c and 128c + 64 for tile class c = t % 4); R > 128 uses two of N = R
@@ -652,7 +648,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = s_tmem;
-  if (kP1 && a.nu_zero != nullptr && warp < kFEpiWarps) {   // this chunk's value norms start from zero
+  if (a.nu_zero != nullptr && warp < kFEpiWarps) {   // this chunk's value norms start from zero
     float* z = a.nu_zero + static_cast<size_t>(a.rq.soff[b]) + static_cast<size_t>(h) * n;
     for (int k = key_begin + static_cast<int>(threadIdx.x); k < key_end; k += kFEpiWarps * 32) z[k] = 0.f;
   }
@@ -663,15 +659,12 @@ __global__ void __launch_bounds__(kFThreads, 1)
       tma_prefetch_desc(&tk);
       mbar_arrive_expect_tx(&q_bar, R * 256);
       load_q_rows(&tq, (b * a.rq.H + h) * R, R, kQHalf, sQ, &q_bar);
-      // pass 1 tiles, then the same tiles again for pass 2 (ring positions count from 0
-      // for whichever passes this launch runs)
-      const int T1 = kP1 ? ntiles : 0, Tend = T1 + (kP2 ? ntiles : 0);
       int T = 0;
-      for (; T < Tend; ++T) {
+      for (; T < 2 * ntiles; ++T) {   // pass 1 tiles, then the same tiles again for pass 2
         const int s = T % STAGES, u = T / STAGES;
         if (!mbar_wait(&empty_bar[s], (u & 1) ^ 1, &s_abort, a.wc)) break;
         mbar_arrive_expect_tx(&full_bar[s], kKStage);
-        const int t = T < T1 ? T : T - T1;
+        const int t = T < ntiles ? T : T - ntiles;
         load_kv_tile(&tk, a.src, b, h, n, key_begin + t * NT, NT, sK + s * kKStage, &full_bar[s], status);
       }
       for (int tt = max(0, T - STAGES); tt < T; ++tt) mbar_drain(&full_bar[tt % STAGES], (tt / STAGES) & 1, status);
@@ -684,8 +677,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
       const uint64_t qd0 = sdesc_kmajor_sw128(smem_u32(sQ));
       // pass 1: A = window rows, B = keys (accumulator t % 2 = iss)
       constexpr uint32_t idesc1 = idesc_bf16_f32(128, NT);
-      const int T1 = kP1 ? ntiles : 0;   // ring position of pass-2 tile 0
-      for (int t = iss; kP1 && ok && t < ntiles; t += 2) {
+      for (int t = iss; ok && t < ntiles; t += 2) {
         const int s = t % STAGES, u = t / STAGES;
         const int acc = t % kAcc, ua = t / kAcc;
         if (!mbar_wait(&full_bar[s], u & 1, &s_abort, a.wc) ||
@@ -739,8 +731,8 @@ __global__ void __launch_bounds__(kFThreads, 1)
           umma_bf16(tbase + hcol, onesd, sdesc_kmajor_sw32(smem_u32(sC + r0 * 32)), idesc_h, 1u);
         };
         const int early = min(ntiles, 4);
-        for (int t = iss; kP2 && ok && t < ntiles; t += 2) {
-          const int T = T1 + t;
+        for (int t = iss; ok && t < ntiles; t += 2) {
+          const int T = ntiles + t;
           const int s = T % STAGES, u = T / STAGES;
           const int c = t & 3, uc = t >> 2;
           if (!mbar_wait(&full_bar[s], u & 1, &s_abort, a.wc)) {
@@ -752,7 +744,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
             const int ai = 2 * c + hh;
             if (t < 4) {
               // columns 128c .. 128c + 127 were pass-1 accumulator c: wait for its last release
-              if (kP1 && hh == 0 && c < kAcc) {
+              if (hh == 0 && c < kAcc) {
                 const int last1 = ((ntiles - 1 - c) >= 0) ? ntiles - 1 - ((ntiles - 1 - c) % kAcc) : -1;
                 if (last1 >= 0 && !mbar_wait(&acce1[c], (last1 / kAcc) & 1, &s_abort, a.wc)) ok = false;
               }
@@ -784,8 +776,8 @@ __global__ void __launch_bounds__(kFThreads, 1)
         }
       } else {
         const int early = min(ntiles, kAcc2);
-        for (int t = iss; kP2 && ok && t < ntiles; t += 2) {
-          const int T = T1 + t;
+        for (int t = iss; ok && t < ntiles; t += 2) {
+          const int T = ntiles + t;
           const int s = T % STAGES, u = T / STAGES;
           const int acc = t % kAcc2, ua = t / kAcc2;
           if (!mbar_wait(&full_bar[s], u & 1, &s_abort, a.wc)) {
@@ -794,7 +786,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
           }
           if (t < kAcc2) {
             // first pass-2 use of these columns: pass 1's last use of them is released
-            if (kP1 && acc < kAcc) {
+            if (acc < kAcc) {
               const int last1 = ((ntiles - 1 - acc) >= 0) ? ntiles - 1 - ((ntiles - 1 - acc) % kAcc) : -1;
               if (last1 >= 0 && !mbar_wait(&acce1[acc], (last1 / kAcc) & 1, &s_abort, a.wc)) {
                 ok = false;
@@ -843,17 +835,13 @@ __global__ void __launch_bounds__(kFThreads, 1)
     const float s2 = a.s2;
     const int W = a.W;
     const int lim_all = a.causal ? (n - W + 1) : n;
-    bool alive = true;
-    const int nch = a.ck.per_head[b], ncp = chunk_pad(nch);
-    float* pm = a.part + (static_cast<size_t>(a.ck.pbase[b]) + static_cast<size_t>(h) * ncp) * 2 * RP;
-    float* pz = pm + static_cast<size_t>(RP) * ncp;
-    if constexpr (kP1) {
     float m[MT], z[MT];
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt) {
       m[mt] = kNegBig;
       z[mt] = 0.f;
     }
+    bool alive = true;
     for (int t = 0; t < ntiles; ++t) {
       const int acc = t % kAcc, ua = t / kAcc;
       bool ok = mbar_wait(&accf1[acc], ua & 1, &s_abort, a.wc);
@@ -893,6 +881,9 @@ __global__ void __launch_bounds__(kFThreads, 1)
       s_xz[mt][cg][q4 * 32 + lane] = z[mt];
     }
     fused_epi_bar();
+    const int nch = a.ck.per_head[b], ncp = chunk_pad(nch);
+    float* pm = a.part + (static_cast<size_t>(a.ck.pbase[b]) + static_cast<size_t>(h) * ncp) * 2 * RP;
+    float* pz = pm + static_cast<size_t>(RP) * ncp;
     if (cg == 0) {
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt) {
@@ -914,9 +905,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
         }
       }
     }
-    }   // pass 1
     // ---------------- grid barrier: every chunk's partials are in memory ----------------
-    if constexpr (PH == 0) {
     fused_epi_bar();
     if (threadIdx.x == 0) {
       // only the chunks of this (request, head) are needed: an arrival and a departure
@@ -944,9 +933,8 @@ __global__ void __launch_bounds__(kFThreads, 1)
         atomicExch(depart, 0u);
       }
     }
-    }   // grid barrier
-    if (kP2 && fused_epi_any(!alive || *reinterpret_cast<volatile int*>(&s_abort) != 0)) alive = false;
-    if (kP2 && alive) {
+    if (fused_epi_any(!alive || *reinterpret_cast<volatile int*>(&s_abort) != 0)) alive = false;
+    if (alive) {
       // merged row statistics c2[r] = m_r + log2 Z_r (log2 units): kTpr threads per row
       // split its chunk partials (float4 groups, all loads issued first), then combine
       {
@@ -1133,16 +1121,25 @@ cudaError_t launch_win_rowstats(const WinScoreArgs& a, const CUtensorMap& tq, co
   }
 }
 
-namespace {
-
-template <int MT, int PH>
-cudaError_t launch_fused_t(const WinScoreArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
-                           unsigned int* grid_count, cudaStream_t st) {
-  const void* fn = reinterpret_cast<const void*>(win_fused_kernel<MT, PH>);
-  const size_t smem = 1024 + 2 * static_cast<size_t>(MT) * 128 * 128 + (MT == 1 ? 5 : 4) * 128 * 256 +
-                      128 * 32 + static_cast<size_t>(MT) * 128 * 32;   // ones and row constants
+// One cooperative launch for both passes when every chunk's CTA fits on the device at
+// once (R <= 256, one CTA per SM); returns cudaErrorNotSupported otherwise.
+cudaError_t launch_win_fused(const WinScoreArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
+                             unsigned int* grid_count, cudaStream_t st) {
+  if (a.ck.total <= 0) return cudaSuccess;
+  if (a.R > 256 || a.R_pad != a.R || a.R % 64 != 0) return cudaErrorNotSupported;   // 32-row halves
+  const int mt = a.R <= 128 ? 1 : 2;
+  const void* fn = mt == 1 ? reinterpret_cast<const void*>(win_fused_kernel<1>)
+                           : reinterpret_cast<const void*>(win_fused_kernel<2>);
+  const size_t smem = 1024 + 2 * static_cast<size_t>(mt) * 128 * 128 + (mt == 1 ? 5 : 4) * 128 * 256 +
+                      128 * 32 + static_cast<size_t>(mt) * 128 * 32;   // ones and row constants
   cudaError_t e = ensure_smem(fn, smem);
   if (e != cudaSuccess) return e;
+  int dev = 0, sms = 0, per_sm = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kFThreads, smem);
+  if (e != cudaSuccess) return e;
+  if (per_sm < 1 || a.ck.total > per_sm * sms) return cudaErrorNotSupported;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.ck.total, 1, 1);
   cfg.blockDim = dim3(kFThreads, 1, 1);
@@ -1152,42 +1149,11 @@ cudaError_t launch_fused_t(const WinScoreArgs& a, const CUtensorMap& tq, const C
   attr[0].id = cudaLaunchAttributeCooperative;
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 0;
-  if (PH == 0) {
-    // every chunk's CTA must be resident at once for the grid barrier
-    int dev = 0, sms = 0, per_sm = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kFThreads, smem);
-    if (e != cudaSuccess) return e;
-    if (per_sm < 1 || a.ck.total > per_sm * sms) return cudaErrorNotSupported;
-    cfg.numAttrs = 1;
-  }
-  e = cudaLaunchKernelEx(&cfg, win_fused_kernel<MT, PH>, tq, tk, a, grid_count);
+  cfg.numAttrs = 1;
+  e = mt == 1 ? cudaLaunchKernelEx(&cfg, win_fused_kernel<1>, tq, tk, a, grid_count)
+              : cudaLaunchKernelEx(&cfg, win_fused_kernel<2>, tq, tk, a, grid_count);
   if (e == cudaSuccess) note_launch();
   return e;
-}
-
-}  // namespace
-
-// One cooperative launch for both passes when every chunk's CTA fits on the device at
-// once (R <= 256, one CTA per SM); returns cudaErrorNotSupported otherwise.
-cudaError_t launch_win_fused(const WinScoreArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
-                             unsigned int* grid_count, cudaStream_t st) {
-  if (a.ck.total <= 0) return cudaSuccess;
-  if (a.R > 256 || a.R_pad != a.R || a.R % 64 != 0) return cudaErrorNotSupported;   // 32-row halves
-  return a.R <= 128 ? launch_fused_t<1, 0>(a, tq, tk, grid_count, st) : launch_fused_t<2, 0>(a, tq, tk, grid_count, st);
-}
-
-// The same two passes as two ordinary launches (pass 1, then pass 2 reading the chunk
-// partials), for calls that may share the device: no CTA waits for another.
-cudaError_t launch_win_two_pass(const WinScoreArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
-                                cudaStream_t st) {
-  if (a.ck.total <= 0) return cudaSuccess;
-  if (a.R > 256 || a.R_pad != a.R || a.R % 64 != 0) return cudaErrorNotSupported;
-  cudaError_t e = a.R <= 128 ? launch_fused_t<1, 1>(a, tq, tk, nullptr, st) : launch_fused_t<2, 1>(a, tq, tk, nullptr, st);
-  if (e != cudaSuccess) return e;
-  return a.R <= 128 ? launch_fused_t<1, 2>(a, tq, tk, nullptr, st) : launch_fused_t<2, 2>(a, tq, tk, nullptr, st);
 }
 
 cudaError_t launch_win_keysum(const WinScoreArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, cudaStream_t st) {
