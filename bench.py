@@ -769,6 +769,9 @@ def main():
                     layer_call(i, p)
         t1.record(stream)
         torch.cuda.synchronize()
+        bad = [B.kvsel_get_device_status(x) for x in ws_s]
+        if any(bad):
+            raise RuntimeError(f"device status {bad} in a timed variant")
         return max_over_ranks(t0.elapsed_time(t1), world) / (K * L)
 
     Bh = int(wl.budget_ratio * n)
