@@ -157,6 +157,7 @@ __global__ void __launch_bounds__(kApThreads, 1)
       // drain copies still in flight
       for (int tt = max(0, t - kApStages); tt < t; ++tt) mbar_drain(&afull[tt % kApStages], (tt / kApStages) & 1, status);
       if (bl > 0) mbar_drain(&bfull, (bl - 1) & 1, status);
+      ring_tail(aempty, kApStages, t, &s_abort, a.wc);
     }
   } else if (warp == kApMma) {
     if (lane == 0 && hi > lo) {

@@ -152,6 +152,7 @@ __global__ void __launch_bounds__(kPtThreads, 1)
       }
       for (int tt = max(0, t - kPtKStages); tt < t; ++tt) mbar_drain(&kfull[tt % kPtKStages], (tt / kPtKStages) & 1, status);
       mbar_drain(&qfull, 0, status);
+      ring_tail(kempty, kPtKStages, t, &s_abort, a.wc);
     }
   } else if (warp == kPtMma) {
     if (lane == 0 && ntiles > 0) {
@@ -380,6 +381,8 @@ __global__ void __launch_bounds__(kPtThreads, 1)
       for (int tt = max(0, t - kPtKVStages); tt < t; ++tt)
         mbar_drain(&kvfull[tt % kPtKVStages], (tt / kPtKVStages) & 1, status);
       mbar_drain(&qfull, 0, status);
+      ring_tail(kvempty, kPtKVStages, t, &s_abort, a.wc);
+      ring_tail(&cempty, 1, t, &s_abort, a.wc);   // the last tile's C release
     }
   } else if (warp == kPtMma) {
     if (lane == 0 && ntiles > 0) {

@@ -103,6 +103,17 @@ __device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity, int* 
   }
 }
 
+// The last tcgen05.commit arrives on a ring's release barriers have no waiter.  Before the
+// CTA exits, wait until the release of the last use of every stage of the ring (uses
+// [0, issued)) has landed, so that no arrive is still on its way into shared memory that
+// the next CTA on this SM may own.  Gives up at once after an abort (uses that were never
+// consumed get no arrive).
+__device__ __forceinline__ void ring_tail(uint64_t* empty, int stages, int issued, volatile int* s_abort,
+                                          const WaitCtl& wc) {
+  for (int tt = (issued > stages ? issued - stages : 0); tt < issued; ++tt)
+    if (!mbar_wait(&empty[tt % stages], static_cast<uint32_t>((tt / stages) & 1), s_abort, wc)) return;
+}
+
 // ------------------------------------------------------------------------------------
 // TMA (tiled tensor loads into shared memory, completion counted on an mbarrier)
 // ------------------------------------------------------------------------------------

@@ -120,6 +120,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       for (int tt = max(0, t - kStages); tt < t; ++tt) mbar_drain(&full_bar[tt % kStages], (tt / kStages) & 1, status);
       mbar_drain(&q_bar, 0, status);
+      ring_tail(empty_bar, kStages, t, &s_abort, a.wc);
     }
   } else if (warp == kMmaWarp) {
     if (lane == 0) {
@@ -331,6 +332,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       for (int tt = max(0, t - kStages2); tt < t; ++tt) mbar_drain(&full_bar[tt % kStages2], (tt / kStages2) & 1, status);
       mbar_drain(&k_bar, 0, status);
+      ring_tail(empty_bar, kStages2, t, &s_abort, a.wc);
     }
   } else if (warp == kMmaWarp) {
     if (lane == 0 && ntiles > 0) {

@@ -174,6 +174,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // every issued copy lands before the CTA can exit
       for (int tt = max(0, t - STAGES); tt < t; ++tt) mbar_drain(&full_bar[tt % STAGES], (tt / STAGES) & 1, status);
       mbar_drain(&q_bar, 0, status);
+      ring_tail(empty_bar, STAGES, t, &s_abort, a.wc);
     }
   } else if (warp == kMmaWarp) {
     if (lane == 0 && ntiles > 0) {
@@ -357,6 +358,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       for (int tt = max(0, t - stages); tt < t; ++tt) mbar_drain(&full_bar[tt % stages], (tt / stages) & 1, status);
       mbar_drain(&q_bar, 0, status);
+      ring_tail(empty_bar, stages, t, &s_abort, a.wc);
     }
   } else if (warp == kMmaWarp) {
     if (lane == 0 && ntiles > 0) {
@@ -669,6 +671,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
       }
       for (int tt = max(0, T - STAGES); tt < T; ++tt) mbar_drain(&full_bar[tt % STAGES], (tt / STAGES) & 1, status);
       mbar_drain(&q_bar, 0, status);
+      ring_tail(empty_bar, STAGES, T, &s_abort, a.wc);
     }
   } else if (warp == kFMmaWarp || warp == kFMmaWarp + 1) {
     const int iss = warp - kFMmaWarp;   // this warp issues tiles iss, iss + 2, ...

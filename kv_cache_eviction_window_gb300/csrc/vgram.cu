@@ -111,6 +111,7 @@ __global__ void __launch_bounds__(kGfThreads, 1)
       for (int t = max(0, issued - raw_stages); t < issued; ++t) mbar_drain(&rfull[t % raw_stages], (t / raw_stages) & 1, wc.status);
       umma_commit(&done_bar);
       mbar_drain(&done_bar, 0, wc.status);
+      ring_tail(aempty, 2, nb, &s_abort, wc);
     }
   } else {
     const int tid = threadIdx.x;
@@ -305,6 +306,7 @@ __global__ void __launch_bounds__(kVgThreads, 1)
       // drain copies still in flight
       for (int tt = max(0, t - kVgStages); tt < t; ++tt) mbar_drain(&vfull[tt % kVgStages], (tt / kVgStages) & 1, status);
       if (gl > 0) mbar_drain(&gfull, (gl - 1) & 1, status);
+      ring_tail(&gempty, 1, gl, &s_abort, a.wc);   // the last Gamma's release (V stages are released by threads)
     }
   } else if (warp == kVgMma) {
     if (lane == 0 && hi > lo) {

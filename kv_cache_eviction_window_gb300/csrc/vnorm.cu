@@ -188,6 +188,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       for (int tt = max(0, wt - kWStages); tt < wt; ++tt) mbar_drain(&wfull[tt % kWStages], (tt / kWStages) & 1, status);
+      ring_tail(wempty, kWStages, wt, &s_abort, a.wc);
     }
   } else if (warp == kMmaWarp) {
     if (lane == 0 && nseg > 0) {
