@@ -303,7 +303,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sK = smem + 2 * qhalf;
   float* s_c2 = reinterpret_cast<float*>(sK + stages * kKTileBytes);
 
-  __shared__ __align__(8) uint64_t full_bar[4], empty_bar[4], accf_bar[2], acce_bar[2];
+  __shared__ __align__(8) uint64_t full_bar[4], empty_bar[4], accf_bar[4], acce_bar[4];
   __shared__ __align__(8) uint64_t q_bar, done_bar;
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
@@ -326,7 +326,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int s = 0; s < nacc; ++s) {
       mbar_init(&accf_bar[s], 1);
-      mbar_init(&acce_bar[s], kEpiWarps);
+      // two or four accumulators: the four warps of one column group read each of them
+      mbar_init(&acce_bar[s], nacc >= 2 ? 4 : kEpiWarps);
     }
     mbar_init(&q_bar, 1);
     mbar_init(&done_bar, 1);
@@ -416,56 +417,119 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           c2 = mm + lg2_approx(zz);
         }
-        s_c2[r] = c2;
+        s_c2[r] = -c2;   // stored negated: the epilogue adds it with a fused multiply-add
       }
     }
     epi_bar();
     const int q4 = warp & 3, cg = warp >> 2;
     const float s2 = a.s2;
     const int W = a.W;
-    const int half_cols = RP / 2;                  // multiple of 32
-    const int col0 = cg * half_cols;
-    const int col_end = min(R, col0 + half_cols);
     const bool is_max = (a.reduce == 2);
     const float row_scale = (a.reduce == 1) ? 1.f / static_cast<float>(R) : 1.f;
     const size_t out_base = static_cast<size_t>(a.rq.soff[b]) + static_cast<size_t>(h) * n;
-    for (int t = 0; t < ntiles; ++t) {
-      const int acc = t % nacc, ua = t / nacc;
-      const bool ok = mbar_wait(&accf_bar[acc], ua & 1, &s_abort, a.wc);
-      if (epi_any(!ok)) break;
-      tc_fence_after();
-      const int key = key_begin + t * kTileKeys + q4 * 32 + lane;
-      // causal: row r sees this key iff (r % W) >= key - (n - W)
-      const int wmin = a.causal ? key - (n - W) : -1;
-      float acc_sum = 0.f, acc_max = -INFINITY;
-      const uint32_t trow = tbase + (static_cast<uint32_t>(q4 * 32) << 16) + acc * RP;
-      for (int c0 = col0; c0 < col_end; c0 += 64) {
-        float v[64];
-        const int cnt = min(64, col_end - c0);   // warp-uniform
-        tmem_ld32(trow + c0, v);
-        if (cnt > 32) tmem_ld32(trow + c0 + 32, v + 32);
-        tmem_ld_wait();
-        if (wmin <= 0 && cnt == 64) {
-          if (is_max) {
+    if (nacc >= 2) {
+      // warp (q4, cg) takes tiles cg, cg + 2, ... (accumulators of parity cg) and sums
+      // every window row of its key alone: no exchange between the warps of a tile.
+      // Rows go in blocks of 32 (one TMEM load each, the next one issued before the
+      // current block is summed); masked rows (causal tail, rows past R) become -inf.
+      const uint64_t s2p = pack2(s2, s2);
+      auto rows32 = [&](float (&v)[32], int ca, int wmin, float& acc_sum, float& acc_max) {
+        if (wmin > 0 || ca + 32 > R) {
+          int w = ca % W;
 #pragma unroll
-            for (int j = 0; j < 64; ++j) acc_max = fmaxf(acc_max, fmaf(v[j], s2, -s_c2[c0 + j]));
-          } else {
-            float p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
+          for (int j = 0; j < 32; ++j) {
+            if (ca + j >= R || w < wmin) v[j] = -INFINITY;
+            w = (w + 1 == W) ? 0 : w + 1;
+          }
+        }
+        const float4* nc4 = reinterpret_cast<const float4*>(s_c2 + ca);   // -c2 of rows ca ..
+        if (is_max) {
 #pragma unroll
-            for (int j = 0; j < 64; j += 4) {
-              p0 += ex2_approx(fmaf(v[j + 0], s2, -s_c2[c0 + j + 0]));
-              p1 += ex2_approx(fmaf(v[j + 1], s2, -s_c2[c0 + j + 1]));
-              p2 += ex2_approx(fmaf(v[j + 2], s2, -s_c2[c0 + j + 2]));
-              p3 += ex2_approx(fmaf(v[j + 3], s2, -s_c2[c0 + j + 3]));
-            }
-            acc_sum += (p0 + p1) + (p2 + p3);
+          for (int j = 0; j < 32; j += 4) {
+            const float4 c = nc4[j >> 2];
+            acc_max = fmax3(acc_max, fmaf(v[j], s2, c.x), fmaf(v[j + 1], s2, c.y));
+            acc_max = fmax3(acc_max, fmaf(v[j + 2], s2, c.z), fmaf(v[j + 3], s2, c.w));
           }
         } else {
+          uint64_t p2[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+          for (int j = 0; j < 32; j += 4) {
+            const float4 c = nc4[j >> 2];
+            float x0, x1, x2, x3;
+            unpack2(ffma2(pack2(v[j], v[j + 1]), s2p, pack2(c.x, c.y)), x0, x1);
+            unpack2(ffma2(pack2(v[j + 2], v[j + 3]), s2p, pack2(c.z, c.w)), x2, x3);
+            p2[(j >> 2) & 3] = fadd2(p2[(j >> 2) & 3], pack2(ex2_approx(x0), ex2_approx(x1)));
+            p2[(j >> 2) & 3] = fadd2(p2[(j >> 2) & 3], pack2(ex2_approx(x2), ex2_approx(x3)));
+          }
+          float q0, q1;
+          unpack2(fadd2(fadd2(p2[0], p2[1]), fadd2(p2[2], p2[3])), q0, q1);
+          acc_sum += q0 + q1;
+        }
+      };
+      for (int t = cg; t < ntiles; t += 2) {
+        const int acc = t % nacc, ua = t / nacc;
+        const bool ok = mbar_wait(&accf_bar[acc], ua & 1, &s_abort, a.wc);
+        if (!__all_sync(0xffffffffu, ok)) break;
+        tc_fence_after();
+        const int key = key_begin + t * kTileKeys + q4 * 32 + lane;
+        // causal: row r sees this key iff (r % W) >= key - (n - W)
+        const int wmin = a.causal ? key - (n - W) : -1;
+        float acc_sum = 0.f, acc_max = -INFINITY;
+        const uint32_t trow = tbase + (static_cast<uint32_t>(q4 * 32) << 16) + acc * RP;
+        float va[32], vb[32];
+        tmem_ld32(trow, va);
+#pragma unroll 1
+        for (int c0 = 0; c0 < R; c0 += 64) {
+          tmem_ld_wait();   // rows c0 .. c0 + 31
+          const bool second = c0 + 32 < R;
+          if (second) tmem_ld32(trow + c0 + 32, vb);
+          const bool last_a = !second;
+          if (last_a) {   // every row of the tile is in registers: release the accumulator
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acce_bar[acc]);
+          }
+          rows32(va, c0, wmin, acc_sum, acc_max);
+          if (second) {
+            tmem_ld_wait();   // rows c0 + 32 .. c0 + 63
+            const bool more = c0 + 64 < R;
+            if (more) {
+              tmem_ld32(trow + c0 + 64, va);
+            } else {
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&acce_bar[acc]);
+            }
+            rows32(vb, c0 + 32, wmin, acc_sum, acc_max);
+          }
+        }
+        if (key < n) a.s_raw[out_base + key] = is_max ? ex2_approx(acc_max) : acc_sum * row_scale;
+      }
+    } else {
+      // one accumulator (R > 256): both column groups read every tile, each half the rows
+      const int half_cols = RP / 2;   // multiple of 32
+      const int col0 = cg * half_cols;
+      const int col_end = min(R, col0 + half_cols);
+      for (int t = 0; t < ntiles; ++t) {
+        const int acc = t % nacc, ua = t / nacc;
+        const bool ok = mbar_wait(&accf_bar[acc], ua & 1, &s_abort, a.wc);
+        if (epi_any(!ok)) break;
+        tc_fence_after();
+        const int key = key_begin + t * kTileKeys + q4 * 32 + lane;
+        const int wmin = a.causal ? key - (n - W) : -1;
+        float acc_sum = 0.f, acc_max = -INFINITY;
+        const uint32_t trow = tbase + (static_cast<uint32_t>(q4 * 32) << 16) + acc * RP;
+        for (int c0 = col0; c0 < col_end; c0 += 64) {
+          float v[64];
+          const int cnt = min(64, col_end - c0);   // warp-uniform
+          tmem_ld32(trow + c0, v);
+          if (cnt > 32) tmem_ld32(trow + c0 + 32, v + 32);
+          tmem_ld_wait();
 #pragma unroll
           for (int j = 0; j < 64; ++j) {
             const int r = c0 + j;
             if (j < cnt && (r % W) >= wmin) {
-              const float y = fmaf(v[j], s2, -s_c2[r]);
+              const float y = fmaf(v[j], s2, s_c2[r]);
               if (is_max)
                 acc_max = fmaxf(acc_max, y);
               else
@@ -473,23 +537,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acce_bar[acc]);
+        float part_v = is_max ? acc_max : acc_sum;
+        if (cg == 1) s_x[q4][lane] = part_v;
+        epi_bar();
+        if (cg == 0 && key < n) {
+          const float o = s_x[q4][lane];
+          a.s_raw[out_base + key] = is_max ? ex2_approx(fmaxf(part_v, o)) : (part_v + o) * row_scale;
+        }
+        epi_bar();
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&acce_bar[acc]);
-      float part_v = is_max ? acc_max : acc_sum;
-      if (cg == 1) s_x[q4][lane] = part_v;
-      epi_bar();
-      if (cg == 0 && key < n) {
-        const float o = s_x[q4][lane];
-        float res;
-        if (is_max)
-          res = ex2_approx(fmaxf(part_v, o));
-        else
-          res = (part_v + o) * row_scale;
-        a.s_raw[out_base + key] = res;
-      }
-      epi_bar();
     }
   }
   __syncwarp();
@@ -1162,7 +1221,8 @@ cudaError_t launch_win_fused(const WinScoreArgs& a, const CUtensorMap& tq, const
 cudaError_t launch_win_keysum(const WinScoreArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, cudaStream_t st) {
   if (a.ck.total <= 0) return cudaSuccess;
   const int RP = a.R_pad;
-  const int nacc = (2 * RP <= 512) ? 2 : 1;
+  // accumulators: four (R <= 128) or two (R <= 256), one column group of warps per parity
+  const int nacc = RP <= 128 ? 4 : (RP <= 256 ? 2 : 1);
   const uint32_t cols = pow2_cols(static_cast<uint32_t>(nacc * RP));
   const size_t fixed = 1024 + 2 * static_cast<size_t>(RP) * 128 + static_cast<size_t>(RP) * 4;
   const size_t budget = 232448 - 4096;  // opt-in limit minus static shared memory

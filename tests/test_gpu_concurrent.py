@@ -39,6 +39,21 @@ def test_two_launch_scoring_matches_the_oracle(group, window, value_aware):
     _check_layer(wl, inp, gpu, ora)
 
 
+@pytest.mark.parametrize("reduce,causal,group,window", [("sum", True, 4, 24), ("max", True, 5, 32),
+                                                         ("mean", False, 1, 32), ("max", False, 8, 40),
+                                                         ("sum", True, 2, 48)])
+def test_two_launch_reductions_and_ragged_window_rows(reduce, causal, group, window):
+    # window rows R = group * window: 96, 160, 32, 320 (one pass-2 accumulator) and 96, so
+    # that pass 2's last block of rows is a lone 32-row block and the causal tail
+    # crosses the row blocks
+    wl = datagen.WORKLOADS[1].replace(reduce=reduce, causal=causal, group=group, window=window, h_kv=2,
+                                      pool="max", pool_kernel=5)
+    inp = datagen.make_layer(wl, 5, n_ctx=2345)
+    ora = O.run_workload_layer(wl, inp)
+    gpu = GH.run_gpu_layer(wl, inp, concurrent=True, sm_budget=40)
+    _check_layer(wl, inp, gpu, ora)
+
+
 def test_layers_over_three_streams_match_one_stream():
     import torch
 
