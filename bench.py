@@ -864,9 +864,13 @@ def main():
                     x_done[i].record(copy)
                 stream.wait_event(x_done[i])
                 layer_call(i)
+                c_done[i].record(stream)
+            # the results come back once every layer's inputs are on their way: a read-back
+            # queued between two layers' uploads could hold the later upload behind the
+            # earlier layer's compute when both directions share a copy queue
+            for i in range(L):
                 pin[i]["idx"].copy_(bufs[i].idx, non_blocking=True)
                 pin[i]["counts"].copy_(bufs[i].counts, non_blocking=True)
-                c_done[i].record(stream)
 
         for i in range(L):
             c_done[i].record(stream)
@@ -892,8 +896,8 @@ def main():
                                             "against the measured e2e step"},
                       "how": "kvsel_run_layer per layer; per-layer H2D of the request's Q/K/V from pinned host on a "
                              "copy stream overlapped with the previous layer's compute (the model's prepared W_h "
-                             "stays resident); idx/counts D2H per layer; the compacted K/V and the scores stay on "
-                             "the device for the decode step that reads them"}
+                             "stays resident); every layer's idx/counts D2H after the step's last layer; the compacted K/V and the "
+                             "scores stay on the device for the decode step that reads them"}
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = run_cpu_baseline(wl, host)

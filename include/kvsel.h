@@ -140,7 +140,10 @@ typedef struct kvsel_params {
                            which needs every key chunk's CTA resident at once; two such
                            calls running at the same time can each hold SMs the other
                            waits for, until their bounded waits end them with
-                           KVSEL_ETIMEOUT.  Set 1 whenever calls overlap                 */
+                           KVSEL_ETIMEOUT.  Set 1 whenever calls overlap.  With 1 the
+                           selection also runs on clusters of 4 CTAs per segment instead of
+                           8 or 16 (longer alone, half the SM time beside other calls);
+                           results are the same either way                                */
 } kvsel_params;
 
 /* K/V cache view, contiguous or paged (block_size tokens per block). */

@@ -261,7 +261,7 @@ struct SelectArgs {
   const int64_t* dev_offsets;
 };
 cudaError_t launch_select(const SelectArgs& a, int cluster, int chunk_cap, cudaStream_t st);
-int select_cluster_size(int max_len, int segments, int* chunk_cap);
+int select_cluster_size(int max_len, int segments, bool small, int* chunk_cap);   // small: calls overlap
 
 struct CompactArgs {
   ReqTable rq;

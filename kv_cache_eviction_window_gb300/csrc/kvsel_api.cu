@@ -635,7 +635,7 @@ int do_select(const kvsel_params* p, const Plan& pl, const float* s_attn, const 
   const int max_len = p->budget_mode == KVSEL_BUDGET_PER_LAYER ? pl.H * pl.n_max : pl.n_max;
   int cap = 0;
   const int segs = p->budget_mode == KVSEL_BUDGET_PER_LAYER ? pl.B : pl.B * pl.H;
-  const int cs = select_cluster_size(std::max(max_len, 1), segs, &cap);
+  const int cs = select_cluster_size(std::max(max_len, 1), segs, p->concurrent != 0, &cap);
   if (cs < 0) return KVSEL_EUNSUPPORTED;
   StageScope sc(KVSEL_STAGE_SELECT, st);
   if (p->budget_mode != KVSEL_BUDGET_PER_LAYER || !p->value_aware) return launch_rc(launch_select(a, cs, cap, st));
@@ -658,7 +658,7 @@ int do_select(const kvsel_params* p, const Plan& pl, const float* s_attn, const 
   h.dev_counts = counts;
   h.dev_offsets = offsets;
   int cap2 = 0;
-  const int cs2 = select_cluster_size(std::max(pl.n_max, 1), pl.B * pl.H, &cap2);
+  const int cs2 = select_cluster_size(std::max(pl.n_max, 1), pl.B * pl.H, p->concurrent != 0, &cap2);
   if (cs2 < 0) return KVSEL_EUNSUPPORTED;
   return launch_rc(launch_select(h, cs2, cap2, st));
 }

@@ -6,6 +6,7 @@
     python profile_case.py --workload 2 --perturb   # + output perturbation
     python profile_case.py --workload 5 --n-ctx 8192  # query-agnostic, smaller n
     python profile_case.py --workload 2 --plain --partition   # + kept/evicted partition
+    python profile_case.py --workload 2 --plain --concurrent --sm-budget 76   # two-launch scoring
 
 The inputs are the same seeded synthetic tensors as the benchmark (each layer distinct,
 larger than L2 for the 32K stack), so per-launch counters taken here scale to the
@@ -32,6 +33,8 @@ def main():
     ap.add_argument("--perturb", action="store_true", help="also run kvsel_perturbation on each layer's kept set")
     ap.add_argument("--n-ctx", type=int, default=None, help="context length override (a smaller case of the shape)")
     ap.add_argument("--partition", action="store_true", help="also run kvsel_partition on each layer's kept set")
+    ap.add_argument("--concurrent", action="store_true", help="kvsel_params.concurrent = 1 (two-launch scoring)")
+    ap.add_argument("--sm-budget", type=int, default=0, help="kvsel_params.sm_budget")
     args = ap.parse_args()
     import numpy as np
     import torch
@@ -60,7 +63,8 @@ def main():
     for layer in range(args.layers):
         x = datagen.make_layer(wl, layer)
         lens = x["n_ctx"]
-        p = B.params_from_workload(wl, n_ctx_per_req=lens if len(lens) > 1 else None, n_ctx=lens[0])
+        p = B.params_from_workload(wl, n_ctx_per_req=lens if len(lens) > 1 else None, n_ctx=lens[0],
+                                   concurrent=args.concurrent, sm_budget=args.sm_budget)
         if wl.paged:
             pg = x["paged"]
             kt, vt = to_dev(pg["k_pool"]), to_dev(pg["v_pool"])

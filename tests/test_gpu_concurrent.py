@@ -54,6 +54,19 @@ def test_two_launch_reductions_and_ragged_window_rows(reduce, causal, group, win
     _check_layer(wl, inp, gpu, ora)
 
 
+@pytest.mark.parametrize("cid,n,kw", [(3, 3333, dict()), (3, 2500, dict(value_aware=True, d_model=1024)),
+                                      (4, None, dict(batch=4, n_min=300, n_ctx=1400))])
+def test_concurrent_selection_per_layer_and_batched(cid, n, kw):
+    # overlapping calls select on 4-CTA clusters: per-layer budgets with floors (one
+    # segment per layer), the value-aware two-stage selection under a per-layer budget,
+    # and the ragged paged batch, each against the oracle
+    wl = datagen.WORKLOADS[cid].replace(**kw)
+    inp = datagen.make_layer(wl, 9, n_ctx=n) if n else datagen.make_layer(wl, 9)
+    ora = O.run_workload_layer(wl, inp)
+    gpu = GH.run_gpu_layer(wl, inp, concurrent=True, sm_budget=76)
+    _check_layer(wl, inp, gpu, ora)
+
+
 def test_layers_over_three_streams_match_one_stream():
     import torch
 
