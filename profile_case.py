@@ -7,6 +7,13 @@
     python profile_case.py --workload 5 --n-ctx 8192  # query-agnostic, smaller n
     python profile_case.py --workload 2 --plain --partition   # + kept/evicted partition
     python profile_case.py --workload 2 --plain --concurrent --sm-budget 76   # two-launch scoring
+    python profile_case.py --workload 2 --plain --layers 8 --graph-streams 8 --concurrent --sm-budget 76
+
+With --graph-streams S the layers are issued round-robin over S streams (one workspace
+each) and captured as one CUDA graph; after --steps warm-up replays, one more replay runs
+between cudaProfilerStart and cudaProfilerStop, for `ncu --profile-from-start off
+--graph-profiling graph`, which measures the whole replay (all layers, overlapped) as one
+result.
 
 The inputs are the same seeded synthetic tensors as the benchmark (each layer distinct,
 larger than L2 for the 32K stack), so per-launch counters taken here scale to the
@@ -35,6 +42,8 @@ def main():
     ap.add_argument("--partition", action="store_true", help="also run kvsel_partition on each layer's kept set")
     ap.add_argument("--concurrent", action="store_true", help="kvsel_params.concurrent = 1 (two-launch scoring)")
     ap.add_argument("--sm-budget", type=int, default=0, help="kvsel_params.sm_budget")
+    ap.add_argument("--graph-streams", type=int, default=0,
+                    help="issue the layers over this many streams as one CUDA graph (see above)")
     args = ap.parse_args()
     import numpy as np
     import torch
@@ -82,6 +91,8 @@ def main():
         buf = B.LayerBuffers(p, device=dev)
         x_w[id(buf)] = to_dev(x["w_o"]) if x["w_o"] is not None else None
         layers.append((p, q, kv, w, buf, keep))
+    if args.graph_streams > 0:
+        return run_graph(args, B, layers, dev)
     nst = len(B.STAGES)
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * nst)]
     for e in ev:
@@ -130,6 +141,49 @@ def main():
     for i, name in enumerate(B.STAGES):
         print(f"  {name:9s} {tot[i] / cnt * 1e3:9.2f} us/layer (event-timed, includes launch gaps)")
     return 0 if st == 0 else 1
+
+
+def run_graph(args, B, layers, dev):
+    """The layers over S streams as one CUDA graph; the last replay is the profiled one."""
+    import torch
+
+    S = args.graph_streams
+    p0 = layers[0][0]
+    wss = [torch.zeros(B.kvsel_workspace_size(p0) // 4 + 64, dtype=torch.int32, device=dev) for _ in range(S)]
+    for x in wss:
+        B.kvsel_workspace_init(x)
+    ss = [torch.cuda.Stream() for _ in range(S)]
+
+    def issue():
+        for i, (p, q, kv, w, b, _k) in enumerate(layers):
+            B.kvsel_run_layer(p, q, kv, w, b.s_attn, b.s_val, b.idx, b.counts, b.offsets, b.k_out, b.v_out,
+                              wss[i % S], ss[i % S])
+
+    issue()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=ss[0]):
+        for x in ss[1:]:
+            x.wait_stream(ss[0])
+        issue()
+        for x in ss[1:]:
+            ss[0].wait_stream(x)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    times = []
+    for _ in range(max(args.steps, 1)):
+        t0.record()
+        g.replay()
+        t1.record()
+        torch.cuda.synchronize()
+        times.append(t0.elapsed_time(t1))
+    torch.cuda.profiler.start()
+    g.replay()
+    torch.cuda.synchronize()
+    torch.cuda.profiler.stop()
+    st = [B.kvsel_get_device_status(x) for x in wss]
+    print(f"{len(layers)} layers over {S} streams as one graph: best replay {min(times) * 1e3 / len(layers):.2f} "
+          f"us/layer, device status {st}")
+    return 0 if not any(st) else 1
 
 
 if __name__ == "__main__":
