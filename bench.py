@@ -841,8 +841,11 @@ def main():
         h2d = sum(t[k].numel() * 2 for t in pin for k in ("q", "k", "v"))
         d2h = sum(t["idx"].numel() * 4 + t["counts"].numel() * 4 for t in pin)
         copy = torch.cuda.Stream()
-        # the host link's own rate: one layer's K copied from pinned memory, best of three
+        # the host link's own rate: one layer's K copied from pinned memory, best of three,
+        # and every layer's Q/K/V copied back to back with no compute (the step's uploads
+        # alone), best of two; per-layer K rates show pinned pages that sit farther away
         link_gbs = 0.0
+        layer_gbs = []
         with torch.cuda.stream(copy):
             for _ in range(3):
                 a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -851,6 +854,25 @@ def main():
                 a1.record(copy)
                 a1.synchronize()
                 link_gbs = max(link_gbs, pin[0]["k"].numel() * 2 / (a0.elapsed_time(a1) * 1e-3) / 1e9)
+            for i in range(L):
+                a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a0.record(copy)
+                k_d[i].copy_(pin[i]["k"], non_blocking=True)
+                a1.record(copy)
+                a1.synchronize()
+                layer_gbs.append(pin[i]["k"].numel() * 2 / (a0.elapsed_time(a1) * 1e-3) / 1e9)
+            uploads_ms = None
+            for _ in range(2):
+                a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a0.record(copy)
+                for i in range(L):
+                    q_d[i].copy_(pin[i]["q"], non_blocking=True)
+                    k_d[i].copy_(pin[i]["k"], non_blocking=True)
+                    v_d[i].copy_(pin[i]["v"], non_blocking=True)
+                a1.record(copy)
+                a1.synchronize()
+                t_up = a0.elapsed_time(a1)
+                uploads_ms = t_up if uploads_ms is None else min(uploads_ms, t_up)
         c_done = [torch.cuda.Event() for _ in range(L)]
         x_done = [torch.cuda.Event() for _ in range(L)]
 
@@ -880,20 +902,30 @@ def main():
         barrier(world)
         w0 = time.perf_counter()
         t0.record(stream)
+        marks = []
         for _ in range(K):
             e2e_step()
+            marks.append(torch.cuda.Event(enable_timing=True))
+            marks[-1].record(stream)
         t1.record(stream)
         torch.cuda.synchronize()
         wall = time.perf_counter() - w0
         ems = max_over_ranks(max(t0.elapsed_time(t1), wall * 1e3), world)
+        step_ms = [t0.elapsed_time(marks[0])] + [marks[j - 1].elapsed_time(marks[j]) for j in range(1, K)]
         link_ms = h2d / (link_gbs * 1e9) * 1e3 if link_gbs > 0 else None
         out["e2e"] = {"value": job_value(K * L * H * n, ems, world), "unit": UNIT, "h2d_bytes_per_step": h2d,
                       "d2h_bytes_per_step": d2h, "ms_per_step": ems / K,
+                      "step_ms_min_max": [round(min(step_ms), 3), round(max(step_ms), 3)],
+                      "wall_ms_per_step": round(wall * 1e3 / K, 3),
                       "host_link": {"h2d_gbs": round(link_gbs, 1),
                                     "ms_per_step_at_link_rate": round(link_ms, 3) if link_ms else None,
                                     "frac": round(link_ms / (ems / K), 3) if link_ms else None,
-                                    "what": "the step's H2D bytes at the measured pinned-host copy rate, "
-                                            "against the measured e2e step"},
+                                    "uploads_only_ms_per_step": round(uploads_ms, 3),
+                                    "uploads_only_frac": round(uploads_ms / (ems / K), 3),
+                                    "layer_k_gbs_min_max": [round(min(layer_gbs), 1), round(max(layer_gbs), 1)],
+                                    "what": "the step's H2D bytes at the best pinned-host copy rate of one layer's "
+                                            "K (frac), and the step's uploads alone, back to back with no compute "
+                                            "(uploads_only_frac), each against the measured e2e step"},
                       "how": "kvsel_run_layer per layer; per-layer H2D of the request's Q/K/V from pinned host on a "
                              "copy stream overlapped with the previous layer's compute (the model's prepared W_h "
                              "stays resident); every layer's idx/counts D2H after the step's last layer; the compacted K/V and the "
