@@ -339,6 +339,10 @@ def test_c2_full_layer_plain_full_oracle():
     ora = O.run_workload_layer(wl, inp, compact_out=False)
     gpu = GH.run_gpu_layer(wl, inp)
     _check_layer(wl, inp, gpu, ora)
+    # the benchmark's plain-path configuration: overlapping calls on half the SMs (two
+    # scoring launches, 4-CTA selection clusters)
+    gpu = GH.run_gpu_layer(wl, inp, concurrent=True, sm_budget=76)
+    _check_layer(wl, inp, gpu, ora)
 
 
 def test_c2_full_layer_value_aware_full_oracle():
@@ -351,6 +355,10 @@ def test_c2_full_layer_value_aware_full_oracle():
     inp = datagen.make_layer(wl, 0)
     ora = O.run_workload_layer(wl, inp, compact_out=False)
     gpu = GH.run_gpu_layer(wl, inp)
+    _check_layer(wl, inp, gpu, ora)
+    # the benchmark's headline configuration: overlapping calls on every SM (two scoring
+    # launches, 4-CTA selection clusters)
+    gpu = GH.run_gpu_layer(wl, inp, concurrent=True)
     _check_layer(wl, inp, gpu, ora)
 
 

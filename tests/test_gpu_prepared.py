@@ -56,12 +56,14 @@ def test_prepared_weights_are_bit_identical(override):
     _same_bits(_run(wl, inp, False, **override), _run(wl, inp, True, **override))
 
 
-def test_prepared_weights_full_size_layer():
+@pytest.mark.parametrize("concurrent", [False, True])
+def test_prepared_weights_full_size_layer(concurrent):
     """The benchmark's 32K layer: prepared and per-call weights give the same outputs, bit
-    for bit (the per-call path is compared with the full oracle in test_gpu_parity)."""
+    for bit (the per-call path is compared with the full oracle in test_gpu_parity), alone
+    and as an overlapping call (the benchmark's configuration)."""
     wl = datagen.WORKLOADS[2]
     inp = datagen.make_layer(wl, 0)
-    _same_bits(_run(wl, inp, False), _run(wl, inp, True))
+    _same_bits(_run(wl, inp, False, concurrent=concurrent), _run(wl, inp, True, concurrent=concurrent))
 
 
 def test_prepared_sizes_and_rejections():
