@@ -260,6 +260,8 @@ constexpr int kKBlock2 = kMT2 * 32768;        // bytes of the resident keys
 constexpr int kTile2 = kNT2 * 256;            // bytes of one streamed tile (two 64-column halves)
 constexpr uint32_t kSlotCols2 = kNT2;         // one 256-column accumulator slot per M tile
 constexpr int kRowsPerWarp2 = kNT2 / 4;       // query rows (accumulator columns) per epilogue warp
+constexpr uint32_t kTmemCols2 = kMT2 * kSlotCols2;
+static_assert(kTmemCols2 <= 512, "TMEM");
 
 __global__ void __launch_bounds__(kThreads, 1)
     qa_keymax_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
@@ -303,7 +305,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_mbar_init();
   }
   if (warp == kMmaWarp) {
-    tmem_alloc(&s_tmem, kTmemCols);
+    tmem_alloc(&s_tmem, kTmemCols2);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -441,7 +443,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   if (warp == kMmaWarp) {
     tc_fence_after();
-    tmem_dealloc(tbase, kTmemCols);
+    tmem_dealloc(tbase, kTmemCols2);
   }
 }
 
