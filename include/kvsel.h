@@ -142,8 +142,9 @@ typedef struct kvsel_params {
                            waits for, until their bounded waits end them with
                            KVSEL_ETIMEOUT.  Set 1 whenever calls overlap.  With 1 the
                            selection also runs on clusters of 4 CTAs per segment instead of
-                           8 or 16 (longer alone, half the SM time beside other calls);
-                           results are the same either way                                */
+                           8 or 16 (longer alone, half the SM time beside other calls), or
+                           of 2 when 4 per segment would exceed sm_budget; results are the
+                           same either way                                                */
 } kvsel_params;
 
 /* K/V cache view, contiguous or paged (block_size tokens per block). */

@@ -261,7 +261,8 @@ struct SelectArgs {
   const int64_t* dev_offsets;
 };
 cudaError_t launch_select(const SelectArgs& a, int cluster, int chunk_cap, cudaStream_t st);
-int select_cluster_size(int max_len, int segments, bool small, int* chunk_cap);   // small: calls overlap
+// min_cs: 0 for a call alone on the device, else the smallest cluster to try (calls overlap)
+int select_cluster_size(int max_len, int segments, int min_cs, int* chunk_cap);
 
 struct CompactArgs {
   ReqTable rq;

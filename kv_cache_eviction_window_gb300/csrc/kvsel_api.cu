@@ -635,7 +635,13 @@ int do_select(const kvsel_params* p, const Plan& pl, const float* s_attn, const 
   const int max_len = p->budget_mode == KVSEL_BUDGET_PER_LAYER ? pl.H * pl.n_max : pl.n_max;
   int cap = 0;
   const int segs = p->budget_mode == KVSEL_BUDGET_PER_LAYER ? pl.B : pl.B * pl.H;
-  const int cs = select_cluster_size(std::max(max_len, 1), segs, p->concurrent != 0, &cap);
+  // overlapping calls: 4-CTA clusters, or 2 when four per segment would exceed the SMs the
+  // call is sized for (many calls in flight)
+  const auto min_cs = [&](int nseg) {
+    if (!p->concurrent) return 0;
+    return (p->sm_budget > 0 && 4ll * nseg > p->sm_budget) ? 2 : 4;
+  };
+  const int cs = select_cluster_size(std::max(max_len, 1), segs, min_cs(segs), &cap);
   if (cs < 0) return KVSEL_EUNSUPPORTED;
   StageScope sc(KVSEL_STAGE_SELECT, st);
   if (p->budget_mode != KVSEL_BUDGET_PER_LAYER || !p->value_aware) return launch_rc(launch_select(a, cs, cap, st));
@@ -658,7 +664,7 @@ int do_select(const kvsel_params* p, const Plan& pl, const float* s_attn, const 
   h.dev_counts = counts;
   h.dev_offsets = offsets;
   int cap2 = 0;
-  const int cs2 = select_cluster_size(std::max(pl.n_max, 1), pl.B * pl.H, p->concurrent != 0, &cap2);
+  const int cs2 = select_cluster_size(std::max(pl.n_max, 1), pl.B * pl.H, min_cs(pl.B * pl.H), &cap2);
   if (cs2 < 0) return KVSEL_EUNSUPPORTED;
   return launch_rc(launch_select(h, cs2, cap2, st));
 }

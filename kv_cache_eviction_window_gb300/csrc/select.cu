@@ -564,21 +564,21 @@ size_t select_smem(int chunk_cap) {
 }  // namespace
 
 // Cluster size for `segments` segments of at most `max_len` entries.  Alone on the
-// device (small = false): the largest of 16 / 8 CTAs whose clusters all fit on the device
+// device (min_cs = 0): the largest of 16 / 8 CTAs whose clusters all fit on the device
 // at once (a cluster must sit inside one GPC), else the one that keeps the most CTAs busy
-// in the first wave.  Beside other work (small = true): the smallest of 4 / 8 / 16 CTAs
-// whose staging fits in shared memory.  A cluster spends most of its time in cluster
-// barriers, so with other calls in flight fewer, longer-running CTAs leave more SMs to
-// them: a 4-CTA cluster per head holds half the SM time of an 8-CTA one for about 17%
-// more latency.
-int select_cluster_size_uncached(int max_len, int segments, bool small, int* chunk_cap);
+// in the first wave.  Beside other work (min_cs = 2 or 4): the smallest of min_cs,
+// 2 min_cs, ... 16 CTAs whose staging fits in shared memory.  A cluster spends most of its
+// time in cluster barriers, so with other calls in flight fewer, longer-running CTAs leave
+// more SMs to them: a 4-CTA cluster per head holds half the SM time of an 8-CTA one for
+// about 17% more latency.
+int select_cluster_size_uncached(int max_len, int segments, int min_cs, int* chunk_cap);
 
-int select_cluster_size(int max_len, int segments, bool small, int* chunk_cap) {
+int select_cluster_size(int max_len, int segments, int min_cs, int* chunk_cap) {
   static std::mutex mu;
-  static std::map<std::tuple<int, int, int, bool>, std::pair<int, int>> cache;
+  static std::map<std::tuple<int, int, int, int>, std::pair<int, int>> cache;
   int dev = 0;
   cudaGetDevice(&dev);
-  const auto key = std::make_tuple(dev, max_len, segments, small);
+  const auto key = std::make_tuple(dev, max_len, segments, min_cs);
   {
     std::lock_guard<std::mutex> lock(mu);
     auto it = cache.find(key);
@@ -588,7 +588,7 @@ int select_cluster_size(int max_len, int segments, bool small, int* chunk_cap) {
     }
   }
   int cap = 0;
-  const int cs = select_cluster_size_uncached(max_len, segments, small, &cap);
+  const int cs = select_cluster_size_uncached(max_len, segments, min_cs, &cap);
   if (cs > 0) {
     std::lock_guard<std::mutex> lock(mu);
     cache[key] = std::make_pair(cs, cap);
@@ -597,14 +597,17 @@ int select_cluster_size(int max_len, int segments, bool small, int* chunk_cap) {
   return cs;
 }
 
-int select_cluster_size_uncached(int max_len, int segments, bool small, int* chunk_cap) {
+int select_cluster_size_uncached(int max_len, int segments, int min_cs, int* chunk_cap) {
   const size_t limit = 232448 - 1024;
   int best_cs = -1, best_cap = 0;
   long long best_busy = -1;
-  const int order_large[] = {16, 8};
-  const int order_small[] = {4, 8, 16};
-  const int* order = small ? order_small : order_large;
-  const int n_order = small ? 3 : 2;
+  const bool small = min_cs > 0;
+  int order[4] = {16, 8, 0, 0};
+  int n_order = 2;
+  if (small) {
+    n_order = 0;
+    for (int cs = min_cs; cs <= 16; cs *= 2) order[n_order++] = cs;
+  }
   for (int i = 0; i < n_order; ++i) {
     const int cs = order[i];
     const int cap = (max_len + cs - 1) / cs;

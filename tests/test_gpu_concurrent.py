@@ -29,13 +29,16 @@ def _lib():
     yield
 
 
-@pytest.mark.parametrize("group,window,value_aware", [(4, 32, True), (4, 32, False), (2, 32, True), (8, 32, False),
-                                                      (4, 64, True)])
-def test_two_launch_scoring_matches_the_oracle(group, window, value_aware):
+@pytest.mark.parametrize("group,window,value_aware,budget", [(4, 32, True, 76), (4, 32, False, 76),
+                                                             (2, 32, True, 76), (8, 32, False, 76),
+                                                             (4, 64, True, 76), (4, 32, True, 24),
+                                                             (4, 32, False, 24)])
+def test_two_launch_scoring_matches_the_oracle(group, window, value_aware, budget):
+    # an SM budget of 24 for 8 heads selects on 2-CTA clusters (4 per head would exceed it)
     wl = datagen.WORKLOADS[2].replace(layers=1, group=group, window=window, value_aware=value_aware)
     inp = datagen.make_layer(wl, 21, n_ctx=3001)
     ora = O.run_workload_layer(wl, inp)
-    gpu = GH.run_gpu_layer(wl, inp, concurrent=True, sm_budget=76)
+    gpu = GH.run_gpu_layer(wl, inp, concurrent=True, sm_budget=budget)
     _check_layer(wl, inp, gpu, ora)
 
 
