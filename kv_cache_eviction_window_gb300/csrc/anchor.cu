@@ -22,6 +22,13 @@
 namespace kvsel {
 namespace {
 
+__device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+
 constexpr int kAnchorMax = 1024;       // anchors per (request, head) held in shared memory
 constexpr int kAnChunk = 256;          // anchors per MMA chain (UMMA N)
 constexpr int kApProducer = 16;        // warps 0-15: epilogue (eight per TMEM accumulator)
@@ -252,10 +259,13 @@ __global__ void __launch_bounds__(kApThreads, 1)
           const float iv[8] = {i0.x, i0.y, i0.z, i0.w, i1.x, i1.y, i1.z, i1.w};
           float kk[8];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const float sc = y[q + e] * iv[e];
-            kk[e] = __int_as_float((__float_as_int(sc) & ~31) | (31 - (q + e)));
+          for (int e = 0; e < 8; e += 2) {
+            float sc0, sc1;   // the products two at a time (mul.rn.f32x2: the same rounding)
+            unpack2(fmul2(pack2(y[q + e], y[q + e + 1]), pack2(iv[e], iv[e + 1])), sc0, sc1);
+            kk[e] = __int_as_float((__float_as_int(sc0) & ~31) | (31 - (q + e)));
+            kk[e + 1] = __int_as_float((__float_as_int(sc1) & ~31) | (31 - (q + e + 1)));
             if (!kFull && q + e >= lim) kk[e] = -INFINITY;
+            if (!kFull && q + e + 1 >= lim) kk[e + 1] = -INFINITY;
           }
           m[(q >> 3) & 3] = fmax3(m[(q >> 3) & 3], fmax3(kk[0], kk[1], kk[2]), fmax3(kk[3], kk[4], kk[5]));
           m[((q >> 3) + 2) & 3] = fmax3(m[((q >> 3) + 2) & 3], kk[6], kk[7]);
