@@ -917,6 +917,7 @@ def main():
         out["e2e"] = {"value": job_value(K * L * H * n, ems, world), "unit": UNIT, "h2d_bytes_per_step": h2d,
                       "d2h_bytes_per_step": d2h, "ms_per_step": ems / K,
                       "step_ms_min_max": [round(min(step_ms), 3), round(max(step_ms), 3)],
+                      "step_ms_median": round(sorted(step_ms)[len(step_ms) // 2], 3),
                       "wall_ms_per_step": round(wall * 1e3 / K, 3),
                       "host_link": {"h2d_gbs": round(link_gbs, 1),
                                     "ms_per_step_at_link_rate": round(link_ms, 3) if link_ms else None,
