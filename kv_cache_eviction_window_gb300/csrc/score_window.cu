@@ -15,9 +15,10 @@
 //     c_r = m_r + log2 Z_r merged from the pass-1 partials (or takes the max).
 //
 // Both passes stream K through a TMA ring (128-byte swizzled K-major tiles); K of a
-// layer is re-read by pass 2 mostly from L2.  Warp roles: warps 0-7 epilogue (two
-// warps per TMEM lane quadrant, splitting the columns), warp 8 TMA producer, warp 9
-// UMMA issuer.  Every wait is bounded (ptx.cuh).
+// layer is re-read by pass 2 from L2 when nothing else ran in between.  Warp roles:
+// warps 0-7 epilogue (two warps per TMEM lane quadrant: pass 1 splits a tile's columns
+// between them, pass 2 gives each its own tiles when R <= 256), warp 8 TMA producer,
+// warp 9 UMMA issuer.  Every wait is bounded (ptx.cuh).
 #include "internal.cuh"
 
 namespace kvsel {
