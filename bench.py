@@ -779,10 +779,10 @@ def main():
     small = int(wl.h_kv * wl.group * wl.window * d * 2) + 2 * H * n * 4
     # ---- the plain-score path on the same layers (spec HBM target)
     if not args.no_plain:
-        # with several layers in flight, the plain layers are sized for a fifth of the SMs
-        # (kvsel_params.sm_budget): fewer, longer scoring CTAs per layer, more layers side
-        # by side (40.7 us per layer at 16 streams against 42.8 at 8 streams and half)
-        sm_plain = torch.cuda.get_device_properties(dev).multi_processor_count // 5 if S > 1 else 0
+        # with several layers in flight, the plain layers are sized for a twelfth of the SMs
+        # (kvsel_params.sm_budget): fewer, longer scoring CTAs per layer (two key chunks per
+        # head on the 32K layer), more layers side by side
+        sm_plain = torch.cuda.get_device_properties(dev).multi_processor_count // 12 if S > 1 else 0
         pms = time_variant(B.params_from_workload(wl, value_aware=False, sm_budget=sm_plain, concurrent=conc))
         alg = H * n * d * 2 + kept_rw + small
         gbs = alg / (pms * 1e-3) / 1e9

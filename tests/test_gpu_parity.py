@@ -339,13 +339,13 @@ def test_c2_full_layer_plain_full_oracle():
     ora = O.run_workload_layer(wl, inp, compact_out=False)
     gpu = GH.run_gpu_layer(wl, inp)
     _check_layer(wl, inp, gpu, ora)
-    # the benchmark's plain-path configuration: overlapping calls sized for a fifth of the
-    # SMs (two scoring launches of a few long chunks per head, 4-CTA selection clusters),
-    # and for half of them
+    # the benchmark's plain-path configuration: overlapping calls sized for a twelfth of
+    # the SMs (two scoring launches of two long chunks per head, 2-CTA selection
+    # clusters), and for a fifth and half of them (4-CTA clusters at half)
     import torch
 
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    for budget in (sms // 5, sms // 2):
+    for budget in (sms // 12, sms // 5, sms // 2):
         gpu = GH.run_gpu_layer(wl, inp, concurrent=True, sm_budget=budget)
         _check_layer(wl, inp, gpu, ora)
 
